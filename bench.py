@@ -1,0 +1,547 @@
+"""Benchmark: segmented paged prefill at 128K over 64 layers, and ragged decode.
+
+One step = one pass of the hot path over a 131072-token sequence through 64
+layers (64 query / 8 KV heads, D=128, pages of 128): per layer, append K/V
+into the segments (local heads keep only their window), prefill attention for
+all 131072 positions, then trim the local heads to what decoding needs.
+value = useful (kept-key) FLOPs per step / step time. The ragged-decode
+workload (32 requests, 2K-32K log-uniform contexts, one token appended per
+request per step) is measured alongside and reported as GB/s of algorithmic
+K/V bytes.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SegPaged prefill ms & useful TFLOP/s at 128K (1 GB300); decode GB/s vs HBM peak"
+UNIT = "TFLOP/s"
+N_INPUT_SETS = 4
+
+
+def useful_flops_layer(w, layer, n):
+    """4*D * sum over query heads and positions of |visible keys|."""
+    W = w.window[layer]
+    G = w.group
+    tot = 0
+    for h in range(w.hkv):
+        if w.head_class[layer][h] == 0:
+            keys = n * (n + 1) // 2
+        else:
+            m = min(n, W)
+            keys = m * (m + 1) // 2 + (n - m) * W
+        tot += G * keys
+    return 4 * w.head_dim * tot
+
+
+def decode_bytes(w, lens):
+    """Kept K/V bytes the decode step must read, plus q and o."""
+    W = w.window[0]
+    b = 0
+    for n in lens:
+        for h in range(w.hkv):
+            keys = n if w.head_class[0][h] == 0 else min(n, W)
+            b += keys * w.head_dim * 2 * 2
+    b += 2 * len(lens) * w.hq * w.head_dim * 2
+    return b
+
+
+class Clocks:
+    """nvidia-smi sampling during a timed region."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 7:
+                try:
+                    rows.append((float(parts[0]), float(parts[1]), parts[3:7]))
+                except ValueError:
+                    pass
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i] == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": rows[0][1],
+                "reasons": reasons, "samples": len(rows)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), \
+            d.get("bf16_tflops_sustained", 1700.0), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world):
+    import numpy as np
+    import torch
+
+    import head_segmented_paged_gb300 as S
+    from head_segmented_paged_gb300 import inputs as I
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    w = I.long_128k_64layer(seed=0)
+    n = w.seq_lens[0]
+    L, hq, hkv, D, P = w.num_layers, w.hq, w.hkv, w.head_dim, w.page_size
+
+    # seeded inputs, generated on the device; layer l uses set l % N_INPUT_SETS
+    sets = []
+    for s in range(N_INPUT_SETS):
+        q = I.normal_bf16(w.seed, I.tensor_stream(I._Q, s), (n, hq, D), device=dev)
+        k = I.normal_bf16(w.seed, I.tensor_stream(I._K, s), (n, hkv, D), device=dev)
+        v = I.normal_bf16(w.seed, I.tensor_stream(I._V, s), (n, hkv, D), device=dev)
+        sets.append((q, k, v))
+    cu = np.array([0, n], np.int32)
+    q_pos = np.arange(n, dtype=np.int32)
+    o = torch.empty((n, hq, D), dtype=torch.bfloat16, device=dev)
+
+    # pool: every global head of every layer keeps 1024 pages; local heads keep
+    # the whole layer until its trim, then about W/P + 1 pages
+    pages_per_head = n // P
+    n_glob = sum(sum(1 for c in w.head_class[l] if c == 0) for l in range(L))
+    num_pages = n_glob * pages_per_head + (L * hkv) * (4096 // P + 2) + hkv * pages_per_head + 64
+    kp = torch.empty((num_pages, P, D), dtype=torch.bfloat16, device=dev)
+    vp = torch.empty_like(kp)
+    h = S.SegKV(L, hq, hkv, D, w.head_class, w.window, P, 1, n, kp, vp)
+    flops = [useful_flops_layer(w, l, n) for l in range(L)]
+    step_flops = sum(flops)
+
+    ev_pf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(L)]
+    ev_ap = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(L)]
+
+    def step(timed):
+        h.free_seq(0)
+        for l in range(L):
+            q, k, v = sets[l % N_INPUT_SETS]
+            if timed:
+                ev_ap[l][0].record(stream)
+            h.append(l, k, v, cu, [0], stream)
+            if timed:
+                ev_ap[l][1].record(stream)
+                ev_pf[l][0].record(stream)
+            h.prefill_attn(l, q, cu, q_pos, [0], o, None, stream)
+            if timed:
+                ev_pf[l][1].record(stream)
+            h.trim(l, [0])
+
+    for _ in range(args.warmup):
+        step(False)
+    torch.cuda.synchronize()
+    if h.status() != 0:
+        raise RuntimeError("device status after warm-up: " + S.segkv_last_error(h.handle))
+
+    clk = Clocks(dev.index)
+    clk.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    pf_ms, ap_ms = [], []
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(True)
+        torch.cuda.synchronize()
+        pf_ms.append(sum(a.elapsed_time(b) for a, b in ev_pf))
+        ap_ms.append(sum(a.elapsed_time(b) for a, b in ev_ap))
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = clk.stop()
+    total_ms = t0.elapsed_time(t1)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if h.status() != 0:
+        raise RuntimeError("device status after timed steps: " + S.segkv_last_error(h.handle))
+    ms_step = total_ms / args.steps
+    prefill_ms = statistics.median(pf_ms)
+    append_ms = statistics.median(ap_ms)
+    value = world * step_flops / (ms_step * 1e-3) / 1e12
+
+    hbm, bf16_burst, bf16_sus, peak_src = measured_peaks()
+    achieved = step_flops / (prefill_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 2), "peak": bf16_sus,
+                "unit": "TFLOP/s", "frac": round(achieved / bf16_sus, 4),
+                "peak_kind": f"bf16 sustained ({peak_src}); kernel runs inside a ~{ms_step:.0f} ms step",
+                "frac_of_burst": round(achieved / bf16_burst, 4),
+                "kernel": "prefill_kernel<128>", "per_launch_flops_mean": step_flops / L,
+                "traffic": None}
+
+    out = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic: seeded splitmix64 + Box-Muller N(0,1), rounded to bf16",
+           "config": {"workload": "128k-64layer prefill", "layers": L, "hq": hq, "hkv": hkv,
+                      "head_dim": D, "page_size": P, "context": n,
+                      "global_kv_heads_total": n_glob, "input_sets": N_INPUT_SETS,
+                      "l2": "inputs larger than L2 (Q is 2 GiB per layer); no flush",
+                      "parallelism": "replicas" if world > 1 else "single GPU"},
+           "prefill_ms": round(prefill_ms, 3), "append_ms": round(append_ms, 3),
+           "useful_tflop_per_step": round(step_flops / 1e12, 3),
+           "prefill_useful_tflops": round(achieved, 2),
+           "roofline": roofline, "clocks": clocks, "gpu_launches": 2 * L * args.steps}
+
+    del h
+    torch.cuda.synchronize()
+    if not args.no_decode:
+        out["decode"] = run_decode(args, dev, stream, hbm, peak_src)
+    if not args.no_dense:
+        out["dense"] = run_dense(args, dev, stream, sets, cu, q_pos, o, prefill_ms)
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(args, dev, stream, w, sets, cu, q_pos, step_flops, num_pages)
+    if rank == 0 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline(sets, w, budget_s=args.cpu_seconds)
+    return out
+
+
+def run_dense(args, dev, stream, sets, cu, q_pos, o, sparse_prefill_ms):
+    """The same library with every head global (full causal), on 4 layers;
+    layers are identical, so the 64-layer time is 16x theirs."""
+    import torch
+
+    import head_segmented_paged_gb300 as S
+    from head_segmented_paged_gb300 import inputs as I
+
+    w = I.long_128k_64layer(seed=0, all_global=True)
+    n, P, D = w.seq_lens[0], w.page_size, w.head_dim
+    Ld = 4
+    kp = torch.empty((w.hkv * (n // P) + 8, P, D), dtype=torch.bfloat16, device=dev)
+    vp = torch.empty_like(kp)
+    h = S.SegKV(Ld, w.hq, w.hkv, D, w.head_class[:Ld], w.window[:Ld], P, 1, n, kp, vp)
+    flops = useful_flops_layer(w, 0, n)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(Ld)]
+    # warm-up one layer
+    q, k, v = sets[0]
+    h.append(0, k, v, cu, [0], stream)
+    h.prefill_attn(0, q, cu, q_pos, [0], o, None, stream)
+    h.free_seq(0)
+    torch.cuda.synchronize()
+    for l in range(Ld):
+        q, k, v = sets[l % len(sets)]
+        h.append(l, k, v, cu, [0], stream)
+        evs[l][0].record(stream)
+        h.prefill_attn(l, q, cu, q_pos, [0], o, None, stream)
+        evs[l][1].record(stream)
+        h.free_seq(0)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in evs]
+    per_layer = statistics.median(ms)
+    return {"layers_timed": Ld, "prefill_ms_per_layer": round(per_layer, 3),
+            "prefill_ms_64_layers_extrapolated": round(per_layer * 64, 1),
+            "useful_tflops": round(flops / (per_layer * 1e-3) / 1e12, 2),
+            "speedup_segpaged_vs_dense": round(per_layer * 64 / sparse_prefill_ms, 2),
+            "note": "all heads global, full causal; 4 identical layers timed, x16"}
+
+
+def run_decode(args, dev, stream, hbm, peak_src):
+    import numpy as np
+    import torch
+
+    import head_segmented_paged_gb300 as S
+    from head_segmented_paged_gb300 import inputs as I
+
+    w = I.ragged_decode(seed=0, steps=128)
+    B, P, D = len(w.seq_lens), w.page_size, w.head_dim
+    steps = w.decode_steps
+    max_len = max(w.seq_lens) + steps + 1
+    num_pages = sum((n + steps) // P + 2 for n in w.seq_lens) * w.hkv + 64
+    kp = torch.empty((num_pages, P, D), dtype=torch.bfloat16, device=dev)
+    vp = torch.empty_like(kp)
+    h = S.SegKV(1, w.hq, w.hkv, D, w.head_class, w.window, P, B, max_len, kp, vp)
+    q, k, v, cu, qp = I.prefill_tensors(w, 0, device=dev)
+    ids = list(range(B))
+    h.append(0, k, v, cu, ids, stream)
+    h.trim(0, ids)
+    del q
+    qd = [I.decode_step_tensors(w, s, device=dev) for s in range(steps)]
+    ws = torch.empty(h.workspace_size(S.SEGKV_WS_DECODE, B, B) // 4 + 64, dtype=torch.float32,
+                     device=dev)
+    o = torch.empty((B, w.hq, D), dtype=torch.bfloat16, device=dev)
+    lens = list(w.seq_lens)
+    one = np.arange(B + 1, dtype=np.int32)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    bytes_step = []
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for s in range(steps):
+        qq, kk, vv = qd[s]
+        ev[s][0].record(stream)
+        h.append(0, kk, vv, one, ids, stream)
+        lens = [x + 1 for x in lens]
+        ev[s][1].record(stream)
+        h.decode_attn(0, qq, lens, ids, o, ws, stream)
+        ev[s][2].record(stream)
+        bytes_step.append(decode_bytes(w, lens))
+    torch.cuda.synchronize()
+    if h.status() != 0:
+        raise RuntimeError("device status after decode: " + S.segkv_last_error(h.handle))
+    warm = 8
+    dec_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(warm, steps)]
+    app_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(warm, steps)]
+    step_ms = [ev[s][0].elapsed_time(ev[s][2]) for s in range(warm, steps)]
+    gbs = [bytes_step[s] / (dec_ms[s - warm] * 1e-3) / 1e9 for s in range(warm, steps)]
+    med = statistics.median(gbs)
+    return {"workload": "ragged decode, 32 requests, 2K-32K log-uniform, 128 steps",
+            "gbs_median": round(med, 1), "hbm_peak_gbs": hbm, "frac": round(med / hbm, 4),
+            "peak_kind": peak_src,
+            "decode_us_median": round(1e3 * statistics.median(dec_ms), 2),
+            "append_us_median": round(1e3 * statistics.median(app_ms), 2),
+            "step_us_median": round(1e3 * statistics.median(step_ms), 2),
+            "tokens_per_s": round(B / (statistics.median(step_ms) * 1e-3), 1),
+            "bytes_per_step_mean": int(statistics.mean(bytes_step)),
+            "steps_timed": steps - warm, "kernels": ["decode_split_kernel<128,4>",
+                                                     "decode_combine_kernel<128,4>"]}
+
+
+def run_e2e(args, dev, stream, w, sets, cu, q_pos, step_flops, num_pages):
+    """The same step through the public API from pinned host buffers: every
+    layer's Q, K, V copied host->device inside the timed region (a side stream
+    overlaps the next layer's copy with this layer's kernels), and the last
+    layer's output copied back."""
+    import torch
+
+    import head_segmented_paged_gb300 as S
+
+    n, L, hq, hkv, D, P = w.seq_lens[0], w.num_layers, w.hq, w.hkv, w.head_dim, w.page_size
+    host = [tuple(t.to("cpu").pin_memory() for t in s) for s in sets]
+    dbuf = [tuple(torch.empty_like(t) for t in sets[0]) for _ in range(2)]
+    o = torch.empty((n, hq, D), dtype=torch.bfloat16, device=dev)
+    o_host = torch.empty((n, hq, D), dtype=torch.bfloat16).pin_memory()
+    kp = torch.empty((num_pages, P, D), dtype=torch.bfloat16, device=dev)
+    vp = torch.empty_like(kp)
+    h = S.SegKV(L, hq, hkv, D, w.head_class, w.window, P, 1, n, kp, vp)
+    copy_stream = torch.cuda.Stream(device=dev)
+    done = [torch.cuda.Event() for _ in range(2)]
+    free = [torch.cuda.Event() for _ in range(2)]
+    h2d = 0
+
+    def step():
+        nonlocal h2d
+        h.free_seq(0)
+        h2d = 0
+        for l in range(L + 1):
+            if l < L:  # issue the copy for layer l
+                b = l % 2
+                copy_stream.wait_event(free[b])
+                with torch.cuda.stream(copy_stream):
+                    for dst, src in zip(dbuf[b], host[l % N_INPUT_SETS]):
+                        dst.copy_(src, non_blocking=True)
+                        h2d += src.numel() * src.element_size()
+                done[b].record(copy_stream)
+            if l >= 1:  # compute layer l-1
+                lb = (l - 1) % 2
+                stream.wait_event(done[lb])
+                qd, kd, vd = dbuf[lb]
+                h.append(l - 1, kd, vd, cu, [0], stream)
+                h.prefill_attn(l - 1, qd, cu, q_pos, [0], o, None, stream)
+                h.trim(l - 1, [0])
+                free[lb].record(stream)
+        o_host.copy_(o, non_blocking=True)
+
+    for b in range(2):
+        free[b].record(stream)
+    step()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    ks = max(1, min(args.steps, 2))
+    t0.record(stream)
+    for _ in range(ks):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / ks
+    return {"value": round(step_flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
+            "ms_per_step": round(ms, 2), "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": o.numel() * o.element_size(),
+            "note": "pinned host Q/K/V per layer copied in the timed region on a side stream; "
+                    "last layer's O copied back"}
+
+
+# ------------------------------------------------------------------ oracle (CPU) arm
+def oracle_rate(sets, w, budget_s):
+    """Time the oracle on sampled query rows of three layer kinds of the
+    128K workload (shallow all-local, deep with no global head, deep with
+    one); return useful FLOPs/s over the sample."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    n = w.seq_lens[0]
+    q, k, v = (t.to("cpu") for t in sets[0]) if not isinstance(sets[0][0], torch.Tensor) or \
+        sets[0][0].device.type != "cpu" else sets[0]
+    kinds = {}
+    for l in range(w.num_layers):
+        g = sum(1 for c in w.head_class[l] if c == 0)
+        kind = "shallow" if l < 8 else ("deep_g1" if g else "deep_g0")
+        kinds.setdefault(kind, l)
+    rng = np.random.default_rng(0)
+    total_flops, total_s = 0, 0.0
+    per = {}
+    rows_per_kind = 2
+    for kind, l in kinds.items():
+        t_kind, f_kind = 0.0, 0
+        while t_kind < budget_s / len(kinds):
+            rows = rng.integers(0, n, rows_per_kind).astype(np.int64)
+            t0 = time.perf_counter()
+            rc, _, _ = oracle.attention(q, k, v, np.zeros(n, np.int32), np.arange(n, dtype=np.int32),
+                                        [0], [n], w.head_class[l], w.window[l],
+                                        np.zeros((1, w.hkv), np.int32), rows=rows)
+            dt = time.perf_counter() - t0
+            assert rc == 0
+            f = 0
+            for p in rows:
+                for hh in range(w.hkv):
+                    vis = p + 1 if w.head_class[l][hh] == 0 else min(p + 1, w.window[l])
+                    f += 4 * w.head_dim * w.group * int(vis)
+            t_kind += dt
+            f_kind += f
+            if dt < 1.0:
+                rows_per_kind *= 2
+        per[kind] = {"layer": l, "seconds": round(t_kind, 2), "useful_flops": f_kind}
+        total_flops += f_kind
+        total_s += t_kind
+    return total_flops / total_s, per, total_s
+
+
+def cpu_baseline(sets, w, budget_s=20.0):
+    import oracle
+    oracle.build()
+    cores = os.cpu_count()
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        pass
+    rate, per, secs = oracle_rate(sets, w, budget_s)
+    return {"value": rate / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": ("fp64 C++ oracle (OpenMP) on random query rows (all 64 query heads) of one "
+                       "shallow, one deep g=0 and one deep g=1 layer of the 128K workload, "
+                       f"{secs:.1f} s total; useful FLOPs / CPU time"),
+            "per_kind": per}
+
+
+def run_reference(args, rank, world):
+    """The oracle, as it stands, on the host cores, on bounded samples of the
+    same 128K workload; each step is one sample."""
+    import torch
+
+    from head_segmented_paged_gb300 import inputs as I
+    import oracle
+
+    oracle.build()
+    w = I.long_128k_64layer(seed=0)
+    n = w.seq_lens[0]
+    q = I.normal_bf16(w.seed, I.tensor_stream(I._Q, 0), (n, w.hq, w.head_dim))
+    k = I.normal_bf16(w.seed, I.tensor_stream(I._K, 0), (n, w.hkv, w.head_dim))
+    v = I.normal_bf16(w.seed, I.tensor_stream(I._V, 0), (n, w.hkv, w.head_dim))
+    sets = [(q, k, v)]
+    per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_rate(sets, w, per_step / 3)
+    rates, secs = [], 0.0
+    for _ in range(args.steps):
+        r, _, s = oracle_rate(sets, w, per_step)
+        rates.append(r)
+        secs += s
+    value = statistics.median(rates) / 1e12
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    ms_step = 1e3 * secs / max(1, args.steps)
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 1), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic: seeded splitmix64 + Box-Muller N(0,1), rounded to bf16",
+            "config": {"workload": "128k-64layer prefill", "layers": w.num_layers, "hq": w.hq,
+                       "hkv": w.hkv, "head_dim": w.head_dim, "page_size": w.page_size,
+                       "context": n},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "per step: random query rows of one shallow, one deep "
+                                       "g=0 and one deep g=1 layer, about "
+                                       f"{per_step:.0f} s of CPU work"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    import torch
+    if world > 1:
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    import __graft_entry__
+    __graft_entry__.build()
+    out = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

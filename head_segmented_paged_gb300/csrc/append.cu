@@ -1,0 +1,49 @@
+// Append / scatter: write each new token's K and V rows into the page that
+// holds its position in every head's segment (RedKnot summary page, section
+// "SegPagedAttention": the store is paged per (layer, head), and each head
+// keeps only the tokens it needs; section "SegPaged Attention(段页注意力）":
+// storage per head). Page ids were chosen on the host; this kernel also
+// writes the new ids into the device block table.
+//
+// HBM bound: every 16-byte vector of K and V is read once and written once.
+#include "segkv_internal.h"
+
+namespace skv {
+
+__global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
+  // block-table entries for the pages this call uses
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < p.n_entries;
+       e += gridDim.x * blockDim.x)
+    p.table[p.table_idx[e]] = p.page_list[e];
+
+  const int row_vecs = p.hkv * p.vec_per_row;  // 16-byte vectors per token
+  for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
+    const AppendTile tile = p.tiles[t];
+    const AppendSeq sq = p.seqs[tile.seq];
+    const int total = tile.ntok * row_vecs;
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+      const int tl = i / row_vecs;
+      const int rem = i - tl * row_vecs;
+      const int h = rem / p.vec_per_row;
+      const int c = rem - h * p.vec_per_row;
+      const int tok = tile.tok0 + tl;
+      const int pos = sq.pos0 + (tok - sq.tok0);
+      const int k = pos / p.page_size;
+      const int id = p.page_list[sq.list_off + h * sq.n_pages + (k - sq.first_k)];
+      const int64_t src = (static_cast<int64_t>(tok) * p.hkv + h) * p.vec_per_row + c;
+      const int64_t dst =
+          (static_cast<int64_t>(id) * p.page_size + (pos - k * p.page_size)) * p.vec_per_row + c;
+      const uint4 kv = __ldg(p.k + src);
+      const uint4 vv = __ldg(p.v + src);
+      p.kpool[dst] = kv;
+      p.vpool[dst] = vv;
+    }
+  }
+}
+
+cudaError_t launch_append(const AppendParams& p, int grid, cudaStream_t s) {
+  append_kernel<<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace skv

@@ -1,0 +1,822 @@
+// Host side of segkv: segment allocator and page-table builder, work
+// planners for the kernels, the upload ring, and the C ABI (include/segkv.h).
+//
+// The page model follows the RedKnot summary page ("让 KV Cache「按头分家」"):
+// section "头分类稀疏" (global heads keep the causal context, local heads a
+// sliding window) and section "SegPagedAttention" (KV paged per (layer, head)
+// segment, each head keeps only what it needs). Readings where the page is
+// silent: window W includes the query; eviction is lazy and frees whole pages
+// k with (k+1)P <= kept start; one pool, lowest free id first, K and V share
+// an id; evictions before allocations, in (seq_ids order, head, page) order.
+// All planning is host-only and never waits on the device.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <deque>
+#include <functional>
+#include <memory>
+#include <new>
+#include <queue>
+#include <string>
+#include <vector>
+
+#include "../../include/segkv.h"
+#include "segkv_internal.h"
+
+using namespace skv;
+
+namespace {
+
+constexpr unsigned long long kTimeoutNs = 2000ull * 1000 * 1000;  // 2 s per wait
+constexpr size_t kRingInitial = size_t(8) << 20;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  }
+  return fn;
+}
+
+// Pinned host staging buffer mirrored by a device buffer of the same size.
+// Each call takes the next region, fills it on the host, copies it with one
+// cudaMemcpyAsync and records an event after its kernels; a region is reused
+// only once its event has completed.
+struct UploadRing {
+  uint8_t* host = nullptr;
+  uint8_t* dev = nullptr;
+  size_t cap = 0, head = 0;
+  struct Chunk {
+    size_t off, len;
+    cudaEvent_t ev;
+  };
+  std::deque<Chunk> live;
+  std::vector<cudaEvent_t> spare;
+
+  cudaError_t init(size_t bytes) {
+    cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&host), bytes, cudaHostAllocDefault);
+    if (e != cudaSuccess) return e;
+    e = cudaMalloc(reinterpret_cast<void**>(&dev), bytes);
+    if (e != cudaSuccess) return e;
+    cap = bytes;
+    head = 0;
+    return cudaSuccess;
+  }
+  void release() {
+    for (auto& c : live) {
+      cudaEventSynchronize(c.ev);
+      cudaEventDestroy(c.ev);
+    }
+    live.clear();
+    for (auto ev : spare) cudaEventDestroy(ev);
+    spare.clear();
+    if (host) cudaFreeHost(host);
+    if (dev) cudaFree(dev);
+    host = dev = nullptr;
+    cap = head = 0;
+  }
+  void retire_front() {
+    cudaEventSynchronize(live.front().ev);
+    spare.push_back(live.front().ev);
+    live.pop_front();
+  }
+  // Reserve len bytes; returns the offset or an error.
+  cudaError_t reserve(size_t len, size_t* off) {
+    len = align_up(std::max<size_t>(len, 256), 256);
+    if (len > cap) {
+      size_t ncap = std::max(len, cap * 2);
+      while (!live.empty()) retire_front();
+      cudaError_t e = cudaDeviceSynchronize();
+      if (e != cudaSuccess) return e;
+      for (auto ev : spare) cudaEventDestroy(ev);
+      spare.clear();
+      cudaFreeHost(host);
+      cudaFree(dev);
+      host = dev = nullptr;
+      e = init(ncap);
+      if (e != cudaSuccess) return e;
+    }
+    if (head + len > cap) head = 0;
+    // the oldest live region is the next one in ring order
+    while (!live.empty()) {
+      const Chunk& c = live.front();
+      const bool overlap = c.off < head + len && head < c.off + c.len;
+      if (!overlap) break;
+      retire_front();
+    }
+    *off = head;
+    head += len;
+    return cudaSuccess;
+  }
+  cudaError_t commit(size_t off, size_t len, cudaStream_t s) {
+    cudaEvent_t ev;
+    if (!spare.empty()) {
+      ev = spare.back();
+      spare.pop_back();
+    } else {
+      cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+      if (e != cudaSuccess) return e;
+    }
+    cudaError_t e = cudaEventRecord(ev, s);
+    if (e != cudaSuccess) {
+      spare.push_back(ev);
+      return e;
+    }
+    live.push_back({off, align_up(std::max<size_t>(len, 256), 256), ev});
+    return cudaSuccess;
+  }
+};
+
+// Bump allocator over one staging region.
+struct Pack {
+  std::vector<uint8_t> buf;
+  template <class T>
+  size_t add(const T* data, size_t count) {
+    size_t off = align_up(buf.size(), 16);
+    buf.resize(off + sizeof(T) * count);
+    if (count) std::memcpy(buf.data() + off, data, sizeof(T) * count);
+    return off;
+  }
+};
+
+}  // namespace
+
+struct segkv {
+  int L = 0, Hq = 0, Hkv = 0, D = 0, G = 0, P = 0, S = 0, max_len = 0, R = 0;
+  int64_t num_pages = 0;
+  float scale = 0.f;
+  bool host_only = true;
+  std::vector<uint8_t> cls;   // [L][Hkv]
+  std::vector<int32_t> win;   // [L]
+  void* kpool = nullptr;
+  void* vpool = nullptr;
+
+  // host page tables
+  std::vector<int32_t> len;    // [L][S]
+  std::vector<int32_t> start;  // [L][Hkv][S]
+  std::vector<int32_t> table;  // [L][Hkv][S][R], -1 = not held
+  std::priority_queue<int32_t, std::vector<int32_t>, std::greater<int32_t>> free_ids;
+
+  // device
+  int device = 0, num_sms = 0;
+  int32_t* d_table = nullptr;
+  int* d_status = nullptr;
+  CUtensorMap tm_k{}, tm_v{};
+  UploadRing ring;
+  int debug = 0;
+  int64_t upload_bytes = 0;
+  std::string err;
+
+  size_t seg(int l, int h, int b) const { return (static_cast<size_t>(l) * Hkv + h) * S + b; }
+  size_t lidx(int l, int b) const { return static_cast<size_t>(l) * S + b; }
+  bool local(int l, int h) const { return cls[l * Hkv + h] != SEGKV_GLOBAL; }
+  int32_t* row(int l, int h, int b) { return table.data() + seg(l, h, b) * R; }
+};
+
+namespace {
+
+std::string g_create_error;
+
+int fail(segkv* h, int code, const char* fmt, ...) {
+  char msg[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(msg, sizeof msg, fmt, ap);
+  va_end(ap);
+  if (h) h->err = msg; else g_create_error = msg;
+  return code;
+}
+
+int cuda_fail(segkv* h, cudaError_t e, const char* what) {
+  return fail(h, SEGKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool ids_valid(const segkv* h, const int32_t* ids, int n) {
+  if (n < 0 || (n > 0 && ids == nullptr)) return false;
+  std::vector<uint8_t> seen(h->S, 0);
+  for (int i = 0; i < n; ++i) {
+    if (ids[i] < 0 || ids[i] >= h->S || seen[ids[i]]) return false;
+    seen[ids[i]] = 1;
+  }
+  return true;
+}
+
+// First position a head must keep for queries starting at q0.
+int32_t needed_start(const segkv* h, int l, int hd, int32_t cur, int64_t q0) {
+  if (!h->local(l, hd)) return cur;
+  int64_t need = q0 - h->win[l] + 1;
+  if (need < 0) need = 0;
+  return need > cur ? static_cast<int32_t>(need) : cur;
+}
+
+// Free every held page k with (k+1) P <= new_s.
+void evict_below(segkv* h, int l, int hd, int b, int32_t new_s) {
+  int32_t* r = h->row(l, hd, b);
+  const int32_t old_s = h->start[h->seg(l, hd, b)];
+  const int32_t n = h->len[h->lidx(l, b)];
+  if (n > 0) {
+    const int k_first = old_s / h->P;
+    const int k_stop = new_s / h->P;  // pages below this are wholly before new_s
+    for (int k = k_first; k < k_stop && k < h->R; ++k)
+      if (r[k] >= 0) {
+        h->free_ids.push(r[k]);
+        r[k] = -1;
+      }
+  }
+  h->start[h->seg(l, hd, b)] = new_s;
+}
+
+int count_evictions(const segkv* h, int l, int hd, int b, int32_t new_s) {
+  const int32_t old_s = h->start[h->seg(l, hd, b)];
+  const int32_t n = h->len[h->lidx(l, b)];
+  if (n == 0) return 0;
+  const int32_t* r = h->table.data() + h->seg(l, hd, b) * h->R;
+  int c = 0;
+  for (int k = old_s / h->P; k < new_s / h->P && k < h->R; ++k) c += r[k] >= 0;
+  return c;
+}
+
+CUresult encode_2d(CUtensorMap* m, void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+}  // namespace
+
+extern "C" {
+
+int segkv_create(segkv_t* out, int num_layers, int num_q_heads, int num_kv_heads, int head_dim,
+                 const uint8_t* head_class, const int32_t* window, int page_size, int max_seqs,
+                 int max_seq_len, void* k_pool, void* v_pool, int64_t num_pages,
+                 float softmax_scale) {
+  if (!out) return fail(nullptr, SEGKV_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (num_layers <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads)
+    return fail(nullptr, SEGKV_ERR_INVALID_ARG, "bad head counts");
+  const int G = num_q_heads / num_kv_heads;
+  if (G > 16 || 128 % G) return fail(nullptr, SEGKV_ERR_INVALID_ARG, "G=%d must divide 16", G);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(nullptr, SEGKV_ERR_INVALID_ARG, "head_dim must be 64 or 128");
+  if (page_size < 8 || page_size % 8 || (page_size < 128 && 128 % page_size) ||
+      (page_size > 128 && page_size % 128))
+    return fail(nullptr, SEGKV_ERR_INVALID_ARG, "bad page_size %d", page_size);
+  if (max_seqs <= 0 || max_seq_len <= 0 || num_pages <= 0 || !head_class || !window)
+    return fail(nullptr, SEGKV_ERR_INVALID_ARG, "bad sizes");
+  if (num_pages * page_size >= (int64_t(1) << 31) - 256 || num_pages >= (int64_t(1) << 31))
+    return fail(nullptr, SEGKV_ERR_INVALID_ARG, "pool too large for 32-bit rows");
+  if ((k_pool == nullptr) != (v_pool == nullptr))
+    return fail(nullptr, SEGKV_ERR_INVALID_ARG, "k_pool and v_pool must both be set or NULL");
+  for (int l = 0; l < num_layers; ++l) {
+    if (window[l] < 1) return fail(nullptr, SEGKV_ERR_INVALID_ARG, "window[%d] < 1", l);
+    for (int x = 0; x < num_kv_heads; ++x)
+      if (head_class[l * num_kv_heads + x] > 1)
+        return fail(nullptr, SEGKV_ERR_INVALID_ARG, "bad head_class");
+  }
+  const int64_t R = (static_cast<int64_t>(max_seq_len) + page_size - 1) / page_size;
+  const int64_t entries = int64_t(num_layers) * num_kv_heads * max_seqs * R;
+  if (entries > (int64_t(1) << 33)) return fail(nullptr, SEGKV_ERR_INVALID_ARG, "table too large");
+
+  std::unique_ptr<segkv> h(new (std::nothrow) segkv());
+  if (!h) return fail(nullptr, SEGKV_ERR_INVALID_ARG, "out of host memory");
+  h->L = num_layers; h->Hq = num_q_heads; h->Hkv = num_kv_heads; h->D = head_dim; h->G = G;
+  h->P = page_size; h->S = max_seqs; h->max_len = max_seq_len; h->R = static_cast<int>(R);
+  h->num_pages = num_pages;
+  h->scale = softmax_scale > 0.f ? softmax_scale : 1.f / std::sqrt(static_cast<float>(head_dim));
+  h->cls.assign(head_class, head_class + num_layers * num_kv_heads);
+  h->win.assign(window, window + num_layers);
+  h->len.assign(static_cast<size_t>(num_layers) * max_seqs, 0);
+  h->start.assign(static_cast<size_t>(num_layers) * num_kv_heads * max_seqs, 0);
+  h->table.assign(static_cast<size_t>(entries), -1);
+  {
+    std::vector<int32_t> ids(static_cast<size_t>(num_pages));
+    for (int64_t i = 0; i < num_pages; ++i) ids[i] = static_cast<int32_t>(i);
+    h->free_ids = decltype(h->free_ids)(std::greater<int32_t>(), std::move(ids));
+  }
+  h->host_only = (k_pool == nullptr);
+  h->kpool = k_pool;
+  h->vpool = v_pool;
+  if (!h->host_only) {
+    if ((reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool)) & 15)
+      return fail(nullptr, SEGKV_ERR_INVALID_ARG, "pools must be 16-byte aligned");
+    if (!encode_fn()) return fail(nullptr, SEGKV_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cudaError_t e = cudaGetDevice(&h->device);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaGetDevice");
+    e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaDeviceGetAttribute");
+    e = cudaMalloc(reinterpret_cast<void**>(&h->d_table), sizeof(int32_t) * entries);
+    if (e != cudaSuccess) return cuda_fail(nullptr, e, "cudaMalloc(table)");
+    e = cudaMemset(h->d_table, 0xff, sizeof(int32_t) * entries);
+    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&h->d_status), sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int));
+    if (e == cudaSuccess) e = h->ring.init(kRingInitial);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+      h->ring.release();
+      cudaFree(h->d_table);
+      cudaFree(h->d_status);
+      return cuda_fail(nullptr, e, "device setup");
+    }
+    const uint64_t rows = static_cast<uint64_t>(num_pages) * page_size;
+    const uint32_t box_rows = page_size <= 128 ? page_size : 128;
+    if (encode_2d(&h->tm_k, k_pool, head_dim, rows, box_rows) != CUDA_SUCCESS ||
+        encode_2d(&h->tm_v, v_pool, head_dim, rows, box_rows) != CUDA_SUCCESS) {
+      h->ring.release();
+      cudaFree(h->d_table);
+      cudaFree(h->d_status);
+      return fail(nullptr, SEGKV_ERR_CUDA, "tensor map encode failed for the pools");
+    }
+  }
+  *out = h.release();
+  return SEGKV_OK;
+}
+
+int segkv_destroy(segkv_t h) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (!h->host_only) {
+    cudaDeviceSynchronize();
+    h->ring.release();
+    cudaFree(h->d_table);
+    cudaFree(h->d_status);
+  }
+  delete h;
+  return SEGKV_OK;
+}
+
+const char* segkv_last_error(segkv_t h) {
+  return h ? h->err.c_str() : g_create_error.c_str();
+}
+
+int segkv_set_debug(segkv_t h, int flags) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  h->debug = flags;
+  return SEGKV_OK;
+}
+
+// ---------------------------------------------------------------- append
+int segkv_append(segkv_t h, int layer, const void* k, const void* v, const int32_t* cu_seqlens,
+                 const int32_t* seq_ids, int n, segkv_stream_t stream) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= h->L) return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer %d", layer);
+  if (!ids_valid(h, seq_ids, n)) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq_ids");
+  if (n == 0) return SEGKV_OK;
+  if (!cu_seqlens || cu_seqlens[0] != 0) return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens[0] != 0");
+  for (int i = 0; i < n; ++i) {
+    const int64_t T = int64_t(cu_seqlens[i + 1]) - cu_seqlens[i];
+    if (T < 0) return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens decreases at %d", i);
+    if (h->len[h->lidx(layer, seq_ids[i])] + T > h->max_len)
+      return fail(h, SEGKV_ERR_INVALID_ARG, "seq %d would exceed max_seq_len", seq_ids[i]);
+  }
+  const int64_t total = cu_seqlens[n];
+  if (total > 0 && !h->host_only && (!k || !v))
+    return fail(h, SEGKV_ERR_INVALID_ARG, "k/v are NULL");
+
+  // plan: evictions (all), then allocations, in (seq_ids order, head, page) order
+  std::vector<int32_t> new_s(static_cast<size_t>(n) * h->Hkv);
+  int64_t freed = 0, need = 0;
+  for (int i = 0; i < n; ++i) {
+    const int b = seq_ids[i];
+    const int32_t a = h->len[h->lidx(layer, b)];
+    const int32_t T = cu_seqlens[i + 1] - cu_seqlens[i];
+    for (int hd = 0; hd < h->Hkv; ++hd) {
+      const int32_t s0 = h->start[h->seg(layer, hd, b)];
+      const int32_t ns = needed_start(h, layer, hd, s0, a);
+      new_s[i * h->Hkv + hd] = ns;
+      freed += count_evictions(h, layer, hd, b, ns);
+      if (T > 0) {
+        const int32_t* r = h->table.data() + h->seg(layer, hd, b) * h->R;
+        for (int kk = a / h->P; kk <= (a + T - 1) / h->P; ++kk) need += r[kk] < 0;
+      }
+    }
+  }
+  if (static_cast<int64_t>(h->free_ids.size()) + freed < need)
+    return fail(h, SEGKV_ERR_OUT_OF_PAGES, "append needs %lld pages, %lld free after eviction",
+                static_cast<long long>(need),
+                static_cast<long long>(h->free_ids.size() + freed));
+
+  for (int i = 0; i < n; ++i)
+    for (int hd = 0; hd < h->Hkv; ++hd)
+      evict_below(h, layer, hd, seq_ids[i], new_s[i * h->Hkv + hd]);
+
+  std::vector<AppendSeq> seqs;
+  std::vector<AppendTile> tiles;
+  std::vector<int32_t> plist;
+  std::vector<int64_t> tidx;
+  for (int i = 0; i < n; ++i) {
+    const int b = seq_ids[i];
+    const int32_t a = h->len[h->lidx(layer, b)];
+    const int32_t T = cu_seqlens[i + 1] - cu_seqlens[i];
+    if (T == 0) continue;
+    AppendSeq sq{};
+    sq.tok0 = cu_seqlens[i];
+    sq.pos0 = a;
+    sq.first_k = a / h->P;
+    sq.n_pages = (a + T - 1) / h->P - sq.first_k + 1;
+    sq.list_off = static_cast<int32_t>(plist.size());
+    for (int hd = 0; hd < h->Hkv; ++hd) {
+      int32_t* r = h->row(layer, hd, b);
+      for (int kk = sq.first_k; kk < sq.first_k + sq.n_pages; ++kk) {
+        if (r[kk] < 0) {
+          r[kk] = h->free_ids.top();
+          h->free_ids.pop();
+        }
+        plist.push_back(r[kk]);
+        tidx.push_back(static_cast<int64_t>(h->seg(layer, hd, b)) * h->R + kk);
+      }
+    }
+    const int seq_index = static_cast<int>(seqs.size());
+    seqs.push_back(sq);
+    constexpr int kTileTok = 16;
+    for (int t0 = 0; t0 < T; t0 += kTileTok)
+      tiles.push_back({seq_index, sq.tok0 + t0, std::min(kTileTok, T - t0), 0});
+  }
+  for (int i = 0; i < n; ++i)
+    h->len[h->lidx(layer, seq_ids[i])] += cu_seqlens[i + 1] - cu_seqlens[i];
+
+  if (h->host_only || tiles.empty()) return SEGKV_OK;
+
+  Pack pk;
+  const size_t o_seq = pk.add(seqs.data(), seqs.size());
+  const size_t o_tile = pk.add(tiles.data(), tiles.size());
+  const size_t o_pl = pk.add(plist.data(), plist.size());
+  const size_t o_ti = pk.add(tidx.data(), tidx.size());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  size_t off;
+  cudaError_t e = h->ring.reserve(pk.buf.size(), &off);
+  if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
+  std::memcpy(h->ring.host + off, pk.buf.data(), pk.buf.size());
+  e = cudaMemcpyAsync(h->ring.dev + off, h->ring.host + off, pk.buf.size(), cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpyAsync(append plan)");
+  h->upload_bytes += static_cast<int64_t>(pk.buf.size());
+  uint8_t* d = h->ring.dev + off;
+  AppendParams p{};
+  p.k = static_cast<const uint4*>(k);
+  p.v = static_cast<const uint4*>(v);
+  p.kpool = static_cast<uint4*>(h->kpool);
+  p.vpool = static_cast<uint4*>(h->vpool);
+  p.seqs = reinterpret_cast<const AppendSeq*>(d + o_seq);
+  p.tiles = reinterpret_cast<const AppendTile*>(d + o_tile);
+  p.page_list = reinterpret_cast<const int32_t*>(d + o_pl);
+  p.table_idx = reinterpret_cast<const int64_t*>(d + o_ti);
+  p.table = h->d_table;
+  p.n_tiles = static_cast<int>(tiles.size());
+  p.n_entries = static_cast<int>(plist.size());
+  p.hkv = h->Hkv;
+  p.vec_per_row = h->D / 8;
+  p.page_size = h->P;
+  const int grid = static_cast<int>(std::min<int64_t>(tiles.size(), int64_t(h->num_sms) * 8));
+  e = launch_append(p, std::max(grid, 1), s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "append kernel launch");
+  e = h->ring.commit(off, pk.buf.size(), s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "event record");
+  return SEGKV_OK;
+}
+
+// ---------------------------------------------------------------- prefill
+int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_seqlens,
+                       const int32_t* q_pos, const int32_t* seq_ids, int n, void* o, float* lse,
+                       void* workspace, size_t workspace_bytes, segkv_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (h->host_only) return fail(h, SEGKV_ERR_INVALID_ARG, "host-only handle has no pools");
+  if (layer < 0 || layer >= h->L) return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer %d", layer);
+  if (!ids_valid(h, seq_ids, n)) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq_ids");
+  if (n == 0) return SEGKV_OK;
+  if (!cu_seqlens || cu_seqlens[0] != 0) return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens[0] != 0");
+  for (int i = 0; i < n; ++i)
+    if (cu_seqlens[i + 1] < cu_seqlens[i])
+      return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens decreases at %d", i);
+  const int64_t total = cu_seqlens[n];
+  if (total == 0) return SEGKV_OK;
+  if (!q || !o || !q_pos) return fail(h, SEGKV_ERR_INVALID_ARG, "q/o/q_pos NULL");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(o)) & 15)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "q and o must be 16-byte aligned");
+  const int W = h->win[layer];
+  // validate positions and kept keys
+  for (int i = 0; i < n; ++i) {
+    const int b = seq_ids[i];
+    const int32_t nlen = h->len[h->lidx(layer, b)];
+    for (int32_t t = cu_seqlens[i]; t < cu_seqlens[i + 1]; ++t) {
+      const int32_t p = q_pos[t];
+      if (p < 0 || p >= nlen)
+        return fail(h, SEGKV_ERR_INVALID_ARG, "q_pos[%d]=%d outside [0,%d) of seq %d", t, p, nlen, b);
+      for (int hd = 0; hd < h->Hkv; ++hd) {
+        const int32_t need = h->local(layer, hd) ? std::max(0, p - W + 1) : 0;
+        if (need < h->start[h->seg(layer, hd, b)])
+          return fail(h, SEGKV_ERR_EVICTED, "seq %d head %d: key %d already evicted", b, hd, need);
+      }
+    }
+  }
+  // units: (KV head, tile of 128/G tokens), LPT order
+  const int tpt = kRowsPerTile / h->G;
+  std::vector<PrefillUnit> units;
+  for (int i = 0; i < n; ++i) {
+    const int b = seq_ids[i];
+    const int32_t nlen = h->len[h->lidx(layer, b)];
+    for (int32_t t0 = cu_seqlens[i]; t0 < cu_seqlens[i + 1]; t0 += tpt) {
+      const int32_t t1 = std::min<int32_t>(t0 + tpt, cu_seqlens[i + 1]);
+      int32_t pmin = q_pos[t0], pmax = q_pos[t0];
+      for (int32_t t = t0; t < t1; ++t) {
+        pmin = std::min(pmin, q_pos[t]);
+        pmax = std::max(pmax, q_pos[t]);
+      }
+      for (int hd = 0; hd < h->Hkv; ++hd) {
+        PrefillUnit u{};
+        u.tok0 = t0;
+        u.ntok = t1 - t0;
+        u.head = hd;
+        u.local = h->local(layer, hd) ? 1 : 0;
+        u.klo = u.local ? std::max(0, pmin - W + 1) : 0;
+        u.khi = pmax;
+        u.kt0 = u.klo / kKeyTile;
+        u.kt1 = u.khi / kKeyTile;
+        const int32_t s0 = h->start[h->seg(layer, hd, b)];
+        u.first_page = s0 / h->P;
+        u.last_page = (nlen - 1) / h->P;
+        u.table_row = static_cast<int32_t>(h->seg(layer, hd, b));
+        units.push_back(u);
+      }
+    }
+  }
+  std::stable_sort(units.begin(), units.end(), [](const PrefillUnit& a, const PrefillUnit& b) {
+    return (a.kt1 - a.kt0) > (b.kt1 - b.kt0);
+  });
+
+  Pack pk;
+  const size_t o_units = pk.add(units.data(), units.size());
+  const size_t o_pos = pk.add(q_pos, static_cast<size_t>(total));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  size_t off;
+  cudaError_t e = h->ring.reserve(pk.buf.size(), &off);
+  if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
+  std::memcpy(h->ring.host + off, pk.buf.data(), pk.buf.size());
+  e = cudaMemcpyAsync(h->ring.dev + off, h->ring.host + off, pk.buf.size(), cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpyAsync(prefill plan)");
+  h->upload_bytes += static_cast<int64_t>(pk.buf.size());
+
+  CUtensorMap tq;
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(h->D), static_cast<cuuint64_t>(h->Hq),
+                          static_cast<cuuint64_t>(total)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(h->D) * 2,
+                             static_cast<cuuint64_t>(h->Hq) * h->D * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(h->G), static_cast<cuuint32_t>(tpt)};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (encode_fn()(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return fail(h, SEGKV_ERR_CUDA, "tensor map encode failed for q");
+  }
+  uint8_t* d = h->ring.dev + off;
+  PrefillParams p{};
+  p.units = reinterpret_cast<const PrefillUnit*>(d + o_units);
+  p.q_pos = reinterpret_cast<const int32_t*>(d + o_pos);
+  p.table = h->d_table;
+  p.o = o;
+  p.lse = lse;
+  p.total_q = total;
+  p.n_units = static_cast<int>(units.size());
+  p.R = h->R;
+  p.hq = h->Hq;
+  p.G = h->G;
+  p.tpt = tpt;
+  p.window = W;
+  p.page_size = h->P;
+  p.oob_row = static_cast<int>(h->num_pages * h->P);
+  p.scale_log2 = h->scale * 1.4426950408889634f;
+  p.status = h->d_status;
+  p.debug = h->debug;
+  p.timeout_ns = kTimeoutNs;
+  h->debug = 0;
+  const int grid = static_cast<int>(std::min<int64_t>(units.size(), h->num_sms));
+  e = launch_prefill(p, tq, h->tm_k, h->tm_v, h->D, grid, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "prefill kernel launch");
+  e = h->ring.commit(off, pk.buf.size(), s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "event record");
+  return SEGKV_OK;
+}
+
+// ---------------------------------------------------------------- decode
+static int64_t decode_units_bound(const segkv* h, int n_seqs) {
+  return int64_t(n_seqs) * h->Hkv * ((h->max_len + kDecodeChunk - 1) / kDecodeChunk + 1);
+}
+
+int segkv_workspace_size(segkv_t h, int kind, int64_t n_tokens, int n_seqs, size_t* bytes) {
+  (void)n_tokens;
+  if (!h || !bytes || n_seqs < 0) return SEGKV_ERR_INVALID_ARG;
+  if (kind == SEGKV_WS_PREFILL) {
+    *bytes = 0;
+    return SEGKV_OK;
+  }
+  if (kind != SEGKV_WS_DECODE) return fail(h, SEGKV_ERR_INVALID_ARG, "bad workspace kind");
+  const int64_t u = decode_units_bound(h, n_seqs);
+  *bytes = align_up(static_cast<size_t>(u) * h->G * h->D * 4, 256) +
+           align_up(static_cast<size_t>(u) * h->G * 2 * 4, 256);
+  return SEGKV_OK;
+}
+
+int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_lens,
+                      const int32_t* seq_ids, int n, void* o, void* workspace,
+                      size_t workspace_bytes, segkv_stream_t stream) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (h->host_only) return fail(h, SEGKV_ERR_INVALID_ARG, "host-only handle has no pools");
+  if (layer < 0 || layer >= h->L) return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer %d", layer);
+  if (!ids_valid(h, seq_ids, n)) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq_ids");
+  if (n == 0) return SEGKV_OK;
+  if (!q || !o || !seq_lens) return fail(h, SEGKV_ERR_INVALID_ARG, "q/o/seq_lens NULL");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(o)) & 15)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "q and o must be 16-byte aligned");
+  const int W = h->win[layer];
+  std::vector<DecodeUnit> units;
+  std::vector<DecodePair> pairs;
+  for (int i = 0; i < n; ++i) {
+    const int b = seq_ids[i];
+    const int32_t nlen = h->len[h->lidx(layer, b)];
+    if (seq_lens[i] != nlen || nlen < 1)
+      return fail(h, SEGKV_ERR_INVALID_ARG, "seq_lens[%d]=%d but seq %d has %d tokens", i,
+                  seq_lens[i], b, nlen);
+    const int32_t p = nlen - 1;
+    for (int hd = 0; hd < h->Hkv; ++hd) {
+      const int32_t lo = h->local(layer, hd) ? std::max(0, p - W + 1) : 0;
+      if (lo < h->start[h->seg(layer, hd, b)])
+        return fail(h, SEGKV_ERR_EVICTED, "seq %d head %d: key %d already evicted", b, hd, lo);
+      DecodePair pr{static_cast<int32_t>(units.size()), 0, i, hd};
+      for (int32_t c = lo / kDecodeChunk; c <= p / kDecodeChunk; ++c) {
+        DecodeUnit u{};
+        u.req = i;
+        u.head = hd;
+        u.k0 = std::max(lo, c * kDecodeChunk);
+        u.k1 = std::min(nlen, (c + 1) * kDecodeChunk);
+        u.table_row = static_cast<int32_t>(h->seg(layer, hd, b));
+        units.push_back(u);
+        ++pr.n_units;
+      }
+      pairs.push_back(pr);
+    }
+  }
+  const size_t acc_bytes = align_up(units.size() * h->G * h->D * 4, 256);
+  const size_t need = acc_bytes + align_up(units.size() * h->G * 2 * 4, 256);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
+    return fail(h, SEGKV_ERR_INVALID_ARG, "workspace needs %zu bytes (256-aligned), got %zu", need,
+                workspace_bytes);
+
+  Pack pk;
+  const size_t o_units = pk.add(units.data(), units.size());
+  const size_t o_pairs = pk.add(pairs.data(), pairs.size());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  size_t off;
+  cudaError_t e = h->ring.reserve(pk.buf.size(), &off);
+  if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
+  std::memcpy(h->ring.host + off, pk.buf.data(), pk.buf.size());
+  e = cudaMemcpyAsync(h->ring.dev + off, h->ring.host + off, pk.buf.size(), cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpyAsync(decode plan)");
+  h->upload_bytes += static_cast<int64_t>(pk.buf.size());
+  uint8_t* d = h->ring.dev + off;
+  DecodeParams p{};
+  p.units = reinterpret_cast<const DecodeUnit*>(d + o_units);
+  p.pairs = reinterpret_cast<const DecodePair*>(d + o_pairs);
+  p.q = q;
+  p.o = o;
+  p.table = h->d_table;
+  p.kpool = h->kpool;
+  p.vpool = h->vpool;
+  p.part_acc = static_cast<float*>(workspace);
+  p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + acc_bytes);
+  p.n_units = static_cast<int>(units.size());
+  p.n_pairs = static_cast<int>(pairs.size());
+  p.R = h->R;
+  p.hq = h->Hq;
+  p.G = h->G;
+  p.page_size = h->P;
+  p.scale_log2 = h->scale * 1.4426950408889634f;
+  p.status = h->d_status;
+  p.timeout_ns = kTimeoutNs;
+  const int grid = static_cast<int>(std::min<int64_t>(units.size(), int64_t(h->num_sms) * 2));
+  e = launch_decode(p, h->D, grid, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "decode kernel launch");
+  e = h->ring.commit(off, pk.buf.size(), s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "event record");
+  return SEGKV_OK;
+}
+
+// ---------------------------------------------------------------- trim / free
+int segkv_trim(segkv_t h, int layer, const int32_t* seq_ids, int n) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (layer < -1 || layer >= h->L) return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer %d", layer);
+  if (!ids_valid(h, seq_ids, n)) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq_ids");
+  const int l0 = layer < 0 ? 0 : layer, l1 = layer < 0 ? h->L : layer + 1;
+  for (int l = l0; l < l1; ++l)
+    for (int i = 0; i < n; ++i) {
+      const int b = seq_ids[i];
+      const int32_t nlen = h->len[h->lidx(l, b)];
+      for (int hd = 0; hd < h->Hkv; ++hd)
+        evict_below(h, l, hd, b, needed_start(h, l, hd, h->start[h->seg(l, hd, b)], nlen));
+    }
+  return SEGKV_OK;
+}
+
+int segkv_free_seq(segkv_t h, int seq_id) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (seq_id < 0 || seq_id >= h->S) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq %d", seq_id);
+  for (int l = 0; l < h->L; ++l) {
+    for (int hd = 0; hd < h->Hkv; ++hd) {
+      int32_t* r = h->row(l, hd, seq_id);
+      for (int k = 0; k < h->R; ++k)
+        if (r[k] >= 0) {
+          h->free_ids.push(r[k]);
+          r[k] = -1;
+        }
+      h->start[h->seg(l, hd, seq_id)] = 0;
+    }
+    h->len[h->lidx(l, seq_id)] = 0;
+  }
+  return SEGKV_OK;
+}
+
+// ---------------------------------------------------------------- queries
+int segkv_get_segment(segkv_t h, int layer, int head, int seq, int32_t* start, int32_t* len,
+                      int32_t* first_page, int32_t* ids, int max_ids, int32_t* n_ids) {
+  if (!h || !start || !len || !first_page || !n_ids) return SEGKV_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= h->L || head < 0 || head >= h->Hkv || seq < 0 || seq >= h->S)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "bad segment index");
+  const int32_t s0 = h->start[h->seg(layer, head, seq)];
+  const int32_t nlen = h->len[h->lidx(layer, seq)];
+  *start = s0;
+  *len = nlen - s0;
+  const int32_t* r = h->table.data() + h->seg(layer, head, seq) * h->R;
+  int c = 0, first = -1;
+  for (int k = 0; k < h->R; ++k)
+    if (r[k] >= 0) {
+      if (first < 0) first = k;
+      if (ids && c < max_ids) ids[c] = r[k];
+      ++c;
+    }
+  *first_page = first < 0 ? 0 : first;
+  *n_ids = c;
+  return c <= max_ids || !ids ? SEGKV_OK : fail(h, SEGKV_ERR_INVALID_ARG, "ids buffer too small");
+}
+
+int segkv_seq_len(segkv_t h, int layer, int seq, int32_t* len) {
+  if (!h || !len || layer < 0 || layer >= h->L || seq < 0 || seq >= h->S)
+    return SEGKV_ERR_INVALID_ARG;
+  *len = h->len[h->lidx(layer, seq)];
+  return SEGKV_OK;
+}
+
+int segkv_stats(segkv_t h, segkv_stats_t* out) {
+  if (!h || !out) return SEGKV_ERR_INVALID_ARG;
+  segkv_stats_t st{};
+  st.num_pages = h->num_pages;
+  for (int l = 0; l < h->L; ++l)
+    for (int hd = 0; hd < h->Hkv; ++hd)
+      for (int b = 0; b < h->S; ++b) {
+        const int32_t* r = h->table.data() + h->seg(l, hd, b) * h->R;
+        int64_t c = 0;
+        for (int k = 0; k < h->R; ++k) c += r[k] >= 0;
+        (h->local(l, hd) ? st.pages_local : st.pages_global) += c;
+        st.kept_tokens += h->len[h->lidx(l, b)] - h->start[h->seg(l, hd, b)];
+      }
+  st.pages_in_use = st.pages_local + st.pages_global;
+  st.upload_bytes = h->upload_bytes;
+  *out = st;
+  return SEGKV_OK;
+}
+
+int segkv_status(segkv_t h, segkv_stream_t stream) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (h->host_only) return SEGKV_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamSynchronize");
+  int v = 0;
+  e = cudaMemcpy(&v, h->d_status, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(h, e, "status read");
+  if (v != 0) {
+    e = cudaMemset(h->d_status, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(h, e, "status clear");
+    return fail(h, SEGKV_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired (code %d)", v);
+  }
+  return SEGKV_OK;
+}
+
+}  // extern "C"

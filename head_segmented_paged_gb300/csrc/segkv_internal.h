@@ -1,0 +1,115 @@
+// Work descriptors shared by the host planner and the kernels, and the
+// kernel launchers. Host code fills these structs into a pinned staging
+// buffer; one cudaMemcpyAsync per call moves them next to the kernel.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace skv {
+
+constexpr int kKeyTile = 128;     // prefill: keys per tile (one MMA N)
+constexpr int kRowsPerTile = 128; // prefill: query rows per tile (MMA M)
+constexpr int kDecodeChunk = 512; // decode: keys per split unit
+constexpr int kDecodeStageKeys = 64;
+
+// ---- append -------------------------------------------------------------
+struct AppendSeq {
+  int32_t tok0;      // first packed token of this sequence's chunk
+  int32_t pos0;      // its position (tracked length before the append)
+  int32_t first_k;   // logical page of pos0
+  int32_t n_pages;   // logical pages the chunk touches
+  int32_t list_off;  // offset of this sequence's [Hkv][n_pages] page ids
+  int32_t pad;
+};
+struct AppendTile {
+  int32_t seq;   // index into AppendSeq
+  int32_t tok0;  // first packed token of the tile
+  int32_t ntok;
+  int32_t pad;
+};
+struct AppendParams {
+  const uint4* k;
+  const uint4* v;
+  uint4* kpool;
+  uint4* vpool;
+  const AppendSeq* seqs;
+  const AppendTile* tiles;
+  const int32_t* page_list;   // page ids, per sequence [Hkv][n_pages]
+  const int64_t* table_idx;   // block-table slot of each page_list entry
+  int32_t* table;
+  int n_tiles;
+  int n_entries;
+  int hkv, vec_per_row, page_size;
+};
+
+// ---- prefill --------------------------------------------------------------
+struct PrefillUnit {
+  int32_t tok0;        // first packed query token of the tile
+  int32_t ntok;        // tokens in the tile (<= 128 / G)
+  int32_t head;        // KV head
+  int32_t local;       // 1 = local head
+  int32_t kt0, kt1;    // key tiles kt0 .. kt1 (inclusive), tile = 128 positions
+  int32_t klo, khi;    // union of the rows' visible keys
+  int32_t first_page;  // first held logical page of the segment
+  int32_t last_page;   // last held logical page
+  int32_t table_row;   // (layer * Hkv + head) * max_seqs + seq
+  int32_t pad;
+};
+struct PrefillParams {
+  const PrefillUnit* units;
+  const int32_t* q_pos;
+  const int32_t* table;
+  void* o;        // bf16 [total_q, Hq, D]
+  float* lse;     // fp32 [Hq, total_q] or null
+  int64_t total_q;
+  int n_units;
+  int R;          // block-table row length
+  int hq, G, tpt, window;
+  int page_size;
+  int oob_row;    // a K/V row coordinate past the end of the pools
+  float scale_log2;
+  int* status;
+  int debug;
+  unsigned long long timeout_ns;
+};
+
+// ---- decode ---------------------------------------------------------------
+struct DecodeUnit {
+  int32_t req;         // row of q / o
+  int32_t head;        // KV head
+  int32_t k0, k1;      // keys [k0, k1)
+  int32_t table_row;
+  int32_t pad[3];
+};
+struct DecodePair {
+  int32_t unit0;   // first unit of this (req, head)
+  int32_t n_units;
+  int32_t req;
+  int32_t head;
+};
+struct DecodeParams {
+  const DecodeUnit* units;
+  const DecodePair* pairs;
+  const void* q;          // bf16 [n, Hq, D]
+  void* o;                // bf16 [n, Hq, D]
+  const int32_t* table;
+  const void* kpool;
+  const void* vpool;
+  float* part_acc;        // [n_units, G, D]
+  float* part_ml;         // [n_units, G, 2]
+  int n_units, n_pairs;
+  int R, hq, G, page_size;
+  float scale_log2;
+  int* status;
+  unsigned long long timeout_ns;
+};
+
+cudaError_t launch_append(const AppendParams& p, int grid, cudaStream_t s);
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, int head_dim, int grid, cudaStream_t s);
+int prefill_smem_bytes(int head_dim);
+cudaError_t launch_decode(const DecodeParams& p, int head_dim, int grid, cudaStream_t s);
+
+}  // namespace skv

@@ -1,0 +1,212 @@
+/*
+ * segkv — head-segmented paged KV attention for one GB300 (sm_103a).
+ *
+ * The KV cache is paged per (layer, KV head) segment. Each head keeps only
+ * the keys it needs: a global head the whole causal context, a local head a
+ * sliding window. Attention runs over those segments with no mask ever
+ * materialised. Sources (RedKnot summary page, "让 KV Cache「按头分家」：小红书
+ * RedKnot 如何重做长文本推理新引擎"):
+ *   - section "头分类稀疏（Head-Class Sparsification）": offline global/local
+ *     classification of every (layer, head);
+ *   - section "SegPagedAttention（存储与执行底座）": paged KV store segmented per
+ *     (layer, head), one fused varlen attention kernel over it, each head keeps
+ *     only the tokens it needs, no attn_mask;
+ *   - section "SegPaged Attention(段页注意力）": storage per head, not per token;
+ * and the KV-cache architecture page ("KV Cache管理架构演进概述"), section 3.1
+ * (pages of a fixed token count mapped through a logical-to-physical table)
+ * and section 5.2 (block-wise softmax merged with a running maximum).
+ *
+ * Conventions shared by every call:
+ *   - Shapes. Lq query heads per KV head: G = num_q_heads / num_kv_heads;
+ *     query head hq reads KV head hq / G. D = head_dim (64 or 128).
+ *     P = page_size tokens per page.
+ *   - Readings where the pages are silent. Window W counts the query: a
+ *     local head at position p sees keys max(0, p-W+1) .. p. Eviction is lazy
+ *     and page-granular: an append of positions [a, a+T) lets a local head
+ *     drop keys below a-W+1 (what the new tokens' queries still need); a
+ *     trim drops them below n-W+1 (what the next token needs); a page k
+ *     (positions [kP, (k+1)P)) is freed once (k+1)P <= kept start. Page ids
+ *     come from one pool, lowest free id first; K and V of a page share its
+ *     id; within one call all evictions precede all allocations, both in the
+ *     order (seq_ids order, head ascending, logical page ascending).
+ *   - Memory. Pointers named "device" are device memory owned by the caller;
+ *     arrays named "host" are host memory read during the call only, so the
+ *     host never waits on the device to plan work. K/V pools are bf16
+ *     [num_pages, P, D] each, owned by the caller for the handle's lifetime.
+ *   - Streams. Every device-side effect is ordered on the stream passed in
+ *     (NULL = legacy default stream). Host-side state (lengths, page tables)
+ *     changes when the call returns, so calls must be made in stream order
+ *     and all calls on one handle must use one stream (or the caller orders
+ *     them). A handle is not thread-safe.
+ *   - Errors. Every call returns SEGKV_OK or a negative SEGKV_ERR_* code and
+ *     records a message (segkv_last_error). A failing call changes no state.
+ *     Device-side faults that the kernels catch themselves (a bounded wait
+ *     that timed out) are reported by segkv_status.
+ */
+#ifndef SEGKV_H_
+#define SEGKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct segkv* segkv_t;
+/* A cudaStream_t passed as an opaque pointer (NULL = legacy default stream). */
+typedef void* segkv_stream_t;
+
+enum { SEGKV_GLOBAL = 0, SEGKV_LOCAL = 1 };
+
+enum {
+  SEGKV_OK = 0,
+  SEGKV_ERR_INVALID_ARG = -1,   /* bad argument or shape; nothing changed */
+  SEGKV_ERR_OUT_OF_PAGES = -2,  /* the pool cannot hold the append; nothing changed */
+  SEGKV_ERR_EVICTED = -3,       /* a query needs a key its head no longer keeps */
+  SEGKV_ERR_CUDA = -4,          /* a CUDA runtime call failed */
+  SEGKV_ERR_DEVICE_TIMEOUT = -5 /* a kernel's bounded wait expired (segkv_status) */
+};
+
+enum { SEGKV_WS_PREFILL = 0, SEGKV_WS_DECODE = 1 };
+
+typedef struct segkv_stats {
+  int64_t num_pages;         /* pool size */
+  int64_t pages_in_use;      /* pages held by any segment */
+  int64_t pages_global;      /* held by global-head segments */
+  int64_t pages_local;       /* held by local-head segments */
+  int64_t kept_tokens;       /* sum over segments of kept length */
+  int64_t upload_bytes;      /* bytes of plans uploaded so far (host -> device) */
+} segkv_stats_t;
+
+/*
+ * segkv_create — set up the segment tables over caller-owned page pools.
+ * Defines the head classes (summary page, section "头分类稀疏") and the paged
+ * per-(layer, head) store (section "SegPagedAttention").
+ *   head_class  host uint8 [num_layers * num_kv_heads], SEGKV_GLOBAL/LOCAL.
+ *   window      host int32 [num_layers], W >= 1, used by local heads.
+ *   page_size   P, a multiple of 8 that divides 128 or is a multiple of 128.
+ *   max_seqs    sequence slots; seq ids are 0 .. max_seqs-1.
+ *   max_seq_len longest sequence (positions 0 .. max_seq_len-1).
+ *   k_pool, v_pool  device bf16 [num_pages, P, D], 16-byte aligned. Both
+ *               NULL (with num_pages > 0) gives a host-only handle that plans
+ *               and tracks pages but launches nothing (attention calls then
+ *               return SEGKV_ERR_INVALID_ARG).
+ *   softmax_scale  <= 0 selects 1/sqrt(D).
+ * Allocates the device block table int32 [L][Hkv][max_seqs][ceil(max_seq_len/P)],
+ * a device status word and pinned/device upload rings. The current CUDA
+ * device at create is the handle's device.
+ * Errors: INVALID_ARG for bad shapes (G must divide 128; D in {64, 128}),
+ * CUDA if an allocation fails.
+ */
+int segkv_create(segkv_t* out, int num_layers, int num_q_heads, int num_kv_heads, int head_dim,
+                 const uint8_t* head_class, const int32_t* window, int page_size, int max_seqs,
+                 int max_seq_len, void* k_pool, void* v_pool, int64_t num_pages,
+                 float softmax_scale);
+
+/* segkv_destroy — synchronises the device and frees what segkv_create made. */
+int segkv_destroy(segkv_t h);
+
+/*
+ * segkv_append — write new tokens into every head's segment (BUILDSTATE).
+ * Each head physically keeps only the keys its pending queries need (summary
+ * page, section "SegPagedAttention"): first the local heads' pages that fell
+ * out of the window are freed, then pages for the new tokens are taken, then
+ * the append kernel scatters K/V rows into them.
+ *   k, v        device bf16 [cu_seqlens[n], Hkv, D], token-major.
+ *   cu_seqlens  host int32 [n+1], cu_seqlens[0] = 0, non-decreasing; sequence
+ *               i appends tokens cu_seqlens[i] .. cu_seqlens[i+1]-1 at its
+ *               positions a_i .. a_i+T_i-1, a_i = its tracked length in layer.
+ *   seq_ids     host int32 [n], distinct.
+ * Errors: INVALID_ARG (bad ids, length beyond max_seq_len), OUT_OF_PAGES.
+ */
+int segkv_append(segkv_t h, int layer, const void* k, const void* v, const int32_t* cu_seqlens,
+                 const int32_t* seq_ids, int n, segkv_stream_t stream);
+
+/*
+ * segkv_prefill_attn — varlen attention of packed queries over the segments
+ * (EXECUTE; summary page, section "SegPagedAttention": one fused varlen
+ * kernel, no attn_mask). For query token t of sequence i at position
+ * p = q_pos[t] and query head hq (KV head h = hq / G):
+ *   O[t, hq] = softmax_j(scale * q . k_j) v_j over kept keys j <= p, and for a
+ *   local head also j >= p-W+1;  lse[hq, t] = log sum_j exp(scale * q . k_j).
+ *   q       device bf16 [cu_seqlens[n], Hq, D].
+ *   cu_seqlens host int32 [n+1]; q_pos host int32 [cu_seqlens[n]], each < the
+ *           sequence's tracked length (append first); seq_ids host int32 [n].
+ *   o       device bf16 [cu_seqlens[n], Hq, D]; lse device fp32 [Hq, cu_seqlens[n]]
+ *           (natural log) or NULL.
+ *   workspace, workspace_bytes  unused by this call (pass NULL, 0).
+ * Errors: INVALID_ARG, EVICTED (a local head already dropped a needed key).
+ */
+int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_seqlens,
+                       const int32_t* q_pos, const int32_t* seq_ids, int n, void* o, float* lse,
+                       void* workspace, size_t workspace_bytes, segkv_stream_t stream);
+
+/*
+ * segkv_decode_attn — one query token per sequence at position seq_len-1
+ * against its segments: split-KV partials over key chunks, then a combine
+ * pass that merges them with the running-maximum rule (KV-cache architecture
+ * page, section 5.2).
+ *   q         device bf16 [n, Hq, D]; o device bf16 [n, Hq, D].
+ *   seq_lens  host int32 [n], must equal each sequence's tracked length.
+ *   seq_ids   host int32 [n], distinct.
+ *   workspace device, >= segkv_workspace_size(SEGKV_WS_DECODE, n, n) bytes,
+ *             256-byte aligned; holds the fp32 partials.
+ * Errors: INVALID_ARG (length mismatch, small workspace), EVICTED.
+ */
+int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_lens,
+                      const int32_t* seq_ids, int n, void* o, void* workspace,
+                      size_t workspace_bytes, segkv_stream_t stream);
+
+/*
+ * segkv_trim — let local heads of the listed sequences drop every key the
+ * next token's query will not see (keep the W-1 newest); layer -1 = all
+ * layers. Host-only bookkeeping: freed pages are reused by later appends,
+ * which are stream-ordered after earlier reads.
+ */
+int segkv_trim(segkv_t h, int layer, const int32_t* seq_ids, int n);
+
+/* segkv_free_seq — return every page of a sequence in every layer; its
+ * tracked lengths become 0. */
+int segkv_free_seq(segkv_t h, int seq_id);
+
+/* segkv_workspace_size — device workspace a call needs. kind SEGKV_WS_DECODE:
+ * n_seqs sequences (n_tokens ignored); SEGKV_WS_PREFILL: 0. */
+int segkv_workspace_size(segkv_t h, int kind, int64_t n_tokens, int n_seqs, size_t* bytes);
+
+/*
+ * segkv_get_segment — host copy of one segment's table: kept start, kept
+ * length, first logical page and the page ids in logical order (at most
+ * max_ids written; *n_ids gets the count).
+ */
+int segkv_get_segment(segkv_t h, int layer, int head, int seq, int32_t* start, int32_t* len,
+                      int32_t* first_page, int32_t* ids, int max_ids, int32_t* n_ids);
+
+/* segkv_seq_len — tracked length of a sequence in a layer (host). */
+int segkv_seq_len(segkv_t h, int layer, int seq, int32_t* len);
+
+/* segkv_stats — page and token counts (host). */
+int segkv_stats(segkv_t h, segkv_stats_t* out);
+
+/*
+ * segkv_status — synchronise the stream, read and clear the device status
+ * word. Returns SEGKV_OK, SEGKV_ERR_DEVICE_TIMEOUT if a kernel's bounded wait
+ * expired (that launch's outputs are undefined; the context stays usable),
+ * or SEGKV_ERR_CUDA.
+ */
+int segkv_status(segkv_t h, segkv_stream_t stream);
+
+/* segkv_last_error — message of the last failing call on h (or of a failed
+ * create when h is NULL). */
+const char* segkv_last_error(segkv_t h);
+
+/* segkv_set_debug — test hook. Bit 0: the next prefill launch makes one wait
+ * on a barrier that nothing signals, with a short limit, so the timeout path
+ * runs (status becomes SEGKV_ERR_DEVICE_TIMEOUT). Bits are cleared on use. */
+int segkv_set_debug(segkv_t h, int flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SEGKV_H_ */

@@ -10,10 +10,15 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+    # The library and the oracle are built from source in-tree (nvcc cross-compiles
+    # without a GPU); a stale or missing build is rebuilt once per session.
+    import __graft_entry__
+    __graft_entry__.build()
+    import oracle
+    oracle.build()
 
 
 def pytest_collection_modifyitems(config, items):
-    # GPU tests cannot run without a device; keep them selected only where one exists.
     import torch
     if torch.cuda.is_available():
         return
