@@ -407,18 +407,16 @@ def run_e2e(args, dev, stream, w, sets, cu, q_pos, step_flops, num_pages):
 
 
 # ------------------------------------------------------------------ oracle (CPU) arm
-def oracle_rate(sets, w, budget_s):
+def oracle_rate(q_rows, k, v, w, budget_s):
     """Time the oracle on sampled query rows of three layer kinds of the
     128K workload (shallow all-local, deep with no global head, deep with
-    one); return useful FLOPs/s over the sample."""
+    one); return useful FLOPs/s over the sample. q_rows(rows) gives those
+    rows of Q (bf16, CPU); k, v are the layer's full K and V on the CPU."""
     import numpy as np
-    import torch
 
     import oracle
 
     n = w.seq_lens[0]
-    q, k, v = (t.to("cpu") for t in sets[0]) if not isinstance(sets[0][0], torch.Tensor) or \
-        sets[0][0].device.type != "cpu" else sets[0]
     kinds = {}
     for l in range(w.num_layers):
         g = sum(1 for c in w.head_class[l] if c == 0)
@@ -427,42 +425,51 @@ def oracle_rate(sets, w, budget_s):
     rng = np.random.default_rng(0)
     total_flops, total_s = 0, 0.0
     per = {}
-    rows_per_kind = 2
     for kind, l in kinds.items():
-        t_kind, f_kind = 0.0, 0
+        t_kind, f_kind, nrows = 0.0, 0, 2
         while t_kind < budget_s / len(kinds):
-            rows = rng.integers(0, n, rows_per_kind).astype(np.int64)
+            pos = np.sort(rng.integers(0, n, nrows)).astype(np.int32)
+            qs = q_rows(pos)
             t0 = time.perf_counter()
-            rc, _, _ = oracle.attention(q, k, v, np.zeros(n, np.int32), np.arange(n, dtype=np.int32),
-                                        [0], [n], w.head_class[l], w.window[l],
-                                        np.zeros((1, w.hkv), np.int32), rows=rows)
+            rc, _, _ = oracle.attention(qs, k, v, np.zeros(len(pos), np.int32), pos, [0], [n],
+                                        w.head_class[l], w.window[l],
+                                        np.zeros((1, w.hkv), np.int32))
             dt = time.perf_counter() - t0
             assert rc == 0
             f = 0
-            for p in rows:
+            for p in pos:
                 for hh in range(w.hkv):
                     vis = p + 1 if w.head_class[l][hh] == 0 else min(p + 1, w.window[l])
                     f += 4 * w.head_dim * w.group * int(vis)
             t_kind += dt
             f_kind += f
             if dt < 1.0:
-                rows_per_kind *= 2
+                nrows *= 2
         per[kind] = {"layer": l, "seconds": round(t_kind, 2), "useful_flops": f_kind}
         total_flops += f_kind
         total_s += t_kind
     return total_flops / total_s, per, total_s
 
 
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
 def cpu_baseline(sets, w, budget_s=20.0):
     import oracle
     oracle.build()
-    cores = os.cpu_count()
-    try:
-        cores = len(os.sched_getaffinity(0))
-    except AttributeError:
-        pass
-    rate, per, secs = oracle_rate(sets, w, budget_s)
-    return {"value": rate / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+    q, k, v = sets[0]
+    kc, vc = k.to("cpu"), v.to("cpu")
+
+    def q_rows(pos):
+        import torch
+        return q[torch.as_tensor(pos, dtype=torch.long, device=q.device)].to("cpu")
+
+    rate, per, secs = oracle_rate(q_rows, kc, vc, w, budget_s)
+    return {"value": rate / 1e12, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
             "sample": ("fp64 C++ oracle (OpenMP) on random query rows (all 64 query heads) of one "
                        "shallow, one deep g=0 and one deep g=1 layer of the 128K workload, "
                        f"{secs:.1f} s total; useful FLOPs / CPU time"),
@@ -480,20 +487,23 @@ def run_reference(args, rank, world):
     oracle.build()
     w = I.long_128k_64layer(seed=0)
     n = w.seq_lens[0]
-    q = I.normal_bf16(w.seed, I.tensor_stream(I._Q, 0), (n, w.hq, w.head_dim))
+    shape_q = (n, w.hq, w.head_dim)
     k = I.normal_bf16(w.seed, I.tensor_stream(I._K, 0), (n, w.hkv, w.head_dim))
     v = I.normal_bf16(w.seed, I.tensor_stream(I._V, 0), (n, w.hkv, w.head_dim))
-    sets = [(q, k, v)]
+
+    def q_rows(pos):
+        return I.normal_bf16_rows(w.seed, I.tensor_stream(I._Q, 0), shape_q, pos)
+
     per_step = max(2.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        oracle_rate(sets, w, per_step / 3)
+        oracle_rate(q_rows, k, v, w, per_step / 3)
     rates, secs = [], 0.0
     for _ in range(args.steps):
-        r, _, s = oracle_rate(sets, w, per_step)
+        r, _, s = oracle_rate(q_rows, k, v, w, per_step)
         rates.append(r)
         secs += s
     value = statistics.median(rates) / 1e12
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    cores = host_cores()
     ms_step = 1e3 * secs / max(1, args.steps)
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

@@ -84,23 +84,40 @@ def f64_to_bf16_rne(x: torch.Tensor) -> torch.Tensor:
     return y.to(torch.float32).to(torch.bfloat16)
 
 
+def _normal_range(seed: int, stream: int, start: int, count: int, scale: float, device):
+    """Elements start .. start+count-1 of the normal stream, as bf16."""
+    u = uniform01(seed, stream, 2 * count, device, offset=2 * start).view(count, 2)
+    z = torch.sqrt(-2.0 * torch.log1p(-u[:, 0])) * torch.cos((2.0 * math.pi) * u[:, 1])
+    if scale != 1.0:
+        z = z * scale
+    return f64_to_bf16_rne(z)
+
+
 def normal_bf16(seed: int, stream: int, shape, scale: float = 1.0, device="cpu",
-                chunk: int = 1 << 26) -> torch.Tensor:
+                chunk: int | None = None) -> torch.Tensor:
     """N(0,1)*scale drawn in fp64 and rounded once to bf16."""
     n = 1
     for s in shape:
         n *= int(s)
+    if chunk is None:  # cache-sized chunks on the host, large ones on a GPU
+        chunk = (1 << 26) if torch.device(device).type == "cuda" else (1 << 20)
     out = torch.empty(n, dtype=torch.bfloat16, device=device)
-    two_pi = 2.0 * math.pi
     for c0 in range(0, n, chunk):
         c = min(chunk, n - c0)
-        u = uniform01(seed, stream, 2 * c, device, offset=2 * c0).view(c, 2)
-        z = torch.sqrt(-2.0 * torch.log1p(-u[:, 0])) * torch.cos(two_pi * u[:, 1])
-        if scale != 1.0:
-            z = z * scale
-        out[c0:c0 + c] = f64_to_bf16_rne(z)
-        del u, z
+        out[c0:c0 + c] = _normal_range(seed, stream, c0, c, scale, device)
     return out.view(*shape)
+
+
+def normal_bf16_rows(seed: int, stream: int, shape, rows, scale: float = 1.0) -> torch.Tensor:
+    """Only the listed leading-index rows of normal_bf16(seed, stream, shape),
+    bit for bit, without drawing the rest."""
+    inner = 1
+    for s in shape[1:]:
+        inner *= int(s)
+    out = torch.empty((len(rows), inner), dtype=torch.bfloat16)
+    for i, r in enumerate(rows):
+        out[i] = _normal_range(seed, stream, int(r) * inner, inner, scale, "cpu")
+    return out.view(len(rows), *shape[1:])
 
 
 def randint_list(seed: int, stream: int, count: int, lo: int, hi: int) -> list[int]:

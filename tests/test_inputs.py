@@ -89,3 +89,10 @@ def test_sink_rows_scaled_by_8():
     assert torch.equal(k[3].float(), 8 * k0[3].float())
     assert torch.equal(k[300].float(), 8 * k0[300].float())
     assert torch.equal(k[4], k0[4])
+
+
+def test_row_subset_matches_full_draw():
+    full = I.normal_bf16(3, 44, (50, 3, 8))
+    rows = [0, 7, 49, 7]
+    sub = I.normal_bf16_rows(3, 44, (50, 3, 8), rows)
+    assert torch.equal(sub.view(torch.int16), full[rows].view(torch.int16))
