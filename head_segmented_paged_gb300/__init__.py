@@ -31,7 +31,8 @@ SEGKV_WS_PREFILL, SEGKV_WS_DECODE = 0, 1
 SYMBOLS = ["segkv_create", "segkv_destroy", "segkv_append", "segkv_prefill_attn",
            "segkv_decode_attn", "segkv_trim", "segkv_free_seq", "segkv_workspace_size",
            "segkv_get_segment", "segkv_seq_len", "segkv_stats", "segkv_status",
-           "segkv_last_error", "segkv_set_debug"]
+           "segkv_last_error", "segkv_set_debug", "segkv_decode_attn_noalloc"]
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class SegKVStats(ctypes.Structure):
@@ -60,6 +61,7 @@ def _load():
         "segkv_status": [P, P],
         "segkv_last_error": [P],
         "segkv_set_debug": [P, I],
+        "segkv_decode_attn_noalloc": [P, I, P, P, P, I, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -144,6 +146,14 @@ def segkv_decode_attn(h, layer, q, seq_lens, seq_ids, o, workspace, workspace_by
         workspace_bytes = workspace.numel() * workspace.element_size()
     return _lib.segkv_decode_attn(h, layer, _ptr(q), sl.ctypes.data, ids.ctypes.data, len(ids),
                                   _ptr(o), _ptr(workspace), workspace_bytes, _stream_ptr(stream))
+
+
+def segkv_decode_attn_noalloc(h, layer, q, seq_lens, seq_ids, o, stream=None):
+    """Decode with the library's fixed scratch instead of a workspace, for
+    callers that cannot allocate when they decode."""
+    sl, ids = _host_i32(seq_lens), _host_i32(seq_ids)
+    return _lib.segkv_decode_attn_noalloc(h, layer, _ptr(q), sl.ctypes.data, ids.ctypes.data,
+                                          len(ids), _ptr(o), _stream_ptr(stream))
 
 
 def segkv_trim(h, layer, seq_ids):
@@ -256,6 +266,10 @@ class SegKV:
     def decode_attn(self, layer, q, seq_lens, seq_ids, o, workspace, stream=None):
         return self._check(segkv_decode_attn(self._h, layer, q, seq_lens, seq_ids, o, workspace,
                                              None, stream))
+
+    def decode_attn_noalloc(self, layer, q, seq_lens, seq_ids, o, stream=None):
+        return self._check(segkv_decode_attn_noalloc(self._h, layer, q, seq_lens, seq_ids, o,
+                                                     stream))
 
     def trim(self, layer, seq_ids):
         return self._check(segkv_trim(self._h, layer, seq_ids))

@@ -820,3 +820,33 @@ int segkv_status(segkv_t h, segkv_stream_t stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- helpers for
+// the no-allocation decode entry point (decode_noalloc.cu)
+namespace skv {
+
+// Bytes of fp32 partials segkv_decode_attn would need for this call; 0 when
+// the arguments are not valid (the decode call itself then reports why).
+size_t decode_partials_bytes(segkv* h, int layer, const int32_t* seq_lens,
+                             const int32_t* seq_ids, int n) {
+  if (!h || layer < 0 || layer >= h->L || !seq_lens || !ids_valid(h, seq_ids, n)) return 0;
+  const int W = h->win[layer];
+  int64_t units = 0;
+  for (int i = 0; i < n; ++i) {
+    const int32_t nlen = seq_lens[i];
+    if (nlen < 1) return 0;
+    const int32_t p = nlen - 1;
+    for (int hd = 0; hd < h->Hkv; ++hd) {
+      const int32_t lo = h->local(layer, hd) ? std::max(0, p - W + 1) : 0;
+      units += p / kDecodeChunk - lo / kDecodeChunk + 1;
+    }
+  }
+  return align_up(static_cast<size_t>(units) * h->G * h->D * 4, 256) +
+         align_up(static_cast<size_t>(units) * h->G * 2 * 4, 256);
+}
+
+int set_error(segkv* h, int code, const char* msg) { return fail(h, code, "%s", msg); }
+
+int handle_device(const segkv* h) { return h->host_only ? -1 : h->device; }
+
+}  // namespace skv

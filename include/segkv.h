@@ -200,6 +200,30 @@ int segkv_status(segkv_t h, segkv_stream_t stream);
  * create when h is NULL). */
 const char* segkv_last_error(segkv_t h);
 
+/*
+ * segkv_decode_attn_noalloc — segkv_decode_attn without a caller workspace,
+ * for callers that cannot allocate device memory when they decode (runtimes
+ * that forbid cudaMalloc on the serving path, or that cannot size a
+ * workspace per call). The paper has no counterpart; this is a packaging
+ * choice of the library.
+ *   The split partials live in a fixed device array inside the library,
+ *   SEGKV_NOALLOC_SCRATCH_BYTES (8 MiB) per GPU, held by every GPU that loads
+ *   the library until the process exits. A call whose partials would not fit
+ *   (about 4000 split units at G=4, D=128; units are 512-key chunks of each
+ *   (sequence, KV head)) returns SEGKV_ERR_INVALID_ARG with a message; use
+ *   segkv_decode_attn then.
+ *   The call allocates no memory. Its first call on a device looks up the
+ *   array's device address (cudaGetSymbolAddress) with the handle's device
+ *   current, so make that first call before any stream capture.
+ *   Every call shares the one array: calls that overlap on the GPU (other
+ *   streams, other handles) race. Nothing in it needs clearing between calls.
+ *   Other arguments, errors and results are those of segkv_decode_attn; the
+ *   handle's device must be the current device.
+ */
+#define SEGKV_NOALLOC_SCRATCH_BYTES (8u << 20)
+int segkv_decode_attn_noalloc(segkv_t h, int layer, const void* q, const int32_t* seq_lens,
+                              const int32_t* seq_ids, int n, void* o, segkv_stream_t stream);
+
 /* segkv_set_debug — test hook. Bit 0: the next prefill launch makes one wait
  * on a barrier that nothing signals, with a short limit, so the timeout path
  * runs (status becomes SEGKV_ERR_DEVICE_TIMEOUT). Bits are cleared on use. */
