@@ -521,6 +521,53 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_case(args):
+    """Single-kernel cases for profiling: one layer of prefill at 32K tokens
+    (64/8 heads, D=128, pages of 128; KV head 0 global, the rest local with
+    window 1024, or all global with --case dense-32k), or the ragged decode
+    workload. Prints one JSON line with per-launch times."""
+    import numpy as np
+    import torch
+
+    import head_segmented_paged_gb300 as S
+    from head_segmented_paged_gb300 import inputs as I
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    if args.case == "decode":
+        out = run_decode(args, dev, stream, *measured_peaks()[::3])
+        print(json.dumps({"case": args.case, **out}), flush=True)
+        return
+    n, hq, hkv, D, P = 32768, 64, 8, 128, 128
+    glob = args.case == "dense-32k"
+    hc = [[0] * 8] if glob else [[0] + [1] * 7]
+    w = I.Workload(args.case, 1, hq, hkv, D, P, hc, [n if glob else 1024], [n])
+    q = I.normal_bf16(0, I.tensor_stream(I._Q, 0), (n, hq, D), device=dev)
+    k = I.normal_bf16(0, I.tensor_stream(I._K, 0), (n, hkv, D), device=dev)
+    v = I.normal_bf16(0, I.tensor_stream(I._V, 0), (n, hkv, D), device=dev)
+    kp = torch.empty((hkv * n // P + 8, P, D), dtype=torch.bfloat16, device=dev)
+    vp = torch.empty_like(kp)
+    h = S.SegKV(1, hq, hkv, D, hc, w.window, P, 1, n, kp, vp)
+    cu = np.array([0, n], np.int32)
+    q_pos = np.arange(n, dtype=np.int32)
+    o = torch.empty((n, hq, D), dtype=torch.bfloat16, device=dev)
+    h.append(0, k, v, cu, [0], stream)
+    flops = useful_flops_layer(w, 0, n)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.warmup + args.steps)]
+    for i in range(args.warmup + args.steps):
+        ev[i][0].record(stream)
+        h.prefill_attn(0, q, cu, q_pos, [0], o, None, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    assert h.status() == 0
+    ms = [a.elapsed_time(b) for a, b in ev[args.warmup:]]
+    med = statistics.median(ms)
+    print(json.dumps({"case": args.case, "prefill_ms": ms, "useful_tflops":
+                      round(flops / (med * 1e-3) / 1e12, 1), "useful_flops": flops}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -532,7 +579,14 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--case", default=None, choices=["prefill-32k", "dense-32k", "decode"],
+                    help="run one kernel's profiling case instead of the benchmark")
     args = ap.parse_args()
+    if args.case:
+        import __graft_entry__
+        __graft_entry__.build()
+        run_case(args)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
