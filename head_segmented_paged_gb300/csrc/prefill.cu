@@ -4,24 +4,31 @@
 // head on the fast path, no attn_mask). Online softmax with a running maximum
 // (KV-cache architecture page, section 5.2).
 //
-// One work unit = one KV head x one tile of 128 query rows. Rows pack the G
-// query heads that share the KV head: row r = token (r / G) x head (r % G), so
-// one K/V tile feeds every head of the group (GQA packing). Keys are visited
-// in tiles of 128 positions; each tile's pages are fetched by TMA through the
-// segment's block table. Pages outside the segment are read as zeros (an
-// out-of-range TMA coordinate), and per-row masks keep every row to its own
-// key set: j <= p, and j >= p-W+1 for a local head.
+// Work unit: one KV head x two tiles (A, B) of 128 query rows. Rows pack the
+// G query heads that share the KV head: row r of a tile = token (r / G) x head
+// (r % G), so each K/V tile feeds every head of the group (GQA packing), and
+// the two Q tiles share every K/V tile fetched. Keys are visited in tiles of
+// 128 positions whose pages TMA fetches through the segment's block table;
+// pages outside the segment are read as zeros (out-of-range TMA coordinate)
+// and per-row masks keep every row to its own key set: j <= p, and j >= p-W+1
+// for a local head.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over an LPT-sorted
+// Warp roles (320 threads, one CTA per SM, persistent over an LPT-sorted
 // unit list):
-//   warp 0      TMA producer: Q tile, then K and V tiles into a 2-stage ring;
-//   warp 1      TMEM owner and MMA issuer: S = Q K^T into a double-buffered
-//               TMEM accumulator, then O += P V into a TMEM accumulator;
-//   warps 2..5  softmax (one thread per row): read S from TMEM, mask, update
+//   warp 0      TMA producer: Q tiles A and B, then K and V tiles (2 stages);
+//   warp 1      TMEM owner and MMA issuer: S_X = Q_X K^T (X = A, B) into TMEM,
+//               then O_X += P_X V with P_X read back from TMEM;
+//   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B (one thread
+//               per row): read S from TMEM, mask only on edge tiles, update
 //               the running max (O is rescaled in TMEM only when the max grows
-//               by more than 2^8, which is exact), write P as bf16 to shared
-//               memory; after the last tile, normalise O and store it.
-// TMEM columns: S buffers [0,128) and [128,256), O [256, 256+D).
+//               by more than 2^8, which is exact), write P as bf16 over S; at
+//               the end of a unit, normalise O and store it.
+// TMEM columns: S_A [0,128), S_B [128,256) (P_X aliases the first 64 columns
+// of S_X), O_A [256, 256+D), O_B [384, 384+D).
+//
+// Ordering: the MMA issuer issues S_X of tile j+1 after P_X V of tile j, and
+// tcgen05 operations of one thread complete in order, so when the softmax sees
+// S_X(j+1) complete, P_X(j) has been consumed and O_X is stable.
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -34,51 +41,52 @@ namespace {
 
 constexpr int BM = kRowsPerTile;
 constexpr int BN = kKeyTile;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr float kRescaleLog2 = 8.0f;
+constexpr int kEmuPer8 = 2;  // of every 8 score columns, this many use exp2_poly
 constexpr uint32_t kAtom = BM * 128;  // one 64-column, 128-row swizzle block (16 KB)
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 constexpr uint64_t kDebugWaitNs = 20ull * 1000 * 1000;
 
 enum {
-  B_Q_FULL = 0,
-  B_Q_EMPTY = 1,
-  B_K_FULL = 2,    // +stage
-  B_V_FULL = 4,    // +stage
-  B_KV_EMPTY = 6,  // +stage
-  B_S_FULL = 8,    // +buffer
-  B_S_EMPTY = 10,  // +buffer
-  B_P_FULL = 12,
-  B_O_DONE = 13,
-  B_O_EMPTY = 14,
-  B_NEVER = 15,
-  B_DRAIN = 16,
-  NUM_BARS = 17
+  B_Q_FULL = 0,    // +X
+  B_Q_EMPTY = 2,   // +X
+  B_K_FULL = 4,    // +stage
+  B_V_FULL = 6,    // +stage
+  B_KV_EMPTY = 8,  // +stage
+  B_S_FULL = 10,   // +X
+  B_P_FULL = 12,   // +X
+  B_O_FULL = 14,   // +X
+  B_O_EMPTY = 16,  // +X
+  B_NEVER = 18,
+  B_DRAIN = 19,
+  NUM_BARS = 20
 };
 
 template <int D>
 struct Layout {
-  static constexpr uint32_t Q_BYTES = BM * D * 2;
+  static constexpr uint32_t Q_BYTES = BM * D * 2;  // one Q tile
   static constexpr uint32_t KV_BYTES = BN * D * 2;
-  static constexpr uint32_t P_BYTES = BM * BN * 2;
-  static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
+  static constexpr uint32_t OFF_Q = 0;              // tiles A, B
+  static constexpr uint32_t OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + 2 * KV_BYTES;
-  static constexpr uint32_t OFF_P = OFF_V + 2 * KV_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_P + P_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_V + 2 * KV_BYTES;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
   // + slack to align to 1 KB; at least 116 KB so that one CTA holds an SM (and
   // its 512 TMEM columns) alone
   static constexpr uint32_t RAW = OFF_MISC + 16 + 1024;
   static constexpr uint32_t BYTES = RAW > 116u * 1024 ? RAW : 116u * 1024;
+  static constexpr uint32_t TM_O = 256;             // TMEM column of O_A
+  static constexpr uint32_t TM_O_STRIDE = 128;      // O_B = O_A + this
 };
 
 struct Ctx {
   uint8_t* smem;
   uint32_t sbase;
   uint32_t tmem;
+  uint32_t off_bar;
   WaitCtx wc;
-  __device__ uint32_t bar(int i, uint32_t off_bar) const { return sbase + off_bar + 8u * i; }
+  __device__ uint32_t bar(int i) const { return sbase + off_bar + 8u * i; }
 };
 
 // ---------------------------------------------------------------- producer
@@ -89,24 +97,27 @@ __device__ void producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const C
   constexpr int NC = D / 64;
   const int box_rows = p.page_size <= BN ? p.page_size : BN;
   const int boxes = BN / box_rows;
-  int armed_q = -1, armed_kv[2] = {-1, -1};
+  int armed_q[2] = {-1, -1}, armed_kv[2] = {-1, -1};
   bool ok = true;
   int g = 0, ui = 0;
   for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++ui) {
     const PrefillUnit U = p.units[u];
-    if (!wait1(c.bar(B_Q_EMPTY, L::OFF_BAR), (ui & 1) ^ 1, c.wc)) { ok = false; break; }
-    mbar_expect_tx(c.bar(B_Q_FULL, L::OFF_BAR), L::Q_BYTES);
-    for (int cc = 0; cc < NC; ++cc)
-      tma_load_3d(c.sbase + L::OFF_Q + cc * kAtom, tmq, cc * 64, U.head * p.G, U.tok0,
-                  c.bar(B_Q_FULL, L::OFF_BAR));
-    armed_q = ui & 1;
+    for (int x = 0; x < 2; ++x) {
+      if (!wait1(c.bar(B_Q_EMPTY + x), (ui & 1) ^ 1, c.wc)) { ok = false; break; }
+      mbar_expect_tx(c.bar(B_Q_FULL + x), L::Q_BYTES);
+      for (int cc = 0; cc < NC; ++cc)
+        tma_load_3d(c.sbase + L::OFF_Q + x * L::Q_BYTES + cc * kAtom, tmq, cc * 64, U.head * p.G,
+                    U.tok0 + x * p.tpt, c.bar(B_Q_FULL + x));
+      armed_q[x] = ui & 1;
+    }
+    if (!ok) break;
     const int32_t* trow = p.table + static_cast<int64_t>(U.table_row) * p.R;
     for (int kt = U.kt0; kt <= U.kt1; ++kt, ++g) {
       const int st = g & 1;
       const uint32_t ph = (g >> 1) & 1;
-      if (!wait1(c.bar(B_KV_EMPTY + st, L::OFF_BAR), ph ^ 1, c.wc)) { ok = false; break; }
-      mbar_expect_tx(c.bar(B_K_FULL + st, L::OFF_BAR), L::KV_BYTES);
-      mbar_expect_tx(c.bar(B_V_FULL + st, L::OFF_BAR), L::KV_BYTES);
+      if (!wait1(c.bar(B_KV_EMPTY + st), ph ^ 1, c.wc)) { ok = false; break; }
+      mbar_expect_tx(c.bar(B_K_FULL + st), L::KV_BYTES);
+      mbar_expect_tx(c.bar(B_V_FULL + st), L::KV_BYTES);
       armed_kv[st] = static_cast<int>(ph);
       for (int bi = 0; bi < boxes; ++bi) {
         const int pos = kt * BN + bi * box_rows;
@@ -115,106 +126,120 @@ __device__ void producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const C
         if (k >= U.first_page && k <= U.last_page) y = trow[k] * p.page_size + (pos - k * p.page_size);
         const uint32_t off = st * L::KV_BYTES + bi * box_rows * 128;
         for (int cc = 0; cc < NC; ++cc) {
-          tma_load_2d(c.sbase + L::OFF_K + off + cc * kAtom, tmk, cc * 64, y,
-                      c.bar(B_K_FULL + st, L::OFF_BAR));
-          tma_load_2d(c.sbase + L::OFF_V + off + cc * kAtom, tmv, cc * 64, y,
-                      c.bar(B_V_FULL + st, L::OFF_BAR));
+          tma_load_2d(c.sbase + L::OFF_K + off + cc * kAtom, tmk, cc * 64, y, c.bar(B_K_FULL + st));
+          tma_load_2d(c.sbase + L::OFF_V + off + cc * kAtom, tmv, cc * 64, y, c.bar(B_V_FULL + st));
         }
       }
     }
   }
   if (!ok) {  // aborting: let our own copies land before the block exits
-    if (armed_q >= 0) wait_drain(c.bar(B_Q_FULL, L::OFF_BAR), armed_q, kDrainNs);
+    for (int x = 0; x < 2; ++x)
+      if (armed_q[x] >= 0) wait_drain(c.bar(B_Q_FULL + x), armed_q[x], kDrainNs);
     for (int st = 0; st < 2; ++st)
       if (armed_kv[st] >= 0) {
-        wait_drain(c.bar(B_K_FULL + st, L::OFF_BAR), armed_kv[st], kDrainNs);
-        wait_drain(c.bar(B_V_FULL + st, L::OFF_BAR), armed_kv[st], kDrainNs);
+        wait_drain(c.bar(B_K_FULL + st), armed_kv[st], kDrainNs);
+        wait_drain(c.bar(B_V_FULL + st), armed_kv[st], kDrainNs);
       }
   }
 }
 
 // ---------------------------------------------------------------- MMA issuer
 template <int D>
-__device__ bool issue_pv(const Ctx& c, int gj, bool first, int ui) {
+__device__ __forceinline__ void issue_s(const Ctx& c, int x, int st) {
+  using L = Layout<D>;
+  constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t a = c.sbase + L::OFF_Q + x * L::Q_BYTES + (kk >> 2) * kAtom + (kk & 3) * 32;
+    const uint32_t b = c.sbase + L::OFF_K + st * L::KV_BYTES + (kk >> 2) * kAtom + (kk & 3) * 32;
+    mma_bf16(c.tmem + x * BN, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, 16, 1024), IDESC_QK,
+             kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(const Ctx& c, int x, int st, bool first) {
   using L = Layout<D>;
   constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, 1);
-  if (first && !wait1(c.bar(B_O_EMPTY, L::OFF_BAR), (ui & 1) ^ 1, c.wc)) return false;
-  if (!wait1(c.bar(B_P_FULL, L::OFF_BAR), gj & 1, c.wc)) return false;
-  const int st = gj & 1;
-  if (!wait1(c.bar(B_V_FULL + st, L::OFF_BAR), (gj >> 1) & 1, c.wc)) return false;
-  tc_fence_after();
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk) {
-    const uint32_t a = c.sbase + L::OFF_P + (kk >> 2) * kAtom + (kk & 3) * 32;
     const uint32_t b = c.sbase + L::OFF_V + st * L::KV_BYTES + kk * 2048;
-    mma_bf16(c.tmem + 256, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, kAtom, 1024), IDESC_PV,
-             (first && kk == 0) ? 0u : 1u);
+    mma_bf16_ts(c.tmem + L::TM_O + x * L::TM_O_STRIDE, c.tmem + x * BN + kk * 8,
+                sdesc_sw128(b, kAtom, 1024), IDESC_PV, (first && kk == 0) ? 0u : 1u);
   }
-  mma_commit(c.bar(B_O_DONE, L::OFF_BAR));
-  mma_commit(c.bar(B_KV_EMPTY + st, L::OFF_BAR));
-  return true;
 }
 
 template <int D>
 __device__ void mma_issuer(const PrefillParams& p, const Ctx& c) {
-  using L = Layout<D>;
-  constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0);
   bool ok = true;
   if (p.debug & 1) {  // test hook: one wait on a barrier nothing signals
     WaitCtx w = c.wc;
     w.limit_ns = kDebugWaitNs;
-    wait1(c.bar(B_NEVER, L::OFF_BAR), 0, w);
+    wait1(c.bar(B_NEVER), 0, w);
     ok = false;
   }
   int g = 0, ui = 0;
   for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++ui) {
     const PrefillUnit U = p.units[u];
     const int nt = U.kt1 - U.kt0 + 1;
-    if (!wait1(c.bar(B_Q_FULL, L::OFF_BAR), ui & 1, c.wc)) { ok = false; break; }
-    tc_fence_after();
-    for (int i = 0; i < nt; ++i) {
+    const uint32_t qpar = ui & 1;
+    // prologue: S_A and S_B of the first key tile
+    if (!wait1(c.bar(B_K_FULL + (g & 1)), (g >> 1) & 1, c.wc)) { ok = false; break; }
+    for (int x = 0; x < 2; ++x) {
+      if (!wait1(c.bar(B_Q_FULL + x), qpar, c.wc)) { ok = false; break; }
+      tc_fence_after();
+      issue_s<D>(c, x, g & 1);
+      mma_commit(c.bar(B_S_FULL + x));
+      if (nt == 1) mma_commit(c.bar(B_Q_EMPTY + x));
+    }
+    if (!ok) break;
+    for (int i = 0; i < nt && ok; ++i) {
       const int gi = g + i, st = gi & 1;
       const uint32_t ph = (gi >> 1) & 1;
-      if (!wait1(c.bar(B_K_FULL + st, L::OFF_BAR), ph, c.wc) ||
-          !wait1(c.bar(B_S_EMPTY + st, L::OFF_BAR), ph ^ 1, c.wc)) {
-        ok = false;
-        break;
+      const bool last = (i + 1 == nt);
+      for (int x = 0; x < 2; ++x) {
+        if (i == 0 && !wait1(c.bar(B_O_EMPTY + x), qpar ^ 1, c.wc)) { ok = false; break; }
+        if (!wait1(c.bar(B_P_FULL + x), gi & 1, c.wc)) { ok = false; break; }
+        if (x == 0 && !wait1(c.bar(B_V_FULL + st), ph, c.wc)) { ok = false; break; }
+        tc_fence_after();
+        issue_pv<D>(c, x, st, i == 0);
+        if (x == 1) mma_commit(c.bar(B_KV_EMPTY + st));
+        if (!last) {
+          const int gn = gi + 1;
+          if (x == 0 && !wait1(c.bar(B_K_FULL + (gn & 1)), (gn >> 1) & 1, c.wc)) { ok = false; break; }
+          tc_fence_after();
+          issue_s<D>(c, x, gn & 1);
+          mma_commit(c.bar(B_S_FULL + x));
+          if (i + 2 == nt) mma_commit(c.bar(B_Q_EMPTY + x));
+        } else {
+          mma_commit(c.bar(B_O_FULL + x));
+        }
       }
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t a = c.sbase + L::OFF_Q + (kk >> 2) * kAtom + (kk & 3) * 32;
-        const uint32_t b = c.sbase + L::OFF_K + st * L::KV_BYTES + (kk >> 2) * kAtom + (kk & 3) * 32;
-        mma_bf16(c.tmem + st * BN, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, 16, 1024), IDESC_QK,
-                 kk > 0 ? 1u : 0u);
-      }
-      mma_commit(c.bar(B_S_FULL + st, L::OFF_BAR));
-      if (i > 0 && !issue_pv<D>(c, gi - 1, i == 1, ui)) { ok = false; break; }
     }
-    if (!ok || !issue_pv<D>(c, g + nt - 1, nt == 1, ui)) { ok = false; break; }
-    mma_commit(c.bar(B_Q_EMPTY, L::OFF_BAR));
     g += nt;
   }
   if (!ok) {  // aborting: let issued MMAs finish before TMEM is freed
-    mma_commit(c.bar(B_DRAIN, L::OFF_BAR));
-    wait_drain(c.bar(B_DRAIN, L::OFF_BAR), 0, kDrainNs);
+    mma_commit(c.bar(B_DRAIN));
+    wait_drain(c.bar(B_DRAIN), 0, kDrainNs);
   }
 }
 
 // ---------------------------------------------------------------- softmax
 template <int D>
-__device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int warp, int lane) {
+__device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int x, int warp, int lane) {
   using L = Layout<D>;
   constexpr int NC = D / 64;
   const int wq = warp & 3;  // TMEM lane quarter this warp may access
   const int r = wq * 32 + lane;
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-  const uint32_t t_o = c.tmem + lane_off + 256;
+  const uint32_t t_s = c.tmem + lane_off + x * BN;
+  const uint32_t t_o = c.tmem + lane_off + L::TM_O + x * L::TM_O_STRIDE;
+  const float scale = p.scale_log2;
   int g = 0, ui = 0;
   for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++ui) {
     const PrefillUnit U = p.units[u];
     const int nt = U.kt1 - U.kt0 + 1;
-    const int t = r / p.G, gg = r - t * p.G;
+    const int t = x * p.tpt + r / p.G, gg = r % p.G;
     const bool row_ok = t < U.ntok;
     const int tok = U.tok0 + t;
     int hi = -1, lo = 1 << 30;  // an invalid row sees no key
@@ -228,76 +253,72 @@ __device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int warp,
       const int gi = g + i, st = gi & 1;
       const uint32_t ph = (gi >> 1) & 1;
       const int j0 = (U.kt0 + i) * BN;
-      if (!waitw(c.bar(B_S_FULL + st, L::OFF_BAR), ph, c.wc)) { ok = false; break; }
+      if (!waitw(c.bar(B_S_FULL + x), gi & 1, c.wc)) { ok = false; break; }
       tc_fence_after();
       float s[BN];
+      tmem_ld32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+      tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+      tmem_ld32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+      tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+      tmem_wait_ld();
+      // mask only where some row of this warp does not see the whole tile
+      const bool whole = (j0 >= lo) && (j0 + BN - 1 <= hi);
+      if (!__all_sync(0xffffffffu, whole)) {
+        const int c_lo = lo - j0, c_hi = hi - j0;
 #pragma unroll
-      for (int q = 0; q < BN / 32; ++q) {
-        uint32_t v[32];
-        tmem_ld32(c.tmem + lane_off + st * BN + q * 32, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int x = 0; x < 32; ++x) s[q * 32 + x] = __uint_as_float(v[x]);
+        for (int e = 0; e < BN; ++e) s[e] = (e >= c_lo && e <= c_hi) ? s[e] : -INFINITY;
       }
-      tc_fence_before();
-      mbar_arrive(c.bar(B_S_EMPTY + st, L::OFF_BAR));
-
-      float mx = -INFINITY;
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int x = 0; x < BN; ++x) {
-        const int j = j0 + x;
-        const float y = (j >= lo && j <= hi) ? s[x] * p.scale_log2 : -INFINITY;
-        s[x] = y;
-        mx = fmaxf(mx, y);
+      for (int e = 0; e < BN; e += 8) {
+        m4[0] = max3(m4[0], s[e + 0], s[e + 1]);
+        m4[1] = max3(m4[1], s[e + 2], s[e + 3]);
+        m4[2] = max3(m4[2], s[e + 4], s[e + 5]);
+        m4[3] = max3(m4[3], s[e + 6], s[e + 7]);
       }
+      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale;
       const float m_new = fmaxf(m_used, mx);
       const bool resc = m_new > m_used + kRescaleLog2;
       const float m_tgt = resc ? m_new : m_used;
       const float alpha = resc ? ex2(m_used - m_new) : 1.f;
-      const float m_sub = (m_tgt == -INFINITY) ? 0.f : m_tgt;
+      const float neg_m = (m_tgt == -INFINITY) ? 0.f : -m_tgt;
 
-      if (i > 0) {  // P buffer and O are free once the previous P V finished
-        if (!waitw(c.bar(B_O_DONE, L::OFF_BAR), (gi - 1) & 1, c.wc)) { ok = false; break; }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
-            uint32_t v[32];
-            tmem_ld32(t_o + q * 32, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) v[x] = __float_as_uint(__uint_as_float(v[x]) * alpha);
-            tmem_st32(t_o + q * 32, v);
-          }
-          tmem_wait_st();
-        }
-      }
       l *= alpha;
 
-      float rs = 0.f;
-      uint8_t* prow = c.smem + L::OFF_P + r * 128;
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int q = 0; q < BN / 8; ++q) {
-        float e[8];
+      for (int q = 0; q < BN / 32; ++q) {
+        uint32_t pk[16];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          e[x] = ex2(s[q * 8 + x] - m_sub);
-          rs += e[x];
+        for (int e = 0; e < 16; ++e) {
+          const int col = q * 32 + 2 * e;
+          const float x0 = fmaf(s[col], scale, neg_m);
+          const float x1 = fmaf(s[col + 1], scale, neg_m);
+          const float p0 = ((col & 7) >= 8 - kEmuPer8) ? exp2_poly(x0) : ex2(x0);
+          const float p1 = (((col + 1) & 7) >= 8 - kEmuPer8) ? exp2_poly(x1) : ex2(x1);
+          rs[e & 3] += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
         }
-        uint4 w;
-        w.x = pack_bf16x2(e[0], e[1]);
-        w.y = pack_bf16x2(e[2], e[3]);
-        w.z = pack_bf16x2(e[4], e[5]);
-        w.w = pack_bf16x2(e[6], e[7]);
-        const int half = q >> 3, cq = q & 7;
-        *reinterpret_cast<uint4*>(prow + half * kAtom + ((cq ^ (r & 7)) << 4)) = w;
+        tmem_st16(t_s + q * 16, pk);
       }
-      l += rs;
+      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
 
-      if (i == 0 || i == nt - 1) {
+      if (i > 0 && __any_sync(0xffffffffu, resc)) {  // O_X is stable: P V of tile i-1 is done
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          uint32_t v[32];
+          tmem_ld32(t_o + q * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+          tmem_st32(t_o + q * 32, v);
+        }
+      }
+
+      if (x == 0 && (i == 0 || i == nt - 1)) {
         // Edge tiles: zero the V rows of keys outside every row's range
-        // (stale page heads, unwritten page tails) so P = 0 never meets NaN.
-        if (!waitw(c.bar(B_V_FULL + st, L::OFF_BAR), ph, c.wc)) { ok = false; break; }
+        // (stale page heads, unwritten page tails) so P never meets NaN.
+        if (!waitw(c.bar(B_V_FULL + st), ph, c.wc)) { ok = false; break; }
         const int jr = j0 + r;
         if (jr < U.klo || jr > U.khi) {
           uint8_t* vrow = c.smem + L::OFF_V + st * L::KV_BYTES + r * 128;
@@ -307,15 +328,16 @@ __device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int warp,
             for (int q = 0; q < 8; ++q)
               *reinterpret_cast<uint4*>(vrow + cc * kAtom + q * 16) = make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(c.bar(B_P_FULL, L::OFF_BAR));
+      mbar_arrive(c.bar(B_P_FULL + x));
       m_used = m_tgt;
     }
     if (!ok) break;
 
-    if (!waitw(c.bar(B_O_DONE, L::OFF_BAR), (g + nt - 1) & 1, c.wc)) break;
+    if (!waitw(c.bar(B_O_FULL + x), ui & 1, c.wc)) break;
     tc_fence_after();
     const float inv_l = row_ok ? 1.f / l : 0.f;
     __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) +
@@ -328,13 +350,13 @@ __device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int warp,
       if (row_ok) {
         uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
+        for (int e = 0; e < 4; ++e) {
           uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(v[8 * x + 0]) * inv_l, __uint_as_float(v[8 * x + 1]) * inv_l);
-          w.y = pack_bf16x2(__uint_as_float(v[8 * x + 2]) * inv_l, __uint_as_float(v[8 * x + 3]) * inv_l);
-          w.z = pack_bf16x2(__uint_as_float(v[8 * x + 4]) * inv_l, __uint_as_float(v[8 * x + 5]) * inv_l);
-          w.w = pack_bf16x2(__uint_as_float(v[8 * x + 6]) * inv_l, __uint_as_float(v[8 * x + 7]) * inv_l);
-          dst[x] = w;
+          w.x = pack_bf16x2(__uint_as_float(v[8 * e + 0]) * inv_l, __uint_as_float(v[8 * e + 1]) * inv_l);
+          w.y = pack_bf16x2(__uint_as_float(v[8 * e + 2]) * inv_l, __uint_as_float(v[8 * e + 3]) * inv_l);
+          w.z = pack_bf16x2(__uint_as_float(v[8 * e + 4]) * inv_l, __uint_as_float(v[8 * e + 5]) * inv_l);
+          w.w = pack_bf16x2(__uint_as_float(v[8 * e + 6]) * inv_l, __uint_as_float(v[8 * e + 7]) * inv_l);
+          dst[e] = w;
         }
       }
     }
@@ -342,7 +364,7 @@ __device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int warp,
       p.lse[static_cast<int64_t>(U.head * p.G + gg) * p.total_q + tok] =
           (m_used + log2f(l)) * 0.69314718055994530942f;
     tc_fence_before();
-    mbar_arrive(c.bar(B_O_EMPTY, L::OFF_BAR));
+    mbar_arrive(c.bar(B_O_EMPTY + x));
     g += nt;
   }
 }
@@ -363,21 +385,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   Ctx c;
   c.smem = smem;
   c.sbase = smem_addr(smem);
+  c.off_bar = L::OFF_BAR;
   if (threadIdx.x == 0) {
-    mbar_init(c.bar(B_Q_FULL, L::OFF_BAR), 1);
-    mbar_init(c.bar(B_Q_EMPTY, L::OFF_BAR), 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(c.bar(B_K_FULL + s, L::OFF_BAR), 1);
-      mbar_init(c.bar(B_V_FULL + s, L::OFF_BAR), 1);
-      mbar_init(c.bar(B_KV_EMPTY + s, L::OFF_BAR), 1);
-      mbar_init(c.bar(B_S_FULL + s, L::OFF_BAR), 1);
-      mbar_init(c.bar(B_S_EMPTY + s, L::OFF_BAR), 128);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(c.bar(B_Q_FULL + x), 1);
+      mbar_init(c.bar(B_Q_EMPTY + x), 1);
+      mbar_init(c.bar(B_S_FULL + x), 1);
+      mbar_init(c.bar(B_P_FULL + x), 128);
+      mbar_init(c.bar(B_O_FULL + x), 1);
+      mbar_init(c.bar(B_O_EMPTY + x), 128);
     }
-    mbar_init(c.bar(B_P_FULL, L::OFF_BAR), 128);
-    mbar_init(c.bar(B_O_DONE, L::OFF_BAR), 1);
-    mbar_init(c.bar(B_O_EMPTY, L::OFF_BAR), 128);
-    mbar_init(c.bar(B_NEVER, L::OFF_BAR), 1);
-    mbar_init(c.bar(B_DRAIN, L::OFF_BAR), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(c.bar(B_K_FULL + s), 1);
+      mbar_init(c.bar(B_V_FULL + s), 1);
+      mbar_init(c.bar(B_KV_EMPTY + s), 1);
+    }
+    mbar_init(c.bar(B_NEVER), 1);
+    mbar_init(c.bar(B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmq);
@@ -403,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mma_issuer<D>(p, c);
     __syncwarp();
   } else {
-    softmax_epilogue<D>(p, c, warp, lane);
+    softmax_epilogue<D>(p, c, (warp - 2) >> 2, warp, lane);
   }
   tc_fence_before();
   __syncthreads();
@@ -416,6 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 int prefill_smem_bytes(int head_dim) {
   return head_dim == 64 ? static_cast<int>(Layout<64>::BYTES) : static_cast<int>(Layout<128>::BYTES);
 }
+
+int prefill_unit_tokens(int G) { return 2 * (kRowsPerTile / G); }
 
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, int head_dim, int grid, cudaStream_t s) {

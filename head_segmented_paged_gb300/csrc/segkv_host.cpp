@@ -526,14 +526,15 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
       }
     }
   }
-  // units: (KV head, tile of 128/G tokens), LPT order
+  // units: (KV head, two Q tiles of 128/G tokens each), LPT order
   const int tpt = kRowsPerTile / h->G;
+  const int unit_tok = prefill_unit_tokens(h->G);
   std::vector<PrefillUnit> units;
   for (int i = 0; i < n; ++i) {
     const int b = seq_ids[i];
     const int32_t nlen = h->len[h->lidx(layer, b)];
-    for (int32_t t0 = cu_seqlens[i]; t0 < cu_seqlens[i + 1]; t0 += tpt) {
-      const int32_t t1 = std::min<int32_t>(t0 + tpt, cu_seqlens[i + 1]);
+    for (int32_t t0 = cu_seqlens[i]; t0 < cu_seqlens[i + 1]; t0 += unit_tok) {
+      const int32_t t1 = std::min<int32_t>(t0 + unit_tok, cu_seqlens[i + 1]);
       int32_t pmin = q_pos[t0], pmax = q_pos[t0];
       for (int32_t t = t0; t < t1; ++t) {
         pmin = std::min(pmin, q_pos[t]);

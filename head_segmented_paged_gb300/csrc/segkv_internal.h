@@ -47,7 +47,7 @@ struct AppendParams {
 // ---- prefill --------------------------------------------------------------
 struct PrefillUnit {
   int32_t tok0;        // first packed query token of the tile
-  int32_t ntok;        // tokens in the tile (<= 128 / G)
+  int32_t ntok;        // tokens in the unit (<= 2 * 128 / G: two Q tiles)
   int32_t head;        // KV head
   int32_t local;       // 1 = local head
   int32_t kt0, kt1;    // key tiles kt0 .. kt1 (inclusive), tile = 128 positions
@@ -66,7 +66,7 @@ struct PrefillParams {
   int64_t total_q;
   int n_units;
   int R;          // block-table row length
-  int hq, G, tpt, window;
+  int hq, G, tpt, window;  // tpt = tokens per 128-row Q tile
   int page_size;
   int oob_row;    // a K/V row coordinate past the end of the pools
   float scale_log2;
@@ -110,6 +110,7 @@ cudaError_t launch_append(const AppendParams& p, int grid, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, int head_dim, int grid, cudaStream_t s);
 int prefill_smem_bytes(int head_dim);
+int prefill_unit_tokens(int G);  // query tokens per prefill work unit
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, int grid, cudaStream_t s);
 
 }  // namespace skv
