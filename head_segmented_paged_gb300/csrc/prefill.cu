@@ -43,7 +43,11 @@ constexpr int BM = kRowsPerTile;
 constexpr int BN = kKeyTile;
 constexpr int kThreads = 320;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int kEmuPer8 = 2;  // of every 8 score columns, this many use exp2_poly
+// Of every 8 score columns, how many use exp2_poly instead of the MUFU unit.
+// GB300's MUFU exp rate keeps up with the D=128 MMAs, so there all use MUFU;
+// at D=64 the MMAs per key tile halve and a quarter go to the FMA pipe.
+template <int D>
+constexpr int kEmuPer8 = D == 64 ? 2 : 0;
 constexpr uint32_t kAtom = BM * 128;  // one 64-column, 128-row swizzle block (16 KB)
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 constexpr uint64_t kDebugWaitNs = 20ull * 1000 * 1000;
@@ -285,23 +289,24 @@ __device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int x, in
 
       l *= alpha;
 
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      // p = 2^(s * scale - m), two columns per packed FMA/add
+      const float2 sc2 = make_float2(scale, scale), nm2 = make_float2(neg_m, neg_m);
+      float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int q = 0; q < BN / 32; ++q) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int col = q * 32 + 2 * e;
-          const float x0 = fmaf(s[col], scale, neg_m);
-          const float x1 = fmaf(s[col + 1], scale, neg_m);
-          const float p0 = ((col & 7) >= 8 - kEmuPer8) ? exp2_poly(x0) : ex2(x0);
-          const float p1 = (((col + 1) & 7) >= 8 - kEmuPer8) ? exp2_poly(x1) : ex2(x1);
-          rs[e & 3] += p0 + p1;
+          const float2 xx = __ffma2_rn(make_float2(s[col], s[col + 1]), sc2, nm2);
+          const float p0 = ((col & 7) >= 8 - kEmuPer8<D>) ? exp2_poly(xx.x) : ex2(xx.x);
+          const float p1 = (((col + 1) & 7) >= 8 - kEmuPer8<D>) ? exp2_poly(xx.y) : ex2(xx.y);
+          rs[e & 1] = __fadd2_rn(rs[e & 1], make_float2(p0, p1));
           pk[e] = pack_bf16x2(p0, p1);
         }
         tmem_st16(t_s + q * 16, pk);
       }
-      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      l += (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
 
       if (i > 0 && __any_sync(0xffffffffu, resc)) {  // O_X is stable: P V of tile i-1 is done
 #pragma unroll
