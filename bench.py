@@ -337,8 +337,8 @@ def run_decode(args, dev, stream, hbm, peak_src):
             "step_us_median": round(1e3 * statistics.median(step_ms), 2),
             "tokens_per_s": round(B / (statistics.median(step_ms) * 1e-3), 1),
             "bytes_per_step_mean": int(statistics.mean(bytes_step)),
-            "steps_timed": steps - warm, "kernels": ["decode_split_kernel<128,4>",
-                                                     "decode_combine_kernel<128,4>"]}
+            "steps_timed": steps - warm,
+            "kernels": ["decode_split_kernel<128,4> (split-KV with the merge fused in)"]}
 
 
 def run_e2e(args, dev, stream, w, sets, cu, q_pos, step_flops, num_pages):

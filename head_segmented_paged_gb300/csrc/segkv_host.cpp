@@ -618,8 +618,15 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
 }
 
 // ---------------------------------------------------------------- decode
-static int64_t decode_units_bound(const segkv* h, int n_seqs) {
-  return int64_t(n_seqs) * h->Hkv * ((h->max_len + kDecodeChunk - 1) / kDecodeChunk + 1);
+// Split units: at most one per (sequence, KV head) pair plus one per CTA slice
+// boundary.
+static int decode_max_grid(const segkv* h) { return h->num_sms > 0 ? 2 * h->num_sms : 1024; }
+
+static size_t decode_ws_bytes(const segkv* h, int64_t units, int64_t pairs, size_t* acc_bytes,
+                              size_t* ml_bytes) {
+  *acc_bytes = align_up(static_cast<size_t>(units) * h->G * h->D * 4, 256);
+  *ml_bytes = align_up(static_cast<size_t>(units) * h->G * 2 * 4, 256);
+  return *acc_bytes + *ml_bytes + align_up(static_cast<size_t>(pairs) * 4, 256);
 }
 
 int segkv_workspace_size(segkv_t h, int kind, int64_t n_tokens, int n_seqs, size_t* bytes) {
@@ -630,9 +637,9 @@ int segkv_workspace_size(segkv_t h, int kind, int64_t n_tokens, int n_seqs, size
     return SEGKV_OK;
   }
   if (kind != SEGKV_WS_DECODE) return fail(h, SEGKV_ERR_INVALID_ARG, "bad workspace kind");
-  const int64_t u = decode_units_bound(h, n_seqs);
-  *bytes = align_up(static_cast<size_t>(u) * h->G * h->D * 4, 256) +
-           align_up(static_cast<size_t>(u) * h->G * 2 * 4, 256);
+  const int64_t pairs = int64_t(n_seqs) * h->Hkv;
+  size_t a, m;
+  *bytes = decode_ws_bytes(h, pairs + decode_max_grid(h), pairs, &a, &m);
   return SEGKV_OK;
 }
 
@@ -648,8 +655,10 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
   if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(o)) & 15)
     return fail(h, SEGKV_ERR_INVALID_ARG, "q and o must be 16-byte aligned");
   const int W = h->win[layer];
-  std::vector<DecodeUnit> units;
-  std::vector<DecodePair> pairs;
+  // pairs (req, head) with their key ranges [lo, n)
+  struct Range { int32_t req, head, lo, n, row; };
+  std::vector<Range> ranges;
+  int64_t total = 0;
   for (int i = 0; i < n; ++i) {
     const int b = seq_ids[i];
     const int32_t nlen = h->len[h->lidx(layer, b)];
@@ -661,22 +670,48 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
       const int32_t lo = h->local(layer, hd) ? std::max(0, p - W + 1) : 0;
       if (lo < h->start[h->seg(layer, hd, b)])
         return fail(h, SEGKV_ERR_EVICTED, "seq %d head %d: key %d already evicted", b, hd, lo);
-      DecodePair pr{static_cast<int32_t>(units.size()), 0, i, hd};
-      for (int32_t c = lo / kDecodeChunk; c <= p / kDecodeChunk; ++c) {
-        DecodeUnit u{};
-        u.req = i;
-        u.head = hd;
-        u.k0 = std::max(lo, c * kDecodeChunk);
-        u.k1 = std::min(nlen, (c + 1) * kDecodeChunk);
-        u.table_row = static_cast<int32_t>(h->seg(layer, hd, b));
-        units.push_back(u);
-        ++pr.n_units;
-      }
-      pairs.push_back(pr);
+      ranges.push_back({i, hd, lo, nlen, static_cast<int32_t>(h->seg(layer, hd, b))});
+      total += nlen - lo;
     }
   }
-  const size_t acc_bytes = align_up(units.size() * h->G * h->D * 4, 256);
-  const size_t need = acc_bytes + align_up(units.size() * h->G * 2 * 4, 256);
+  // stream-K split: CTA c streams keys [c*per, (c+1)*per) of the concatenated ranges
+  const int64_t sk = decode_stage_keys(h->G);
+  const int grid = static_cast<int>(std::max<int64_t>(
+      1, std::min<int64_t>(decode_max_grid(h), (total + sk - 1) / sk)));
+  const int64_t per = (total + grid - 1) / grid;
+  std::vector<DecodeUnit> units;
+  std::vector<DecodePair> pairs(ranges.size());
+  std::vector<int32_t> cta_begin(grid + 1);
+  size_t r = 0;
+  int32_t off = 0;
+  for (int c = 0; c < grid; ++c) {
+    cta_begin[c] = static_cast<int32_t>(units.size());
+    int64_t left = (c + 1 == grid) ? total : per;
+    while (left > 0 && r < ranges.size()) {
+      const Range& R = ranges[r];
+      const int32_t take = static_cast<int32_t>(std::min<int64_t>(left, R.n - R.lo - off));
+      if (off == 0) pairs[r] = {static_cast<int32_t>(units.size()), 0, R.req, R.head};
+      DecodeUnit u{};
+      u.req = R.req;
+      u.head = R.head;
+      u.k0 = R.lo + off;
+      u.k1 = R.lo + off + take;
+      u.table_row = R.row;
+      u.pair = static_cast<int32_t>(r);
+      units.push_back(u);
+      ++pairs[r].n_units;
+      off += take;
+      left -= take;
+      if (off == R.n - R.lo) {
+        ++r;
+        off = 0;
+      }
+    }
+  }
+  cta_begin[grid] = static_cast<int32_t>(units.size());
+  size_t acc_bytes, ml_bytes;
+  const size_t need = decode_ws_bytes(h, static_cast<int64_t>(units.size()),
+                                      static_cast<int64_t>(pairs.size()), &acc_bytes, &ml_bytes);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return fail(h, SEGKV_ERR_INVALID_ARG, "workspace needs %zu bytes (256-aligned), got %zu", need,
                 workspace_bytes);
@@ -684,18 +719,24 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
   Pack pk;
   const size_t o_units = pk.add(units.data(), units.size());
   const size_t o_pairs = pk.add(pairs.data(), pairs.size());
+  const size_t o_cta = pk.add(cta_begin.data(), cta_begin.size());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  size_t off;
-  cudaError_t e = h->ring.reserve(pk.buf.size(), &off);
+  size_t off_ring;
+  cudaError_t e = h->ring.reserve(pk.buf.size(), &off_ring);
   if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
-  std::memcpy(h->ring.host + off, pk.buf.data(), pk.buf.size());
-  e = cudaMemcpyAsync(h->ring.dev + off, h->ring.host + off, pk.buf.size(), cudaMemcpyHostToDevice, s);
+  std::memcpy(h->ring.host + off_ring, pk.buf.data(), pk.buf.size());
+  e = cudaMemcpyAsync(h->ring.dev + off_ring, h->ring.host + off_ring, pk.buf.size(),
+                      cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpyAsync(decode plan)");
   h->upload_bytes += static_cast<int64_t>(pk.buf.size());
-  uint8_t* d = h->ring.dev + off;
+  int* cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + acc_bytes + ml_bytes);
+  e = cudaMemsetAsync(cnt, 0, pairs.size() * sizeof(int), s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemsetAsync(pair counters)");
+  uint8_t* d = h->ring.dev + off_ring;
   DecodeParams p{};
   p.units = reinterpret_cast<const DecodeUnit*>(d + o_units);
   p.pairs = reinterpret_cast<const DecodePair*>(d + o_pairs);
+  p.cta_begin = reinterpret_cast<const int32_t*>(d + o_cta);
   p.q = q;
   p.o = o;
   p.table = h->d_table;
@@ -703,6 +744,7 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
   p.vpool = h->vpool;
   p.part_acc = static_cast<float*>(workspace);
   p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + acc_bytes);
+  p.pair_cnt = cnt;
   p.n_units = static_cast<int>(units.size());
   p.n_pairs = static_cast<int>(pairs.size());
   p.R = h->R;
@@ -712,10 +754,9 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
   p.scale_log2 = h->scale * 1.4426950408889634f;
   p.status = h->d_status;
   p.timeout_ns = kTimeoutNs;
-  const int grid = static_cast<int>(std::min<int64_t>(units.size(), int64_t(h->num_sms) * 2));
   e = launch_decode(p, h->D, grid, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "decode kernel launch");
-  e = h->ring.commit(off, pk.buf.size(), s);
+  e = h->ring.commit(off_ring, pk.buf.size(), s);
   if (e != cudaSuccess) return cuda_fail(h, e, "event record");
   return SEGKV_OK;
 }
@@ -831,19 +872,9 @@ namespace skv {
 size_t decode_partials_bytes(segkv* h, int layer, const int32_t* seq_lens,
                              const int32_t* seq_ids, int n) {
   if (!h || layer < 0 || layer >= h->L || !seq_lens || !ids_valid(h, seq_ids, n)) return 0;
-  const int W = h->win[layer];
-  int64_t units = 0;
-  for (int i = 0; i < n; ++i) {
-    const int32_t nlen = seq_lens[i];
-    if (nlen < 1) return 0;
-    const int32_t p = nlen - 1;
-    for (int hd = 0; hd < h->Hkv; ++hd) {
-      const int32_t lo = h->local(layer, hd) ? std::max(0, p - W + 1) : 0;
-      units += p / kDecodeChunk - lo / kDecodeChunk + 1;
-    }
-  }
-  return align_up(static_cast<size_t>(units) * h->G * h->D * 4, 256) +
-         align_up(static_cast<size_t>(units) * h->G * 2 * 4, 256);
+  const int64_t pairs = int64_t(n) * h->Hkv;
+  size_t a, m;
+  return decode_ws_bytes(h, pairs + decode_max_grid(h), pairs, &a, &m);
 }
 
 int set_error(segkv* h, int code, const char* msg) { return fail(h, code, "%s", msg); }

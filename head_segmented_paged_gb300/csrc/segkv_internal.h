@@ -11,8 +11,6 @@ namespace skv {
 
 constexpr int kKeyTile = 128;     // prefill: keys per tile (one MMA N)
 constexpr int kRowsPerTile = 128; // prefill: query rows per tile (MMA M)
-constexpr int kDecodeChunk = 512; // decode: keys per split unit
-constexpr int kDecodeStageKeys = 64;
 
 // ---- append -------------------------------------------------------------
 struct AppendSeq {
@@ -81,7 +79,8 @@ struct DecodeUnit {
   int32_t head;        // KV head
   int32_t k0, k1;      // keys [k0, k1)
   int32_t table_row;
-  int32_t pad[3];
+  int32_t pair;        // index of its (req, head) pair
+  int32_t pad[2];
 };
 struct DecodePair {
   int32_t unit0;   // first unit of this (req, head)
@@ -90,15 +89,17 @@ struct DecodePair {
   int32_t head;
 };
 struct DecodeParams {
-  const DecodeUnit* units;
+  const DecodeUnit* units;   // grouped by CTA
   const DecodePair* pairs;
-  const void* q;          // bf16 [n, Hq, D]
-  void* o;                // bf16 [n, Hq, D]
+  const int32_t* cta_begin;  // [grid + 1]: CTA c runs units cta_begin[c] .. cta_begin[c+1]-1
+  const void* q;             // bf16 [n, Hq, D]
+  void* o;                   // bf16 [n, Hq, D]
   const int32_t* table;
   const void* kpool;
   const void* vpool;
-  float* part_acc;        // [n_units, G, D]
-  float* part_ml;         // [n_units, G, 2]
+  float* part_acc;           // [n_units, G, D]
+  float* part_ml;            // [n_units, G, 2]
+  int* pair_cnt;             // [n_pairs], zero before the launch
   int n_units, n_pairs;
   int R, hq, G, page_size;
   float scale_log2;
@@ -112,5 +113,6 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const 
 int prefill_smem_bytes(int head_dim);
 int prefill_unit_tokens(int G);  // query tokens per prefill work unit
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, int grid, cudaStream_t s);
+int decode_stage_keys(int G);  // keys per decode pipeline stage
 
 }  // namespace skv

@@ -208,15 +208,16 @@ const char* segkv_last_error(segkv_t h);
  * choice of the library.
  *   The split partials live in a fixed device array inside the library,
  *   SEGKV_NOALLOC_SCRATCH_BYTES (8 MiB) per GPU, held by every GPU that loads
- *   the library until the process exits. A call whose partials would not fit
- *   (about 4000 split units at G=4, D=128; units are 512-key chunks of each
- *   (sequence, KV head)) returns SEGKV_ERR_INVALID_ARG with a message; use
- *   segkv_decode_attn then.
+ *   the library until the process exits. A call whose partials could exceed
+ *   it (a decode plan has at most n*Hkv + 2*SMs split units of G*(D+2)*4
+ *   bytes each: about 3,700 (sequence, KV head) pairs at G=4, D=128) returns
+ *   SEGKV_ERR_INVALID_ARG with a message; use segkv_decode_attn then.
  *   The call allocates no memory. Its first call on a device looks up the
  *   array's device address (cudaGetSymbolAddress) with the handle's device
  *   current, so make that first call before any stream capture.
  *   Every call shares the one array: calls that overlap on the GPU (other
- *   streams, other handles) race. Nothing in it needs clearing between calls.
+ *   streams, other handles) race. The caller clears nothing: each call
+ *   resets, on its stream, the counters it keeps there.
  *   Other arguments, errors and results are those of segkv_decode_attn; the
  *   handle's device must be the current device.
  */

@@ -44,22 +44,22 @@ def test_noalloc_decode_matches_workspace_decode_on_consecutive_calls():
 
 
 def test_noalloc_decode_refuses_plans_beyond_its_scratch():
-    hkv, G, d, P, n, B = 8, 4, 128, 128, 32768, 8
-    hc = [[I.GLOBAL] * 8]
-    pages = B * hkv * (n // P) + 8
-    kp = torch.zeros((pages, P, d), dtype=torch.bfloat16, device="cuda")
+    # 512 one-token sequences x 8 KV heads: up to 4096 + 2*SMs split units of
+    # 2 KiB each, more than the 8 MiB the entry point holds.
+    hkv, G, d, P, B = 8, 4, 128, 16, 512
+    hc = [[I.GLOBAL] + [I.LOCAL] * 7]
+    kp = torch.zeros((B * hkv + 8, P, d), dtype=torch.bfloat16, device="cuda")
     vp = torch.zeros_like(kp)
-    h = S.SegKV(1, hkv * G, hkv, d, hc, [n], P, B, n, kp, vp)
-    kv = torch.zeros((n, hkv, d), dtype=torch.bfloat16, device="cuda")
-    for b in range(B):
-        h.append(0, kv, kv, [0, n], [b])
+    h = S.SegKV(1, hkv * G, hkv, d, hc, [64], P, B, 64, kp, vp)
+    kv = torch.zeros((B, hkv, d), dtype=torch.bfloat16, device="cuda")
+    h.append(0, kv, kv, list(range(B + 1)), list(range(B)))
     q = torch.zeros((B, hkv * G, d), dtype=torch.bfloat16, device="cuda")
     o = torch.empty_like(q)
-    # 8 sequences x 8 heads x 64 chunks of 512 keys: 4096 units, over 8 MiB
-    rc = S.segkv_decode_attn_noalloc(h.handle, 0, q, [n] * B, list(range(B)), o)
+    rc = S.segkv_decode_attn_noalloc(h.handle, 0, q, [1] * B, list(range(B)), o)
     assert rc == S.SEGKV_ERR_INVALID_ARG
     assert "no-alloc" in S.segkv_last_error(h.handle)
     # a smaller call on the same handle still works
-    assert S.segkv_decode_attn_noalloc(h.handle, 0, q[:2], [n] * 2, [0, 1], o[:2]) == 0
+    assert S.segkv_decode_attn_noalloc(h.handle, 0, q[:64], [1] * 64, list(range(64)),
+                                       o[:64]) == 0
     assert h.status() == 0
     h.close()
