@@ -8,14 +8,16 @@
 // sequence is cut into equal slices, one per CTA, so every CTA streams the
 // same number of K/V bytes; a slice may hold the tail of one (sequence, head)
 // pair and the head of the next. In each CTA a producer lane streams page
-// runs into a 3-stage shared-memory ring with bulk copies. Four consumer
-// warps each own a fixed quarter of every stage and keep their own online
-// softmax state, so a stage needs no block-wide synchronisation:
-//   scores: 16-byte K row reads, packed f32x2 FMAs for the G query heads that
-//           share the KV head, a 16-lane reduce-scatter;
+// runs into a 4-stage shared-memory ring with bulk copies. Six consumer
+// warps (four when G != 4) each own a fixed share of every stage and keep their
+// own online softmax state, so a stage needs no block-wide synchronisation:
+//   scores: 16-byte K chunk reads (lane i of a group of 8 takes chunks i and
+//           i+8 of a row, so every read is free of bank conflicts), packed
+//           f32x2 FMAs for the G query heads that share the KV head, an
+//           8-lane reduce-scatter;
 //   softmax: max and sum over the lanes holding one head (shuffles);
 //   P V:    8-byte V row reads, packed f32x2 FMAs into per-lane accumulators.
-// At the end of a slice the four warps merge in shared memory. A pair that
+// At the end of a slice the warps merge in shared memory. A pair that
 // lies inside one slice writes O directly; otherwise each slice writes fp32
 // partials and the last slice to finish (an atomic count per pair) merges
 // them and writes O.
@@ -29,64 +31,54 @@ using namespace ptx;
 
 namespace {
 
-constexpr int kConsumers = 128;
-constexpr int kThreadsSplit = kConsumers + 32;
-constexpr int NS = 3;
+constexpr int NS = 4;
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 
 template <int D, int G>
 struct DCfg {
-  static constexpr int KW = (32 / G > 16) ? 32 / G : 16;  // keys per consumer warp per stage
-  static constexpr int SK = 4 * KW;                       // keys per stage
-  static constexpr int KPG = 16 / G;                      // keys per half-warp per round
-  static constexpr int ROUNDS = KW / (2 * KPG);
-  static constexpr int DPL = D / 16;                      // score dims per lane
-  static constexpr int DPV = D / 32;                      // P V dims per lane
+  static constexpr int NW = G == 4 ? 6 : 4;               // consumer warps
+  static constexpr int THREADS = 32 * (NW + 1);            // + one producer warp
+  static constexpr int LG = G > 8 ? G : 8;                 // lanes per score group
+  static constexpr int KPG = LG / G;                       // keys per group per round
+  static constexpr int KR = (32 / LG) * KPG;               // keys per warp per round (= 32/G)
+  static constexpr int KW = KR > 8 ? KR : 8;               // keys per consumer warp per stage
+  static constexpr int ROUNDS = KW / KR;
+  static constexpr int SK = NW * KW;                       // keys per stage
+  static constexpr int DPL = D / LG;                       // score dims per lane
+  static constexpr int DPV = D / 32;                       // P V dims per lane
   static constexpr int ROW = D * 2;
-  static constexpr int STAGE = SK * ROW;                  // bytes of K (or V) per stage
+  static constexpr int STAGE = SK * ROW;                   // bytes of K (or V) per stage
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NS * STAGE;
-  static constexpr int OFF_P = OFF_V + NS * STAGE;        // float [4][KW][G]
-  static constexpr int OFF_MRG = OFF_P + 4 * KW * G * 4;  // float [4][G][D]
-  static constexpr int OFF_ML = OFF_MRG + 4 * G * D * 4;  // float [4][G][2]
-  static constexpr int OFF_BAR = (OFF_ML + 4 * G * 2 * 4 + 15) & ~15;
+  static constexpr int OFF_P = OFF_V + NS * STAGE;         // float [NW][KW][G]
+  static constexpr int OFF_MRG = OFF_P + NW * KW * G * 4;  // float [NW/2][G][D]
+  static constexpr int OFF_ML = OFF_MRG + (NW / 2) * G * D * 4;  // float [NW/2][G][2]
+  static constexpr int OFF_BAR = (OFF_ML + (NW / 2) * G * 2 * 4 + 15) & ~15;
   static constexpr int OFF_MISC = OFF_BAR + 2 * NS * 8;
   static constexpr int BYTES = OFF_MISC + 16;
+  // two CTAs per SM when their shared memory fits
+  static constexpr int MIN_BLOCKS = BYTES <= 110 * 1024 ? 2 : 1;
 };
 
+template <int N>
 __device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
 }
 
-// Sum 16 per-lane values over the 16 lanes of a half-warp; lane (sub) ends
-// with the total of value index sub.
-__device__ __forceinline__ float reduce_scatter16(float (&v)[16], int sub) {
+// Sum LG per-lane values over each group of LG consecutive lanes; lane
+// (lane % LG) ends with the total of value index lane % LG. Each level sends
+// the half of the values the partner keeps and adds the half it receives.
+template <int LG>
+__device__ __forceinline__ float reduce_scatter(float (&v)[LG], int sub) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const bool up = sub & 8;
-    const float send = up ? v[i] : v[i + 8];
-    const float keep = up ? v[i + 8] : v[i];
-    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-  }
+  for (int w = LG / 2; w >= 1; w >>= 1) {
+    const bool up = sub & w;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const bool up = sub & 4;
-    const float send = up ? v[i] : v[i + 4];
-    const float keep = up ? v[i + 4] : v[i];
-    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const bool up = sub & 2;
-    const float send = up ? v[i] : v[i + 2];
-    const float keep = up ? v[i + 2] : v[i];
-    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
-  }
-  {
-    const bool up = sub & 1;
-    const float send = up ? v[0] : v[1];
-    const float keep = up ? v[1] : v[0];
-    v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+    for (int i = 0; i < w; ++i) {
+      const float send = up ? v[i] : v[i + w];
+      const float keep = up ? v[i + w] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
   }
   return v[0];
 }
@@ -98,9 +90,12 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
 }  // namespace
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreadsSplit)
+__global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
     decode_split_kernel(const DecodeParams p) {
   using C = DCfg<D, G>;
+  constexpr int NCONS = 32 * C::NW;
+  constexpr int HALF = C::NW / 2;
+  constexpr int CPL = C::DPL >= 8 ? C::DPL / 8 : 1;  // 16-byte K chunks per lane
   extern __shared__ __align__(128) uint8_t sm[];
   const uint32_t sbase = smem_addr(sm);
   float* pbuf = reinterpret_cast<float*>(sm + C::OFF_P);
@@ -115,7 +110,7 @@ __global__ void __launch_bounds__(kThreadsSplit)
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), kConsumers / 32);
+      mbar_init(empty(s), C::NW);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -124,7 +119,7 @@ __global__ void __launch_bounds__(kThreadsSplit)
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
   const int u_begin = p.cta_begin[blockIdx.x], u_end = p.cta_begin[blockIdx.x + 1];
 
-  if (warp == kConsumers / 32) {
+  if (warp == C::NW) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int armed[NS];
@@ -163,31 +158,36 @@ __global__ void __launch_bounds__(kThreadsSplit)
   }
 
   // -------------------------------------------------------------- consumers
-  const int sub = lane & 15, half = lane >> 4;
+  const int sub = lane % C::LG, grp = lane / C::LG;
   const int g_own = lane % G;  // the query head whose softmax state this lane keeps
   float* my_p = pbuf + warp * C::KW * G;
   int gs = 0;
   for (int u = u_begin; u < u_end; ++u) {
     const DecodeUnit U = p.units[u];
-    // this lane's slice of the G query rows, pre-scaled to log2 units
+    // this lane's dims of the G query rows (chunks sub, sub+LG, ... of 8 dims,
+    // or 4 dims at sub*4 when D/LG = 4), pre-scaled to log2 units
     float2 q2[G][C::DPL / 2];
     {
       const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(p.q) +
-                                (static_cast<int64_t>(U.req) * p.hq + U.head * G) * D + sub * C::DPL;
+                                (static_cast<int64_t>(U.req) * p.hq + U.head * G) * D;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        uint32_t w[C::DPL / 2];
-        if constexpr (C::DPL == 8) {
-          const uint4 x = *reinterpret_cast<const uint4*>(qb + g * D);
-          w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
-        } else {
-          const uint2 x = *reinterpret_cast<const uint2*>(qb + g * D);
-          w[0] = x.x; w[1] = x.y;
-        }
+        if constexpr (C::DPL >= 8) {
 #pragma unroll
-        for (int e = 0; e < C::DPL / 2; ++e) {
-          const float2 f = bf16x2_to_float2(w[e]);
-          q2[g][e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
+          for (int c = 0; c < CPL; ++c) {
+            const uint4 x = *reinterpret_cast<const uint4*>(qb + g * D + (sub + C::LG * c) * 8);
+            const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 f = bf16x2_to_float2(w4[e]);
+              q2[g][c * 4 + e] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
+            }
+          }
+        } else {
+          const uint2 x = *reinterpret_cast<const uint2*>(qb + g * D + sub * 4);
+          const float2 f0 = bf16x2_to_float2(x.x), f1 = bf16x2_to_float2(x.y);
+          q2[g][0] = make_float2(f0.x * p.scale_log2, f0.y * p.scale_log2);
+          q2[g][1] = make_float2(f1.x * p.scale_log2, f1.y * p.scale_log2);
         }
       }
     }
@@ -213,19 +213,25 @@ __global__ void __launch_bounds__(kThreadsSplit)
         float sr[C::ROUNDS];
 #pragma unroll
         for (int r = 0; r < C::ROUNDS; ++r) {
-          const int key0 = mine0 + r * 2 * C::KPG + half * C::KPG;
-          float part[16];
+          const int key0 = mine0 + r * C::KR + grp * C::KPG;
+          float part[C::LG];
 #pragma unroll
           for (int kk = 0; kk < C::KPG; ++kk) {
-            const uint8_t* krow = sK + (key0 + kk) * C::ROW + sub * C::DPL * 2;
+            const uint8_t* krow = sK + (key0 + kk) * C::ROW;
             float2 k2[C::DPL / 2];
-            if constexpr (C::DPL == 8) {
-              const uint4 x = *reinterpret_cast<const uint4*>(krow);
-              k2[0] = bf16x2_to_float2(x.x); k2[1] = bf16x2_to_float2(x.y);
-              k2[2] = bf16x2_to_float2(x.z); k2[3] = bf16x2_to_float2(x.w);
+            if constexpr (C::DPL >= 8) {
+#pragma unroll
+              for (int c = 0; c < CPL; ++c) {
+                const uint4 x = *reinterpret_cast<const uint4*>(krow + (sub + C::LG * c) * 16);
+                k2[c * 4 + 0] = bf16x2_to_float2(x.x);
+                k2[c * 4 + 1] = bf16x2_to_float2(x.y);
+                k2[c * 4 + 2] = bf16x2_to_float2(x.z);
+                k2[c * 4 + 3] = bf16x2_to_float2(x.w);
+              }
             } else {
-              const uint2 x = *reinterpret_cast<const uint2*>(krow);
-              k2[0] = bf16x2_to_float2(x.x); k2[1] = bf16x2_to_float2(x.y);
+              const uint2 x = *reinterpret_cast<const uint2*>(krow + sub * 8);
+              k2[0] = bf16x2_to_float2(x.x);
+              k2[1] = bf16x2_to_float2(x.y);
             }
 #pragma unroll
             for (int g = 0; g < G; ++g) {
@@ -235,7 +241,7 @@ __global__ void __launch_bounds__(kThreadsSplit)
               part[kk * G + g] = a.x + a.y;
             }
           }
-          const float tot = reduce_scatter16(part, sub);
+          const float tot = reduce_scatter<C::LG>(part, sub);
           const int kidx = key0 + sub / G;
           sr[r] = (kidx >= vlo && kidx < vhi) ? tot : -INFINITY;
         }
@@ -253,8 +259,7 @@ __global__ void __launch_bounds__(kThreadsSplit)
         for (int r = 0; r < C::ROUNDS; ++r) {
           const float pr = ex2(sr[r] - msub);
           psum += pr;
-          const int kl = r * 2 * C::KPG + half * C::KPG + sub / G;
-          my_p[kl * G + g_own] = pr;
+          my_p[(r * C::KR + grp * C::KPG + sub / G) * G + g_own] = pr;
         }
 #pragma unroll
         for (int o = G; o < 32; o <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
@@ -269,8 +274,7 @@ __global__ void __launch_bounds__(kThreadsSplit)
 #pragma unroll
           for (int e = 0; e < C::DPV / 2; ++e) acc[g][e] = __fmul2_rn(acc[g][e], a2);
         }
-        const int kl0 = max(vlo - mine0, 0), kl1 = min(vhi - mine0, C::KW);
-        for (int kl = kl0; kl < kl1; ++kl) {
+        auto pv_key = [&](int kl) {
           const uint8_t* vrow = sV + (mine0 + kl) * C::ROW + lane * C::DPV * 2;
           float2 v2[C::DPV / 2];
           if constexpr (C::DPV == 4) {
@@ -287,6 +291,13 @@ __global__ void __launch_bounds__(kThreadsSplit)
 #pragma unroll
             for (int e = 0; e < C::DPV / 2; ++e) acc[g][e] = __ffma2_rn(pg, v2[e], acc[g][e]);
           }
+        };
+        const int kl0 = max(vlo - mine0, 0), kl1 = min(vhi - mine0, C::KW);
+        if (kl0 == 0 && kl1 == C::KW) {
+#pragma unroll
+          for (int kl = 0; kl < C::KW; ++kl) pv_key(kl);
+        } else {
+          for (int kl = kl0; kl < kl1; ++kl) pv_key(kl);
         }
         __syncwarp();
       }
@@ -294,30 +305,58 @@ __global__ void __launch_bounds__(kThreadsSplit)
     }
     if (!ok) break;
 
-    // merge the four warps' states
-    if (lane < G) {
-      mls[(warp * G + lane) * 2 + 0] = m;
-      mls[(warp * G + lane) * 2 + 1] = l;
+    // merge the warps' states: the upper half hands its state to the lower half,
+    // which folds it into its own, then every thread combines the lower half's
+    if (warp >= HALF) {
+      const int slot = warp - HALF;
+      if (lane < G) {
+        mls[(slot * G + lane) * 2 + 0] = m;
+        mls[(slot * G + lane) * 2 + 1] = l;
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int e = 0; e < C::DPV / 2; ++e)
+          *reinterpret_cast<float2*>(mrg + (slot * G + g) * D + lane * C::DPV + 2 * e) = acc[g][e];
     }
+    consumer_sync<NCONS>();
+    if (warp < HALF) {
+      const int slot = warp;
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+      for (int g = 0; g < G; ++g) {
+        const float m1 = __shfl_sync(0xffffffffu, m, g), l1 = __shfl_sync(0xffffffffu, l, g);
+        const float m2 = mls[(slot * G + g) * 2], l2 = mls[(slot * G + g) * 2 + 1];
+        const float M = fmaxf(m1, m2);
+        const float ms = (M == -INFINITY) ? 0.f : M;
+        const float a1 = ex2(m1 - ms), a2 = ex2(m2 - ms);
+        const float2 w1 = make_float2(a1, a1), w2 = make_float2(a2, a2);
 #pragma unroll
-      for (int e = 0; e < C::DPV / 2; ++e)
-        *reinterpret_cast<float2*>(mrg + (warp * G + g) * D + lane * C::DPV + 2 * e) = acc[g][e];
-    consumer_sync();
+        for (int e = 0; e < C::DPV / 2; ++e) {
+          float2* dst = reinterpret_cast<float2*>(mrg + (slot * G + g) * D + lane * C::DPV + 2 * e);
+          *dst = __ffma2_rn(acc[g][e], w1, __fmul2_rn(*dst, w2));
+        }
+        __syncwarp();
+        if (lane == 0) {
+          mls[(slot * G + g) * 2] = M;
+          mls[(slot * G + g) * 2 + 1] = l1 * a1 + l2 * a2;
+        }
+      }
+    }
+    consumer_sync<NCONS>();
     const DecodePair pr = p.pairs[U.pair];
     const bool single = pr.n_units == 1;
     __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) +
                           (static_cast<int64_t>(pr.req) * p.hq + pr.head * G) * D;
-    for (int idx = tid; idx < G * D; idx += kConsumers) {
+    for (int idx = tid; idx < G * D; idx += NCONS) {
       const int g = idx / D, d = idx - g * D;
       float M = -INFINITY;
 #pragma unroll
-      for (int x = 0; x < 4; ++x) M = fmaxf(M, mls[(x * G + g) * 2]);
+      for (int x = 0; x < HALF; ++x) M = fmaxf(M, mls[(x * G + g) * 2]);
+      const float ms = (M == -INFINITY) ? 0.f : M;
       float Ls = 0.f, o = 0.f;
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        const float wgt = ex2(mls[(x * G + g) * 2] - M);
+      for (int x = 0; x < HALF; ++x) {
+        const float wgt = ex2(mls[(x * G + g) * 2] - ms);
         Ls = fmaf(wgt, mls[(x * G + g) * 2 + 1], Ls);
         o = fmaf(wgt, mrg[(x * G + g) * D + d], o);
       }
@@ -333,12 +372,12 @@ __global__ void __launch_bounds__(kThreadsSplit)
     }
     if (!single) {
       __threadfence();
-      consumer_sync();
+      consumer_sync<NCONS>();
       if (tid == 0) *last_flag = atomicAdd(p.pair_cnt + U.pair, 1) == pr.n_units - 1;
-      consumer_sync();
+      consumer_sync<NCONS>();
       if (*last_flag) {
         __threadfence();
-        for (int idx = tid; idx < G * D; idx += kConsumers) {
+        for (int idx = tid; idx < G * D; idx += NCONS) {
           const int g = idx / D, d = idx - g * D;
           float M = -INFINITY;
           for (int c = 0; c < pr.n_units; ++c)
@@ -354,7 +393,7 @@ __global__ void __launch_bounds__(kThreadsSplit)
         }
       }
     }
-    consumer_sync();  // merge buffers are free again
+    consumer_sync<NCONS>();  // merge buffers are free again
   }
 }
 
@@ -364,7 +403,7 @@ static cudaError_t launch_dg(const DecodeParams& p, int grid, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
   if (e != cudaSuccess) return e;
-  decode_split_kernel<D, G><<<grid, kThreadsSplit, C::BYTES, s>>>(p);
+  decode_split_kernel<D, G><<<grid, C::THREADS, C::BYTES, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -380,7 +419,15 @@ static cudaError_t launch_d(const DecodeParams& p, int grid, cudaStream_t s) {
   }
 }
 
-int decode_stage_keys(int G) { return G == 1 ? 128 : 64; }
+int decode_stage_keys(int G) {
+  switch (G) {
+    case 1: return DCfg<128, 1>::SK;
+    case 2: return DCfg<128, 2>::SK;
+    case 4: return DCfg<128, 4>::SK;
+    case 8: return DCfg<128, 8>::SK;
+    default: return DCfg<128, 16>::SK;
+  }
+}
 
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, int grid, cudaStream_t s) {
   return head_dim == 64 ? launch_d<64>(p, grid, s) : launch_d<128>(p, grid, s);
