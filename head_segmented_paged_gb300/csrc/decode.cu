@@ -120,39 +120,47 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
   const int u_begin = p.cta_begin[blockIdx.x], u_end = p.cta_begin[blockIdx.x + 1];
 
   if (warp == C::NW) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int armed[NS];
-      for (int s = 0; s < NS; ++s) armed[s] = -1;
-      bool ok = true;
-      int gs = 0;
-      for (int u = u_begin; ok && u < u_end; ++u) {
-        const DecodeUnit U = p.units[u];
-        const int32_t* trow = p.table + static_cast<int64_t>(U.table_row) * p.R;
-        for (int w = U.k0 / C::SK; w <= (U.k1 - 1) / C::SK; ++w, ++gs) {
-          const int st = gs % NS;
-          const uint32_t ph = (gs / NS) & 1;
-          if (!wait1(empty(st), ph ^ 1, wc)) { ok = false; break; }
-          const int vlo = max(U.k0, w * C::SK), vhi = min(U.k1, w * C::SK + C::SK);
-          mbar_expect_tx(full(st), static_cast<uint32_t>((vhi - vlo) * C::ROW * 2));
-          armed[st] = static_cast<int>(ph);
-          for (int pos = vlo; pos < vhi;) {
-            const int k = pos / p.page_size;
-            const int pend = min(vhi, (k + 1) * p.page_size);
+    // The whole warp runs the loop: its lanes fetch 32 block-table entries at
+    // a time (one coalesced load instead of a dependent load per page run) and
+    // lane 0 issues the copies.
+    int armed[NS];
+    for (int s = 0; s < NS; ++s) armed[s] = -1;
+    bool ok = true;
+    int gs = 0;
+    for (int u = u_begin; ok && u < u_end; ++u) {
+      const DecodeUnit U = p.units[u];
+      const int32_t* trow = p.table + static_cast<int64_t>(U.table_row) * p.R;
+      int kbase = -(1 << 30), my_id = 0;
+      for (int w = U.k0 / C::SK; w <= (U.k1 - 1) / C::SK; ++w, ++gs) {
+        const int st = gs % NS;
+        const uint32_t ph = (gs / NS) & 1;
+        if (!waitw(empty(st), ph ^ 1, wc)) { ok = false; break; }
+        const int vlo = max(U.k0, w * C::SK), vhi = min(U.k1, w * C::SK + C::SK);
+        if (lane == 0) mbar_expect_tx(full(st), static_cast<uint32_t>((vhi - vlo) * C::ROW * 2));
+        armed[st] = static_cast<int>(ph);
+        for (int pos = vlo; pos < vhi;) {
+          const int k = pos / p.page_size;
+          if (k >= kbase + 32) {
+            kbase = k;
+            my_id = (k + lane < p.R) ? trow[k + lane] : 0;
+          }
+          const int id = __shfl_sync(0xffffffffu, my_id, k - kbase);
+          const int pend = min(vhi, (k + 1) * p.page_size);
+          if (lane == 0) {
             const int64_t src =
-                (static_cast<int64_t>(trow[k]) * p.page_size + (pos - k * p.page_size)) * C::ROW;
+                (static_cast<int64_t>(id) * p.page_size + (pos - k * p.page_size)) * C::ROW;
             const uint32_t dst = st * C::STAGE + (pos - w * C::SK) * C::ROW;
             const uint32_t n = static_cast<uint32_t>((pend - pos) * C::ROW);
             bulk_g2s(sbase + C::OFF_K + dst, static_cast<const uint8_t*>(p.kpool) + src, n, full(st));
             bulk_g2s(sbase + C::OFF_V + dst, static_cast<const uint8_t*>(p.vpool) + src, n, full(st));
-            pos = pend;
           }
+          pos = pend;
         }
       }
-      if (!ok)
-        for (int s = 0; s < NS; ++s)
-          if (armed[s] >= 0) wait_drain(full(s), armed[s], kDrainNs);
     }
+    if (!ok && lane == 0)
+      for (int s = 0; s < NS; ++s)
+        if (armed[s] >= 0) wait_drain(full(s), armed[s], kDrainNs);
     __syncwarp();
     return;
   }

@@ -15,7 +15,8 @@
 //
 // Warp roles (320 threads, one CTA per SM, persistent over an LPT-sorted
 // unit list):
-//   warp 0      TMA producer: Q tiles A and B, then K and V tiles (2 stages);
+//   warp 0      TMA producer: Q tiles A and B, then K and V tiles (2 stages),
+//               block-table entries fetched 32 at a time by the whole warp;
 //   warp 1      TMEM owner and MMA issuer: S_X = Q_X K^T (X = A, B) into TMEM,
 //               then O_X += P_X V with P_X read back from TMEM;
 //   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B (one thread
@@ -94,9 +95,12 @@ struct Ctx {
 };
 
 // ---------------------------------------------------------------- producer
+// Run by the whole warp: lanes fetch 32 block-table entries at a time (one
+// coalesced load instead of a dependent load per key tile); lane 0 issues the
+// TMA copies.
 template <int D>
 __device__ void producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const CUtensorMap* tmv,
-                         const PrefillParams& p, const Ctx& c) {
+                         const PrefillParams& p, const Ctx& c, int lane) {
   using L = Layout<D>;
   constexpr int NC = D / 64;
   const int box_rows = p.page_size <= BN ? p.page_size : BN;
@@ -107,36 +111,49 @@ __device__ void producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const C
   for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++ui) {
     const PrefillUnit U = p.units[u];
     for (int x = 0; x < 2; ++x) {
-      if (!wait1(c.bar(B_Q_EMPTY + x), (ui & 1) ^ 1, c.wc)) { ok = false; break; }
-      mbar_expect_tx(c.bar(B_Q_FULL + x), L::Q_BYTES);
-      for (int cc = 0; cc < NC; ++cc)
-        tma_load_3d(c.sbase + L::OFF_Q + x * L::Q_BYTES + cc * kAtom, tmq, cc * 64, U.head * p.G,
-                    U.tok0 + x * p.tpt, c.bar(B_Q_FULL + x));
+      if (!waitw(c.bar(B_Q_EMPTY + x), (ui & 1) ^ 1, c.wc)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_expect_tx(c.bar(B_Q_FULL + x), L::Q_BYTES);
+        for (int cc = 0; cc < NC; ++cc)
+          tma_load_3d(c.sbase + L::OFF_Q + x * L::Q_BYTES + cc * kAtom, tmq, cc * 64,
+                      U.head * p.G, U.tok0 + x * p.tpt, c.bar(B_Q_FULL + x));
+      }
       armed_q[x] = ui & 1;
     }
     if (!ok) break;
     const int32_t* trow = p.table + static_cast<int64_t>(U.table_row) * p.R;
+    int kbase = -(1 << 30), my_id = 0;
     for (int kt = U.kt0; kt <= U.kt1; ++kt, ++g) {
       const int st = g & 1;
       const uint32_t ph = (g >> 1) & 1;
-      if (!wait1(c.bar(B_KV_EMPTY + st), ph ^ 1, c.wc)) { ok = false; break; }
-      mbar_expect_tx(c.bar(B_K_FULL + st), L::KV_BYTES);
-      mbar_expect_tx(c.bar(B_V_FULL + st), L::KV_BYTES);
+      if (!waitw(c.bar(B_KV_EMPTY + st), ph ^ 1, c.wc)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_expect_tx(c.bar(B_K_FULL + st), L::KV_BYTES);
+        mbar_expect_tx(c.bar(B_V_FULL + st), L::KV_BYTES);
+      }
       armed_kv[st] = static_cast<int>(ph);
       for (int bi = 0; bi < boxes; ++bi) {
         const int pos = kt * BN + bi * box_rows;
         const int k = pos / p.page_size;
         int y = p.oob_row;  // zero fill: page not held by this segment
-        if (k >= U.first_page && k <= U.last_page) y = trow[k] * p.page_size + (pos - k * p.page_size);
-        const uint32_t off = st * L::KV_BYTES + bi * box_rows * 128;
-        for (int cc = 0; cc < NC; ++cc) {
-          tma_load_2d(c.sbase + L::OFF_K + off + cc * kAtom, tmk, cc * 64, y, c.bar(B_K_FULL + st));
-          tma_load_2d(c.sbase + L::OFF_V + off + cc * kAtom, tmv, cc * 64, y, c.bar(B_V_FULL + st));
+        if (k >= U.first_page && k <= U.last_page) {
+          if (k >= kbase + 32) {
+            kbase = k;
+            my_id = (k + lane < p.R) ? trow[k + lane] : 0;
+          }
+          y = __shfl_sync(0xffffffffu, my_id, k - kbase) * p.page_size + (pos - k * p.page_size);
+        }
+        if (lane == 0) {
+          const uint32_t off = st * L::KV_BYTES + bi * box_rows * 128;
+          for (int cc = 0; cc < NC; ++cc) {
+            tma_load_2d(c.sbase + L::OFF_K + off + cc * kAtom, tmk, cc * 64, y, c.bar(B_K_FULL + st));
+            tma_load_2d(c.sbase + L::OFF_V + off + cc * kAtom, tmv, cc * 64, y, c.bar(B_V_FULL + st));
+          }
         }
       }
     }
   }
-  if (!ok) {  // aborting: let our own copies land before the block exits
+  if (!ok && lane == 0) {  // aborting: let our own copies land before the block exits
     for (int x = 0; x < 2; ++x)
       if (armed_q[x] >= 0) wait_drain(c.bar(B_Q_FULL + x), armed_q[x], kDrainNs);
     for (int st = 0; st < 2; ++st)
@@ -426,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   c.wc.limit_ns = p.timeout_ns;
 
   if (warp == 0) {
-    if (lane == 0) producer<D>(&tmq, &tmk, &tmv, p, c);
+    producer<D>(&tmq, &tmk, &tmv, p, c, lane);
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) mma_issuer<D>(p, c);
