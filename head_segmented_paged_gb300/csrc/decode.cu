@@ -53,7 +53,9 @@ struct DCfg {
   static constexpr int OFF_P = OFF_V + NS * STAGE;         // float [NW][KW][G]
   static constexpr int OFF_MRG = OFF_P + NW * KW * G * 4;  // float [NW/2][G][D]
   static constexpr int OFF_ML = OFF_MRG + (NW / 2) * G * D * 4;  // float [NW/2][G][2]
-  static constexpr int OFF_BAR = (OFF_ML + (NW / 2) * G * 2 * 4 + 15) & ~15;
+  static constexpr int OFF_META = (OFF_ML + (NW / 2) * G * 2 * 4 + 31) & ~31;  // DecodeUnit [NS]
+  static constexpr int OFF_QB = OFF_META + NS * 32;                            // bf16 [NS][G][D]
+  static constexpr int OFF_BAR = (OFF_QB + NS * G * D * 2 + 15) & ~15;
   static constexpr int OFF_MISC = OFF_BAR + 2 * NS * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   // two CTAs per SM when their shared memory fits
@@ -136,7 +138,20 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
         const uint32_t ph = (gs / NS) & 1;
         if (!waitw(empty(st), ph ^ 1, wc)) { ok = false; break; }
         const int vlo = max(U.k0, w * C::SK), vhi = min(U.k1, w * C::SK + C::SK);
-        if (lane == 0) mbar_expect_tx(full(st), static_cast<uint32_t>((vhi - vlo) * C::ROW * 2));
+        const bool first = (w == U.k0 / C::SK);
+        if (lane == 0) {
+          uint32_t bytes = static_cast<uint32_t>((vhi - vlo) * C::ROW * 2);
+          if (first) {  // the unit's descriptor and its G query rows travel with its first stage
+            *reinterpret_cast<DecodeUnit*>(sm + C::OFF_META + st * 32) = U;
+            bytes += G * D * 2;
+          }
+          mbar_expect_tx(full(st), bytes);
+          if (first)
+            bulk_g2s(sbase + C::OFF_QB + st * G * D * 2,
+                     static_cast<const __nv_bfloat16*>(p.q) +
+                         (static_cast<int64_t>(U.req) * p.hq + U.head * G) * D,
+                     G * D * 2, full(st));
+        }
         armed[st] = static_cast<int>(ph);
         for (int pos = vlo; pos < vhi;) {
           const int k = pos / p.page_size;
@@ -171,13 +186,15 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
   float* my_p = pbuf + warp * C::KW * G;
   int gs = 0;
   for (int u = u_begin; u < u_end; ++u) {
-    const DecodeUnit U = p.units[u];
+    // the unit's descriptor and query rows arrive with its first stage
+    if (!waitw(full(gs % NS), (gs / NS) & 1, wc)) break;
+    const DecodeUnit U = *reinterpret_cast<const DecodeUnit*>(sm + C::OFF_META + (gs % NS) * 32);
     // this lane's dims of the G query rows (chunks sub, sub+LG, ... of 8 dims,
     // or 4 dims at sub*4 when D/LG = 4), pre-scaled to log2 units
     float2 q2[G][C::DPL / 2];
     {
-      const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(p.q) +
-                                (static_cast<int64_t>(U.req) * p.hq + U.head * G) * D;
+      const __nv_bfloat16* qb =
+          reinterpret_cast<const __nv_bfloat16*>(sm + C::OFF_QB + (gs % NS) * G * D * 2);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         if constexpr (C::DPL >= 8) {
@@ -351,10 +368,9 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
       }
     }
     consumer_sync<NCONS>();
-    const DecodePair pr = p.pairs[U.pair];
-    const bool single = pr.n_units == 1;
+    const bool single = U.pair_units == 1;
     __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) +
-                          (static_cast<int64_t>(pr.req) * p.hq + pr.head * G) * D;
+                          (static_cast<int64_t>(U.req) * p.hq + U.head * G) * D;
     for (int idx = tid; idx < G * D; idx += NCONS) {
       const int g = idx / D, d = idx - g * D;
       float M = -INFINITY;
@@ -381,24 +397,39 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
     if (!single) {
       __threadfence();
       consumer_sync<NCONS>();
-      if (tid == 0) *last_flag = atomicAdd(p.pair_cnt + U.pair, 1) == pr.n_units - 1;
+      if (tid == 0) *last_flag = atomicAdd(p.pair_cnt + U.pair, 1) == U.pair_units - 1;
       consumer_sync<NCONS>();
       if (*last_flag) {
+        // the last slice of the pair merges every slice's partials; four
+        // slices per step keep their loads in flight together
         __threadfence();
         for (int idx = tid; idx < G * D; idx += NCONS) {
           const int g = idx / D, d = idx - g * D;
-          float M = -INFINITY;
-          for (int c = 0; c < pr.n_units; ++c)
-            M = fmaxf(M, __ldcg(p.part_ml + (static_cast<int64_t>(pr.unit0 + c) * G + g) * 2));
-          float Ls = 0.f, o = 0.f;
-          for (int c = 0; c < pr.n_units; ++c) {
-            const int64_t uu = pr.unit0 + c;
-            const float wgt = ex2(__ldcg(p.part_ml + (uu * G + g) * 2) - M);
-            Ls = fmaf(wgt, __ldcg(p.part_ml + (uu * G + g) * 2 + 1), Ls);
-            o = fmaf(wgt, __ldcg(p.part_acc + (uu * G + g) * D + d), o);
+          float M = -INFINITY, Ls = 0.f, o = 0.f;
+          for (int c0 = 0; c0 < U.pair_units; c0 += 4) {
+            float mm[4], ll[4], aa[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int64_t uu = U.pair_unit0 + min(c0 + j, U.pair_units - 1);
+              mm[j] = (c0 + j < U.pair_units) ? __ldcg(p.part_ml + (uu * G + g) * 2) : -INFINITY;
+              ll[j] = __ldcg(p.part_ml + (uu * G + g) * 2 + 1);
+              aa[j] = __ldcg(p.part_acc + (uu * G + g) * D + d);
+            }
+            const float Mn = fmaxf(fmaxf(M, fmaxf(mm[0], mm[1])), fmaxf(mm[2], mm[3]));
+            const float sc = ex2(M - Mn);
+            Ls *= sc;
+            o *= sc;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float wgt = ex2(mm[j] - Mn);
+              Ls = fmaf(wgt, ll[j], Ls);
+              o = fmaf(wgt, aa[j], o);
+            }
+            M = Mn;
           }
           orow[g * D + d] = __float2bfloat16_rn(o / Ls);
         }
+        if (tid == 0) p.pair_cnt[U.pair] = 0;  // ready for the next call
       }
     }
     consumer_sync<NCONS>();  // merge buffers are free again

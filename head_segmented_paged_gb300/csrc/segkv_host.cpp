@@ -175,6 +175,7 @@ struct segkv {
   int device = 0, num_sms = 0;
   int32_t* d_table = nullptr;
   int* d_status = nullptr;
+  int* d_pair_cnt = nullptr;  // decode merge counters, [max_seqs * Hkv], kept at zero
   CUtensorMap tm_k{}, tm_v{};
   UploadRing ring;
   int debug = 0;
@@ -327,12 +328,16 @@ int segkv_create(segkv_t* out, int num_layers, int num_q_heads, int num_kv_heads
     e = cudaMemset(h->d_table, 0xff, sizeof(int32_t) * entries);
     if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&h->d_status), sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int));
+    const size_t cnt_bytes = sizeof(int) * static_cast<size_t>(max_seqs) * num_kv_heads;
+    if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&h->d_pair_cnt), cnt_bytes);
+    if (e == cudaSuccess) e = cudaMemset(h->d_pair_cnt, 0, cnt_bytes);
     if (e == cudaSuccess) e = h->ring.init(kRingInitial);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
       h->ring.release();
       cudaFree(h->d_table);
       cudaFree(h->d_status);
+      cudaFree(h->d_pair_cnt);
       return cuda_fail(nullptr, e, "device setup");
     }
     const uint64_t rows = static_cast<uint64_t>(num_pages) * page_size;
@@ -342,6 +347,7 @@ int segkv_create(segkv_t* out, int num_layers, int num_q_heads, int num_kv_heads
       h->ring.release();
       cudaFree(h->d_table);
       cudaFree(h->d_status);
+      cudaFree(h->d_pair_cnt);
       return fail(nullptr, SEGKV_ERR_CUDA, "tensor map encode failed for the pools");
     }
   }
@@ -356,6 +362,7 @@ int segkv_destroy(segkv_t h) {
     h->ring.release();
     cudaFree(h->d_table);
     cudaFree(h->d_status);
+    cudaFree(h->d_pair_cnt);
   }
   delete h;
   return SEGKV_OK;
@@ -626,7 +633,8 @@ static size_t decode_ws_bytes(const segkv* h, int64_t units, int64_t pairs, size
                               size_t* ml_bytes) {
   *acc_bytes = align_up(static_cast<size_t>(units) * h->G * h->D * 4, 256);
   *ml_bytes = align_up(static_cast<size_t>(units) * h->G * 2 * 4, 256);
-  return *acc_bytes + *ml_bytes + align_up(static_cast<size_t>(pairs) * 4, 256);
+  (void)pairs;
+  return *acc_bytes + *ml_bytes;
 }
 
 int segkv_workspace_size(segkv_t h, int kind, int64_t n_tokens, int n_seqs, size_t* bytes) {
@@ -680,7 +688,7 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
       1, std::min<int64_t>(decode_max_grid(h), (total + sk - 1) / sk)));
   const int64_t per = (total + grid - 1) / grid;
   std::vector<DecodeUnit> units;
-  std::vector<DecodePair> pairs(ranges.size());
+  std::vector<int32_t> pair_unit0(ranges.size()), pair_units(ranges.size(), 0);
   std::vector<int32_t> cta_begin(grid + 1);
   size_t r = 0;
   int32_t off = 0;
@@ -690,7 +698,7 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
     while (left > 0 && r < ranges.size()) {
       const Range& R = ranges[r];
       const int32_t take = static_cast<int32_t>(std::min<int64_t>(left, R.n - R.lo - off));
-      if (off == 0) pairs[r] = {static_cast<int32_t>(units.size()), 0, R.req, R.head};
+      if (off == 0) pair_unit0[r] = static_cast<int32_t>(units.size());
       DecodeUnit u{};
       u.req = R.req;
       u.head = R.head;
@@ -699,7 +707,7 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
       u.table_row = R.row;
       u.pair = static_cast<int32_t>(r);
       units.push_back(u);
-      ++pairs[r].n_units;
+      ++pair_units[r];
       off += take;
       left -= take;
       if (off == R.n - R.lo) {
@@ -709,16 +717,19 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
     }
   }
   cta_begin[grid] = static_cast<int32_t>(units.size());
+  for (DecodeUnit& u : units) {
+    u.pair_unit0 = pair_unit0[u.pair];
+    u.pair_units = pair_units[u.pair];
+  }
   size_t acc_bytes, ml_bytes;
   const size_t need = decode_ws_bytes(h, static_cast<int64_t>(units.size()),
-                                      static_cast<int64_t>(pairs.size()), &acc_bytes, &ml_bytes);
+                                      static_cast<int64_t>(ranges.size()), &acc_bytes, &ml_bytes);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return fail(h, SEGKV_ERR_INVALID_ARG, "workspace needs %zu bytes (256-aligned), got %zu", need,
                 workspace_bytes);
 
   Pack pk;
   const size_t o_units = pk.add(units.data(), units.size());
-  const size_t o_pairs = pk.add(pairs.data(), pairs.size());
   const size_t o_cta = pk.add(cta_begin.data(), cta_begin.size());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   size_t off_ring;
@@ -729,13 +740,9 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
                       cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpyAsync(decode plan)");
   h->upload_bytes += static_cast<int64_t>(pk.buf.size());
-  int* cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + acc_bytes + ml_bytes);
-  e = cudaMemsetAsync(cnt, 0, pairs.size() * sizeof(int), s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemsetAsync(pair counters)");
   uint8_t* d = h->ring.dev + off_ring;
   DecodeParams p{};
   p.units = reinterpret_cast<const DecodeUnit*>(d + o_units);
-  p.pairs = reinterpret_cast<const DecodePair*>(d + o_pairs);
   p.cta_begin = reinterpret_cast<const int32_t*>(d + o_cta);
   p.q = q;
   p.o = o;
@@ -744,9 +751,9 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
   p.vpool = h->vpool;
   p.part_acc = static_cast<float*>(workspace);
   p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + acc_bytes);
-  p.pair_cnt = cnt;
+  p.pair_cnt = h->d_pair_cnt;
   p.n_units = static_cast<int>(units.size());
-  p.n_pairs = static_cast<int>(pairs.size());
+  p.n_pairs = static_cast<int>(ranges.size());
   p.R = h->R;
   p.hq = h->Hq;
   p.G = h->G;
@@ -854,7 +861,9 @@ int segkv_status(segkv_t h, segkv_stream_t stream) {
   e = cudaMemcpy(&v, h->d_status, sizeof v, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(h, e, "status read");
   if (v != 0) {
-    e = cudaMemset(h->d_status, 0, sizeof(int));
+    // a launch that gave up may have left decode merge counters non-zero
+    e = cudaMemset(h->d_pair_cnt, 0, sizeof(int) * static_cast<size_t>(h->S) * h->Hkv);
+    if (e == cudaSuccess) e = cudaMemset(h->d_status, 0, sizeof(int));
     if (e != cudaSuccess) return cuda_fail(h, e, "status clear");
     return fail(h, SEGKV_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired (code %d)", v);
   }

@@ -80,17 +80,11 @@ struct DecodeUnit {
   int32_t k0, k1;      // keys [k0, k1)
   int32_t table_row;
   int32_t pair;        // index of its (req, head) pair
-  int32_t pad[2];
-};
-struct DecodePair {
-  int32_t unit0;   // first unit of this (req, head)
-  int32_t n_units;
-  int32_t req;
-  int32_t head;
+  int32_t pair_unit0;  // first unit of that pair
+  int32_t pair_units;  // units of that pair
 };
 struct DecodeParams {
   const DecodeUnit* units;   // grouped by CTA
-  const DecodePair* pairs;
   const int32_t* cta_begin;  // [grid + 1]: CTA c runs units cta_begin[c] .. cta_begin[c+1]-1
   const void* q;             // bf16 [n, Hq, D]
   void* o;                   // bf16 [n, Hq, D]
@@ -99,7 +93,7 @@ struct DecodeParams {
   const void* vpool;
   float* part_acc;           // [n_units, G, D]
   float* part_ml;            // [n_units, G, 2]
-  int* pair_cnt;             // [n_pairs], zero before the launch
+  int* pair_cnt;             // [>= n_pairs]: zero before the launch, left zero after it
   int n_units, n_pairs;
   int R, hq, G, page_size;
   float scale_log2;
