@@ -308,21 +308,37 @@ def run_decode(args, dev, stream, hbm, peak_src):
     lens = list(w.seq_lens)
     one = np.arange(B + 1, dtype=np.int32)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
-    bytes_step = []
+    lens_at = [[x + s + 1 for x in lens] for s in range(steps)]  # lengths after step s
+    bytes_step = [decode_bytes(w, ls) for ls in lens_at]
     torch.cuda.synchronize()
-    t0 = time.time()
+    t_host = time.perf_counter()
     for s in range(steps):
         qq, kk, vv = qd[s]
         ev[s][0].record(stream)
         h.append(0, kk, vv, one, ids, stream)
-        lens = [x + 1 for x in lens]
         ev[s][1].record(stream)
-        h.decode_attn(0, qq, lens, ids, o, ws, stream)
+        h.decode_attn(0, qq, lens_at[s], ids, o, ws, stream)
         ev[s][2].record(stream)
-        bytes_step.append(decode_bytes(w, lens))
+    t_host = time.perf_counter() - t_host  # host time to issue all steps
     torch.cuda.synchronize()
     if h.status() != 0:
         raise RuntimeError("device status after decode: " + S.segkv_last_error(h.handle))
+    lens = lens_at[-1]
+    # back to back: decode is read-only for the segment state, so the last
+    # step's call is repeated to time the GPU without host-issue gaps
+    reps = 30
+    qq = qd[-1][0]
+    for _ in range(3):
+        h.decode_attn(0, qq, lens, ids, o, ws, stream)
+    b0 = torch.cuda.Event(enable_timing=True)
+    b1 = torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    for _ in range(reps):
+        h.decode_attn(0, qq, lens, ids, o, ws, stream)
+    b1.record(stream)
+    torch.cuda.synchronize()
+    b2b_us = 1e3 * b0.elapsed_time(b1) / reps
+    b2b_gbs = decode_bytes(w, lens) / (b2b_us * 1e-6) / 1e9
     warm = 8
     dec_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(warm, steps)]
     app_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(warm, steps)]
@@ -331,12 +347,15 @@ def run_decode(args, dev, stream, hbm, peak_src):
     med = statistics.median(gbs)
     return {"workload": "ragged decode, 32 requests, 2K-32K log-uniform, 128 steps",
             "gbs_median": round(med, 1), "hbm_peak_gbs": hbm, "frac": round(med / hbm, 4),
+            "back_to_back_gbs": round(b2b_gbs, 1), "back_to_back_frac": round(b2b_gbs / hbm, 4),
+            "back_to_back_us": round(b2b_us, 2),
             "peak_kind": peak_src,
             "decode_us_median": round(1e3 * statistics.median(dec_ms), 2),
             "append_us_median": round(1e3 * statistics.median(app_ms), 2),
             "step_us_median": round(1e3 * statistics.median(step_ms), 2),
             "tokens_per_s": round(B / (statistics.median(step_ms) * 1e-3), 1),
             "bytes_per_step_mean": int(statistics.mean(bytes_step)),
+            "host_issue_us_per_step": round(1e6 * t_host / steps, 2),
             "steps_timed": steps - warm,
             "kernels": ["decode_split_kernel<128,4> (split-KV with the merge fused in)"]}
 

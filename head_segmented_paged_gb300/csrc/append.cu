@@ -10,7 +10,17 @@
 
 namespace skv {
 
-__global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
+template <class T>
+__device__ __forceinline__ const T* plan_ptr(const T* p, const AppendBlob& blob, int inl) {
+  return inl ? reinterpret_cast<const T*>(blob.data + reinterpret_cast<uintptr_t>(p)) : p;
+}
+
+__global__ void __launch_bounds__(256)
+    append_kernel(AppendParams p, const __grid_constant__ AppendBlob blob) {
+  p.seqs = plan_ptr(p.seqs, blob, p.plan_inline);
+  p.tiles = plan_ptr(p.tiles, blob, p.plan_inline);
+  p.page_list = plan_ptr(p.page_list, blob, p.plan_inline);
+  p.table_idx = plan_ptr(p.table_idx, blob, p.plan_inline);
   // block-table entries for the pages this call uses
   for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < p.n_entries;
        e += gridDim.x * blockDim.x)
@@ -41,8 +51,9 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
   }
 }
 
-cudaError_t launch_append(const AppendParams& p, int grid, cudaStream_t s) {
-  append_kernel<<<grid, 256, 0, s>>>(p);
+cudaError_t launch_append(const AppendParams& p, const AppendBlob* blob, int grid, cudaStream_t s) {
+  static const AppendBlob empty_blob{};
+  append_kernel<<<grid, 256, 0, s>>>(p, blob ? *blob : empty_blob);
   return cudaGetLastError();
 }
 

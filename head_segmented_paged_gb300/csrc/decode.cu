@@ -93,7 +93,7 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
 
 template <int D, int G>
 __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
-    decode_split_kernel(const DecodeParams p) {
+    decode_split_kernel(const DecodeParams p, const __grid_constant__ PlanBlob blob) {
   using C = DCfg<D, G>;
   constexpr int NCONS = 32 * C::NW;
   constexpr int HALF = C::NW / 2;
@@ -119,7 +119,13 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
   }
   __syncthreads();
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
-  const int u_begin = p.cta_begin[blockIdx.x], u_end = p.cta_begin[blockIdx.x + 1];
+  const DecodeUnit* units =
+      p.plan_inline ? reinterpret_cast<const DecodeUnit*>(blob.data + reinterpret_cast<uintptr_t>(p.units))
+                    : p.units;
+  const int32_t* cta_begin =
+      p.plan_inline ? reinterpret_cast<const int32_t*>(blob.data + reinterpret_cast<uintptr_t>(p.cta_begin))
+                    : p.cta_begin;
+  const int u_begin = cta_begin[blockIdx.x], u_end = cta_begin[blockIdx.x + 1];
 
   if (warp == C::NW) {
     // The whole warp runs the loop: its lanes fetch 32 block-table entries at
@@ -130,7 +136,7 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
     bool ok = true;
     int gs = 0;
     for (int u = u_begin; ok && u < u_end; ++u) {
-      const DecodeUnit U = p.units[u];
+      const DecodeUnit U = units[u];
       const int32_t* trow = p.table + static_cast<int64_t>(U.table_row) * p.R;
       int kbase = -(1 << 30), my_id = 0;
       for (int w = U.k0 / C::SK; w <= (U.k1 - 1) / C::SK; ++w, ++gs) {
@@ -437,23 +443,30 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
 }
 
 template <int D, int G>
-static cudaError_t launch_dg(const DecodeParams& p, int grid, cudaStream_t s) {
+static cudaError_t launch_dg(const DecodeParams& p, const PlanBlob* blob, int grid, cudaStream_t s) {
   using C = DCfg<D, G>;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
-  if (e != cudaSuccess) return e;
-  decode_split_kernel<D, G><<<grid, C::THREADS, C::BYTES, s>>>(p);
+  static const PlanBlob empty_blob{};
+  static bool attr_set[kMaxDevices] = {};  // the attribute outlives the launch
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= kMaxDevices || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev < kMaxDevices) attr_set[dev] = true;
+  }
+  decode_split_kernel<D, G><<<grid, C::THREADS, C::BYTES, s>>>(p, blob ? *blob : empty_blob);
   return cudaGetLastError();
 }
 
 template <int D>
-static cudaError_t launch_d(const DecodeParams& p, int grid, cudaStream_t s) {
+static cudaError_t launch_d(const DecodeParams& p, const PlanBlob* blob, int grid, cudaStream_t s) {
   switch (p.G) {
-    case 1: return launch_dg<D, 1>(p, grid, s);
-    case 2: return launch_dg<D, 2>(p, grid, s);
-    case 4: return launch_dg<D, 4>(p, grid, s);
-    case 8: return launch_dg<D, 8>(p, grid, s);
-    case 16: return launch_dg<D, 16>(p, grid, s);
+    case 1: return launch_dg<D, 1>(p, blob, grid, s);
+    case 2: return launch_dg<D, 2>(p, blob, grid, s);
+    case 4: return launch_dg<D, 4>(p, blob, grid, s);
+    case 8: return launch_dg<D, 8>(p, blob, grid, s);
+    case 16: return launch_dg<D, 16>(p, blob, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -468,8 +481,9 @@ int decode_stage_keys(int G) {
   }
 }
 
-cudaError_t launch_decode(const DecodeParams& p, int head_dim, int grid, cudaStream_t s) {
-  return head_dim == 64 ? launch_d<64>(p, grid, s) : launch_d<128>(p, grid, s);
+cudaError_t launch_decode(const DecodeParams& p, const PlanBlob* blob, int head_dim, int grid,
+                          cudaStream_t s) {
+  return head_dim == 64 ? launch_d<64>(p, blob, grid, s) : launch_d<128>(p, blob, grid, s);
 }
 
 }  // namespace skv

@@ -178,6 +178,7 @@ struct segkv {
   int* d_pair_cnt = nullptr;  // decode merge counters, [max_seqs * Hkv], kept at zero
   CUtensorMap tm_k{}, tm_v{};
   UploadRing ring;
+  PlanBlob blob;  // staging for plans small enough to travel as kernel parameters
   int debug = 0;
   int64_t upload_bytes = 0;
   std::string err;
@@ -466,15 +467,24 @@ int segkv_append(segkv_t h, int layer, const void* k, const void* v, const int32
   const size_t o_pl = pk.add(plist.data(), plist.size());
   const size_t o_ti = pk.add(tidx.data(), tidx.size());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  size_t off;
-  cudaError_t e = h->ring.reserve(pk.buf.size(), &off);
-  if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
-  std::memcpy(h->ring.host + off, pk.buf.data(), pk.buf.size());
-  e = cudaMemcpyAsync(h->ring.dev + off, h->ring.host + off, pk.buf.size(), cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpyAsync(append plan)");
+  const bool inl = pk.buf.size() <= sizeof(AppendBlob);
+  size_t off = 0;
+  uintptr_t d = 0;  // device address of the plan; 0 (offsets alone) when it is inline
+  cudaError_t e;
+  if (inl) {
+    std::memcpy(h->blob.data, pk.buf.data(), pk.buf.size());
+  } else {
+    e = h->ring.reserve(pk.buf.size(), &off);
+    if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
+    std::memcpy(h->ring.host + off, pk.buf.data(), pk.buf.size());
+    e = cudaMemcpyAsync(h->ring.dev + off, h->ring.host + off, pk.buf.size(),
+                        cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpyAsync(append plan)");
+    d = reinterpret_cast<uintptr_t>(h->ring.dev + off);
+  }
   h->upload_bytes += static_cast<int64_t>(pk.buf.size());
-  uint8_t* d = h->ring.dev + off;
   AppendParams p{};
+  p.plan_inline = inl ? 1 : 0;
   p.k = static_cast<const uint4*>(k);
   p.v = static_cast<const uint4*>(v);
   p.kpool = static_cast<uint4*>(h->kpool);
@@ -490,10 +500,13 @@ int segkv_append(segkv_t h, int layer, const void* k, const void* v, const int32
   p.vec_per_row = h->D / 8;
   p.page_size = h->P;
   const int grid = static_cast<int>(std::min<int64_t>(tiles.size(), int64_t(h->num_sms) * 8));
-  e = launch_append(p, std::max(grid, 1), s);
+  e = launch_append(p, inl ? reinterpret_cast<const AppendBlob*>(&h->blob) : nullptr,
+                    std::max(grid, 1), s);
   if (e != cudaSuccess) return cuda_fail(h, e, "append kernel launch");
-  e = h->ring.commit(off, pk.buf.size(), s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "event record");
+  if (!inl) {
+    e = h->ring.commit(off, pk.buf.size(), s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "event record");
+  }
   return SEGKV_OK;
 }
 
@@ -732,16 +745,24 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
   const size_t o_units = pk.add(units.data(), units.size());
   const size_t o_cta = pk.add(cta_begin.data(), cta_begin.size());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  size_t off_ring;
-  cudaError_t e = h->ring.reserve(pk.buf.size(), &off_ring);
-  if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
-  std::memcpy(h->ring.host + off_ring, pk.buf.data(), pk.buf.size());
-  e = cudaMemcpyAsync(h->ring.dev + off_ring, h->ring.host + off_ring, pk.buf.size(),
-                      cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpyAsync(decode plan)");
+  const bool inl = pk.buf.size() <= sizeof(PlanBlob);
+  size_t off_ring = 0;
+  uintptr_t d = 0;  // device address of the plan; 0 (offsets alone) when it is inline
+  cudaError_t e;
+  if (inl) {
+    std::memcpy(h->blob.data, pk.buf.data(), pk.buf.size());
+  } else {
+    e = h->ring.reserve(pk.buf.size(), &off_ring);
+    if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
+    std::memcpy(h->ring.host + off_ring, pk.buf.data(), pk.buf.size());
+    e = cudaMemcpyAsync(h->ring.dev + off_ring, h->ring.host + off_ring, pk.buf.size(),
+                        cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpyAsync(decode plan)");
+    d = reinterpret_cast<uintptr_t>(h->ring.dev + off_ring);
+  }
   h->upload_bytes += static_cast<int64_t>(pk.buf.size());
-  uint8_t* d = h->ring.dev + off_ring;
   DecodeParams p{};
+  p.plan_inline = inl ? 1 : 0;
   p.units = reinterpret_cast<const DecodeUnit*>(d + o_units);
   p.cta_begin = reinterpret_cast<const int32_t*>(d + o_cta);
   p.q = q;
@@ -761,10 +782,12 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
   p.scale_log2 = h->scale * 1.4426950408889634f;
   p.status = h->d_status;
   p.timeout_ns = kTimeoutNs;
-  e = launch_decode(p, h->D, grid, s);
+  e = launch_decode(p, inl ? &h->blob : nullptr, h->D, grid, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "decode kernel launch");
-  e = h->ring.commit(off_ring, pk.buf.size(), s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "event record");
+  if (!inl) {
+    e = h->ring.commit(off_ring, pk.buf.size(), s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "event record");
+  }
   return SEGKV_OK;
 }
 

@@ -12,6 +12,16 @@ namespace skv {
 constexpr int kKeyTile = 128;     // prefill: keys per tile (one MMA N)
 constexpr int kRowsPerTile = 128; // prefill: query rows per tile (MMA M)
 
+// A small plan travels inside the kernel's parameters (no separate copy
+// before the launch); larger ones go through the upload ring.
+template <int N>
+struct alignas(16) Blob {
+  unsigned char data[N];
+};
+using PlanBlob = Blob<30 * 1024>;  // decode plans
+using AppendBlob = Blob<8 * 1024>; // append plans (kernel parameters cost launch time)
+constexpr int kMaxDevices = 64;
+
 // ---- append -------------------------------------------------------------
 struct AppendSeq {
   int32_t tok0;      // first packed token of this sequence's chunk
@@ -37,6 +47,7 @@ struct AppendParams {
   const int32_t* page_list;   // page ids, per sequence [Hkv][n_pages]
   const int64_t* table_idx;   // block-table slot of each page_list entry
   int32_t* table;
+  int plan_inline;            // 1: the four arrays above are offsets into the AppendBlob
   int n_tiles;
   int n_entries;
   int hkv, vec_per_row, page_size;
@@ -86,6 +97,7 @@ struct DecodeUnit {
 struct DecodeParams {
   const DecodeUnit* units;   // grouped by CTA
   const int32_t* cta_begin;  // [grid + 1]: CTA c runs units cta_begin[c] .. cta_begin[c+1]-1
+  int plan_inline;           // 1: units and cta_begin are offsets into the PlanBlob
   const void* q;             // bf16 [n, Hq, D]
   void* o;                   // bf16 [n, Hq, D]
   const int32_t* table;
@@ -101,12 +113,13 @@ struct DecodeParams {
   unsigned long long timeout_ns;
 };
 
-cudaError_t launch_append(const AppendParams& p, int grid, cudaStream_t s);
+cudaError_t launch_append(const AppendParams& p, const AppendBlob* blob, int grid, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, int head_dim, int grid, cudaStream_t s);
 int prefill_smem_bytes(int head_dim);
 int prefill_unit_tokens(int G);  // query tokens per prefill work unit
-cudaError_t launch_decode(const DecodeParams& p, int head_dim, int grid, cudaStream_t s);
+cudaError_t launch_decode(const DecodeParams& p, const PlanBlob* blob, int head_dim, int grid,
+                          cudaStream_t s);
 int decode_stage_keys(int G);  // keys per decode pipeline stage
 
 }  // namespace skv
