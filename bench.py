@@ -29,6 +29,10 @@ sys.path.insert(0, ROOT)
 METRIC = "SegPaged prefill ms & useful TFLOP/s at 128K (1 GB300); decode GB/s vs HBM peak"
 UNIT = "TFLOP/s"
 N_INPUT_SETS = 4
+# DRAM read+write bytes per prefill launch of the 64-layer step, weighted by
+# layer kind, from one one-pass ncu capture of the current prefill kernel on
+# full-size layers (--case prefill-128k-layers); None once the kernel changes.
+PREFILL_TRAFFIC_PER_LAUNCH = 12.93e9
 
 
 def useful_flops_layer(w, layer, n):
@@ -212,7 +216,9 @@ def run_ours(args, rank, world):
                 "peak_kind": f"bf16 sustained ({peak_src}); kernel runs inside a ~{ms_step:.0f} ms step",
                 "frac_of_burst": round(achieved / bf16_burst, 4),
                 "kernel": "prefill_kernel<128>", "per_launch_flops_mean": step_flops / L,
-                "traffic": None}
+                "traffic": PREFILL_TRAFFIC_PER_LAUNCH,
+                "traffic_note": "DRAM read+write bytes per launch (ncu, full-size layers weighted by "
+                                "kind); algorithmic bytes per launch are 4.83e9"}
 
     out = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
@@ -540,6 +546,49 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_case_128k_layers(args, dev, stream):
+    """One layer of each kind of the 128K workload (shallow all-local, deep
+    without and with a global head), one prefill launch each; for capturing
+    per-launch counters at full size."""
+    import numpy as np
+    import torch
+
+    import head_segmented_paged_gb300 as S
+    from head_segmented_paged_gb300 import inputs as I
+
+    w = I.long_128k_64layer(seed=0)
+    n, P, D = w.seq_lens[0], w.page_size, w.head_dim
+    kinds = {}
+    for l in range(w.num_layers):
+        g = sum(1 for c in w.head_class[l] if c == 0)
+        kinds.setdefault("shallow" if l < 8 else ("deep_g1" if g else "deep_g0"), l)
+    q = I.normal_bf16(0, I.tensor_stream(I._Q, 0), (n, w.hq, D), device=dev)
+    k = I.normal_bf16(0, I.tensor_stream(I._K, 0), (n, w.hkv, D), device=dev)
+    v = I.normal_bf16(0, I.tensor_stream(I._V, 0), (n, w.hkv, D), device=dev)
+    o = torch.empty_like(q)
+    cu = np.array([0, n], np.int32)
+    q_pos = np.arange(n, dtype=np.int32)
+    out = {"case": args.case}
+    for kind, l in sorted(kinds.items(), key=lambda x: x[1]):
+        kp = torch.empty((w.hkv * n // P + 8, P, D), dtype=torch.bfloat16, device=dev)
+        vp = torch.empty_like(kp)
+        h = S.SegKV(1, w.hq, w.hkv, D, [w.head_class[l]], [w.window[l]], P, 1, n, kp, vp)
+        h.append(0, k, v, cu, [0], stream)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        h.prefill_attn(0, q, cu, q_pos, [0], o, None, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert h.status() == 0
+        ms = e0.elapsed_time(e1)
+        f = useful_flops_layer(w, l, n)
+        out[kind] = {"layer": l, "ms": round(ms, 3), "useful_tflops": round(f / (ms * 1e-3) / 1e12, 1)}
+        h.close()
+        del kp, vp
+    print(json.dumps(out), flush=True)
+
+
 def run_case(args):
     """Single-kernel cases for profiling: one layer of prefill at 32K tokens
     (64/8 heads, D=128, pages of 128; KV head 0 global, the rest local with
@@ -557,6 +606,9 @@ def run_case(args):
     if args.case == "decode":
         out = run_decode(args, dev, stream, *measured_peaks()[::3])
         print(json.dumps({"case": args.case, **out}), flush=True)
+        return
+    if args.case == "prefill-128k-layers":
+        run_case_128k_layers(args, dev, stream)
         return
     n, hq, hkv, D, P = 32768, 64, 8, 128, 128
     glob = args.case == "dense-32k"
@@ -598,7 +650,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
-    ap.add_argument("--case", default=None, choices=["prefill-32k", "dense-32k", "decode"],
+    ap.add_argument("--case", default=None,
+                    choices=["prefill-32k", "dense-32k", "decode", "prefill-128k-layers"],
                     help="run one kernel's profiling case instead of the benchmark")
     args = ap.parse_args()
     if args.case:
