@@ -52,6 +52,7 @@ def lib():
         att = [I, I, I, ctypes.c_double, P, P, P, P, P, P, P, P, I, P, P, I64]
         _lib.orc_attention.argtypes = att + [P, P]
         _lib.orc_attention_blocked.argtypes = att + [I, P, P]
+        _lib.orc_rope.argtypes = [P, I64, I, I, I, ctypes.c_double, P]
     return _lib
 
 
@@ -150,3 +151,23 @@ def attention(q, k, v, row_seq, row_pos, kv_off, kv_len, head_class, window, seg
     else:
         rc = lib().orc_attention_blocked(*args, int(block), _ptr(o), _ptr(lse))
     return rc, o, lse
+
+
+def rope(x, pos, rotary_dim, style, base):
+    """fp64 rotary rotation of rows x [rows, d] by pos[row] positions (see
+    orc_rope). x may be bf16 (widened exactly) or float; returns fp64."""
+    import torch
+    if hasattr(x, "dtype") and x.dtype == torch.bfloat16:
+        xs = x.to(torch.float64).numpy()
+    else:
+        xs = np.asarray(x, dtype=np.float64)
+    shape = xs.shape
+    v = np.ascontiguousarray(xs.reshape(-1, shape[-1]).copy())
+    p = np.ascontiguousarray(np.broadcast_to(np.asarray(pos, dtype=np.float64).reshape(-1),
+                                             (v.shape[0],)) if np.ndim(pos) == 0 else
+                             np.asarray(pos, dtype=np.float64).reshape(-1))
+    rc = lib().orc_rope(_ptr(v), ctypes.c_int64(v.shape[0]), v.shape[1], rotary_dim, style,
+                        ctypes.c_double(base), _ptr(p))
+    if rc != OK:
+        raise ValueError("orc_rope: bad arguments")
+    return v.reshape(shape)

@@ -391,3 +391,33 @@ int orc_attention_blocked(int hq, int hkv, int d, double scale, const uint16_t* 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Part 4: rotary position re-alignment of cached keys (RedKnot summary page,
+// section "Elastic Sparsity（弹性稀疏恢复）": reuse starts by aligning RoPE
+// positions). A key rotated for position p becomes the key for position
+// p + delta by rotating every dimension pair i by delta * theta_i, with
+// theta_i = base^(-2i / rotary_dim). Pairs are (2i, 2i+1) for the interleaved
+// layout (style 0) or (i, i + rotary_dim/2) for the split-half layout
+// (style 1); dimensions at or beyond rotary_dim are left unchanged.
+// x: rows x d values (fp64), rotated in place by pos[row] positions.
+extern "C" int orc_rope(double* x, int64_t rows, int d, int rotary_dim, int style, double base,
+                        const double* pos) {
+  if (d <= 0 || rotary_dim <= 0 || rotary_dim > d || rotary_dim % 2 || style < 0 || style > 1)
+    return INVALID_ARG;
+  const int half = rotary_dim / 2;
+  for (int64_t r = 0; r < rows; ++r) {
+    double* v = x + r * d;
+    for (int i = 0; i < half; ++i) {
+      const double theta = std::pow(base, -2.0 * i / rotary_dim);
+      const double ang = pos[r] * theta;
+      const double c = std::cos(ang), s = std::sin(ang);
+      const int a = style == 0 ? 2 * i : i;
+      const int b = style == 0 ? 2 * i + 1 : i + half;
+      const double xa = v[a], xb = v[b];
+      v[a] = xa * c - xb * s;
+      v[b] = xa * s + xb * c;
+    }
+  }
+  return OK;
+}
