@@ -238,6 +238,7 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     if not args.no_decode:
         out["decode"] = run_decode(args, dev, stream, hbm, peak_src)
+        out["rope_shift"] = run_rope(dev, stream, hbm)
     if not args.no_dense:
         out["dense"] = run_dense(args, dev, stream, sets, cu, q_pos, o, prefill_ms)
     if not args.no_e2e:
@@ -364,6 +365,41 @@ def run_decode(args, dev, stream, hbm, peak_src):
             "host_issue_us_per_step": round(1e6 * t_host / steps, 2),
             "steps_timed": steps - warm,
             "kernels": ["decode_split_kernel<128,4> (split-KV with the merge fused in)"]}
+
+
+def run_rope(dev, stream, hbm):
+    """Rotary re-alignment of one 32768-token sequence's cached keys (8 KV
+    heads, D=128, pages of 64), every head global so every key is rotated:
+    HBM bytes = keys read + keys written."""
+    import numpy as np
+    import torch
+
+    import head_segmented_paged_gb300 as S
+    from head_segmented_paged_gb300 import inputs as I
+
+    n, hkv, D, P = 32768, 8, 128, 64
+    kp = torch.empty((hkv * n // P + 8, P, D), dtype=torch.bfloat16, device=dev)
+    vp = torch.empty_like(kp)
+    h = S.SegKV(1, 32, hkv, D, [[0] * hkv], [n], P, 1, n, kp, vp)
+    k = I.normal_bf16(0, I.tensor_stream(I._K, 9), (n, hkv, D), device=dev)
+    h.append(0, k, k, np.array([0, n], np.int32), [0], stream)
+    for _ in range(3):
+        h.rope_shift(0, 0, 1000, 10000.0, D, S.SEGKV_ROPE_HALF, stream=stream)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    reps = 20
+    e0.record(stream)
+    for _ in range(reps):
+        h.rope_shift(0, 0, 1000, 10000.0, D, S.SEGKV_ROPE_HALF, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert h.status() == 0
+    us = 1e3 * e0.elapsed_time(e1) / reps
+    nbytes = 2 * n * hkv * D * 2
+    return {"workload": "rope re-alignment of one 32768-token sequence, 8 KV heads, D=128",
+            "us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+            "frac_hbm": round(nbytes / (us * 1e-6) / 1e9 / hbm, 4), "bytes": nbytes,
+            "kernel": "rope_kernel"}
 
 
 def run_e2e(args, dev, stream, w, sets, cu, q_pos, step_flops, num_pages):
@@ -607,6 +643,10 @@ def run_case(args):
         out = run_decode(args, dev, stream, *measured_peaks()[::3])
         print(json.dumps({"case": args.case, **out}), flush=True)
         return
+    if args.case == "rope":
+        print(json.dumps({"case": args.case, **run_rope(dev, stream, measured_peaks()[0])}),
+              flush=True)
+        return
     if args.case == "prefill-128k-layers":
         run_case_128k_layers(args, dev, stream)
         return
@@ -651,7 +691,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--case", default=None,
-                    choices=["prefill-32k", "dense-32k", "decode", "prefill-128k-layers"],
+                    choices=["prefill-32k", "dense-32k", "decode", "prefill-128k-layers", "rope"],
                     help="run one kernel's profiling case instead of the benchmark")
     args = ap.parse_args()
     if args.case:

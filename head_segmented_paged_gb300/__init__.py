@@ -27,11 +27,12 @@ SEGKV_ERR_EVICTED = -3
 SEGKV_ERR_CUDA = -4
 SEGKV_ERR_DEVICE_TIMEOUT = -5
 SEGKV_WS_PREFILL, SEGKV_WS_DECODE = 0, 1
+SEGKV_ROPE_INTERLEAVED, SEGKV_ROPE_HALF = 0, 1
 
 SYMBOLS = ["segkv_create", "segkv_destroy", "segkv_append", "segkv_prefill_attn",
            "segkv_decode_attn", "segkv_trim", "segkv_free_seq", "segkv_workspace_size",
            "segkv_get_segment", "segkv_seq_len", "segkv_stats", "segkv_status",
-           "segkv_last_error", "segkv_set_debug", "segkv_decode_attn_noalloc"]
+           "segkv_last_error", "segkv_set_debug", "segkv_decode_attn_noalloc", "segkv_rope_shift"]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -62,6 +63,7 @@ def _load():
         "segkv_last_error": [P],
         "segkv_set_debug": [P, I],
         "segkv_decode_attn_noalloc": [P, I, P, P, P, I, P, P],
+        "segkv_rope_shift": [P, I, I, ctypes.c_int32, ctypes.c_double, I, I, ctypes.c_uint64, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -154,6 +156,12 @@ def segkv_decode_attn_noalloc(h, layer, q, seq_lens, seq_ids, o, stream=None):
     sl, ids = _host_i32(seq_lens), _host_i32(seq_ids)
     return _lib.segkv_decode_attn_noalloc(h, layer, _ptr(q), sl.ctypes.data, ids.ctypes.data,
                                           len(ids), _ptr(o), _stream_ptr(stream))
+
+
+def segkv_rope_shift(h, layer, seq, delta, base, rotary_dim, style, head_mask=(1 << 64) - 1,
+                     stream=None):
+    return _lib.segkv_rope_shift(h, layer, seq, int(delta), float(base), rotary_dim, style,
+                                 head_mask, _stream_ptr(stream))
 
 
 def segkv_trim(h, layer, seq_ids):
@@ -270,6 +278,12 @@ class SegKV:
     def decode_attn_noalloc(self, layer, q, seq_lens, seq_ids, o, stream=None):
         return self._check(segkv_decode_attn_noalloc(self._h, layer, q, seq_lens, seq_ids, o,
                                                      stream))
+
+    def rope_shift(self, layer, seq, delta, base=10000.0, rotary_dim=None, style=SEGKV_ROPE_HALF,
+                   head_mask=(1 << 64) - 1, stream=None):
+        rd = self.head_dim if rotary_dim is None else rotary_dim
+        return self._check(segkv_rope_shift(self._h, layer, seq, delta, base, rd, style, head_mask,
+                                            stream))
 
     def trim(self, layer, seq_ids):
         return self._check(segkv_trim(self._h, layer, seq_ids))

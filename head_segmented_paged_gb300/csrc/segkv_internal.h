@@ -113,6 +113,22 @@ struct DecodeParams {
   unsigned long long timeout_ns;
 };
 
+// ---- rotary re-alignment ------------------------------------------------------
+struct RopeRun {
+  int32_t page;   // physical page
+  int32_t slot0;  // first row in the page
+  int32_t nrows;  // rows to rotate
+  int32_t pad;
+};
+struct RopeParams {
+  const RopeRun* runs;
+  const float2* cos_sin;  // [rotary_dim / 2]
+  void* kpool;
+  int plan_inline;        // 1: runs and cos_sin are offsets into the AppendBlob
+  int n_runs, page_size, head_dim, rotary_dim, style;
+};
+cudaError_t launch_rope(const RopeParams& p, const AppendBlob* blob, int grid, cudaStream_t s);
+
 cudaError_t launch_append(const AppendParams& p, const AppendBlob* blob, int grid, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, int head_dim, int grid, cudaStream_t s);

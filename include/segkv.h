@@ -175,6 +175,25 @@ int segkv_free_seq(segkv_t h, int seq_id);
 int segkv_workspace_size(segkv_t h, int kind, int64_t n_tokens, int n_seqs, size_t* bytes);
 
 /*
+ * segkv_rope_shift — re-align the cached keys of one sequence to a position
+ * offset (RedKnot summary page, section "Elastic Sparsity（弹性稀疏恢复）": reuse
+ * of a cached segment at another position starts with RoPE position
+ * alignment). Every kept key of the selected KV heads of (layer, seq) is
+ * rotated in place: dimension pair i turns by delta * base^(-2i/rotary_dim),
+ * which maps a key encoded for position p to the key for position p + delta.
+ *   style       SEGKV_ROPE_INTERLEAVED: pairs (2i, 2i+1);
+ *               SEGKV_ROPE_HALF: pairs (i, i + rotary_dim/2).
+ *   rotary_dim  even, 2 .. head_dim; dimensions beyond it are unchanged.
+ *   head_mask   bit h selects KV head h.
+ * Angles are formed in fp64 on the host; the rotation runs in fp32 and each
+ * key is rounded once to bf16. V, page tables and tracked lengths are
+ * unchanged. Errors: INVALID_ARG.
+ */
+enum { SEGKV_ROPE_INTERLEAVED = 0, SEGKV_ROPE_HALF = 1 };
+int segkv_rope_shift(segkv_t h, int layer, int seq, int32_t delta, double base, int rotary_dim,
+                     int style, uint64_t head_mask, segkv_stream_t stream);
+
+/*
  * segkv_get_segment — host copy of one segment's table: kept start, kept
  * length, first logical page and the page ids in logical order (at most
  * max_ids written; *n_ids gets the count).
