@@ -48,6 +48,7 @@ def lib():
         _lib.orc_append.argtypes = [P, I, P, P, I]
         _lib.orc_trim.argtypes = [P, I, P, I]
         _lib.orc_free_seq.argtypes = [P, I]
+        _lib.orc_import.argtypes = [P, I, I, I, P]
         _lib.orc_segment.argtypes = [P, I, I, I, P, P, P, P, I, P]
         att = [I, I, I, ctypes.c_double, P, P, P, P, P, P, P, P, I, P, P, I64]
         _lib.orc_attention.argtypes = att + [P, P]
@@ -92,6 +93,10 @@ class PageModel:
 
     def free_seq(self, seq) -> int:
         return lib().orc_free_seq(self._h, seq)
+
+    def import_segment(self, layer, seq, n, starts) -> int:
+        st = _i32(starts)
+        return lib().orc_import(self._h, layer, seq, n, _ptr(st))
 
     def free_pages(self) -> int:
         return lib().orc_free_pages(self._h)

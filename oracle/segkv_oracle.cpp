@@ -233,6 +233,34 @@ int orc_free_seq(void* hnd, int seq) {
   return OK;
 }
 
+// Install a transferred segment set into an empty (layer, seq): every head
+// gets length n and its own kept start s[h]; pages floor(s/P) .. floor((n-1)/P)
+// are taken lowest id first, in (head ascending, page ascending) order.
+// Transactional: on any error nothing changes.
+int orc_import(void* hnd, int layer, int seq, int n, const int32_t* starts) {
+  State& st = *static_cast<State*>(hnd);
+  if (layer < 0 || layer >= st.L || seq < 0 || seq >= st.S || n < 0 || n > st.max_len)
+    return INVALID_ARG;
+  if (st.n[static_cast<size_t>(layer) * st.S + seq] != 0) return INVALID_ARG;
+  size_t need = 0;
+  for (int h = 0; h < st.H; ++h) {
+    if (starts[h] < 0 || starts[h] > n) return INVALID_ARG;
+    if (n > 0 && (n - 1) / st.P >= starts[h] / st.P) need += (n - 1) / st.P - starts[h] / st.P + 1;
+  }
+  if (st.free_ids.size() < need) return OUT_OF_PAGES;
+  for (int h = 0; h < st.H; ++h) {
+    Segment& g = st.at(layer, h, seq);
+    g.s = starts[h];
+    if (n == 0) continue;
+    for (int k = starts[h] / st.P; k <= (n - 1) / st.P; ++k) {
+      g.page_of[k] = *st.free_ids.begin();
+      st.free_ids.erase(st.free_ids.begin());
+    }
+  }
+  st.n[static_cast<size_t>(layer) * st.S + seq] = n;
+  return OK;
+}
+
 // Segment (layer, head, seq): kept start, kept length, first logical page and
 // the ids of its pages in logical order.
 int orc_segment(void* hnd, int layer, int head, int seq, int32_t* start, int32_t* len,

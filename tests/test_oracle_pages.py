@@ -27,6 +27,8 @@ def apply_step(m, st):
         return m.trim(st["layer"], st["seq_ids"])
     if st["op"] == "free_seq":
         return m.free_seq(st["seq"])
+    if st["op"] == "import":
+        return m.import_segment(st["layer"], st["seq"], st["n"], st["starts"])
     raise ValueError(st["op"])
 
 
