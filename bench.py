@@ -239,6 +239,7 @@ def run_ours(args, rank, world):
     if not args.no_decode:
         out["decode"] = run_decode(args, dev, stream, hbm, peak_src)
         out["rope_shift"] = run_rope(dev, stream, hbm)
+        out["pd_transfer"] = run_transfer(dev, stream, hbm)
     if not args.no_dense:
         out["dense"] = run_dense(args, dev, stream, sets, cu, q_pos, o, prefill_ms)
     if not args.no_e2e:
@@ -400,6 +401,66 @@ def run_rope(dev, stream, hbm):
             "us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
             "frac_hbm": round(nbytes / (us * 1e-6) / 1e9 / hbm, 4), "bytes": nbytes,
             "kernel": "rope_kernel"}
+
+
+def run_transfer(dev, stream, hbm):
+    """Prefill-to-decode transfer of one 32768-token session (1 global + 7
+    local heads, window 1024, D=128, pages of 64) after its post-prefill trim:
+    bytes moved by segkv_export versus a dense [n, Hkv, D] K/V export, the
+    export and import rates, and how many such sessions fit per GB of KV."""
+    import numpy as np
+    import torch
+
+    import head_segmented_paged_gb300 as S
+    from head_segmented_paged_gb300 import inputs as I
+
+    n, hkv, D, P, W = 32768, 8, 128, 64, 1024
+    hc = [[0] + [1] * 7]
+    kp = torch.empty((hkv * n // P + 64, P, D), dtype=torch.bfloat16, device=dev)
+    vp = torch.empty_like(kp)
+    src = S.SegKV(1, 32, hkv, D, hc, [W], P, 1, n + 8, kp, vp)
+    k = I.normal_bf16(0, I.tensor_stream(I._K, 11), (n, hkv, D), device=dev)
+    src.append(0, k, k, np.array([0, n], np.int32), [0], stream)
+    src.trim(0, [0])
+    buf, hdr = src.export_segment(0, 0, stream)
+    kp2 = torch.empty_like(kp)
+    vp2 = torch.empty_like(kp)
+    dst = S.SegKV(1, 32, hkv, D, hc, [W], P, 1, n + 8, kp2, vp2)
+
+    def timed(fn, reps=20):
+        for _ in range(3):
+            fn()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return 1e3 * e0.elapsed_time(e1) / reps
+
+    hnd = src.handle
+    header = np.zeros(1 + hkv, np.int32)
+    exp_us = timed(lambda: S.segkv_export(hnd, 0, 0, buf, header, stream))
+
+    def imp():
+        dst.free_seq(0)
+        dst.import_segment(0, 0, buf, hdr, stream)
+    imp_us = timed(imp)
+    assert src.status() == 0 and dst.status() == 0
+    seg_bytes = buf.numel() * 2
+    dense_bytes = n * hkv * D * 2 * 2
+    return {"workload": "one 32768-token session, 1 global + 7 local heads (W=1024), D=128, "
+                        "after the post-prefill trim",
+            "export_bytes": seg_bytes, "dense_bytes": dense_bytes,
+            "bytes_ratio_dense_over_segmented": round(dense_bytes / seg_bytes, 3),
+            "export_us": round(exp_us, 2),
+            "export_gbs": round(2 * seg_bytes / (exp_us * 1e-6) / 1e9, 1),
+            "import_us": round(imp_us, 2),
+            "import_gbs": round(2 * seg_bytes / (imp_us * 1e-6) / 1e9, 1),
+            "kv_sessions_per_gb": {"segmented": round(1e9 / seg_bytes, 2),
+                                   "dense": round(1e9 / dense_bytes, 2)},
+            "kernels": ["transfer_kernel"]}
 
 
 def run_e2e(args, dev, stream, w, sets, cu, q_pos, step_flops, num_pages):
@@ -643,6 +704,10 @@ def run_case(args):
         out = run_decode(args, dev, stream, *measured_peaks()[::3])
         print(json.dumps({"case": args.case, **out}), flush=True)
         return
+    if args.case == "transfer":
+        print(json.dumps({"case": args.case, **run_transfer(dev, stream, measured_peaks()[0])}),
+              flush=True)
+        return
     if args.case == "rope":
         print(json.dumps({"case": args.case, **run_rope(dev, stream, measured_peaks()[0])}),
               flush=True)
@@ -691,7 +756,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--case", default=None,
-                    choices=["prefill-32k", "dense-32k", "decode", "prefill-128k-layers", "rope"],
+                    choices=["prefill-32k", "dense-32k", "decode", "prefill-128k-layers", "rope",
+                             "transfer"],
                     help="run one kernel's profiling case instead of the benchmark")
     args = ap.parse_args()
     if args.case:

@@ -32,7 +32,8 @@ SEGKV_ROPE_INTERLEAVED, SEGKV_ROPE_HALF = 0, 1
 SYMBOLS = ["segkv_create", "segkv_destroy", "segkv_append", "segkv_prefill_attn",
            "segkv_decode_attn", "segkv_trim", "segkv_free_seq", "segkv_workspace_size",
            "segkv_get_segment", "segkv_seq_len", "segkv_stats", "segkv_status",
-           "segkv_last_error", "segkv_set_debug", "segkv_decode_attn_noalloc", "segkv_rope_shift"]
+           "segkv_last_error", "segkv_set_debug", "segkv_decode_attn_noalloc", "segkv_rope_shift",
+           "segkv_export_size", "segkv_export", "segkv_import"]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -64,6 +65,9 @@ def _load():
         "segkv_set_debug": [P, I],
         "segkv_decode_attn_noalloc": [P, I, P, P, P, I, P, P],
         "segkv_rope_shift": [P, I, I, ctypes.c_int32, ctypes.c_double, I, I, ctypes.c_uint64, P],
+        "segkv_export_size": [P, I, I, ctypes.POINTER(SZ)],
+        "segkv_export": [P, I, I, P, SZ, P, P],
+        "segkv_import": [P, I, I, P, SZ, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -162,6 +166,25 @@ def segkv_rope_shift(h, layer, seq, delta, base, rotary_dim, style, head_mask=(1
                      stream=None):
     return _lib.segkv_rope_shift(h, layer, seq, int(delta), float(base), rotary_dim, style,
                                  head_mask, _stream_ptr(stream))
+
+
+def segkv_export_size(h, layer, seq):
+    b = ctypes.c_size_t()
+    rc = _lib.segkv_export_size(h, layer, seq, ctypes.byref(b))
+    return rc, b.value
+
+
+def segkv_export(h, layer, seq, out, header, stream=None):
+    """header: host int32 numpy array of length 1 + Hkv, filled by the call."""
+    nbytes = 0 if out is None else out.numel() * out.element_size()
+    return _lib.segkv_export(h, layer, seq, _ptr(out), nbytes, header.ctypes.data,
+                             _stream_ptr(stream))
+
+
+def segkv_import(h, layer, seq, src, header, stream=None):
+    hd = _host_i32(header)
+    nbytes = 0 if src is None else src.numel() * src.element_size()
+    return _lib.segkv_import(h, layer, seq, _ptr(src), nbytes, hd.ctypes.data, _stream_ptr(stream))
 
 
 def segkv_trim(h, layer, seq_ids):
@@ -284,6 +307,21 @@ class SegKV:
         rd = self.head_dim if rotary_dim is None else rotary_dim
         return self._check(segkv_rope_shift(self._h, layer, seq, delta, base, rd, style, head_mask,
                                             stream))
+
+    def export_segment(self, layer, seq, stream=None):
+        """Returns (buffer, header): the kept K/V rows packed for transfer."""
+        import torch
+        rc, nbytes = segkv_export_size(self._h, layer, seq)
+        self._check(rc)
+        header = np.zeros(1 + self.hkv, dtype=np.int32)
+        dev = self.k_pool.device if self.k_pool is not None else "cpu"
+        buf = torch.empty(max(nbytes // 2, 8), dtype=torch.bfloat16, device=dev)
+        self._check(segkv_export(self._h, layer, seq, buf if self.k_pool is not None else None,
+                                 header, stream))
+        return buf[: nbytes // 2], header
+
+    def import_segment(self, layer, seq, buf, header, stream=None):
+        return self._check(segkv_import(self._h, layer, seq, buf, header, stream))
 
     def trim(self, layer, seq_ids):
         return self._check(segkv_trim(self._h, layer, seq_ids))

@@ -860,6 +860,185 @@ int segkv_rope_shift(segkv_t h, int layer, int seq, int32_t delta, double base, 
   return SEGKV_OK;
 }
 
+// ---------------------------------------------------------------- transfer
+// A packed plan goes inside the kernel parameters when it fits, else through
+// the upload ring. base is the plan's device address, 0 when it is inline.
+struct PlanPlace {
+  bool inl = false;
+  size_t off = 0;
+  uintptr_t base = 0;
+};
+
+static int place_small_plan(segkv* h, const Pack& pk, cudaStream_t s, PlanPlace* pp) {
+  pp->inl = pk.buf.size() <= sizeof(AppendBlob);
+  if (pp->inl) {
+    std::memcpy(h->blob.data, pk.buf.data(), pk.buf.size());
+  } else {
+    cudaError_t e = h->ring.reserve(pk.buf.size(), &pp->off);
+    if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
+    std::memcpy(h->ring.host + pp->off, pk.buf.data(), pk.buf.size());
+    e = cudaMemcpyAsync(h->ring.dev + pp->off, h->ring.host + pp->off, pk.buf.size(),
+                        cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpyAsync(plan)");
+    pp->base = reinterpret_cast<uintptr_t>(h->ring.dev + pp->off);
+  }
+  h->upload_bytes += static_cast<int64_t>(pk.buf.size());
+  return SEGKV_OK;
+}
+
+static int finish_small_plan(segkv* h, const PlanPlace& pp, const Pack& pk, cudaStream_t s) {
+  if (pp.inl) return SEGKV_OK;
+  cudaError_t e = h->ring.commit(pp.off, pk.buf.size(), s);
+  return e == cudaSuccess ? SEGKV_OK : cuda_fail(h, e, "event record");
+}
+
+int segkv_export_size(segkv_t h, int layer, int seq, size_t* bytes) {
+  if (!h || !bytes) return SEGKV_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= h->L || seq < 0 || seq >= h->S)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer or seq");
+  const int32_t n = h->len[h->lidx(layer, seq)];
+  size_t rows = 0;
+  for (int hd = 0; hd < h->Hkv; ++hd) rows += n - h->start[h->seg(layer, hd, seq)];
+  *bytes = rows * h->D * 2 * 2;
+  return SEGKV_OK;
+}
+
+int segkv_export(segkv_t h, int layer, int seq, void* out, size_t out_bytes, int32_t* header,
+                 segkv_stream_t stream) {
+  size_t need = 0;
+  int rc = segkv_export_size(h, layer, seq, &need);
+  if (rc != SEGKV_OK) return rc;
+  if (!header) return fail(h, SEGKV_ERR_INVALID_ARG, "header is NULL");
+  const int32_t n = h->len[h->lidx(layer, seq)];
+  header[0] = n;
+  for (int hd = 0; hd < h->Hkv; ++hd) header[1 + hd] = h->start[h->seg(layer, hd, seq)];
+  if (!out && out_bytes == 0) return SEGKV_OK;  // header and size only
+  if (h->host_only) return fail(h, SEGKV_ERR_INVALID_ARG, "host-only handle has no pools");
+  if (!out || out_bytes < need || (reinterpret_cast<uintptr_t>(out) & 15))
+    return fail(h, SEGKV_ERR_INVALID_ARG, "export needs %zu bytes (16-aligned), got %zu", need,
+                out_bytes);
+  std::vector<TransferRun> runs;
+  int32_t row = 0;
+  for (int hd = 0; hd < h->Hkv; ++hd) {
+    const int32_t s0 = h->start[h->seg(layer, hd, seq)];
+    const int32_t* r = h->table.data() + h->seg(layer, hd, seq) * h->R;
+    const int32_t len = n - s0;
+    for (int32_t pos = s0; pos < n;) {
+      const int k = pos / h->P;
+      const int32_t pend = std::min<int32_t>(n, (k + 1) * h->P);
+      runs.push_back({r[k], pos - k * h->P, pend - pos, row + (pos - s0), row + len + (pos - s0),
+                      {0, 0, 0}});
+      pos = pend;
+    }
+    row += 2 * len;
+  }
+  if (runs.empty()) return SEGKV_OK;
+  Pack pk;
+  const size_t o_runs = pk.add(runs.data(), runs.size());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PlanPlace pp;
+  rc = place_small_plan(h, pk, s, &pp);
+  if (rc != SEGKV_OK) return rc;
+  TransferParams p{};
+  p.runs = reinterpret_cast<const TransferRun*>(pp.base + o_runs);
+  p.kpool = static_cast<uint4*>(h->kpool);
+  p.vpool = static_cast<uint4*>(h->vpool);
+  p.buf_out = static_cast<uint4*>(out);
+  p.table = h->d_table;
+  p.plan_inline = pp.inl ? 1 : 0;
+  p.to_pool = 0;
+  p.n_runs = static_cast<int>(runs.size());
+  p.vec_per_row = h->D / 8;
+  p.page_size = h->P;
+  const int grid = static_cast<int>(std::min<int64_t>(runs.size(), int64_t(h->num_sms) * 16));
+  cudaError_t e = launch_transfer(p, pp.inl ? reinterpret_cast<const AppendBlob*>(&h->blob) : nullptr,
+                                  grid, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "export kernel launch");
+  return finish_small_plan(h, pp, pk, s);
+}
+
+int segkv_import(segkv_t h, int layer, int seq, const void* in, size_t in_bytes,
+                 const int32_t* header, segkv_stream_t stream) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= h->L || seq < 0 || seq >= h->S || !header)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer, seq or header");
+  if (h->len[h->lidx(layer, seq)] != 0)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "seq %d is not empty in layer %d", seq, layer);
+  const int32_t n = header[0];
+  if (n < 0 || n > h->max_len) return fail(h, SEGKV_ERR_INVALID_ARG, "bad length %d", n);
+  int64_t need = 0;
+  size_t rows = 0;
+  for (int hd = 0; hd < h->Hkv; ++hd) {
+    const int32_t s0 = header[1 + hd];
+    if (s0 < 0 || s0 > n) return fail(h, SEGKV_ERR_INVALID_ARG, "bad kept start %d", s0);
+    rows += n - s0;
+    if (n > 0 && (n - 1) / h->P >= s0 / h->P) need += (n - 1) / h->P - s0 / h->P + 1;
+  }
+  const size_t bytes = rows * h->D * 2 * 2;
+  if (!h->host_only && bytes > 0 &&
+      (!in || in_bytes < bytes || (reinterpret_cast<uintptr_t>(in) & 15)))
+    return fail(h, SEGKV_ERR_INVALID_ARG, "import needs %zu bytes (16-aligned), got %zu", bytes,
+                in_bytes);
+  if (static_cast<int64_t>(h->free_ids.size()) < need)
+    return fail(h, SEGKV_ERR_OUT_OF_PAGES, "import needs %lld pages, %lld free",
+                static_cast<long long>(need), static_cast<long long>(h->free_ids.size()));
+  std::vector<TransferRun> runs;
+  std::vector<int32_t> plist;
+  std::vector<int64_t> tidx;
+  int32_t row = 0;
+  for (int hd = 0; hd < h->Hkv; ++hd) {
+    const int32_t s0 = header[1 + hd];
+    h->start[h->seg(layer, hd, seq)] = s0;
+    int32_t* r = h->row(layer, hd, seq);
+    if (n > 0)
+      for (int k = s0 / h->P; k <= (n - 1) / h->P; ++k) {
+        r[k] = h->free_ids.top();
+        h->free_ids.pop();
+        plist.push_back(r[k]);
+        tidx.push_back(static_cast<int64_t>(h->seg(layer, hd, seq)) * h->R + k);
+      }
+    const int32_t len = n - s0;
+    for (int32_t pos = s0; pos < n;) {
+      const int k = pos / h->P;
+      const int32_t pend = std::min<int32_t>(n, (k + 1) * h->P);
+      runs.push_back({r[k], pos - k * h->P, pend - pos, row + (pos - s0), row + len + (pos - s0),
+                      {0, 0, 0}});
+      pos = pend;
+    }
+    row += 2 * len;
+  }
+  h->len[h->lidx(layer, seq)] = n;
+  if (h->host_only || (runs.empty() && plist.empty())) return SEGKV_OK;
+  Pack pk;
+  const size_t o_runs = pk.add(runs.data(), runs.size());
+  const size_t o_pl = pk.add(plist.data(), plist.size());
+  const size_t o_ti = pk.add(tidx.data(), tidx.size());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  PlanPlace pp;
+  int rc = place_small_plan(h, pk, s, &pp);
+  if (rc != SEGKV_OK) return rc;
+  TransferParams p{};
+  p.runs = reinterpret_cast<const TransferRun*>(pp.base + o_runs);
+  p.page_list = reinterpret_cast<const int32_t*>(pp.base + o_pl);
+  p.table_idx = reinterpret_cast<const int64_t*>(pp.base + o_ti);
+  p.kpool = static_cast<uint4*>(h->kpool);
+  p.vpool = static_cast<uint4*>(h->vpool);
+  p.buf = static_cast<const uint4*>(in);
+  p.table = h->d_table;
+  p.plan_inline = pp.inl ? 1 : 0;
+  p.to_pool = 1;
+  p.n_runs = static_cast<int>(runs.size());
+  p.n_entries = static_cast<int>(plist.size());
+  p.vec_per_row = h->D / 8;
+  p.page_size = h->P;
+  const int grid = static_cast<int>(
+      std::max<int64_t>(1, std::min<int64_t>(runs.size(), int64_t(h->num_sms) * 16)));
+  cudaError_t e = launch_transfer(p, pp.inl ? reinterpret_cast<const AppendBlob*>(&h->blob) : nullptr,
+                                  grid, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "import kernel launch");
+  return finish_small_plan(h, pp, pk, s);
+}
+
 // ---------------------------------------------------------------- trim / free
 int segkv_trim(segkv_t h, int layer, const int32_t* seq_ids, int n) {
   if (!h) return SEGKV_ERR_INVALID_ARG;

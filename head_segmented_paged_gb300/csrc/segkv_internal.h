@@ -129,6 +129,28 @@ struct RopeParams {
 };
 cudaError_t launch_rope(const RopeParams& p, const AppendBlob* blob, int grid, cudaStream_t s);
 
+// ---- segment transfer -------------------------------------------------------
+struct TransferRun {
+  int32_t page, slot0, nrows;  // pool rows
+  int32_t k_row, v_row;        // first buffer row of these keys / values
+  int32_t pad[3];
+};
+struct TransferParams {
+  const TransferRun* runs;
+  const int32_t* page_list;  // import: new block-table entries ...
+  const int64_t* table_idx;  // ... and their slots
+  uint4* kpool;
+  uint4* vpool;
+  const uint4* buf;          // import source
+  uint4* buf_out;            // export destination
+  int32_t* table;
+  int plan_inline;           // 1: the plan arrays are offsets into the AppendBlob
+  int to_pool;               // 1: import (buffer -> pages), 0: export
+  int n_runs, n_entries, vec_per_row, page_size;
+};
+cudaError_t launch_transfer(const TransferParams& p, const AppendBlob* blob, int grid,
+                            cudaStream_t s);
+
 cudaError_t launch_append(const AppendParams& p, const AppendBlob* blob, int grid, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, int head_dim, int grid, cudaStream_t s);

@@ -194,6 +194,35 @@ int segkv_rope_shift(segkv_t h, int layer, int seq, int32_t delta, double base, 
                      int style, uint64_t head_mask, segkv_stream_t stream);
 
 /*
+ * segkv_export — pack one sequence's kept K/V of a layer into a contiguous
+ * buffer for transfer (RedKnot summary page, section "系统收益": with prefill
+ * and decode disaggregated, only each head's kept tokens need to move).
+ * Layout: for KV head h = 0 .. Hkv-1: K rows [s_h, n) then V rows [s_h, n),
+ * each bf16 [n - s_h, D]; heads back to back.
+ *   header   host int32 [1 + Hkv], written: n, then s_h for every head.
+ *   out      device, 16-byte aligned, >= segkv_export_size bytes. out = NULL
+ *            with out_bytes = 0 only fills the header.
+ * The segment itself is unchanged. Errors: INVALID_ARG.
+ */
+int segkv_export_size(segkv_t h, int layer, int seq, size_t* bytes);
+int segkv_export(segkv_t h, int layer, int seq, void* out, size_t out_bytes, int32_t* header,
+                 segkv_stream_t stream);
+
+/*
+ * segkv_import — install an exported sequence as (layer, seq), which must be
+ * empty in that layer: tracked length n and kept start s_h per head from the
+ * header; pages floor(s_h/P) .. floor((n-1)/P) are taken lowest id first in
+ * (head ascending, page ascending) order and the rows are scattered into
+ * them. The exporter must have had the same Hkv and D.
+ *   in       device buffer from segkv_export (NULL on a host-only handle).
+ *   header   host int32 [1 + Hkv] from segkv_export.
+ * Errors: INVALID_ARG (seq not empty, bad header, short buffer),
+ * OUT_OF_PAGES; both change nothing.
+ */
+int segkv_import(segkv_t h, int layer, int seq, const void* in, size_t in_bytes,
+                 const int32_t* header, segkv_stream_t stream);
+
+/*
  * segkv_get_segment — host copy of one segment's table: kept start, kept
  * length, first logical page and the page ids in logical order (at most
  * max_ids written; *n_ids gets the count).

@@ -68,6 +68,10 @@ def test_worked_examples_match_golden_and_oracle():
             elif st["op"] == "trim":
                 rc = S.segkv_trim(h.handle, st["layer"], st["seq_ids"])
                 rm = m.trim(st["layer"], st["seq_ids"])
+            elif st["op"] == "import":
+                hdr = [st["n"]] + list(st["starts"])
+                rc = S.segkv_import(h.handle, st["layer"], st["seq"], None, hdr)
+                rm = m.import_segment(st["layer"], st["seq"], st["n"], st["starts"])
             else:
                 rc = S.segkv_free_seq(h.handle, st["seq"])
                 rm = m.free_seq(st["seq"])
@@ -102,9 +106,15 @@ def test_random_scripts_bit_exact_with_oracle(seed):
             ids = rnd.sample(range(Smax), rnd.randint(1, Smax))
             tl = rnd.choice([-1, l])
             assert S.segkv_trim(h.handle, tl, ids) == m.trim(tl, ids) == 0
-        else:
+        elif op < 0.93:
             b = rnd.randrange(Smax)
             assert S.segkv_free_seq(h.handle, b) == m.free_seq(b) == 0
+        else:  # import a transferred segment set, valid or not
+            b = rnd.randrange(Smax)
+            n = rnd.choice([0, 1, 17, 100, 300, max_len + 1])
+            starts = [rnd.randint(0, max(n, 0)) if rnd.random() < 0.5 else 0 for _ in range(H)]
+            rc = S.segkv_import(h.handle, l, b, None, [n] + starts)
+            assert rc == m.import_segment(l, b, n, starts)
         same_state(h, m, L, H, Smax)
 
 
