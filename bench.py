@@ -299,8 +299,8 @@ def run_decode(args, dev, stream, hbm, peak_src):
     w = I.ragged_decode(seed=0, steps=128)
     B, P, D = len(w.seq_lens), w.page_size, w.head_dim
     steps = w.decode_steps
-    max_len = max(w.seq_lens) + steps + 1
-    num_pages = sum((n + steps) // P + 2 for n in w.seq_lens) * w.hkv + 64
+    max_len = max(w.seq_lens) + steps + 8  # + the multi-query tokens
+    num_pages = sum((n + steps + 8) // P + 2 for n in w.seq_lens) * w.hkv + 64
     kp = torch.empty((num_pages, P, D), dtype=torch.bfloat16, device=dev)
     vp = torch.empty_like(kp)
     h = S.SegKV(1, w.hq, w.hkv, D, w.head_class, w.window, P, B, max_len, kp, vp)
@@ -347,6 +347,24 @@ def run_decode(args, dev, stream, hbm, peak_src):
     torch.cuda.synchronize()
     b2b_us = 1e3 * b0.elapsed_time(b1) / reps
     b2b_gbs = decode_bytes(w, lens) / (b2b_us * 1e-6) / 1e9
+    # four query tokens per request (speculative decoding): append four
+    # tokens each, then time the multi-query call back to back
+    T = 4
+    kt = I.normal_bf16(w.seed, I.tensor_stream(I._KD, 1, 9999), (B * T, w.hkv, D), device=dev)
+    qt = I.normal_bf16(w.seed, I.tensor_stream(I._QD, 1, 9999), (B * T, w.hq, D), device=dev)
+    h.append(0, kt, kt, np.arange(0, B * T + 1, T, dtype=np.int32), ids, stream)
+    lens_t = [x + T for x in lens]
+    ot = torch.empty((B * T, w.hq, D), dtype=torch.bfloat16, device=dev)
+    for _ in range(3):
+        h.decode_attn_multi(0, qt, T, lens_t, ids, ot, None, stream)
+    b0.record(stream)
+    for _ in range(reps):
+        h.decode_attn_multi(0, qt, T, lens_t, ids, ot, None, stream)
+    b1.record(stream)
+    torch.cuda.synchronize()
+    multi_us = 1e3 * b0.elapsed_time(b1) / reps
+    multi_bytes = decode_bytes(w, lens_t) + sum(
+        (T - 1) * w.head_dim * 4 for n in lens_t for hh in range(w.hkv) if w.head_class[0][hh])
     warm = 8
     dec_ms = [ev[s][1].elapsed_time(ev[s][2]) for s in range(warm, steps)]
     app_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(warm, steps)]
@@ -357,6 +375,10 @@ def run_decode(args, dev, stream, hbm, peak_src):
             "gbs_median": round(med, 1), "hbm_peak_gbs": hbm, "frac": round(med / hbm, 4),
             "back_to_back_gbs": round(b2b_gbs, 1), "back_to_back_frac": round(b2b_gbs / hbm, 4),
             "back_to_back_us": round(b2b_us, 2),
+            "multi_query_t4": {"us": round(multi_us, 2),
+                               "gbs": round(multi_bytes / (multi_us * 1e-6) / 1e9, 1),
+                               "frac": round(multi_bytes / (multi_us * 1e-6) / 1e9 / hbm, 4),
+                               "kernel": "prefill_kernel<128> (T*G rows per KV head)"},
             "peak_kind": peak_src,
             "decode_us_median": round(1e3 * statistics.median(dec_ms), 2),
             "append_us_median": round(1e3 * statistics.median(app_ms), 2),

@@ -28,12 +28,14 @@ SEGKV_ERR_CUDA = -4
 SEGKV_ERR_DEVICE_TIMEOUT = -5
 SEGKV_WS_PREFILL, SEGKV_WS_DECODE = 0, 1
 SEGKV_ROPE_INTERLEAVED, SEGKV_ROPE_HALF = 0, 1
+SEGKV_WINDOW_INCLUSIVE, SEGKV_WINDOW_FA = 0, 1
 
 SYMBOLS = ["segkv_create", "segkv_destroy", "segkv_append", "segkv_prefill_attn",
            "segkv_decode_attn", "segkv_trim", "segkv_free_seq", "segkv_workspace_size",
            "segkv_get_segment", "segkv_seq_len", "segkv_stats", "segkv_status",
            "segkv_last_error", "segkv_set_debug", "segkv_decode_attn_noalloc", "segkv_rope_shift",
-           "segkv_export_size", "segkv_export", "segkv_import"]
+           "segkv_export_size", "segkv_export", "segkv_import", "segkv_set_window_convention",
+           "segkv_decode_attn_multi"]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -66,6 +68,8 @@ def _load():
         "segkv_decode_attn_noalloc": [P, I, P, P, P, I, P, P],
         "segkv_rope_shift": [P, I, I, ctypes.c_int32, ctypes.c_double, I, I, ctypes.c_uint64, P],
         "segkv_export_size": [P, I, I, ctypes.POINTER(SZ)],
+        "segkv_set_window_convention": [P, I],
+        "segkv_decode_attn_multi": [P, I, P, I, P, P, I, P, P, P],
         "segkv_export": [P, I, I, P, SZ, P, P],
         "segkv_import": [P, I, I, P, SZ, P, P],
     }
@@ -185,6 +189,16 @@ def segkv_import(h, layer, seq, src, header, stream=None):
     hd = _host_i32(header)
     nbytes = 0 if src is None else src.numel() * src.element_size()
     return _lib.segkv_import(h, layer, seq, _ptr(src), nbytes, hd.ctypes.data, _stream_ptr(stream))
+
+
+def segkv_set_window_convention(h, convention):
+    return _lib.segkv_set_window_convention(h, convention)
+
+
+def segkv_decode_attn_multi(h, layer, q, T, seq_lens, seq_ids, o, lse=None, stream=None):
+    sl, ids = _host_i32(seq_lens), _host_i32(seq_ids)
+    return _lib.segkv_decode_attn_multi(h, layer, _ptr(q), T, sl.ctypes.data, ids.ctypes.data,
+                                        len(ids), _ptr(o), _ptr(lse), _stream_ptr(stream))
 
 
 def segkv_trim(h, layer, seq_ids):
@@ -322,6 +336,13 @@ class SegKV:
 
     def import_segment(self, layer, seq, buf, header, stream=None):
         return self._check(segkv_import(self._h, layer, seq, buf, header, stream))
+
+    def set_window_convention(self, convention):
+        return self._check(segkv_set_window_convention(self._h, convention))
+
+    def decode_attn_multi(self, layer, q, T, seq_lens, seq_ids, o, lse=None, stream=None):
+        return self._check(segkv_decode_attn_multi(self._h, layer, q, T, seq_lens, seq_ids, o, lse,
+                                                   stream))
 
     def trim(self, layer, seq_ids):
         return self._check(segkv_trim(self._h, layer, seq_ids))

@@ -180,6 +180,7 @@ struct segkv {
   UploadRing ring;
   PlanBlob blob;  // staging for plans small enough to travel as kernel parameters
   int debug = 0;
+  bool window_fa = false;  // win[] holds W+1 for the FlashAttention convention
   int64_t upload_bytes = 0;
   std::string err;
 
@@ -858,6 +859,42 @@ int segkv_rope_shift(segkv_t h, int layer, int seq, int32_t delta, double base, 
     if (e != cudaSuccess) return cuda_fail(h, e, "event record");
   }
   return SEGKV_OK;
+}
+
+// ---------------------------------------------------------------- variants
+int segkv_set_window_convention(segkv_t h, int convention) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (convention != SEGKV_WINDOW_INCLUSIVE && convention != SEGKV_WINDOW_FA)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "bad window convention %d", convention);
+  for (int32_t n : h->len)
+    if (n != 0) return fail(h, SEGKV_ERR_INVALID_ARG, "the handle already holds tokens");
+  // the FA window (W, 0) covers W+1 keys: the same as an inclusive window of W+1
+  const int add = (convention == SEGKV_WINDOW_FA) - (h->window_fa ? 1 : 0);
+  for (int32_t& w : h->win) w += add;
+  h->window_fa = convention == SEGKV_WINDOW_FA;
+  return SEGKV_OK;
+}
+
+int segkv_decode_attn_multi(segkv_t h, int layer, const void* q, int T, const int32_t* seq_lens,
+                            const int32_t* seq_ids, int n, void* o, float* lse,
+                            segkv_stream_t stream) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (T < 1 || n < 0 || (n > 0 && !seq_lens))
+    return fail(h, SEGKV_ERR_INVALID_ARG, "bad T or seq_lens");
+  if (layer < 0 || layer >= h->L) return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer %d", layer);
+  if (!ids_valid(h, seq_ids, n)) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq_ids");
+  std::vector<int32_t> cu(n + 1), pos(static_cast<size_t>(n) * T);
+  for (int i = 0; i < n; ++i) {
+    const int32_t nlen = h->len[h->lidx(layer, seq_ids[i])];
+    if (seq_lens[i] != nlen || nlen < T)
+      return fail(h, SEGKV_ERR_INVALID_ARG, "seq_lens[%d]=%d but seq %d has %d tokens (T=%d)", i,
+                  seq_lens[i], seq_ids[i], nlen, T);
+    cu[i] = i * T;
+    for (int t = 0; t < T; ++t) pos[static_cast<size_t>(i) * T + t] = nlen - T + t;
+  }
+  cu[n] = n * T;
+  return segkv_prefill_attn(h, layer, q, cu.data(), pos.data(), seq_ids, n, o, lse, nullptr, 0,
+                            stream);
 }
 
 // ---------------------------------------------------------------- transfer

@@ -223,6 +223,35 @@ int segkv_import(segkv_t h, int layer, int seq, const void* in, size_t in_bytes,
                  const int32_t* header, segkv_stream_t stream);
 
 /*
+ * segkv_set_window_convention — choose what a local head's window W covers.
+ *   SEGKV_WINDOW_INCLUSIVE (default): W keys including the query,
+ *     p-W+1 .. p (the reading this library takes of the summary page's
+ *     "sliding window", section "头分类稀疏").
+ *   SEGKV_WINDOW_FA: W+1 keys p-W .. p, the convention of FlashAttention's
+ *     window_size = (W, 0).
+ * Allowed only while the handle holds no tokens (every tracked length 0);
+ * kept sets, eviction and attention all follow the chosen convention.
+ * Errors: INVALID_ARG.
+ */
+enum { SEGKV_WINDOW_INCLUSIVE = 0, SEGKV_WINDOW_FA = 1 };
+int segkv_set_window_convention(segkv_t h, int convention);
+
+/*
+ * segkv_decode_attn_multi — decode with T query tokens per sequence
+ * (speculative or chunked decoding): the T newest tokens of each sequence,
+ * at positions seq_len-T .. seq_len-1, attend causally over their segments
+ * (each also to the earlier of the T). Runs on the prefill tensor-core
+ * kernel, which shares every K/V tile among the T*G query rows of a KV head.
+ *   q         device bf16 [n*T, Hq, D], sequence i's tokens at rows i*T .. i*T+T-1.
+ *   seq_lens  host int32 [n], must equal each sequence's tracked length (>= T).
+ *   o         device bf16 [n*T, Hq, D]; lse device fp32 [Hq, n*T] or NULL.
+ * Errors: INVALID_ARG, EVICTED.
+ */
+int segkv_decode_attn_multi(segkv_t h, int layer, const void* q, int T, const int32_t* seq_lens,
+                            const int32_t* seq_ids, int n, void* o, float* lse,
+                            segkv_stream_t stream);
+
+/*
  * segkv_get_segment — host copy of one segment's table: kept start, kept
  * length, first logical page and the page ids in logical order (at most
  * max_ids written; *n_ids gets the count).

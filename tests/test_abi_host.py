@@ -166,3 +166,25 @@ def test_stats_count_pages_by_class():
     st = h.stats()
     # local head keeps positions 85..99: pages 5 and 6
     assert st["pages_local"] == 2 and st["kept_tokens"] == 100 + 15
+
+
+def test_fa_window_convention_equals_inclusive_window_plus_one():
+    # FlashAttention's window (W, 0) covers W+1 keys; the kept sets and pages
+    # must equal those of the inclusive reading with W+1 (oracle page model).
+    rnd = random.Random(7)
+    W, P = 20, 8
+    fa = host_handle(1, 2, [[0, 1]], [W], P, 2, 500, 300)
+    fa.set_window_convention(S.SEGKV_WINDOW_FA)
+    m = oracle.PageModel(1, 2, [[0, 1]], [W + 1], P, 2, 500, 300)
+    for _ in range(60):
+        ids = rnd.sample(range(2), rnd.randint(1, 2))
+        ts = [rnd.choice([1, 3, 9, 30]) for _ in ids]
+        cu = np.concatenate([[0], np.cumsum(ts)]).astype(np.int32)
+        assert S.segkv_append(fa.handle, 0, None, None, cu, ids) == m.append(0, cu, ids)
+        if rnd.random() < 0.3:
+            assert S.segkv_trim(fa.handle, 0, ids) == m.trim(0, ids)
+        same_state(fa, m, 1, 2, 2)
+    # only while empty
+    assert S.segkv_set_window_convention(fa.handle, S.SEGKV_WINDOW_INCLUSIVE) == \
+        S.SEGKV_ERR_INVALID_ARG
+    assert S.segkv_set_window_convention(fa.handle, 7) == S.SEGKV_ERR_INVALID_ARG
