@@ -355,14 +355,18 @@ def run_decode(args, dev, stream, hbm, peak_src):
     h.append(0, kt, kt, np.arange(0, B * T + 1, T, dtype=np.int32), ids, stream)
     lens_t = [x + T for x in lens]
     ot = torch.empty((B * T, w.hq, D), dtype=torch.bfloat16, device=dev)
+    wst_bytes = h.workspace_size(S.SEGKV_WS_DECODE, B * T, B)
+    wst = torch.empty(wst_bytes // 4 + 64, dtype=torch.float32, device=dev) if wst_bytes else None
     for _ in range(3):
-        h.decode_attn_multi(0, qt, T, lens_t, ids, ot, None, stream)
+        h.decode_attn_multi(0, qt, T, lens_t, ids, ot, None, wst, stream)
     b0.record(stream)
     for _ in range(reps):
-        h.decode_attn_multi(0, qt, T, lens_t, ids, ot, None, stream)
+        h.decode_attn_multi(0, qt, T, lens_t, ids, ot, None, wst, stream)
     b1.record(stream)
     torch.cuda.synchronize()
     multi_us = 1e3 * b0.elapsed_time(b1) / reps
+    multi_kernel = ("decode_split_kernel<128,%d> (T*G query rows per KV head)"
+                    % (T * w.hq // w.hkv)) if wst_bytes else "prefill_kernel<128>"
     multi_bytes = decode_bytes(w, lens_t) + sum(
         (T - 1) * w.head_dim * 4 for n in lens_t for hh in range(w.hkv) if w.head_class[0][hh])
     warm = 8
@@ -378,7 +382,7 @@ def run_decode(args, dev, stream, hbm, peak_src):
             "multi_query_t4": {"us": round(multi_us, 2),
                                "gbs": round(multi_bytes / (multi_us * 1e-6) / 1e9, 1),
                                "frac": round(multi_bytes / (multi_us * 1e-6) / 1e9 / hbm, 4),
-                               "kernel": "prefill_kernel<128> (T*G rows per KV head)"},
+                               "kernel": multi_kernel},
             "peak_kind": peak_src,
             "decode_us_median": round(1e3 * statistics.median(dec_ms), 2),
             "append_us_median": round(1e3 * statistics.median(app_ms), 2),

@@ -69,7 +69,7 @@ def _load():
         "segkv_rope_shift": [P, I, I, ctypes.c_int32, ctypes.c_double, I, I, ctypes.c_uint64, P],
         "segkv_export_size": [P, I, I, ctypes.POINTER(SZ)],
         "segkv_set_window_convention": [P, I],
-        "segkv_decode_attn_multi": [P, I, P, I, P, P, I, P, P, P],
+        "segkv_decode_attn_multi": [P, I, P, I, P, P, I, P, P, P, SZ, P],
         "segkv_export": [P, I, I, P, SZ, P, P],
         "segkv_import": [P, I, I, P, SZ, P, P],
     }
@@ -195,10 +195,14 @@ def segkv_set_window_convention(h, convention):
     return _lib.segkv_set_window_convention(h, convention)
 
 
-def segkv_decode_attn_multi(h, layer, q, T, seq_lens, seq_ids, o, lse=None, stream=None):
+def segkv_decode_attn_multi(h, layer, q, T, seq_lens, seq_ids, o, lse=None, workspace=None,
+                            workspace_bytes=None, stream=None):
     sl, ids = _host_i32(seq_lens), _host_i32(seq_ids)
+    if workspace_bytes is None:
+        workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     return _lib.segkv_decode_attn_multi(h, layer, _ptr(q), T, sl.ctypes.data, ids.ctypes.data,
-                                        len(ids), _ptr(o), _ptr(lse), _stream_ptr(stream))
+                                        len(ids), _ptr(o), _ptr(lse), _ptr(workspace),
+                                        workspace_bytes, _stream_ptr(stream))
 
 
 def segkv_trim(h, layer, seq_ids):
@@ -340,9 +344,10 @@ class SegKV:
     def set_window_convention(self, convention):
         return self._check(segkv_set_window_convention(self._h, convention))
 
-    def decode_attn_multi(self, layer, q, T, seq_lens, seq_ids, o, lse=None, stream=None):
+    def decode_attn_multi(self, layer, q, T, seq_lens, seq_ids, o, lse=None, workspace=None,
+                          stream=None):
         return self._check(segkv_decode_attn_multi(self._h, layer, q, T, seq_lens, seq_ids, o, lse,
-                                                   stream))
+                                                   workspace, None, stream))
 
     def trim(self, layer, seq_ids):
         return self._check(segkv_trim(self._h, layer, seq_ids))

@@ -1,5 +1,6 @@
 // Decode attention over head-segmented pages: one query token per sequence
-// against every KV head's kept keys (RedKnot summary page, section
+// (or a few: T tokens x Gm heads form the G query rows of a KV head) against
+// every KV head's kept keys (RedKnot summary page, section
 // "SegPagedAttention": each head keeps only the keys it needs; "系统收益": many
 // concurrent long sessions per GPU). Split-KV with a running-maximum merge of
 // the pieces (KV-cache architecture page, section 5.2).
@@ -53,13 +54,16 @@ struct DCfg {
   static constexpr int OFF_P = OFF_V + NS * STAGE;         // float [NW][KW][G]
   static constexpr int OFF_MRG = OFF_P + NW * KW * G * 4;  // float [NW/2][G][D]
   static constexpr int OFF_ML = OFF_MRG + (NW / 2) * G * D * 4;  // float [NW/2][G][2]
+  static constexpr int META = sizeof(DecodeUnit);
   static constexpr int OFF_META = (OFF_ML + (NW / 2) * G * 2 * 4 + 31) & ~31;  // DecodeUnit [NS]
-  static constexpr int OFF_QB = OFF_META + NS * 32;                            // bf16 [NS][G][D]
+  static constexpr int OFF_QB = OFF_META + NS * META;                          // bf16 [NS][G][D]
   static constexpr int OFF_BAR = (OFF_QB + NS * G * D * 2 + 15) & ~15;
   static constexpr int OFF_MISC = OFF_BAR + 2 * NS * 8;
   static constexpr int BYTES = OFF_MISC + 16;
-  // two CTAs per SM when their shared memory fits
-  static constexpr int MIN_BLOCKS = BYTES <= 110 * 1024 ? 2 : 1;
+  // two CTAs per SM when their shared memory fits and the query rows leave
+  // registers for two; 8 or more rows of 128 dims take one CTA and 255
+  // registers (two would spill the per-lane query and accumulator rows)
+  static constexpr int MIN_BLOCKS = (BYTES <= 110 * 1024 && !(D == 128 && G >= 8)) ? 2 : 1;
 };
 
 template <int N>
@@ -91,7 +95,8 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
 
 }  // namespace
 
-template <int D, int G>
+// MQ: several query tokens per sequence (T > 1), each row with its own key limits
+template <int D, int G, bool MQ>
 __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
     decode_split_kernel(const DecodeParams p, const __grid_constant__ PlanBlob blob) {
   using C = DCfg<D, G>;
@@ -148,15 +153,24 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
         if (lane == 0) {
           uint32_t bytes = static_cast<uint32_t>((vhi - vlo) * C::ROW * 2);
           if (first) {  // the unit's descriptor and its G query rows travel with its first stage
-            *reinterpret_cast<DecodeUnit*>(sm + C::OFF_META + st * 32) = U;
+            *reinterpret_cast<DecodeUnit*>(sm + C::OFF_META + st * C::META) = U;
             bytes += G * D * 2;
           }
           mbar_expect_tx(full(st), bytes);
-          if (first)
-            bulk_g2s(sbase + C::OFF_QB + st * G * D * 2,
-                     static_cast<const __nv_bfloat16*>(p.q) +
-                         (static_cast<int64_t>(U.req) * p.hq + U.head * G) * D,
-                     G * D * 2, full(st));
+          if (first) {
+            if constexpr (MQ) {  // row t * Gm + j = token t, query head head * Gm + j
+              for (int t = 0; t < p.T; ++t)
+                bulk_g2s(sbase + C::OFF_QB + (st * G + t * p.Gm) * D * 2,
+                         static_cast<const __nv_bfloat16*>(p.q) +
+                             (static_cast<int64_t>(U.req * p.T + t) * p.hq + U.head * p.Gm) * D,
+                         p.Gm * D * 2, full(st));
+            } else {
+              bulk_g2s(sbase + C::OFF_QB + st * G * D * 2,
+                       static_cast<const __nv_bfloat16*>(p.q) +
+                           (static_cast<int64_t>(U.req) * p.hq + U.head * G) * D,
+                       G * D * 2, full(st));
+            }
+          }
         }
         armed[st] = static_cast<int>(ph);
         for (int pos = vlo; pos < vhi;) {
@@ -194,7 +208,15 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
   for (int u = u_begin; u < u_end; ++u) {
     // the unit's descriptor and query rows arrive with its first stage
     if (!waitw(full(gs % NS), (gs / NS) & 1, wc)) break;
-    const DecodeUnit U = *reinterpret_cast<const DecodeUnit*>(sm + C::OFF_META + (gs % NS) * 32);
+    const DecodeUnit U = *reinterpret_cast<const DecodeUnit*>(sm + C::OFF_META + (gs % NS) * C::META);
+    // the keys this lane's query row may see: up to its own position, and for
+    // a local head no further back than its window (with one query token per
+    // sequence the unit's key range holds exactly these)
+    int p_own = 0, lo_own = 0;
+    if constexpr (MQ) {
+      p_own = U.q_last - (p.T - 1) + g_own / p.Gm;
+      lo_own = U.local ? p_own - p.window + 1 : 0;
+    }
     // this lane's dims of the G query rows (chunks sub, sub+LG, ... of 8 dims,
     // or 4 dims at sub*4 when D/LG = 4), pre-scaled to log2 units
     float2 q2[G][C::DPL / 2];
@@ -236,6 +258,9 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
       if (!waitw(full(st), ph, wc)) { ok = false; break; }
       const int base = w * C::SK;
       const int vlo = max(U.k0, base) - base, vhi = min(U.k1, base + C::SK) - base;
+      // the keys of this stage the lane's query row sees
+      const int vlo_own = MQ ? max(vlo, lo_own - base) : vlo;
+      const int vhi_own = MQ ? min(vhi, p_own + 1 - base) : vhi;
       const int mine0 = warp * C::KW;
       if (mine0 < vhi && mine0 + C::KW > vlo) {
         const uint8_t* sK = sm + C::OFF_K + st * C::STAGE;
@@ -274,7 +299,7 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
           }
           const float tot = reduce_scatter<C::LG>(part, sub);
           const int kidx = key0 + sub / G;
-          sr[r] = (kidx >= vlo && kidx < vhi) ? tot : -INFINITY;
+          sr[r] = (kidx >= vlo_own && kidx < vhi_own) ? tot : -INFINITY;
         }
         // online softmax for head g_own over this warp's keys
         float mx = sr[0];
@@ -375,8 +400,20 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
     }
     consumer_sync<NCONS>();
     const bool single = U.pair_units == 1;
-    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) +
-                          (static_cast<int64_t>(U.req) * p.hq + U.head * G) * D;
+    const int pair = U.req * p.hkv + U.head;
+    // query row g is token g / Gm of the sequence, query head head * Gm + g % Gm
+    auto out_at = [&](int g) -> __nv_bfloat16* {
+      if constexpr (!MQ)
+        return static_cast<__nv_bfloat16*>(p.o) + (static_cast<int64_t>(U.req) * p.hq + U.head * G + g) * D;
+      const int t = g / p.Gm;
+      return static_cast<__nv_bfloat16*>(p.o) +
+             (static_cast<int64_t>(U.req * p.T + t) * p.hq + U.head * p.Gm + g - t * p.Gm) * D;
+    };
+    auto put_lse = [&](int g, float M, float Ls) {  // natural-log LSE of row g
+      const int t = g / p.Gm;
+      p.lse[static_cast<int64_t>(U.head * p.Gm + g - t * p.Gm) * p.n_rows + U.req * p.T + t] =
+          (M + log2f(Ls)) * 0.6931471805599453f;
+    };
     for (int idx = tid; idx < G * D; idx += NCONS) {
       const int g = idx / D, d = idx - g * D;
       float M = -INFINITY;
@@ -391,7 +428,8 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
         o = fmaf(wgt, mrg[(x * G + g) * D + d], o);
       }
       if (single) {
-        orow[g * D + d] = __float2bfloat16_rn(o / Ls);
+        out_at(g)[d] = __float2bfloat16_rn(o / Ls);
+        if (MQ && p.lse != nullptr && d == 0) put_lse(g, M, Ls);
       } else {
         p.part_acc[(static_cast<int64_t>(u) * G + g) * D + d] = o;
         if (d == 0) {
@@ -403,7 +441,7 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
     if (!single) {
       __threadfence();
       consumer_sync<NCONS>();
-      if (tid == 0) *last_flag = atomicAdd(p.pair_cnt + U.pair, 1) == U.pair_units - 1;
+      if (tid == 0) *last_flag = atomicAdd(p.pair_cnt + pair, 1) == U.pair_units - 1;
       consumer_sync<NCONS>();
       if (*last_flag) {
         // the last slice of the pair merges every slice's partials; four
@@ -421,42 +459,53 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
               ll[j] = __ldcg(p.part_ml + (uu * G + g) * 2 + 1);
               aa[j] = __ldcg(p.part_acc + (uu * G + g) * D + d);
             }
+            // a slice may hold no key a row sees (several query tokens per
+            // sequence): its maximum is -inf and its weight 0
             const float Mn = fmaxf(fmaxf(M, fmaxf(mm[0], mm[1])), fmaxf(mm[2], mm[3]));
-            const float sc = ex2(M - Mn);
+            const float Mr = (Mn == -INFINITY) ? 0.f : Mn;
+            const float sc = ex2(M - Mr);
             Ls *= sc;
             o *= sc;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-              const float wgt = ex2(mm[j] - Mn);
+              const float wgt = ex2(mm[j] - Mr);
               Ls = fmaf(wgt, ll[j], Ls);
               o = fmaf(wgt, aa[j], o);
             }
             M = Mn;
           }
-          orow[g * D + d] = __float2bfloat16_rn(o / Ls);
+          out_at(g)[d] = __float2bfloat16_rn(o / Ls);
+          if (MQ && p.lse != nullptr && d == 0) put_lse(g, M, Ls);
         }
-        if (tid == 0) p.pair_cnt[U.pair] = 0;  // ready for the next call
+        if (tid == 0) p.pair_cnt[pair] = 0;  // ready for the next call
       }
     }
     consumer_sync<NCONS>();  // merge buffers are free again
   }
 }
 
-template <int D, int G>
-static cudaError_t launch_dg(const DecodeParams& p, const PlanBlob* blob, int grid, cudaStream_t s) {
+template <int D, int G, bool MQ>
+static cudaError_t launch_dgm(const DecodeParams& p, const PlanBlob* blob, int grid, cudaStream_t s) {
   using C = DCfg<D, G>;
   static const PlanBlob empty_blob{};
   static bool attr_set[kMaxDevices] = {};  // the attribute outlives the launch
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= kMaxDevices || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G>,
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G, MQ>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
     if (e != cudaSuccess) return e;
     if (dev < kMaxDevices) attr_set[dev] = true;
   }
-  decode_split_kernel<D, G><<<grid, C::THREADS, C::BYTES, s>>>(p, blob ? *blob : empty_blob);
+  decode_split_kernel<D, G, MQ><<<grid, C::THREADS, C::BYTES, s>>>(p, blob ? *blob : empty_blob);
   return cudaGetLastError();
+}
+
+template <int D, int G>
+static cudaError_t launch_dg(const DecodeParams& p, const PlanBlob* blob, int grid, cudaStream_t s) {
+  // the single-token variant skips the per-row limits and writes no LSE
+  return (p.T > 1 || p.lse != nullptr) ? launch_dgm<D, G, true>(p, blob, grid, s)
+                                       : launch_dgm<D, G, false>(p, blob, grid, s);
 }
 
 template <int D>
@@ -478,6 +527,25 @@ int decode_stage_keys(int G) {
     case 4: return DCfg<128, 4>::SK;
     case 8: return DCfg<128, 8>::SK;
     default: return DCfg<128, 16>::SK;
+  }
+}
+
+int decode_ctas_per_sm(int head_dim, int G) {
+  if (head_dim == 64) {
+    switch (G) {
+      case 1: return DCfg<64, 1>::MIN_BLOCKS;
+      case 2: return DCfg<64, 2>::MIN_BLOCKS;
+      case 4: return DCfg<64, 4>::MIN_BLOCKS;
+      case 8: return DCfg<64, 8>::MIN_BLOCKS;
+      default: return DCfg<64, 16>::MIN_BLOCKS;
+    }
+  }
+  switch (G) {
+    case 1: return DCfg<128, 1>::MIN_BLOCKS;
+    case 2: return DCfg<128, 2>::MIN_BLOCKS;
+    case 4: return DCfg<128, 4>::MIN_BLOCKS;
+    case 8: return DCfg<128, 8>::MIN_BLOCKS;
+    default: return DCfg<128, 16>::MIN_BLOCKS;
   }
 }
 

@@ -643,67 +643,77 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
 // boundary.
 static int decode_max_grid(const segkv* h) { return h->num_sms > 0 ? 2 * h->num_sms : 1024; }
 
-static size_t decode_ws_bytes(const segkv* h, int64_t units, int64_t pairs, size_t* acc_bytes,
+// rows = query rows per KV head (T * G)
+static size_t decode_ws_bytes(const segkv* h, int64_t units, int rows, size_t* acc_bytes,
                               size_t* ml_bytes) {
-  *acc_bytes = align_up(static_cast<size_t>(units) * h->G * h->D * 4, 256);
-  *ml_bytes = align_up(static_cast<size_t>(units) * h->G * 2 * 4, 256);
-  (void)pairs;
+  *acc_bytes = align_up(static_cast<size_t>(units) * rows * h->D * 4, 256);
+  *ml_bytes = align_up(static_cast<size_t>(units) * rows * 2 * 4, 256);
   return *acc_bytes + *ml_bytes;
 }
 
+// The split-KV decode kernel takes up to 16 query rows per KV head.
+static bool decode_kernel_rows(int rows) {
+  return rows == 1 || rows == 2 || rows == 4 || rows == 8 || rows == 16;
+}
+
 int segkv_workspace_size(segkv_t h, int kind, int64_t n_tokens, int n_seqs, size_t* bytes) {
-  (void)n_tokens;
-  if (!h || !bytes || n_seqs < 0) return SEGKV_ERR_INVALID_ARG;
+  if (!h || !bytes || n_seqs < 0 || n_tokens < 0) return SEGKV_ERR_INVALID_ARG;
   if (kind == SEGKV_WS_PREFILL) {
     *bytes = 0;
     return SEGKV_OK;
   }
   if (kind != SEGKV_WS_DECODE) return fail(h, SEGKV_ERR_INVALID_ARG, "bad workspace kind");
+  // T = n_tokens / n_seqs query tokens per sequence (at least 1)
+  const int64_t T = n_seqs > 0 ? std::max<int64_t>(1, (n_tokens + n_seqs - 1) / n_seqs) : 1;
+  const int64_t rows = T * h->G;
+  if (rows > 16 || !decode_kernel_rows(static_cast<int>(rows))) {
+    *bytes = 0;  // served by the prefill kernel, which needs none
+    return SEGKV_OK;
+  }
   const int64_t pairs = int64_t(n_seqs) * h->Hkv;
   size_t a, m;
-  *bytes = decode_ws_bytes(h, pairs + decode_max_grid(h), pairs, &a, &m);
+  *bytes = decode_ws_bytes(h, pairs + decode_max_grid(h), static_cast<int>(rows), &a, &m);
   return SEGKV_OK;
 }
 
-int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_lens,
-                      const int32_t* seq_ids, int n, void* o, void* workspace,
-                      size_t workspace_bytes, segkv_stream_t stream) {
-  if (!h) return SEGKV_ERR_INVALID_ARG;
-  if (h->host_only) return fail(h, SEGKV_ERR_INVALID_ARG, "host-only handle has no pools");
-  if (layer < 0 || layer >= h->L) return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer %d", layer);
-  if (!ids_valid(h, seq_ids, n)) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq_ids");
-  if (n == 0) return SEGKV_OK;
-  if (!q || !o || !seq_lens) return fail(h, SEGKV_ERR_INVALID_ARG, "q/o/seq_lens NULL");
-  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(o)) & 15)
-    return fail(h, SEGKV_ERR_INVALID_ARG, "q and o must be 16-byte aligned");
+// Split-KV decode of the T newest tokens of n sequences: T * G query rows per
+// KV head, each with its own causal (and window) limit.
+static int decode_core(segkv* h, int layer, const void* q, int T, const int32_t* seq_lens,
+                       const int32_t* seq_ids, int n, void* o, float* lse, void* workspace,
+                       size_t workspace_bytes, cudaStream_t s) {
   const int W = h->win[layer];
+  const int rows = T * h->G;
   // pairs (req, head) with their key ranges [lo, n)
-  struct Range { int32_t req, head, lo, n, row; };
+  struct Range { int32_t req, head, lo, n, row, local; };
   std::vector<Range> ranges;
   int64_t total = 0;
   for (int i = 0; i < n; ++i) {
     const int b = seq_ids[i];
     const int32_t nlen = h->len[h->lidx(layer, b)];
-    if (seq_lens[i] != nlen || nlen < 1)
-      return fail(h, SEGKV_ERR_INVALID_ARG, "seq_lens[%d]=%d but seq %d has %d tokens", i,
-                  seq_lens[i], b, nlen);
-    const int32_t p = nlen - 1;
+    if (seq_lens[i] != nlen || nlen < T)
+      return fail(h, SEGKV_ERR_INVALID_ARG, "seq_lens[%d]=%d but seq %d has %d tokens (T=%d)", i,
+                  seq_lens[i], b, nlen, T);
+    const int32_t p0 = nlen - T;  // the oldest query token's position
     for (int hd = 0; hd < h->Hkv; ++hd) {
-      const int32_t lo = h->local(layer, hd) ? std::max(0, p - W + 1) : 0;
+      const int local = h->local(layer, hd) ? 1 : 0;
+      const int32_t lo = local ? std::max(0, p0 - W + 1) : 0;
       if (lo < h->start[h->seg(layer, hd, b)])
         return fail(h, SEGKV_ERR_EVICTED, "seq %d head %d: key %d already evicted", b, hd, lo);
-      ranges.push_back({i, hd, lo, nlen, static_cast<int32_t>(h->seg(layer, hd, b))});
+      ranges.push_back({i, hd, lo, nlen, static_cast<int32_t>(h->seg(layer, hd, b)), local});
       total += nlen - lo;
     }
   }
   // stream-K split: CTA c streams keys [c*per, (c+1)*per) of the concatenated ranges
-  const int64_t sk = decode_stage_keys(h->G);
-  const int grid = static_cast<int>(std::max<int64_t>(
-      1, std::min<int64_t>(decode_max_grid(h), (total + sk - 1) / sk)));
+  const int64_t sk = decode_stage_keys(rows);
+  const int64_t ctas = h->num_sms > 0 ? int64_t(h->num_sms) * decode_ctas_per_sm(h->D, rows)
+                                      : decode_max_grid(h);
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(
+      std::min<int64_t>(ctas, decode_max_grid(h)), (total + sk - 1) / sk)));
   const int64_t per = (total + grid - 1) / grid;
   std::vector<DecodeUnit> units;
   std::vector<int32_t> pair_unit0(ranges.size()), pair_units(ranges.size(), 0);
   std::vector<int32_t> cta_begin(grid + 1);
+  std::vector<int32_t> unit_pair;  // ranges are pushed per (req, head): pair r = req * Hkv + head
   size_t r = 0;
   int32_t off = 0;
   for (int c = 0; c < grid; ++c) {
@@ -715,12 +725,14 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
       if (off == 0) pair_unit0[r] = static_cast<int32_t>(units.size());
       DecodeUnit u{};
       u.req = R.req;
-      u.head = R.head;
+      u.head = static_cast<int16_t>(R.head);
+      u.local = static_cast<int16_t>(R.local);
       u.k0 = R.lo + off;
       u.k1 = R.lo + off + take;
       u.table_row = R.row;
-      u.pair = static_cast<int32_t>(r);
+      u.q_last = R.n - 1;
       units.push_back(u);
+      unit_pair.push_back(static_cast<int32_t>(r));
       ++pair_units[r];
       off += take;
       left -= take;
@@ -731,13 +743,13 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
     }
   }
   cta_begin[grid] = static_cast<int32_t>(units.size());
-  for (DecodeUnit& u : units) {
-    u.pair_unit0 = pair_unit0[u.pair];
-    u.pair_units = pair_units[u.pair];
+  for (size_t x = 0; x < units.size(); ++x) {
+    units[x].pair_unit0 = pair_unit0[unit_pair[x]];
+    units[x].pair_units = pair_units[unit_pair[x]];
   }
   size_t acc_bytes, ml_bytes;
-  const size_t need = decode_ws_bytes(h, static_cast<int64_t>(units.size()),
-                                      static_cast<int64_t>(ranges.size()), &acc_bytes, &ml_bytes);
+  const size_t need =
+      decode_ws_bytes(h, static_cast<int64_t>(units.size()), rows, &acc_bytes, &ml_bytes);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255))
     return fail(h, SEGKV_ERR_INVALID_ARG, "workspace needs %zu bytes (256-aligned), got %zu", need,
                 workspace_bytes);
@@ -745,7 +757,6 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
   Pack pk;
   const size_t o_units = pk.add(units.data(), units.size());
   const size_t o_cta = pk.add(cta_begin.data(), cta_begin.size());
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool inl = pk.buf.size() <= sizeof(PlanBlob);
   size_t off_ring = 0;
   uintptr_t d = 0;  // device address of the plan; 0 (offsets alone) when it is inline
@@ -774,11 +785,17 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
   p.part_acc = static_cast<float*>(workspace);
   p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + acc_bytes);
   p.pair_cnt = h->d_pair_cnt;
+  p.lse = lse;
+  p.n_rows = n * T;
   p.n_units = static_cast<int>(units.size());
   p.n_pairs = static_cast<int>(ranges.size());
   p.R = h->R;
   p.hq = h->Hq;
-  p.G = h->G;
+  p.hkv = h->Hkv;
+  p.G = rows;
+  p.T = T;
+  p.Gm = h->G;
+  p.window = W;
   p.page_size = h->P;
   p.scale_log2 = h->scale * 1.4426950408889634f;
   p.status = h->d_status;
@@ -790,6 +807,21 @@ int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_le
     if (e != cudaSuccess) return cuda_fail(h, e, "event record");
   }
   return SEGKV_OK;
+}
+
+int segkv_decode_attn(segkv_t h, int layer, const void* q, const int32_t* seq_lens,
+                      const int32_t* seq_ids, int n, void* o, void* workspace,
+                      size_t workspace_bytes, segkv_stream_t stream) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (h->host_only) return fail(h, SEGKV_ERR_INVALID_ARG, "host-only handle has no pools");
+  if (layer < 0 || layer >= h->L) return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer %d", layer);
+  if (!ids_valid(h, seq_ids, n)) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq_ids");
+  if (n == 0) return SEGKV_OK;
+  if (!q || !o || !seq_lens) return fail(h, SEGKV_ERR_INVALID_ARG, "q/o/seq_lens NULL");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(o)) & 15)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "q and o must be 16-byte aligned");
+  return decode_core(h, layer, q, 1, seq_lens, seq_ids, n, o, nullptr, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------- rope shift
@@ -876,13 +908,22 @@ int segkv_set_window_convention(segkv_t h, int convention) {
 }
 
 int segkv_decode_attn_multi(segkv_t h, int layer, const void* q, int T, const int32_t* seq_lens,
-                            const int32_t* seq_ids, int n, void* o, float* lse,
-                            segkv_stream_t stream) {
+                            const int32_t* seq_ids, int n, void* o, float* lse, void* workspace,
+                            size_t workspace_bytes, segkv_stream_t stream) {
   if (!h) return SEGKV_ERR_INVALID_ARG;
   if (T < 1 || n < 0 || (n > 0 && !seq_lens))
     return fail(h, SEGKV_ERR_INVALID_ARG, "bad T or seq_lens");
   if (layer < 0 || layer >= h->L) return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer %d", layer);
   if (!ids_valid(h, seq_ids, n)) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq_ids");
+  if (decode_kernel_rows(T * h->G) && !h->host_only) {
+    if (n == 0) return SEGKV_OK;
+    if (!q || !o) return fail(h, SEGKV_ERR_INVALID_ARG, "q/o NULL");
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(o)) & 15)
+      return fail(h, SEGKV_ERR_INVALID_ARG, "q and o must be 16-byte aligned");
+    return decode_core(h, layer, q, T, seq_lens, seq_ids, n, o, lse, workspace, workspace_bytes,
+                       static_cast<cudaStream_t>(stream));
+  }
+  // more than 16 query rows per KV head: the tensor-core prefill kernel
   std::vector<int32_t> cu(n + 1), pos(static_cast<size_t>(n) * T);
   for (int i = 0; i < n; ++i) {
     const int32_t nlen = h->len[h->lidx(layer, seq_ids[i])];
@@ -1191,7 +1232,7 @@ size_t decode_partials_bytes(segkv* h, int layer, const int32_t* seq_lens,
   if (!h || layer < 0 || layer >= h->L || !seq_lens || !ids_valid(h, seq_ids, n)) return 0;
   const int64_t pairs = int64_t(n) * h->Hkv;
   size_t a, m;
-  return decode_ws_bytes(h, pairs + decode_max_grid(h), pairs, &a, &m);
+  return decode_ws_bytes(h, pairs + decode_max_grid(h), h->G, &a, &m);
 }
 
 int set_error(segkv* h, int code, const char* msg) { return fail(h, code, "%s", msg); }

@@ -86,28 +86,35 @@ struct PrefillParams {
 
 // ---- decode ---------------------------------------------------------------
 struct DecodeUnit {
-  int32_t req;         // row of q / o
-  int32_t head;        // KV head
+  int32_t req;         // sequence index i of the call (row i*T of q / o)
+  int16_t head;        // KV head; the unit's pair (req, head) is req * Hkv + head
+  int16_t local;       // 1: local head, each query row sees only its window
   int32_t k0, k1;      // keys [k0, k1)
   int32_t table_row;
-  int32_t pair;        // index of its (req, head) pair
   int32_t pair_unit0;  // first unit of that pair
   int32_t pair_units;  // units of that pair
+  int32_t q_last;      // position of the sequence's newest query token (length - 1)
 };
+static_assert(sizeof(DecodeUnit) == 32, "decode units are staged in 32-byte slots");
 struct DecodeParams {
   const DecodeUnit* units;   // grouped by CTA
   const int32_t* cta_begin;  // [grid + 1]: CTA c runs units cta_begin[c] .. cta_begin[c+1]-1
   int plan_inline;           // 1: units and cta_begin are offsets into the PlanBlob
-  const void* q;             // bf16 [n, Hq, D]
-  void* o;                   // bf16 [n, Hq, D]
+  const void* q;             // bf16 [n * T, Hq, D]
+  void* o;                   // bf16 [n * T, Hq, D]
   const int32_t* table;
   const void* kpool;
   const void* vpool;
   float* part_acc;           // [n_units, G, D]
   float* part_ml;            // [n_units, G, 2]
   int* pair_cnt;             // [>= n_pairs]: zero before the launch, left zero after it
+  float* lse;                // fp32 [Hq, n_rows] or null
+  int n_rows;                // n * T query tokens
   int n_units, n_pairs;
-  int R, hq, G, page_size;
+  int R, hq, hkv, page_size;
+  int G;                     // query rows per KV head, T * Gm: 1, 2, 4, 8 or 16
+  int T, Gm;                 // query tokens per sequence; query heads per KV head
+  int window;                // keys a local head's query sees
   float scale_log2;
   int* status;
   unsigned long long timeout_ns;
@@ -159,5 +166,6 @@ int prefill_unit_tokens(int G);  // query tokens per prefill work unit
 cudaError_t launch_decode(const DecodeParams& p, const PlanBlob* blob, int head_dim, int grid,
                           cudaStream_t s);
 int decode_stage_keys(int G);  // keys per decode pipeline stage
+int decode_ctas_per_sm(int head_dim, int G);  // resident decode CTAs per SM
 
 }  // namespace skv

@@ -171,7 +171,8 @@ int segkv_trim(segkv_t h, int layer, const int32_t* seq_ids, int n);
 int segkv_free_seq(segkv_t h, int seq_id);
 
 /* segkv_workspace_size — device workspace a call needs. kind SEGKV_WS_DECODE:
- * n_seqs sequences (n_tokens ignored); SEGKV_WS_PREFILL: 0. */
+ * n_seqs sequences with n_tokens query tokens in all (n_tokens = n_seqs for
+ * segkv_decode_attn, n*T for segkv_decode_attn_multi); SEGKV_WS_PREFILL: 0. */
 int segkv_workspace_size(segkv_t h, int kind, int64_t n_tokens, int n_seqs, size_t* bytes);
 
 /*
@@ -240,16 +241,21 @@ int segkv_set_window_convention(segkv_t h, int convention);
  * segkv_decode_attn_multi — decode with T query tokens per sequence
  * (speculative or chunked decoding): the T newest tokens of each sequence,
  * at positions seq_len-T .. seq_len-1, attend causally over their segments
- * (each also to the earlier of the T). Runs on the prefill tensor-core
- * kernel, which shares every K/V tile among the T*G query rows of a KV head.
+ * (each also to the earlier of the T; a local head's token at p to keys
+ * p-W+1 .. p). When T * (Hq/Hkv) is 1, 2, 4, 8 or 16 the T*G query rows of
+ * a KV head share every K/V read in the split-KV decode kernel; otherwise
+ * the call runs on the prefill tensor-core kernel.
  *   q         device bf16 [n*T, Hq, D], sequence i's tokens at rows i*T .. i*T+T-1.
  *   seq_lens  host int32 [n], must equal each sequence's tracked length (>= T).
- *   o         device bf16 [n*T, Hq, D]; lse device fp32 [Hq, n*T] or NULL.
+ *   o         device bf16 [n*T, Hq, D]; lse device fp32 [Hq, n*T] or NULL
+ *             (natural log of each row's softmax denominator, scaled scores).
+ *   workspace device, >= segkv_workspace_size(SEGKV_WS_DECODE, n*T, n) bytes,
+ *             256-byte aligned (may be NULL when that size is 0).
  * Errors: INVALID_ARG, EVICTED.
  */
 int segkv_decode_attn_multi(segkv_t h, int layer, const void* q, int T, const int32_t* seq_lens,
-                            const int32_t* seq_ids, int n, void* o, float* lse,
-                            segkv_stream_t stream);
+                            const int32_t* seq_ids, int n, void* o, float* lse, void* workspace,
+                            size_t workspace_bytes, segkv_stream_t stream);
 
 /*
  * segkv_get_segment — host copy of one segment's table: kept start, kept

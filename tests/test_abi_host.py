@@ -153,6 +153,12 @@ def test_workspace_size_and_host_only_attention_refused():
     ws = h.workspace_size(S.SEGKV_WS_DECODE, 0, 4)
     G, D, units = 4, 64, 4 * 2 * (2 + 1)
     assert ws >= units * G * D * 4 + units * G * 8
+    # T query tokens per sequence: T * G rows per KV head; past 16 rows the
+    # prefill kernel serves the call and needs none
+    assert h.workspace_size(S.SEGKV_WS_DECODE, 4, 4) == ws
+    assert h.workspace_size(S.SEGKV_WS_DECODE, 16, 4) >= 4 * ws - 1024
+    assert h.workspace_size(S.SEGKV_WS_DECODE, 12, 4) == 0  # 12 rows
+    assert h.workspace_size(S.SEGKV_WS_DECODE, 32, 4) == 0  # 32 rows
     rc = S.segkv_prefill_attn(h.handle, 0, None, [0, 1], [0], [0], None)
     assert rc == S.SEGKV_ERR_INVALID_ARG
 

@@ -11,7 +11,10 @@ from harness import Cache, check_close
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("T,G", [(1, 4), (4, 4), (7, 8), (16, 2)])
+# T * G in {1, 2, 4, 8, 16} runs on the split-KV decode kernel, the rest on
+# the prefill kernel
+@pytest.mark.parametrize("T,G", [(1, 4), (4, 4), (2, 8), (4, 2), (16, 1), (2, 1),
+                                 (3, 4), (7, 8), (16, 2)])
 def test_multi_query_decode_matches_oracle(T, G):
     hkv, d, P, W = 4, 128, 64, 200
     hc = [[I.GLOBAL, I.LOCAL, I.LOCAL, I.LOCAL]]
@@ -32,7 +35,10 @@ def test_multi_query_decode_matches_oracle(T, G):
     q = I.normal_bf16(52, 3, (B * T, hkv * G, d))
     o = torch.full((B * T, hkv * G, d), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((hkv * G, B * T), dtype=torch.float32, device="cuda")
-    c.h.decode_attn_multi(0, q.cuda(), T, lens, ids, o, lse)
+    wsb = c.h.workspace_size(S.SEGKV_WS_DECODE, B * T, B)
+    assert (wsb > 0) == (T * G in (1, 2, 4, 8, 16))
+    ws = torch.empty(wsb // 4 + 64, device="cuda") if wsb else None
+    c.h.decode_attn_multi(0, q.cuda(), T, lens, ids, o, lse, ws)
     assert c.h.status() == 0
     row_seq = np.repeat(np.arange(B), T).astype(np.int32)
     row_pos = np.concatenate([np.arange(n - T, n) for n in lens]).astype(np.int32)
@@ -45,9 +51,12 @@ def test_multi_query_decode_matches_oracle(T, G):
         o1 = torch.empty_like(o)
         c.h.decode_attn(0, q.cuda(), lens, ids, o1, ws)
         check_close(o1, ref, "split-KV decode")
-    # a too-large T is refused
+    # a too-large T is refused, and so is a short workspace
     assert S.segkv_decode_attn_multi(c.h.handle, 0, q.cuda(), 100, lens, ids, o) == \
         S.SEGKV_ERR_INVALID_ARG
+    if wsb:
+        assert S.segkv_decode_attn_multi(c.h.handle, 0, q.cuda(), T, lens, ids, o, None, ws,
+                                         256) == S.SEGKV_ERR_INVALID_ARG
 
 
 def test_fa_window_convention_prefill_and_decode():
