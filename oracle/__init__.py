@@ -1,7 +1,9 @@
 """Oracle for head-segmented paged attention. TEST INFRASTRUCTURE ONLY.
 
 Python side of the plain fp64 C++ oracle in ``segkv_oracle.cpp``: the page
-model (kept sets, page ids) and attention over explicit per-head key sets.
+model (kept sets, page ids), attention over explicit per-head key sets, the
+attention mass each key receives, and the rotary re-alignment. The token
+selection and FFN of sparse FFN routing are in ``sparse_ffn.py``.
 Only the tests, the smoke check and the benchmark's CPU-baseline leg may use
 it; the library never imports it. See the C++ file for the sources and the
 readings of the pages it follows.
@@ -54,6 +56,8 @@ def lib():
         _lib.orc_attention.argtypes = att + [P, P]
         _lib.orc_attention_blocked.argtypes = att + [I, P, P]
         _lib.orc_rope.argtypes = [P, I64, I, I, I, ctypes.c_double, P]
+        _lib.orc_attn_mass.argtypes = [I, I, I, ctypes.c_double, P, P, P, P, P, I, P, P, I, P,
+                                       I64, I64, P]
     return _lib
 
 
@@ -176,3 +180,25 @@ def rope(x, pos, rotary_dim, style, base):
     if rc != OK:
         raise ValueError("orc_rope: bad arguments")
     return v.reshape(shape)
+
+
+def attn_mass(q, k, row_seq, row_pos, kv_off, kv_len, head_class, window, seg_start, scale=None):
+    """fp64 attention mass each key receives from the listed query tokens
+    (see orc_attn_mass): returns (status, mass [Hkv, sum kv_len]); key j of
+    sequence b is column kv_off[b] + j."""
+    nq, hq, d = q.shape
+    hkv = k.shape[1]
+    qb, kb = _bf16_bits(q), _bf16_bits(k)
+    ko = np.ascontiguousarray(np.asarray(kv_off, dtype=np.int64))
+    kl = _i32(kv_len)
+    hc = np.ascontiguousarray(np.asarray(head_class, dtype=np.uint8))
+    ss = _i32(seg_start).reshape(-1)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    nkeys = k.shape[0]
+    mass = np.zeros((hkv, nkeys), dtype=np.float64)
+    rc = lib().orc_attn_mass(hq, hkv, d, ctypes.c_double(scale), _ptr(qb), _ptr(_i32(row_seq)),
+                             _ptr(_i32(row_pos)), _ptr(ko), _ptr(kl), len(kl), _ptr(kb), _ptr(hc),
+                             int(window), _ptr(ss), ctypes.c_int64(nq), ctypes.c_int64(nkeys),
+                             _ptr(mass))
+    return rc, mass

@@ -449,3 +449,61 @@ extern "C" int orc_rope(double* x, int64_t rows, int d, int rotary_dim, int styl
   }
   return OK;
 }
+
+// ---------------------------------------------------------------------------
+// Part 5: attention mass received by each key (RedKnot summary page, section
+// "稀疏 FFN（Sparse FFN）": the dense FFN runs only on the tokens with the
+// highest attention scores, the others take the residual identity path).
+// Reading: a token's score is the softmax probability it receives as a key,
+// summed over the listed query rows and over every query head. Per KV head h
+// the sum over its query heads goes to mass[h * nkeys + kv_off[b] + j] for
+// key j of sequence b. The probabilities are those of the attention above:
+// each query's softmax over exactly its visible keys.
+extern "C" int orc_attn_mass(int hq, int hkv, int d, double scale, const uint16_t* q,
+                             const int32_t* row_seq, const int32_t* row_pos,
+                             const int64_t* kv_off, const int32_t* kv_len, int nseq,
+                             const uint16_t* k, const uint8_t* head_class, int window,
+                             const int32_t* seg_start, int64_t nq, int64_t nkeys, double* mass) {
+  if (hq <= 0 || hkv <= 0 || hq % hkv != 0 || d <= 0 || window < 1 || nseq < 0) return INVALID_ARG;
+  const int G = hq / hkv;
+  for (int64_t i = 0; i < int64_t(hkv) * nkeys; ++i) mass[i] = 0.0;
+  int status = OK;
+  // one (sequence, KV head) per task: each task owns its slice of mass
+#pragma omp parallel for schedule(dynamic, 1) collapse(2)
+  for (int b = 0; b < nseq; ++b) {
+    for (int h = 0; h < hkv; ++h) {
+      const bool local = head_class[h] != GLOBAL_HEAD;
+      double* mrow = mass + int64_t(h) * nkeys + kv_off[b];
+      std::vector<int> keys;
+      std::vector<double> qv(d), sc;
+      for (int64_t t = 0; t < nq; ++t) {
+        if (row_seq[t] != b) continue;
+        int rc = visible_keys(row_pos[t], kv_len[b], seg_start[b * hkv + h], local, window, &keys);
+        if (rc != OK) {
+#pragma omp critical
+          status = rc;
+          continue;
+        }
+        for (int qh = h * G; qh < (h + 1) * G; ++qh) {
+          for (int c = 0; c < d; ++c) qv[c] = bf16_to_double(q[(t * hq + qh) * d + c]);
+          sc.assign(keys.size(), 0.0);
+          double m = -std::numeric_limits<double>::infinity();
+          for (size_t i = 0; i < keys.size(); ++i) {
+            const uint16_t* kr = k + ((kv_off[b] + keys[i]) * hkv + h) * d;
+            double dot = 0.0;
+            for (int c = 0; c < d; ++c) dot += qv[c] * bf16_to_double(kr[c]);
+            sc[i] = scale * dot;
+            if (sc[i] > m) m = sc[i];
+          }
+          double denom = 0.0;
+          for (size_t i = 0; i < keys.size(); ++i) {
+            sc[i] = std::exp(sc[i] - m);
+            denom += sc[i];
+          }
+          for (size_t i = 0; i < keys.size(); ++i) mrow[keys[i]] += sc[i] / denom;
+        }
+      }
+    }
+  }
+  return status;
+}
