@@ -35,7 +35,7 @@ SYMBOLS = ["segkv_create", "segkv_destroy", "segkv_append", "segkv_prefill_attn"
            "segkv_get_segment", "segkv_seq_len", "segkv_stats", "segkv_status",
            "segkv_last_error", "segkv_set_debug", "segkv_decode_attn_noalloc", "segkv_rope_shift",
            "segkv_export_size", "segkv_export", "segkv_import", "segkv_set_window_convention",
-           "segkv_decode_attn_multi"]
+           "segkv_decode_attn_multi", "segkv_sparse_ffn", "segkv_ffn_workspace_size"]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -70,6 +70,8 @@ def _load():
         "segkv_export_size": [P, I, I, ctypes.POINTER(SZ)],
         "segkv_set_window_convention": [P, I],
         "segkv_decode_attn_multi": [P, I, P, I, P, P, I, P, P, P, SZ, P],
+        "segkv_sparse_ffn": [P, P, P, ctypes.c_int64, P, I, P, P, P, I, I, P, SZ, P],
+        "segkv_ffn_workspace_size": [I, I, I, P],
         "segkv_export": [P, I, I, P, SZ, P, P],
         "segkv_import": [P, I, I, P, SZ, P, P],
     }
@@ -203,6 +205,24 @@ def segkv_decode_attn_multi(h, layer, q, T, seq_lens, seq_ids, o, lse=None, work
     return _lib.segkv_decode_attn_multi(h, layer, _ptr(q), T, sl.ctypes.data, ids.ctypes.data,
                                         len(ids), _ptr(o), _ptr(lse), _ptr(workspace),
                                         workspace_bytes, _stream_ptr(stream))
+
+
+def segkv_ffn_workspace_size(m, d_model, d_ff):
+    b = ctypes.c_size_t(0)
+    rc = _lib.segkv_ffn_workspace_size(m, d_model, d_ff, ctypes.byref(b))
+    return rc, b.value
+
+
+def segkv_sparse_ffn(h, x, residual, idx, m, w_gate, w_up, w_down, workspace,
+                     workspace_bytes=None, stream=None):
+    """residual[idx[r]] += SwiGLU FFN(x[idx[r]]) for r < m (idx None: every row)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    n_rows, d_model = x.shape
+    d_ff = w_gate.shape[0]
+    return _lib.segkv_sparse_ffn(h, _ptr(x), _ptr(residual), n_rows, _ptr(idx), m, _ptr(w_gate),
+                                 _ptr(w_up), _ptr(w_down), d_model, d_ff, _ptr(workspace),
+                                 workspace_bytes, _stream_ptr(stream))
 
 
 def segkv_trim(h, layer, seq_ids):
@@ -348,6 +368,18 @@ class SegKV:
                           stream=None):
         return self._check(segkv_decode_attn_multi(self._h, layer, q, T, seq_lens, seq_ids, o, lse,
                                                    workspace, None, stream))
+
+    def sparse_ffn(self, x, residual, idx, w_gate, w_up, w_down, workspace=None, stream=None):
+        """residual[idx] += SwiGLU FFN(x[idx]) (idx None: every row). Allocates
+        the workspace when none is given."""
+        m = x.shape[0] if idx is None else idx.numel()
+        if workspace is None:
+            rc, b = segkv_ffn_workspace_size(m, x.shape[1], w_gate.shape[0])
+            self._check(rc)
+            import torch
+            workspace = torch.empty(b, dtype=torch.uint8, device=x.device)
+        return self._check(segkv_sparse_ffn(self._h, x, residual, idx, m, w_gate, w_up, w_down,
+                                            workspace, None, stream))
 
     def trim(self, layer, seq_ids):
         return self._check(segkv_trim(self._h, layer, seq_ids))

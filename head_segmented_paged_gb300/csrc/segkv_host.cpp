@@ -1200,6 +1200,85 @@ int segkv_stats(segkv_t h, segkv_stats_t* out) {
   return SEGKV_OK;
 }
 
+// ---------------------------------------------------------------- sparse FFN
+static size_t ffn_ws_parts(int64_t m, int d_model, int d_ff, bool gather, size_t* h_off) {
+  const size_t xs = gather ? align_up(static_cast<size_t>(m) * d_model * 2, 1024) : 0;
+  *h_off = xs;
+  return xs + align_up(static_cast<size_t>(m) * d_ff * 2, 1024);
+}
+
+int segkv_ffn_workspace_size(int m, int d_model, int d_ff, size_t* bytes) {
+  if (m < 0 || d_model <= 0 || d_ff <= 0 || !bytes) return SEGKV_ERR_INVALID_ARG;
+  size_t off;
+  *bytes = ffn_ws_parts(m, d_model, d_ff, true, &off);
+  return SEGKV_OK;
+}
+
+int segkv_sparse_ffn(segkv_t h, const void* x, void* residual, int64_t n_rows, const int32_t* idx,
+                     int m, const void* w_gate, const void* w_up, const void* w_down, int d_model,
+                     int d_ff, void* workspace, size_t workspace_bytes, segkv_stream_t stream) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (h->host_only) return fail(h, SEGKV_ERR_INVALID_ARG, "host-only handle has no device");
+  if (m < 0 || n_rows < 0 || n_rows > INT32_MAX || m > n_rows || (!idx && m != n_rows))
+    return fail(h, SEGKV_ERR_INVALID_ARG, "bad m=%d / n_rows=%lld (idx NULL needs m = n_rows)", m,
+                static_cast<long long>(n_rows));
+  if (d_model < 64 || d_model % 64 || d_ff < 128 || d_ff % 128)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "d_model must be a multiple of 64, d_ff of 128");
+  if (m == 0) return SEGKV_OK;
+  const uintptr_t al = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(residual) |
+                       reinterpret_cast<uintptr_t>(w_gate) | reinterpret_cast<uintptr_t>(w_up) |
+                       reinterpret_cast<uintptr_t>(w_down) | reinterpret_cast<uintptr_t>(workspace);
+  if (!x || !residual || !w_gate || !w_up || !w_down || !workspace || (al & 255))
+    return fail(h, SEGKV_ERR_INVALID_ARG, "x, residual, weights and workspace: 256-byte aligned");
+  size_t h_off;
+  const size_t need = ffn_ws_parts(m, d_model, d_ff, idx != nullptr, &h_off);
+  if (workspace_bytes < need)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "workspace needs %zu bytes, got %zu", need,
+                workspace_bytes);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* hbuf = ws + h_off;
+  const void* a1 = x;
+  cudaError_t e;
+  if (idx) {
+    e = launch_gather_rows(x, idx, ws, m, d_model, n_rows, h->d_status, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "gather kernel launch");
+    a1 = ws;
+  }
+  CUtensorMap ta1, tg, tu, ta2, td;
+  if (encode_2d(&ta1, const_cast<void*>(a1), d_model, m, 128) != CUDA_SUCCESS ||
+      encode_2d(&tg, const_cast<void*>(w_gate), d_model, d_ff, 128) != CUDA_SUCCESS ||
+      encode_2d(&tu, const_cast<void*>(w_up), d_model, d_ff, 128) != CUDA_SUCCESS ||
+      encode_2d(&ta2, hbuf, d_ff, m, 128) != CUDA_SUCCESS ||
+      encode_2d(&td, const_cast<void*>(w_down), d_ff, d_model, 128) != CUDA_SUCCESS)
+    return fail(h, SEGKV_ERR_CUDA, "tensor map encode failed for the FFN operands");
+  const int tr = ffn_tile_rows();
+  FfnGemmParams p{};
+  p.M = m;
+  p.K = d_model;
+  p.tiles_m = (m + tr - 1) / tr;
+  p.tiles_n = d_ff / 128;
+  p.n_out = d_ff;
+  p.n_rows = n_rows;
+  p.out = hbuf;
+  p.idx = nullptr;
+  p.status = h->d_status;
+  p.timeout_ns = kTimeoutNs;
+  const int sms = h->num_sms > 0 ? h->num_sms : 1;
+  e = launch_ffn_gemm(0, ta1, tg, tu, p,
+                      static_cast<int>(std::min<int64_t>(int64_t(p.tiles_m) * p.tiles_n, sms)), s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "FFN gate/up GEMM launch");
+  p.K = d_ff;
+  p.tiles_n = (d_model + 255) / 256;
+  p.n_out = d_model;
+  p.out = residual;
+  p.idx = idx;
+  e = launch_ffn_gemm(1, ta2, td, td, p,
+                      static_cast<int>(std::min<int64_t>(int64_t(p.tiles_m) * p.tiles_n, sms)), s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "FFN down GEMM launch");
+  return SEGKV_OK;
+}
+
 int segkv_status(segkv_t h, segkv_stream_t stream) {
   if (!h) return SEGKV_ERR_INVALID_ARG;
   if (h->host_only) return SEGKV_OK;
@@ -1209,6 +1288,11 @@ int segkv_status(segkv_t h, segkv_stream_t stream) {
   int v = 0;
   e = cudaMemcpy(&v, h->d_status, sizeof v, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(h, e, "status read");
+  if (v == kStatusBadIndex) {
+    e = cudaMemset(h->d_status, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(h, e, "status clear");
+    return fail(h, SEGKV_ERR_INVALID_ARG, "a device row index was out of range");
+  }
   if (v != 0) {
     // a launch that gave up may have left decode merge counters non-zero
     e = cudaMemset(h->d_pair_cnt, 0, sizeof(int) * static_cast<size_t>(h->S) * h->Hkv);

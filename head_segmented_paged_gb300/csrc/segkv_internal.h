@@ -158,6 +158,27 @@ struct TransferParams {
 cudaError_t launch_transfer(const TransferParams& p, const AppendBlob* blob, int grid,
                             cudaStream_t s);
 
+// ---- sparse FFN ------------------------------------------------------------
+constexpr int kStatusBadIndex = 6;  // device status word: a row index was out of range
+struct FfnGemmParams {
+  int M;          // rows (chosen tokens)
+  int K;          // reduction length (d_model for GEMM 1, d_ff for GEMM 2)
+  int tiles_m, tiles_n;
+  int n_out;      // row length of out: d_ff (GEMM 1, H) or d_model (GEMM 2, residual)
+  int64_t n_rows; // GEMM 2: rows of the residual stream
+  void* out;      // GEMM 1: H bf16 [M, d_ff]; GEMM 2: residual bf16 [n_rows, d_model]
+  const int32_t* idx;  // GEMM 2: output row of each accumulator row, or null (row m)
+  int* status;
+  unsigned long long timeout_ns;
+};
+cudaError_t launch_gather_rows(const void* x, const int32_t* idx, void* out, int m, int d_model,
+                               int64_t n_rows, int* status, cudaStream_t s);
+// epilogue 0: H = silu(gate) * up; 1: residual[idx] += acc
+cudaError_t launch_ffn_gemm(int epilogue, const CUtensorMap& ta, const CUtensorMap& tb0,
+                            const CUtensorMap& tb1, const FfnGemmParams& p, int grid,
+                            cudaStream_t s);
+int ffn_tile_rows();
+
 cudaError_t launch_append(const AppendParams& p, const AppendBlob* blob, int grid, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, int head_dim, int grid, cudaStream_t s);

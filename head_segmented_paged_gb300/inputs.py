@@ -269,3 +269,36 @@ def decode_step_tensors(w: Workload, step: int, device="cpu"):
     k = normal_bf16(w.seed, tensor_stream(_KD, 0, step), (B, w.hkv, w.head_dim), s, device)
     v = normal_bf16(w.seed, tensor_stream(_VD, 0, step), (B, w.hkv, w.head_dim), s, device)
     return q, k, v
+
+
+# ---- sparse FFN routing -------------------------------------------------------
+_X, _RES, _WG, _WU, _WD = 7, 8, 9, 10, 11
+
+
+@dataclass
+class FfnWorkload:
+    """One FFN layer over a prefill chunk: n tokens, hidden d_model, FFN
+    width d_ff, m chosen tokens. Synthetic: x and the residual are N(0,1)
+    (the FFN input is a normalised hidden state), weights N(0,1)/sqrt(fan_in)."""
+    name: str
+    n: int
+    d_model: int
+    d_ff: int
+    m: int
+    seed: int = 0
+
+
+def mistral_ffn(seed: int = 0) -> FfnWorkload:
+    """Mistral-7B FFN shape (hidden 4096, SwiGLU width 14336) over the 8192
+    tokens of the Mistral-shaped prefill, a quarter of them chosen."""
+    return FfnWorkload("mistral-ffn-8k", 8192, 4096, 14336, 2048, seed)
+
+
+def ffn_tensors(w: FfnWorkload, device="cpu"):
+    """x, residual [n, d_model]; w_gate, w_up [d_ff, d_model]; w_down [d_model, d_ff] (bf16)."""
+    x = normal_bf16(w.seed, tensor_stream(_X, 0), (w.n, w.d_model), 1.0, device)
+    r = normal_bf16(w.seed, tensor_stream(_RES, 0), (w.n, w.d_model), 1.0, device)
+    wg = normal_bf16(w.seed, tensor_stream(_WG, 0), (w.d_ff, w.d_model), w.d_model ** -0.5, device)
+    wu = normal_bf16(w.seed, tensor_stream(_WU, 0), (w.d_ff, w.d_model), w.d_model ** -0.5, device)
+    wd = normal_bf16(w.seed, tensor_stream(_WD, 0), (w.d_model, w.d_ff), w.d_ff ** -0.5, device)
+    return x, r, wg, wu, wd

@@ -258,6 +258,32 @@ int segkv_decode_attn_multi(segkv_t h, int layer, const void* q, int T, const in
                             size_t workspace_bytes, segkv_stream_t stream);
 
 /*
+ * segkv_sparse_ffn — the dense FFN on chosen rows only (RedKnot summary page,
+ * section "稀疏 FFN（Sparse FFN）": the tokens with the highest attention
+ * scores go through the dense FFN, every other token takes the residual
+ * identity path). The FFN is the gated SwiGLU MLP of the models the page
+ * names (a reading; the page gives no formula):
+ *   for r < m:  residual[idx[r]] += W_down (silu(W_gate x[idx[r]]) * (W_up x[idx[r]]))
+ * with silu(g) = g / (1 + e^-g). Rows not in idx are neither read nor written.
+ *   x         device bf16 [n_rows, d_model], the FFN input (normalised hidden state).
+ *   residual  device bf16 [n_rows, d_model], updated in place (one rounding per element).
+ *   idx       device int32 [m], distinct row ids in [0, n_rows); NULL = every row
+ *             (the dense FFN; then m must equal n_rows). An id out of range is
+ *             skipped and segkv_status reports SEGKV_ERR_INVALID_ARG.
+ *   w_gate, w_up  device bf16 [d_ff, d_model]; w_down device bf16 [d_model, d_ff].
+ *   d_model   a multiple of 64; d_ff a multiple of 128.
+ *   workspace device, >= segkv_ffn_workspace_size(m, d_model, d_ff) bytes; it
+ *             holds the gathered rows and the bf16 hidden activations h.
+ * Pointers 256-byte aligned. The caller owns every buffer. fp32 accumulation
+ * on the tensor cores; h is rounded to bf16 before W_down.
+ * Errors: INVALID_ARG, CUDA.
+ */
+int segkv_sparse_ffn(segkv_t h, const void* x, void* residual, int64_t n_rows, const int32_t* idx,
+                     int m, const void* w_gate, const void* w_up, const void* w_down, int d_model,
+                     int d_ff, void* workspace, size_t workspace_bytes, segkv_stream_t stream);
+int segkv_ffn_workspace_size(int m, int d_model, int d_ff, size_t* bytes);
+
+/*
  * segkv_get_segment — host copy of one segment's table: kept start, kept
  * length, first logical page and the page ids in logical order (at most
  * max_ids written; *n_ids gets the count).
