@@ -35,7 +35,8 @@ SYMBOLS = ["segkv_create", "segkv_destroy", "segkv_append", "segkv_prefill_attn"
            "segkv_get_segment", "segkv_seq_len", "segkv_stats", "segkv_status",
            "segkv_last_error", "segkv_set_debug", "segkv_decode_attn_noalloc", "segkv_rope_shift",
            "segkv_export_size", "segkv_export", "segkv_import", "segkv_set_window_convention",
-           "segkv_decode_attn_multi", "segkv_sparse_ffn", "segkv_ffn_workspace_size"]
+           "segkv_decode_attn_multi", "segkv_sparse_ffn", "segkv_ffn_workspace_size", "segkv_attn_mass",
+           "segkv_topk_tokens"]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -71,6 +72,8 @@ def _load():
         "segkv_set_window_convention": [P, I],
         "segkv_decode_attn_multi": [P, I, P, I, P, P, I, P, P, P, SZ, P],
         "segkv_sparse_ffn": [P, P, P, ctypes.c_int64, P, I, P, P, P, I, I, P, SZ, P],
+        "segkv_attn_mass": [P, I, P, P, P, P, I, P, P, P],
+        "segkv_topk_tokens": [P, P, P, I, P, P, P, P],
         "segkv_ffn_workspace_size": [I, I, I, P],
         "segkv_export": [P, I, I, P, SZ, P, P],
         "segkv_import": [P, I, I, P, SZ, P, P],
@@ -205,6 +208,18 @@ def segkv_decode_attn_multi(h, layer, q, T, seq_lens, seq_ids, o, lse=None, work
     return _lib.segkv_decode_attn_multi(h, layer, _ptr(q), T, sl.ctypes.data, ids.ctypes.data,
                                         len(ids), _ptr(o), _ptr(lse), _ptr(workspace),
                                         workspace_bytes, _stream_ptr(stream))
+
+
+def segkv_attn_mass(h, layer, q, cu_seqlens, q_pos, seq_ids, lse, mass, stream=None):
+    cu, qp, ids = _host_i32(cu_seqlens), _host_i32(q_pos), _host_i32(seq_ids)
+    return _lib.segkv_attn_mass(h, layer, _ptr(q), cu.ctypes.data, qp.ctypes.data, ids.ctypes.data,
+                                len(ids), _ptr(lse), _ptr(mass), _stream_ptr(stream))
+
+
+def segkv_topk_tokens(h, mass, cu_seqlens, k, score, idx, stream=None):
+    cu, kk = _host_i32(cu_seqlens), _host_i32(k)
+    return _lib.segkv_topk_tokens(h, _ptr(mass), cu.ctypes.data, len(kk), kk.ctypes.data,
+                                  _ptr(score), _ptr(idx), _stream_ptr(stream))
 
 
 def segkv_ffn_workspace_size(m, d_model, d_ff):
@@ -368,6 +383,13 @@ class SegKV:
                           stream=None):
         return self._check(segkv_decode_attn_multi(self._h, layer, q, T, seq_lens, seq_ids, o, lse,
                                                    workspace, None, stream))
+
+    def attn_mass(self, layer, q, cu_seqlens, q_pos, seq_ids, lse, mass, stream=None):
+        return self._check(segkv_attn_mass(self._h, layer, q, cu_seqlens, q_pos, seq_ids, lse,
+                                           mass, stream))
+
+    def topk_tokens(self, mass, cu_seqlens, k, score, idx, stream=None):
+        return self._check(segkv_topk_tokens(self._h, mass, cu_seqlens, k, score, idx, stream))
 
     def sparse_ffn(self, x, residual, idx, w_gate, w_up, w_down, workspace=None, stream=None):
         """residual[idx] += SwiGLU FFN(x[idx]) (idx None: every row). Allocates

@@ -1200,6 +1200,155 @@ int segkv_stats(segkv_t h, segkv_stats_t* out) {
   return SEGKV_OK;
 }
 
+// ---------------------------------------------------------------- attention mass
+int segkv_attn_mass(segkv_t h, int layer, const void* q, const int32_t* cu_seqlens,
+                    const int32_t* q_pos, const int32_t* seq_ids, int n, const float* lse,
+                    float* mass, segkv_stream_t stream) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (h->host_only) return fail(h, SEGKV_ERR_INVALID_ARG, "host-only handle has no pools");
+  if (layer < 0 || layer >= h->L) return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer %d", layer);
+  if (!ids_valid(h, seq_ids, n)) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq_ids");
+  if (n == 0) return SEGKV_OK;
+  if (!cu_seqlens || cu_seqlens[0] != 0) return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens[0] != 0");
+  for (int i = 0; i < n; ++i)
+    if (cu_seqlens[i + 1] < cu_seqlens[i])
+      return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens decreases at %d", i);
+  const int64_t total = cu_seqlens[n];
+  if (total == 0) return SEGKV_OK;
+  if (!q || !lse || !mass || !q_pos) return fail(h, SEGKV_ERR_INVALID_ARG, "q/lse/mass/q_pos NULL");
+  if (reinterpret_cast<uintptr_t>(q) & 15)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  const int W = h->win[layer];
+  const int tpt = kRowsPerTile / h->G;
+  std::vector<MassUnit> units;
+  for (int i = 0; i < n; ++i) {
+    const int b = seq_ids[i];
+    const int32_t nlen = h->len[h->lidx(layer, b)];
+    const int32_t T = cu_seqlens[i + 1] - cu_seqlens[i];
+    if (T == 0) continue;
+    const int32_t a = q_pos[cu_seqlens[i]];
+    for (int32_t t = 0; t < T; ++t)
+      if (q_pos[cu_seqlens[i] + t] != a + t)
+        return fail(h, SEGKV_ERR_INVALID_ARG, "q_pos of seq %d are not consecutive", b);
+    if (a < 0 || a + T > nlen)
+      return fail(h, SEGKV_ERR_INVALID_ARG, "chunk [%d,%d) outside seq %d of length %d", a, a + T,
+                  b, nlen);
+    for (int hd = 0; hd < h->Hkv; ++hd) {
+      const int32_t s0 = h->start[h->seg(layer, hd, b)];
+      const bool local = h->local(layer, hd);
+      const int32_t need = local ? std::max(0, a - W + 1) : 0;
+      if (need < s0)
+        return fail(h, SEGKV_ERR_EVICTED, "seq %d head %d: key %d already evicted", b, hd, need);
+      for (int32_t kt = a / kKeyTile; kt <= (a + T - 1) / kKeyTile; ++kt) {
+        const int32_t j0 = std::max(a, kt * kKeyTile);
+        const int32_t j1 = std::min(a + T, (kt + 1) * kKeyTile) - 1;
+        // query tokens that see some key of [j0, j1]
+        const int32_t tlo = j0 - a;
+        const int32_t thi = local ? std::min(T - 1, j1 + W - 1 - a) : T - 1;
+        MassUnit u{};
+        u.tok0 = cu_seqlens[i];
+        u.ntok = T;
+        u.a = a;
+        u.head = hd;
+        u.local = local ? 1 : 0;
+        u.kt = kt;
+        u.qt0 = tlo / tpt;
+        u.qt1 = thi / tpt;
+        u.first_page = s0 / h->P;
+        u.last_page = (nlen - 1) / h->P;
+        u.table_row = static_cast<int32_t>(h->seg(layer, hd, b));
+        units.push_back(u);
+      }
+    }
+  }
+  if (units.empty()) return SEGKV_OK;
+  std::stable_sort(units.begin(), units.end(), [](const MassUnit& x, const MassUnit& y) {
+    return (x.qt1 - x.qt0) > (y.qt1 - y.qt0);
+  });
+  Pack pk;
+  const size_t o_units = pk.add(units.data(), units.size());
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  size_t off;
+  cudaError_t e = h->ring.reserve(pk.buf.size(), &off);
+  if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
+  std::memcpy(h->ring.host + off, pk.buf.data(), pk.buf.size());
+  e = cudaMemcpyAsync(h->ring.dev + off, h->ring.host + off, pk.buf.size(), cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpyAsync(mass plan)");
+  h->upload_bytes += static_cast<int64_t>(pk.buf.size());
+  CUtensorMap tq;
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(h->D), static_cast<cuuint64_t>(h->Hq),
+                          static_cast<cuuint64_t>(total)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(h->D) * 2,
+                             static_cast<cuuint64_t>(h->Hq) * h->D * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(h->G), static_cast<cuuint32_t>(tpt)};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (encode_fn()(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return fail(h, SEGKV_ERR_CUDA, "tensor map encode failed for q");
+  }
+  MassParams p{};
+  p.units = reinterpret_cast<const MassUnit*>(h->ring.dev + off + o_units);
+  p.table = h->d_table;
+  p.lse = lse;
+  p.mass = mass;
+  p.total_q = total;
+  p.n_units = static_cast<int>(units.size());
+  p.R = h->R;
+  p.hq = h->Hq;
+  p.G = h->G;
+  p.tpt = tpt;
+  p.window = W;
+  p.page_size = h->P;
+  p.oob_row = static_cast<int>(h->num_pages * h->P);
+  p.scale_log2 = h->scale * 1.4426950408889634f;
+  p.status = h->d_status;
+  p.timeout_ns = kTimeoutNs;
+  const int grid = static_cast<int>(std::min<int64_t>(units.size(), h->num_sms));
+  e = launch_mass(p, tq, h->tm_k, h->D, grid, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "mass kernel launch");
+  e = h->ring.commit(off, pk.buf.size(), s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "event record");
+  return SEGKV_OK;
+}
+
+int segkv_topk_tokens(segkv_t h, const float* mass, const int32_t* cu_seqlens, int n,
+                      const int32_t* k, float* score, int32_t* idx, segkv_stream_t stream) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (h->host_only) return fail(h, SEGKV_ERR_INVALID_ARG, "host-only handle has no device");
+  if (n < 0 || (n > 0 && (!cu_seqlens || !k || cu_seqlens[0] != 0)))
+    return fail(h, SEGKV_ERR_INVALID_ARG, "bad n, cu_seqlens or k");
+  if (n == 0) return SEGKV_OK;
+  std::vector<TopkSeq> seqs(n);
+  int64_t out = 0;
+  for (int i = 0; i < n; ++i) {
+    const int32_t T = cu_seqlens[i + 1] - cu_seqlens[i];
+    if (T < 0 || k[i] < 0 || k[i] > T)
+      return fail(h, SEGKV_ERR_INVALID_ARG, "k[%d]=%d outside [0, %d]", i, k[i], T);
+    seqs[i] = {cu_seqlens[i], T, k[i], static_cast<int32_t>(out)};
+    out += k[i];
+  }
+  const int64_t total = cu_seqlens[n];
+  if (total > 0 && (!mass || !score)) return fail(h, SEGKV_ERR_INVALID_ARG, "mass/score NULL");
+  if (out > 0 && !idx) return fail(h, SEGKV_ERR_INVALID_ARG, "idx NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Pack pk;
+  const size_t o_seqs = pk.add(seqs.data(), seqs.size());
+  PlanPlace pp;
+  int rc = place_small_plan(h, pk, s, &pp);
+  if (rc != SEGKV_OK) return rc;
+  TopkParams p{};
+  p.seqs = reinterpret_cast<const TopkSeq*>(pp.base + o_seqs);
+  p.idx = idx;
+  p.plan_inline = pp.inl ? 1 : 0;
+  cudaError_t e = launch_topk(mass, score, total, h->Hkv, p,
+                              pp.inl ? reinterpret_cast<const AppendBlob*>(&h->blob) : nullptr, n, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "top-k kernel launch");
+  return finish_small_plan(h, pp, pk, s);
+}
+
 // ---------------------------------------------------------------- sparse FFN
 static size_t ffn_ws_parts(int64_t m, int d_model, int d_ff, bool gather, size_t* h_off) {
   const size_t xs = gather ? align_up(static_cast<size_t>(m) * d_model * 2, 1024) : 0;

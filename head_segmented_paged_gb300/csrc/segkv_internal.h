@@ -158,6 +158,51 @@ struct TransferParams {
 cudaError_t launch_transfer(const TransferParams& p, const AppendBlob* blob, int grid,
                             cudaStream_t s);
 
+// ---- attention mass per key ---------------------------------------------------
+struct MassUnit {
+  int32_t tok0;        // first token row of the chunk (its cu_seqlens entry)
+  int32_t ntok;        // chunk length T
+  int32_t a;           // position of the chunk's first token
+  int32_t head;        // KV head
+  int32_t local;       // 1 = local head
+  int32_t kt;          // key tile: positions [kt * 128, kt * 128 + 128)
+  int32_t qt0, qt1;    // query tiles (chunk-relative, tpt tokens each), inclusive
+  int32_t first_page;  // first held logical page of the segment
+  int32_t last_page;   // last held logical page
+  int32_t table_row;
+  int32_t pad;
+};
+struct MassParams {
+  const MassUnit* units;
+  const int32_t* table;
+  const float* lse;    // fp32 [Hq, total_q], natural log, from the prefill of the chunk
+  float* mass;         // fp32 [Hkv, total_q]
+  int64_t total_q;
+  int n_units;
+  int R, hq, G, tpt, window, page_size;
+  int oob_row;         // a K row coordinate past the end of the pool
+  float scale_log2;
+  int* status;
+  unsigned long long timeout_ns;
+};
+cudaError_t launch_mass(const MassParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                        int head_dim, int grid, cudaStream_t s);
+
+// ---- top-k token choice ------------------------------------------------------
+struct TopkSeq {
+  int32_t tok0;  // first token row of the sequence
+  int32_t ntok;  // its tokens
+  int32_t k;     // how many to choose
+  int32_t out0;  // first output slot
+};
+struct TopkParams {
+  const TopkSeq* seqs;
+  int32_t* idx;      // chosen token rows
+  int plan_inline;   // 1: seqs is an offset into the AppendBlob
+};
+cudaError_t launch_topk(const float* mass, float* score, int64_t total, int hkv,
+                        const TopkParams& p, const AppendBlob* blob, int n_seqs, cudaStream_t s);
+
 // ---- sparse FFN ------------------------------------------------------------
 constexpr int kStatusBadIndex = 6;  // device status word: a row index was out of range
 struct FfnGemmParams {

@@ -258,6 +258,44 @@ int segkv_decode_attn_multi(segkv_t h, int layer, const void* q, int T, const in
                             size_t workspace_bytes, segkv_stream_t stream);
 
 /*
+ * segkv_attn_mass — the attention score of every token of a prefill chunk:
+ * the softmax mass it receives as a key (RedKnot summary page, section
+ * "稀疏 FFN（Sparse FFN）": the dense FFN runs only on the tokens with the
+ * highest attention scores; the page does not define the score, and this
+ * library reads it as the mass a token receives). For sequence i of the
+ * call, the chunk is its tokens cu_seqlens[i] .. cu_seqlens[i+1]-1 at
+ * consecutive positions a_i .. a_i+T_i-1 (q_pos), already appended; for each
+ * key j of the chunk and KV head h:
+ *   mass[h, t(j)] = sum over the chunk's queries p >= j that see j (local
+ *                   heads: j >= p-W+1) and over the G query heads of h of
+ *                   exp(scale q.k_j - lse_q)
+ *   q         device bf16 [Σq, Hq, D], the chunk's queries (as for prefill).
+ *   lse       device fp32 [Hq, Σq]: the LSE segkv_prefill_attn wrote for them.
+ *   mass      device fp32 [Hkv, Σq], written for every token.
+ * Summation order is fixed, so results repeat bit for bit.
+ * Errors: INVALID_ARG (positions not consecutive, chunk beyond the tracked
+ * length), EVICTED.
+ */
+int segkv_attn_mass(segkv_t h, int layer, const void* q, const int32_t* cu_seqlens,
+                    const int32_t* q_pos, const int32_t* seq_ids, int n, const float* lse,
+                    float* mass, segkv_stream_t stream);
+
+/*
+ * segkv_topk_tokens — choose the tokens that go through the FFN (section
+ * "稀疏 FFN（Sparse FFN）"): score[t] = sum over h of mass[h, t] (fp32, in
+ * head order); for sequence i, the k[i] tokens of cu_seqlens[i] ..
+ * cu_seqlens[i+1]-1 with the largest score, ties to the lower position.
+ *   mass      device fp32 [Hkv, Σq] from segkv_attn_mass (scores must be >= 0).
+ *   k         host int32 [n], 0 <= k[i] <= the sequence's tokens.
+ *   score     device fp32 [Σq], receives the summed score.
+ *   idx       device int32 [Σ k]: sequence i's chosen token rows (global
+ *             rows, cu_seqlens[i] + t) at idx[Σ_{j<i} k[j] ...], ascending.
+ * Errors: INVALID_ARG.
+ */
+int segkv_topk_tokens(segkv_t h, const float* mass, const int32_t* cu_seqlens, int n,
+                      const int32_t* k, float* score, int32_t* idx, segkv_stream_t stream);
+
+/*
  * segkv_sparse_ffn — the dense FFN on chosen rows only (RedKnot summary page,
  * section "稀疏 FFN（Sparse FFN）": the tokens with the highest attention
  * scores go through the dense FFN, every other token takes the residual

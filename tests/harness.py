@@ -122,3 +122,22 @@ def prefill_case(w: I.Workload, layer=0, num_pages=None, poison=True, max_seq_le
     ids = list(range(len(w.seq_lens)))
     assert c.append(layer, k.cuda(), v.cuda(), cu, ids) == 0
     return c, q, cu, qp, ids
+
+
+def oracle_mass(c: Cache, layer, q, seq_ids, q_seq_index, q_pos):
+    """fp64 attention mass each logical key of the listed sequences receives
+    from the query rows q (row i of sequence q_seq_index[i] at q_pos[i]):
+    returns (status, mass [Hkv, sum of lengths], offsets per sequence)."""
+    ks, offs, lens = [], [], []
+    off = 0
+    for b in seq_ids:
+        kb = c.k_log[(layer, b)]
+        ks.append(kb)
+        offs.append(off)
+        lens.append(kb.shape[0])
+        off += kb.shape[0]
+    seg_start = np.array([[c.m.segment(layer, hd, b)[0] for hd in range(c.hkv)]
+                          for b in seq_ids], dtype=np.int32)
+    rc, m = oracle.attn_mass(q.cpu(), torch.cat(ks), q_seq_index, q_pos, offs, lens,
+                             c.head_class[layer], c.window[layer], seg_start)
+    return rc, m, offs
