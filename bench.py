@@ -240,6 +240,7 @@ def run_ours(args, rank, world):
         out["decode"] = run_decode(args, dev, stream, hbm, peak_src)
         out["rope_shift"] = run_rope(dev, stream, hbm)
         out["pd_transfer"] = run_transfer(dev, stream, hbm)
+        out["sparse_ffn_routing"] = run_routing(dev, stream, bf16_burst, peak_src)
     if not args.no_dense:
         out["dense"] = run_dense(args, dev, stream, sets, cu, q_pos, o, prefill_ms)
     if not args.no_e2e:
@@ -427,6 +428,80 @@ def run_rope(dev, stream, hbm):
             "us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
             "frac_hbm": round(nbytes / (us * 1e-6) / 1e9 / hbm, 4), "bytes": nbytes,
             "kernel": "rope_kernel"}
+
+
+def run_routing(dev, stream, bf16_burst, peak_src):
+    """Sparse FFN routing on the Mistral-shaped 8K layer: prefill attention
+    (with LSE), attention mass per token, top-k choice of a quarter of the
+    tokens, and the SwiGLU FFN (hidden 4096, width 14336) on the chosen rows,
+    against the dense FFN on every row."""
+    import numpy as np
+    import torch
+
+    import head_segmented_paged_gb300 as S
+    from head_segmented_paged_gb300 import inputs as I
+
+    w = I.mistral_8k()
+    fw = I.mistral_ffn()
+    n, P, D = w.seq_lens[0], w.page_size, w.head_dim
+    q, k, v, cu, qp = I.prefill_tensors(w, 0, device=dev)
+    cu, qp = cu.numpy(), qp.numpy()
+    kp = torch.empty(((n // P + 2) * w.hkv, P, D), dtype=torch.bfloat16, device=dev)
+    h = S.SegKV(1, w.hq, w.hkv, D, w.head_class, w.window, P, 1, n, kp, torch.empty_like(kp))
+    h.append(0, k, v, cu, [0], stream)
+    x, r, wg, wu, wd = I.ffn_tensors(fw, device=dev)
+    o = torch.empty((n, w.hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.hq, n), device=dev)
+    mass = torch.empty((w.hkv, n), device=dev)
+    score = torch.empty((n,), device=dev)
+    idx = torch.empty((fw.m,), dtype=torch.int32, device=dev)
+    res = r.clone()
+    rc, wsb = S.segkv_ffn_workspace_size(n, fw.d_model, fw.d_ff)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    stages = {
+        "prefill": lambda: h.prefill_attn(0, q, cu, qp, [0], o, lse, stream),
+        "mass": lambda: h.attn_mass(0, q, cu, qp, [0], lse, mass, stream),
+        "topk": lambda: h.topk_tokens(mass, cu, [fw.m], score, idx, stream),
+        "sparse_ffn": lambda: h.sparse_ffn(x, res, idx, wg, wu, wd, ws, stream),
+        "dense_ffn": lambda: h.sparse_ffn(x, res, None, wg, wu, wd, ws, stream),
+    }
+    us = {}
+    for name, fn in stages.items():
+        for _ in range(3):
+            fn()
+        reps = 10
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us[name] = 1e3 * e0.elapsed_time(e1) / reps
+    if h.status() != 0:
+        raise RuntimeError("device status after routing: " + S.segkv_last_error(h.handle))
+    att_flops = useful_flops_layer(w, 0, n)
+    ffn_flops = 6.0 * fw.m * fw.d_model * fw.d_ff
+    dense_flops = 6.0 * n * fw.d_model * fw.d_ff
+    sparse_layer = us["prefill"] + us["mass"] + us["topk"] + us["sparse_ffn"]
+    dense_layer = us["prefill"] + us["dense_ffn"]
+    ffn_tf = ffn_flops / (us["sparse_ffn"] * 1e-6) / 1e12
+    return {"workload": "Mistral-shaped 8K layer: prefill, mass, top-k of 2048 tokens, SwiGLU FFN "
+                        "4096x14336 on them; dense FFN on all 8192 for comparison",
+            "us": {kk: round(vv, 2) for kk, vv in us.items()},
+            "prefill_useful_tflops": round(att_flops / (us["prefill"] * 1e-6) / 1e12, 1),
+            "mass_tflops": round(att_flops / 2 / (us["mass"] * 1e-6) / 1e12, 1),
+            "sparse_ffn_tflops": round(ffn_tf, 1),
+            "dense_ffn_tflops": round(dense_flops / (us["dense_ffn"] * 1e-6) / 1e12, 1),
+            "roofline_ffn": {"bound": "tensor", "achieved": round(ffn_tf, 1), "peak": bf16_burst,
+                             "unit": "TFLOP/s", "frac": round(ffn_tf / bf16_burst, 4),
+                             "peak_kind": f"bf16 burst ({peak_src}); GEMMs timed alone"},
+            "ffn_share_of_dense_layer": round(us["dense_ffn"] / dense_layer, 3),
+            "layer_us_sparse": round(sparse_layer, 1), "layer_us_dense": round(dense_layer, 1),
+            "layer_speedup": round(dense_layer / sparse_layer, 3),
+            "kernels": ["prefill_kernel<128>", "mass_kernel<128>", "score_sum_kernel",
+                        "topk_kernel", "gather_rows_kernel", "ffn_gemm_kernel<0>",
+                        "ffn_gemm_kernel<1>"]}
 
 
 def run_transfer(dev, stream, hbm):
@@ -734,6 +809,10 @@ def run_case(args):
         print(json.dumps({"case": args.case, **run_transfer(dev, stream, measured_peaks()[0])}),
               flush=True)
         return
+    if args.case == "routing":
+        hbm, burst, _, src = measured_peaks()
+        print(json.dumps({"case": args.case, **run_routing(dev, stream, burst, src)}), flush=True)
+        return
     if args.case == "rope":
         print(json.dumps({"case": args.case, **run_rope(dev, stream, measured_peaks()[0])}),
               flush=True)
@@ -783,7 +862,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--case", default=None,
                     choices=["prefill-32k", "dense-32k", "decode", "prefill-128k-layers", "rope",
-                             "transfer"],
+                             "transfer", "routing"],
                     help="run one kernel's profiling case instead of the benchmark")
     args = ap.parse_args()
     if args.case:

@@ -15,7 +15,7 @@
 //
 // Warp roles (320 threads, persistent over an LPT-sorted unit list):
 //   warp 0      producer: the unit's K tile through the block table, then the
-//               query tiles (TMA, 2 stages) with each row's position and
+//               query tiles (TMA, 4 stages) with each row's position and
 //               log2-domain lse staged beside them;
 //   warp 1      TMEM owner (256 columns) and MMA issuer: S^T of query tile g
 //               into TMEM buffer g % 2;
@@ -23,6 +23,10 @@
 //               (odd tiles): one thread per key, p = 2^(s c - lse2) over the
 //               visible (key, row) pairs; the groups add their sums at the end
 //               of a unit and group 0 stores them.
+// A key tile seen by many query tiles (a global head's first keys) is cut
+// into pieces that run as separate units; their partial sums meet in a
+// scratch buffer and the last piece to finish adds them in piece order, so
+// the total is still formed in one fixed order.
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -34,6 +38,7 @@ using namespace ptx;
 namespace {
 
 constexpr int MT = 128;           // keys per unit, rows per query tile
+constexpr int NQ = 4;             // query-tile stages
 constexpr int kThreadsM = 320;
 constexpr uint32_t kAtomM = MT * 128;  // one 64-column, 128-row swizzle block
 constexpr uint64_t kDrainNsM = 200ull * 1000 * 1000;
@@ -42,24 +47,24 @@ constexpr float kLog2e = 1.4426950408889634f;
 enum {
   M_K_FULL = 0,
   M_K_EMPTY = 1,
-  M_Q_FULL = 2,   // +stage
-  M_Q_EMPTY = 4,  // +stage
-  M_S_FULL = 6,   // +buffer
-  M_S_EMPTY = 8,  // +buffer
-  M_RED_FULL = 10,
-  M_RED_EMPTY = 11,
-  M_DRAIN = 12,
-  M_NUM = 13
+  M_Q_FULL = 2,        // +stage
+  M_Q_EMPTY = 2 + NQ,  // +stage
+  M_S_FULL = 2 + 2 * NQ,   // +buffer
+  M_S_EMPTY = 4 + 2 * NQ,  // +buffer
+  M_RED_FULL = 6 + 2 * NQ,
+  M_RED_EMPTY = 7 + 2 * NQ,
+  M_DRAIN = 8 + 2 * NQ,
+  M_NUM = 9 + 2 * NQ
 };
 
 template <int D>
 struct MLayout {
   static constexpr uint32_t TILE = MT * D * 2;
   static constexpr uint32_t OFF_K = 0;
-  static constexpr uint32_t OFF_Q = TILE;                 // 2 stages
-  static constexpr uint32_t OFF_ROW = OFF_Q + 2 * TILE;   // per stage: lse2[128], pos[128], meta[4]
+  static constexpr uint32_t OFF_Q = TILE;                 // NQ stages
+  static constexpr uint32_t OFF_ROW = OFF_Q + NQ * TILE;  // per stage: lse2[128], pos[128], meta[4]
   static constexpr uint32_t ROW_BYTES = MT * 8 + 16;
-  static constexpr uint32_t OFF_RED = OFF_ROW + 2 * ROW_BYTES;  // float [128]
+  static constexpr uint32_t OFF_RED = OFF_ROW + NQ * ROW_BYTES;  // float [128]
   static constexpr uint32_t OFF_BAR = (OFF_RED + MT * 4 + 7) & ~7u;
   static constexpr uint32_t OFF_MISC = OFF_BAR + M_NUM * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16 + 1024;  // + slack to align to 1 KB
@@ -81,7 +86,8 @@ __device__ void m_producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const
   constexpr int NC = D / 64;
   const int box_rows = p.page_size <= MT ? p.page_size : MT;
   const int boxes = MT / box_rows;
-  int armed_k = -1, armed_q[2] = {-1, -1};
+  int armed_k = -1, armed_q[NQ];
+  for (int st = 0; st < NQ; ++st) armed_q[st] = -1;
   bool ok = true;
   int g = 0, ui = 0;
   for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++ui) {
@@ -105,10 +111,28 @@ __device__ void m_producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const
                       c.bar(M_K_FULL));
       }
     }
-    // the query tiles that see any key of the tile
+    // the query tiles that see any key of the tile. Row r = token (r / G) x
+    // head (r % G); each row's lse (log2 units) is loaded one tile ahead so
+    // its latency overlaps the wait for a free stage.
+    auto load_lse = [&](int qt, float (&l2)[MT / 32]) {
+#pragma unroll
+      for (int e = 0; e < MT / 32; ++e) {
+        const int r = lane + 32 * e;
+        const int t = qt * p.tpt + r / p.G;
+        l2[e] = t < U.ntok ? __ldg(p.lse + static_cast<int64_t>(U.head * p.G + r % p.G) * p.total_q +
+                                   U.tok0 + t)
+                           : 0.f;
+      }
+    };
+    float l_next[MT / 32];
+    load_lse(U.qt0, l_next);
     for (int qt = U.qt0; qt <= U.qt1; ++qt, ++g) {
-      const int st = g & 1;
-      const uint32_t ph = (g >> 1) & 1;
+      float l_cur[MT / 32];
+#pragma unroll
+      for (int e = 0; e < MT / 32; ++e) l_cur[e] = l_next[e];
+      if (qt < U.qt1) load_lse(qt + 1, l_next);
+      const int st = g % NQ;
+      const uint32_t ph = (g / NQ) & 1;
       if (!waitw(c.bar(M_Q_EMPTY + st), ph ^ 1, c.wc)) { ok = false; break; }
       if (lane == 0) {
         mbar_expect_tx(c.bar(M_Q_FULL + st), L::TILE);
@@ -117,45 +141,29 @@ __device__ void m_producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const
                       U.head * p.G, U.tok0 + qt * p.tpt, c.bar(M_Q_FULL + st));
       }
       armed_q[st] = static_cast<int>(ph);
-      // row r = token (r / G) x head (r % G): position (-1: no such token) and lse in log2 units
       float* lse2 = reinterpret_cast<float*>(c.smem + L::OFF_ROW + st * L::ROW_BYTES);
       int* rpos = reinterpret_cast<int*>(lse2 + MT);
       int* meta = rpos + MT;
-      int pmin = 1 << 30, pmax = -1, all_valid = 1;
+      const int tq0 = qt * p.tpt;  // first token of the tile; position -1: no such token
+      const int last = min(U.ntok, tq0 + p.tpt) - 1;
 #pragma unroll
       for (int e = 0; e < MT / 32; ++e) {
         const int r = lane + 32 * e;
-        const int t = qt * p.tpt + r / p.G;
-        int pos = -1;
-        float l2 = 0.f;
-        if (t < U.ntok) {
-          pos = U.a + t;
-          l2 = p.lse[static_cast<int64_t>(U.head * p.G + r % p.G) * p.total_q + U.tok0 + t] * kLog2e;
-          pmin = min(pmin, pos);
-          pmax = max(pmax, pos);
-        } else {
-          all_valid = 0;
-        }
-        lse2[r] = l2;
-        rpos[r] = pos;
+        const int t = tq0 + r / p.G;
+        lse2[r] = l_cur[e] * kLog2e;
+        rpos[r] = t < U.ntok ? U.a + t : -1;
       }
-#pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) {
-        pmin = min(pmin, __shfl_xor_sync(0xffffffffu, pmin, o));
-        pmax = max(pmax, __shfl_xor_sync(0xffffffffu, pmax, o));
-      }
-      all_valid = __all_sync(0xffffffffu, all_valid);
       if (lane == 0) {
-        meta[0] = pmin;
-        meta[1] = pmax;
-        meta[2] = all_valid;
+        meta[0] = U.a + tq0;             // smallest position of the tile
+        meta[1] = U.a + last;            // largest
+        meta[2] = tq0 + p.tpt <= U.ntok;  // every row is a token
       }
       mbar_arrive(c.bar(M_Q_FULL + st));  // every lane: its rows are written
     }
   }
   if (!ok && lane == 0) {  // aborting: let our own copies land before the block exits
     if (armed_k >= 0) wait_drain(c.bar(M_K_FULL), armed_k, kDrainNsM);
-    for (int st = 0; st < 2; ++st)
+    for (int st = 0; st < NQ; ++st)
       if (armed_q[st] >= 0) wait_drain(c.bar(M_Q_FULL + st), armed_q[st], kDrainNsM);
   }
 }
@@ -170,20 +178,19 @@ __device__ void m_mma(const MassParams& p, const MCtx& c) {
     const MassUnit U = p.units[u];
     if (!wait1(c.bar(M_K_FULL), ui & 1, c.wc)) { ok = false; break; }
     for (int qt = U.qt0; qt <= U.qt1; ++qt, ++g) {
-      const int st = g & 1;
-      const uint32_t ph = (g >> 1) & 1;
-      if (!wait1(c.bar(M_S_EMPTY + st), ph ^ 1, c.wc)) { ok = false; break; }
-      if (!wait1(c.bar(M_Q_FULL + st), ph, c.wc)) { ok = false; break; }
+      const int sb = g & 1, qs = g % NQ;
+      if (!wait1(c.bar(M_S_EMPTY + sb), ((g >> 1) & 1) ^ 1, c.wc)) { ok = false; break; }
+      if (!wait1(c.bar(M_Q_FULL + qs), (g / NQ) & 1, c.wc)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t a = c.sbase + L::OFF_K + (kk >> 2) * kAtomM + (kk & 3) * 32;
-        const uint32_t b = c.sbase + L::OFF_Q + st * L::TILE + (kk >> 2) * kAtomM + (kk & 3) * 32;
-        mma_bf16(c.tmem + st * MT, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, 16, 1024), IDESC,
+        const uint32_t b = c.sbase + L::OFF_Q + qs * L::TILE + (kk >> 2) * kAtomM + (kk & 3) * 32;
+        mma_bf16(c.tmem + sb * MT, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, 16, 1024), IDESC,
                  kk > 0 ? 1u : 0u);
       }
-      mma_commit(c.bar(M_S_FULL + st));
-      mma_commit(c.bar(M_Q_EMPTY + st));
+      mma_commit(c.bar(M_S_FULL + sb));
+      mma_commit(c.bar(M_Q_EMPTY + qs));
     }
     if (ok) mma_commit(c.bar(M_K_EMPTY));
   }
@@ -210,13 +217,14 @@ __device__ void m_consumer(const MassParams& p, const MCtx& c, int grp, int warp
     float acc = 0.f;
     for (int qt = U.qt0; ok && qt <= U.qt1; ++qt, ++g) {
       if ((g & 1) != grp) continue;
-      const uint32_t ph = (g >> 1) & 1;
-      if (!waitw(c.bar(M_Q_FULL + grp), ph, c.wc) || !waitw(c.bar(M_S_FULL + grp), ph, c.wc)) {
+      const int qs = g % NQ;
+      if (!waitw(c.bar(M_Q_FULL + qs), (g / NQ) & 1, c.wc) ||
+          !waitw(c.bar(M_S_FULL + grp), (g >> 1) & 1, c.wc)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const float* lse2 = reinterpret_cast<const float*>(c.smem + L::OFF_ROW + grp * L::ROW_BYTES);
+      const float* lse2 = reinterpret_cast<const float*>(c.smem + L::OFF_ROW + qs * L::ROW_BYTES);
       const int* rpos = reinterpret_cast<const int*>(lse2 + MT);
       const int* meta = rpos + MT;
       // every (key, row) pair of this warp visible: no per-element test
@@ -255,7 +263,7 @@ __device__ void m_consumer(const MassParams& p, const MCtx& c, int grp, int warp
       }
       acc += (part[0] + part[1]) + (part[2] + part[3]);
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(M_Q_EMPTY + grp));
+      if (lane == 0) mbar_arrive(c.bar(M_Q_EMPTY + qs));
     }
     if (!ok) break;
     // group 1 hands its sums to group 0, which adds them and stores
@@ -269,8 +277,29 @@ __device__ void m_consumer(const MassParams& p, const MCtx& c, int grp, int warp
       const float tot = acc + red[jl];
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bar(M_RED_EMPTY));
-      if (j >= U.a && j < U.a + U.ntok)
-        p.mass[static_cast<int64_t>(U.head) * p.total_q + U.tok0 + (j - U.a)] = tot;
+      if (U.n_pieces == 1) {
+        if (j >= U.a && j < U.a + U.ntok)
+          p.mass[static_cast<int64_t>(U.head) * p.total_q + U.tok0 + (j - U.a)] = tot;
+      } else {
+        // a split key tile: each warp posts its 32 sums; the warp that
+        // finishes the tile last adds every piece in piece order
+        p.part[static_cast<int64_t>(U.part0 + U.piece) * MT + jl] = tot;
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(p.tile_cnt + U.tile_id, 1) == 4 * U.n_pieces - 1;
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+          __threadfence();
+          for (int k = lane; k < MT; k += 32) {
+            float sum = 0.f;
+            for (int pc = 0; pc < U.n_pieces; ++pc)
+              sum += __ldcg(p.part + static_cast<int64_t>(U.part0 + pc) * MT + k);
+            const int jk = U.kt * MT + k;
+            if (jk >= U.a && jk < U.a + U.ntok)
+              p.mass[static_cast<int64_t>(U.head) * p.total_q + U.tok0 + (jk - U.a)] = sum;
+          }
+        }
+      }
     }
   }
 }
@@ -295,9 +324,11 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   if (threadIdx.x == 0) {
     mbar_init(c.bar(M_K_FULL), 1);
     mbar_init(c.bar(M_K_EMPTY), 1);
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < NQ; ++x) {
       mbar_init(c.bar(M_Q_FULL + x), 1 + 32);  // the copy's arrival + every producer lane
-      mbar_init(c.bar(M_Q_EMPTY + x), 1 + 4);  // the MMA commit + the group's four warps
+      mbar_init(c.bar(M_Q_EMPTY + x), 1 + 4);  // the MMA commit + the reading group's four warps
+    }
+    for (int x = 0; x < 2; ++x) {
       mbar_init(c.bar(M_S_FULL + x), 1);
       mbar_init(c.bar(M_S_EMPTY + x), 4);
     }

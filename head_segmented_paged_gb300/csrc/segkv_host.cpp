@@ -1262,14 +1262,46 @@ int segkv_attn_mass(segkv_t h, int layer, const void* q, const int32_t* cu_seqle
     }
   }
   if (units.empty()) return SEGKV_OK;
+  // Cut key tiles seen by many query tiles into pieces of at most `cap`
+  // query tiles, so that no unit is much longer than a CTA's fair share.
+  int64_t steps = 0;
+  for (const MassUnit& u : units) steps += u.qt1 - u.qt0 + 1;
+  const int ctas = std::max(1, h->num_sms);
+  const int32_t cap = static_cast<int32_t>(std::max<int64_t>(8, (steps + 2 * ctas - 1) / (2 * ctas)));
+  std::vector<MassUnit> cut;
+  int32_t slots = 0, tiles = 0;
+  for (const MassUnit& u : units) {
+    const int32_t len = u.qt1 - u.qt0 + 1;
+    const int32_t np = (len + cap - 1) / cap;
+    for (int32_t pc = 0; pc < np; ++pc) {
+      MassUnit v = u;
+      v.qt0 = u.qt0 + static_cast<int32_t>(int64_t(len) * pc / np);
+      v.qt1 = u.qt0 + static_cast<int32_t>(int64_t(len) * (pc + 1) / np) - 1;
+      v.piece = pc;
+      v.n_pieces = np;
+      v.part0 = np > 1 ? slots : 0;
+      v.tile_id = np > 1 ? tiles : 0;
+      cut.push_back(v);
+    }
+    if (np > 1) {
+      slots += np;
+      ++tiles;
+    }
+  }
+  units.swap(cut);
   std::stable_sort(units.begin(), units.end(), [](const MassUnit& x, const MassUnit& y) {
     return (x.qt1 - x.qt0) > (y.qt1 - y.qt0);
   });
   Pack pk;
   const size_t o_units = pk.add(units.data(), units.size());
+  const std::vector<int32_t> zeros(std::max(tiles, 1), 0);
+  const size_t o_cnt = pk.add(zeros.data(), zeros.size());  // counters travel as zeros
+  // partial sums live after the plan in the same ring region; they are not uploaded
+  const size_t o_part = align_up(pk.buf.size(), 256);
+  const size_t region = o_part + static_cast<size_t>(slots) * kKeyTile * 4;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   size_t off;
-  cudaError_t e = h->ring.reserve(pk.buf.size(), &off);
+  cudaError_t e = h->ring.reserve(region, &off);
   if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
   std::memcpy(h->ring.host + off, pk.buf.data(), pk.buf.size());
   e = cudaMemcpyAsync(h->ring.dev + off, h->ring.host + off, pk.buf.size(), cudaMemcpyHostToDevice, s);
@@ -1291,6 +1323,8 @@ int segkv_attn_mass(segkv_t h, int layer, const void* q, const int32_t* cu_seqle
   }
   MassParams p{};
   p.units = reinterpret_cast<const MassUnit*>(h->ring.dev + off + o_units);
+  p.tile_cnt = reinterpret_cast<int*>(h->ring.dev + off + o_cnt);
+  p.part = reinterpret_cast<float*>(h->ring.dev + off + o_part);
   p.table = h->d_table;
   p.lse = lse;
   p.mass = mass;
@@ -1309,7 +1343,7 @@ int segkv_attn_mass(segkv_t h, int layer, const void* q, const int32_t* cu_seqle
   const int grid = static_cast<int>(std::min<int64_t>(units.size(), h->num_sms));
   e = launch_mass(p, tq, h->tm_k, h->D, grid, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "mass kernel launch");
-  e = h->ring.commit(off, pk.buf.size(), s);
+  e = h->ring.commit(off, region, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "event record");
   return SEGKV_OK;
 }

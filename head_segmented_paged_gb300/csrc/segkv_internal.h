@@ -170,10 +170,15 @@ struct MassUnit {
   int32_t first_page;  // first held logical page of the segment
   int32_t last_page;   // last held logical page
   int32_t table_row;
-  int32_t pad;
+  int32_t piece;       // a long key tile's query range is cut into n_pieces pieces
+  int32_t n_pieces;
+  int32_t part0;       // partial-sum slot of piece 0 (slots part0 .. part0 + n_pieces - 1)
+  int32_t tile_id;     // counter of the key tile's finished pieces
 };
 struct MassParams {
   const MassUnit* units;
+  float* part;         // [slots][128] partial sums of split key tiles
+  int* tile_cnt;       // [tiles] finished pieces, zero at launch
   const int32_t* table;
   const float* lse;    // fp32 [Hq, total_q], natural log, from the prefill of the chunk
   float* mass;         // fp32 [Hkv, total_q]
