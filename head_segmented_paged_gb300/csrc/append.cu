@@ -6,6 +6,8 @@
 // writes the new ids into the device block table.
 //
 // HBM bound: every 16-byte vector of K and V is read once and written once.
+#include <algorithm>
+
 #include "segkv_internal.h"
 
 namespace skv {
@@ -54,6 +56,25 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_append(const AppendParams& p, const AppendBlob* blob, int grid, cudaStream_t s) {
   static const AppendBlob empty_blob{};
   append_kernel<<<grid, 256, 0, s>>>(p, blob ? *blob : empty_blob);
+  return cudaGetLastError();
+}
+
+// Plan upload on the SMs: copies a plan from mapped pinned host memory into
+// device memory. A copy-engine transfer would queue behind the caller's own
+// large host-to-device copies; this kernel only shares the link's bandwidth.
+__global__ void plan_copy_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t n) {
+  for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < n;
+       i += size_t(gridDim.x) * blockDim.x)
+    dst[i] = src[i];
+}
+
+cudaError_t launch_plan_copy(const void* src, void* dst, size_t bytes, cudaStream_t s) {
+  const size_t n = (bytes + 15) / 16;
+  if (n == 0) return cudaSuccess;
+  const int threads = 256;
+  const size_t blocks = std::min<size_t>((n + threads - 1) / threads, 1024);
+  plan_copy_kernel<<<static_cast<int>(blocks), threads, 0, s>>>(static_cast<const uint4*>(src),
+                                                                static_cast<uint4*>(dst), n);
   return cudaGetLastError();
 }
 

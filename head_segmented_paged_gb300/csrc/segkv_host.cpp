@@ -52,12 +52,15 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Pinned host staging buffer mirrored by a device buffer of the same size.
-// Each call takes the next region, fills it on the host, copies it with one
-// cudaMemcpyAsync and records an event after its kernels; a region is reused
-// only once its event has completed.
+// Pinned, device-mapped host staging buffer mirrored by a device buffer of
+// the same size. Each call takes the next region, fills it on the host, has a
+// small kernel copy it to the device (upload) and records an event after its
+// own kernels; a region is reused only once its event has completed. The
+// copy runs on the SMs: a copy-engine transfer would wait behind the caller's
+// own large host-to-device copies and serialise them with the compute.
 struct UploadRing {
   uint8_t* host = nullptr;
+  uint8_t* hmap = nullptr;  // device address of the host buffer
   uint8_t* dev = nullptr;
   size_t cap = 0, head = 0;
   struct Chunk {
@@ -68,7 +71,9 @@ struct UploadRing {
   std::vector<cudaEvent_t> spare;
 
   cudaError_t init(size_t bytes) {
-    cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&host), bytes, cudaHostAllocDefault);
+    cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&host), bytes, cudaHostAllocMapped);
+    if (e != cudaSuccess) return e;
+    e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&hmap), host, 0);
     if (e != cudaSuccess) return e;
     e = cudaMalloc(reinterpret_cast<void**>(&dev), bytes);
     if (e != cudaSuccess) return e;
@@ -86,7 +91,7 @@ struct UploadRing {
     spare.clear();
     if (host) cudaFreeHost(host);
     if (dev) cudaFree(dev);
-    host = dev = nullptr;
+    host = hmap = dev = nullptr;
     cap = head = 0;
   }
   void retire_front() {
@@ -106,7 +111,7 @@ struct UploadRing {
       spare.clear();
       cudaFreeHost(host);
       cudaFree(dev);
-      host = dev = nullptr;
+      host = hmap = dev = nullptr;
       e = init(ncap);
       if (e != cudaSuccess) return e;
     }
@@ -121,6 +126,10 @@ struct UploadRing {
     *off = head;
     head += len;
     return cudaSuccess;
+  }
+  // Copy len bytes of a reserved region to the device, on stream s.
+  cudaError_t upload(size_t off, size_t len, cudaStream_t s) {
+    return launch_plan_copy(hmap + off, dev + off, len, s);
   }
   cudaError_t commit(size_t off, size_t len, cudaStream_t s) {
     cudaEvent_t ev;
@@ -478,9 +487,8 @@ int segkv_append(segkv_t h, int layer, const void* k, const void* v, const int32
     e = h->ring.reserve(pk.buf.size(), &off);
     if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
     std::memcpy(h->ring.host + off, pk.buf.data(), pk.buf.size());
-    e = cudaMemcpyAsync(h->ring.dev + off, h->ring.host + off, pk.buf.size(),
-                        cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpyAsync(append plan)");
+    e = h->ring.upload(off, pk.buf.size(), s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "plan upload (append)");
     d = reinterpret_cast<uintptr_t>(h->ring.dev + off);
   }
   h->upload_bytes += static_cast<int64_t>(pk.buf.size());
@@ -591,8 +599,8 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
   cudaError_t e = h->ring.reserve(pk.buf.size(), &off);
   if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
   std::memcpy(h->ring.host + off, pk.buf.data(), pk.buf.size());
-  e = cudaMemcpyAsync(h->ring.dev + off, h->ring.host + off, pk.buf.size(), cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpyAsync(prefill plan)");
+  e = h->ring.upload(off, pk.buf.size(), s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "plan upload (prefill)");
   h->upload_bytes += static_cast<int64_t>(pk.buf.size());
 
   CUtensorMap tq;
@@ -767,9 +775,8 @@ static int decode_core(segkv* h, int layer, const void* q, int T, const int32_t*
     e = h->ring.reserve(pk.buf.size(), &off_ring);
     if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
     std::memcpy(h->ring.host + off_ring, pk.buf.data(), pk.buf.size());
-    e = cudaMemcpyAsync(h->ring.dev + off_ring, h->ring.host + off_ring, pk.buf.size(),
-                        cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpyAsync(decode plan)");
+    e = h->ring.upload(off_ring, pk.buf.size(), s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "plan upload (decode)");
     d = reinterpret_cast<uintptr_t>(h->ring.dev + off_ring);
   }
   h->upload_bytes += static_cast<int64_t>(pk.buf.size());
@@ -867,9 +874,8 @@ int segkv_rope_shift(segkv_t h, int layer, int seq, int32_t delta, double base, 
     e = h->ring.reserve(pk.buf.size(), &off);
     if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
     std::memcpy(h->ring.host + off, pk.buf.data(), pk.buf.size());
-    e = cudaMemcpyAsync(h->ring.dev + off, h->ring.host + off, pk.buf.size(),
-                        cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpyAsync(rope plan)");
+    e = h->ring.upload(off, pk.buf.size(), s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "plan upload (rope)");
     d = reinterpret_cast<uintptr_t>(h->ring.dev + off);
   }
   h->upload_bytes += static_cast<int64_t>(pk.buf.size());
@@ -955,9 +961,8 @@ static int place_small_plan(segkv* h, const Pack& pk, cudaStream_t s, PlanPlace*
     cudaError_t e = h->ring.reserve(pk.buf.size(), &pp->off);
     if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
     std::memcpy(h->ring.host + pp->off, pk.buf.data(), pk.buf.size());
-    e = cudaMemcpyAsync(h->ring.dev + pp->off, h->ring.host + pp->off, pk.buf.size(),
-                        cudaMemcpyHostToDevice, s);
-    if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpyAsync(plan)");
+    e = h->ring.upload(pp->off, pk.buf.size(), s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "plan upload");
     pp->base = reinterpret_cast<uintptr_t>(h->ring.dev + pp->off);
   }
   h->upload_bytes += static_cast<int64_t>(pk.buf.size());
@@ -1304,8 +1309,8 @@ int segkv_attn_mass(segkv_t h, int layer, const void* q, const int32_t* cu_seqle
   cudaError_t e = h->ring.reserve(region, &off);
   if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
   std::memcpy(h->ring.host + off, pk.buf.data(), pk.buf.size());
-  e = cudaMemcpyAsync(h->ring.dev + off, h->ring.host + off, pk.buf.size(), cudaMemcpyHostToDevice, s);
-  if (e != cudaSuccess) return cuda_fail(h, e, "cudaMemcpyAsync(mass plan)");
+  e = h->ring.upload(off, pk.buf.size(), s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "plan upload (mass)");
   h->upload_bytes += static_cast<int64_t>(pk.buf.size());
   CUtensorMap tq;
   {

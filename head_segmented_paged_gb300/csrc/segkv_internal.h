@@ -230,6 +230,8 @@ cudaError_t launch_ffn_gemm(int epilogue, const CUtensorMap& ta, const CUtensorM
 int ffn_tile_rows();
 
 cudaError_t launch_append(const AppendParams& p, const AppendBlob* blob, int grid, cudaStream_t s);
+// copy a plan (16-byte aligned, size rounded up to 16) from mapped host memory to the device
+cudaError_t launch_plan_copy(const void* src, void* dst, size_t bytes, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, int head_dim, int grid, cudaStream_t s);
 int prefill_smem_bytes(int head_dim);
