@@ -144,12 +144,13 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
       const DecodeUnit U = units[u];
       const int32_t* trow = p.table + static_cast<int64_t>(U.table_row) * p.R;
       int kbase = -(1 << 30), my_id = 0;
-      for (int w = U.k0 / C::SK; w <= (U.k1 - 1) / C::SK; ++w, ++gs) {
+      // stages start at the unit's first key, so only its last stage is partial
+      for (int w = 0; U.k0 + w * C::SK < U.k1; ++w, ++gs) {
         const int st = gs % NS;
         const uint32_t ph = (gs / NS) & 1;
         if (!waitw(empty(st), ph ^ 1, wc)) { ok = false; break; }
-        const int vlo = max(U.k0, w * C::SK), vhi = min(U.k1, w * C::SK + C::SK);
-        const bool first = (w == U.k0 / C::SK);
+        const int vlo = U.k0 + w * C::SK, vhi = min(U.k1, vlo + C::SK);
+        const bool first = (w == 0);
         if (lane == 0) {
           uint32_t bytes = static_cast<uint32_t>((vhi - vlo) * C::ROW * 2);
           if (first) {  // the unit's descriptor and its G query rows travel with its first stage
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
           if (lane == 0) {
             const int64_t src =
                 (static_cast<int64_t>(id) * p.page_size + (pos - k * p.page_size)) * C::ROW;
-            const uint32_t dst = st * C::STAGE + (pos - w * C::SK) * C::ROW;
+            const uint32_t dst = st * C::STAGE + (pos - vlo) * C::ROW;
             const uint32_t n = static_cast<uint32_t>((pend - pos) * C::ROW);
             bulk_g2s(sbase + C::OFF_K + dst, static_cast<const uint8_t*>(p.kpool) + src, n, full(st));
             bulk_g2s(sbase + C::OFF_V + dst, static_cast<const uint8_t*>(p.vpool) + src, n, full(st));
@@ -252,11 +253,11 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
     float m = -INFINITY, l = 0.f;
 
     bool ok = true;
-    for (int w = U.k0 / C::SK; w <= (U.k1 - 1) / C::SK; ++w, ++gs) {
+    for (int w = 0; U.k0 + w * C::SK < U.k1; ++w, ++gs) {
       const int st = gs % NS;
       const uint32_t ph = (gs / NS) & 1;
       if (!waitw(full(st), ph, wc)) { ok = false; break; }
-      const int base = w * C::SK;
+      const int base = U.k0 + w * C::SK;  // first key of the stage
       const int vlo = max(U.k0, base) - base, vhi = min(U.k1, base + C::SK) - base;
       // the keys of this stage the lane's query row sees
       const int vlo_own = MQ ? max(vlo, lo_own - base) : vlo;
@@ -444,38 +445,62 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
       if (tid == 0) *last_flag = atomicAdd(p.pair_cnt + pair, 1) == U.pair_units - 1;
       consumer_sync<NCONS>();
       if (*last_flag) {
-        // the last slice of the pair merges every slice's partials; four
-        // slices per step keep their loads in flight together
+        // the last slice of the pair merges every slice's partials. Each
+        // thread owns EPT output elements; the loads of CH slices for all of
+        // them are issued together, so a pair of n slices costs about n / CH
+        // dependent L2 round trips instead of n / 4 per element.
+        constexpr int EPT = (G * D + NCONS - 1) / NCONS;
+        constexpr int CH = (24 / EPT) > 8 ? 8 : ((24 / EPT) < 1 ? 1 : 24 / EPT);
         __threadfence();
-        for (int idx = tid; idx < G * D; idx += NCONS) {
-          const int g = idx / D, d = idx - g * D;
-          float M = -INFINITY, Ls = 0.f, o = 0.f;
-          for (int c0 = 0; c0 < U.pair_units; c0 += 4) {
-            float mm[4], ll[4], aa[4];
+        float M[EPT], Ls[EPT], o[EPT];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+        for (int e = 0; e < EPT; ++e) {
+          M[e] = -INFINITY;
+          Ls[e] = 0.f;
+          o[e] = 0.f;
+        }
+        for (int c0 = 0; c0 < U.pair_units; c0 += CH) {
+          float mm[EPT][CH], ll[EPT][CH], aa[EPT][CH];
+#pragma unroll
+          for (int e = 0; e < EPT; ++e) {
+            const int idx = min(tid + e * NCONS, G * D - 1);
+            const int g = idx / D, d = idx - g * D;
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
               const int64_t uu = U.pair_unit0 + min(c0 + j, U.pair_units - 1);
-              mm[j] = (c0 + j < U.pair_units) ? __ldcg(p.part_ml + (uu * G + g) * 2) : -INFINITY;
-              ll[j] = __ldcg(p.part_ml + (uu * G + g) * 2 + 1);
-              aa[j] = __ldcg(p.part_acc + (uu * G + g) * D + d);
+              mm[e][j] = (c0 + j < U.pair_units) ? __ldcg(p.part_ml + (uu * G + g) * 2) : -INFINITY;
+              ll[e][j] = __ldcg(p.part_ml + (uu * G + g) * 2 + 1);
+              aa[e][j] = __ldcg(p.part_acc + (uu * G + g) * D + d);
             }
+          }
+#pragma unroll
+          for (int e = 0; e < EPT; ++e) {
             // a slice may hold no key a row sees (several query tokens per
             // sequence): its maximum is -inf and its weight 0
-            const float Mn = fmaxf(fmaxf(M, fmaxf(mm[0], mm[1])), fmaxf(mm[2], mm[3]));
-            const float Mr = (Mn == -INFINITY) ? 0.f : Mn;
-            const float sc = ex2(M - Mr);
-            Ls *= sc;
-            o *= sc;
+            float Mn = M[e];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float wgt = ex2(mm[j] - Mr);
-              Ls = fmaf(wgt, ll[j], Ls);
-              o = fmaf(wgt, aa[j], o);
+            for (int j = 0; j < CH; ++j) Mn = fmaxf(Mn, mm[e][j]);
+            const float Mr = (Mn == -INFINITY) ? 0.f : Mn;
+            const float sc = ex2(M[e] - Mr);
+            Ls[e] *= sc;
+            o[e] *= sc;
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+              const float wgt = ex2(mm[e][j] - Mr);
+              Ls[e] = fmaf(wgt, ll[e][j], Ls[e]);
+              o[e] = fmaf(wgt, aa[e][j], o[e]);
             }
-            M = Mn;
+            M[e] = Mn;
           }
-          out_at(g)[d] = __float2bfloat16_rn(o / Ls);
-          if (MQ && p.lse != nullptr && d == 0) put_lse(g, M, Ls);
+        }
+#pragma unroll
+        for (int e = 0; e < EPT; ++e) {
+          const int idx = tid + e * NCONS;
+          if (idx < G * D) {
+            const int g = idx / D, d = idx - g * D;
+            out_at(g)[d] = __float2bfloat16_rn(o[e] / Ls[e]);
+            if (MQ && p.lse != nullptr && d == 0) put_lse(g, M[e], Ls[e]);
+          }
         }
         if (tid == 0) p.pair_cnt[pair] = 0;  // ready for the next call
       }

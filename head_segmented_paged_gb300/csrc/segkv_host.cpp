@@ -711,46 +711,78 @@ static int decode_core(segkv* h, int layer, const void* q, int T, const int32_t*
       total += nlen - lo;
     }
   }
-  // stream-K split: CTA c streams keys [c*per, (c+1)*per) of the concatenated ranges
+  // Stream-K split with a cost model: the concatenated key ranges are cut into
+  // one slice per CTA so that keys + kDecodeUnitCost per unit is the same for
+  // every CTA. A unit's epilogue (the warps' merge, the output or partials)
+  // pauses its CTA's memory stream; measured on the ragged-decode workload, a
+  // CTA finished about 3 us later per extra unit, the time it streams about
+  // 128 keys in. The smallest per-CTA budget whose greedy cut fits the grid is
+  // found by bisection.
+  constexpr int64_t kDecodeUnitCost = 128;
   const int64_t sk = decode_stage_keys(rows);
   const int64_t ctas = h->num_sms > 0 ? int64_t(h->num_sms) * decode_ctas_per_sm(h->D, rows)
                                       : decode_max_grid(h);
-  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(
+  const int max_grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(
       std::min<int64_t>(ctas, decode_max_grid(h)), (total + sk - 1) / sk)));
-  const int64_t per = (total + grid - 1) / grid;
   std::vector<DecodeUnit> units;
   std::vector<int32_t> pair_unit0(ranges.size()), pair_units(ranges.size(), 0);
-  std::vector<int32_t> cta_begin(grid + 1);
+  std::vector<int32_t> cta_begin;
   std::vector<int32_t> unit_pair;  // ranges are pushed per (req, head): pair r = req * Hkv + head
-  size_t r = 0;
-  int32_t off = 0;
-  for (int c = 0; c < grid; ++c) {
-    cta_begin[c] = static_cast<int32_t>(units.size());
-    int64_t left = (c + 1 == grid) ? total : per;
-    while (left > 0 && r < ranges.size()) {
-      const Range& R = ranges[r];
-      const int32_t take = static_cast<int32_t>(std::min<int64_t>(left, R.n - R.lo - off));
-      if (off == 0) pair_unit0[r] = static_cast<int32_t>(units.size());
-      DecodeUnit u{};
-      u.req = R.req;
-      u.head = static_cast<int16_t>(R.head);
-      u.local = static_cast<int16_t>(R.local);
-      u.k0 = R.lo + off;
-      u.k1 = R.lo + off + take;
-      u.table_row = R.row;
-      u.q_last = R.n - 1;
-      units.push_back(u);
-      unit_pair.push_back(static_cast<int32_t>(r));
-      ++pair_units[r];
-      off += take;
-      left -= take;
-      if (off == R.n - R.lo) {
-        ++r;
-        off = 0;
+  // Greedy cut with budget T per CTA; returns the CTAs used (INT32_MAX if T is
+  // too small to hold even one key), emitting the units when asked.
+  auto cut = [&](int64_t T, bool emit) -> int64_t {
+    int64_t used = 0;
+    size_t r = 0;
+    int64_t off = 0;
+    while (r < ranges.size()) {
+      if (emit) cta_begin.push_back(static_cast<int32_t>(units.size()));
+      int64_t cost = 0;
+      bool any = false;
+      while (r < ranges.size()) {
+        const Range& R = ranges[r];
+        const int64_t avail = R.n - R.lo - off;
+        const int64_t room = T - cost - kDecodeUnitCost;
+        if (room < 1) {
+          if (!any) return INT32_MAX;
+          break;
+        }
+        const int64_t take = std::min(avail, room);
+        if (emit) {
+          if (off == 0) pair_unit0[r] = static_cast<int32_t>(units.size());
+          DecodeUnit u{};
+          u.req = R.req;
+          u.head = static_cast<int16_t>(R.head);
+          u.local = static_cast<int16_t>(R.local);
+          u.k0 = static_cast<int32_t>(R.lo + off);
+          u.k1 = static_cast<int32_t>(R.lo + off + take);
+          u.table_row = R.row;
+          u.q_last = R.n - 1;
+          units.push_back(u);
+          unit_pair.push_back(static_cast<int32_t>(r));
+          ++pair_units[r];
+        }
+        cost += kDecodeUnitCost + take;
+        any = true;
+        off += take;
+        if (take == avail) {
+          ++r;
+          off = 0;
+        } else {
+          break;  // this CTA's budget is spent
+        }
       }
+      ++used;
     }
+    return used;
+  };
+  int64_t lo = 1, hi = total + kDecodeUnitCost * (static_cast<int64_t>(ranges.size()) + 1);
+  while (lo < hi) {  // smallest budget that fits max_grid CTAs
+    const int64_t mid = lo + (hi - lo) / 2;
+    if (cut(mid, false) <= max_grid) hi = mid;
+    else lo = mid + 1;
   }
-  cta_begin[grid] = static_cast<int32_t>(units.size());
+  const int grid = static_cast<int>(cut(lo, true));
+  cta_begin.push_back(static_cast<int32_t>(units.size()));
   for (size_t x = 0; x < units.size(); ++x) {
     units[x].pair_unit0 = pair_unit0[unit_pair[x]];
     units[x].pair_units = pair_units[unit_pair[x]];
