@@ -241,6 +241,7 @@ def run_ours(args, rank, world):
         out["rope_shift"] = run_rope(dev, stream, hbm)
         out["pd_transfer"] = run_transfer(dev, stream, hbm)
         out["sparse_ffn_routing"] = run_routing(dev, stream, bf16_burst, peak_src)
+        out["prefill_configs"] = run_prefill_configs(dev, stream, bf16_burst, peak_src)
     if not args.no_dense:
         out["dense"] = run_dense(args, dev, stream, sets, cu, q_pos, o, prefill_ms)
     if not args.no_e2e:
@@ -428,6 +429,53 @@ def run_rope(dev, stream, hbm):
             "us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
             "frac_hbm": round(nbytes / (us * 1e-6) / 1e9 / hbm, 4), "bytes": nbytes,
             "kernel": "rope_kernel"}
+
+
+def run_prefill_configs(dev, stream, bf16_burst, peak_src):
+    """Single-layer prefill of the Mistral-shaped 8K sequence and of the
+    Llama-70B-shaped varlen batch (4 sequences of 16K-32K, window 2048, key
+    sinks): prefill kernel time, tokens/s and useful TFLOP/s."""
+    import torch
+
+    import head_segmented_paged_gb300 as S
+    from head_segmented_paged_gb300 import inputs as I
+
+    out = {}
+    for w in (I.mistral_8k(), I.llama70b_varlen()):
+        q, k, v, cu, qp = I.prefill_tensors(w, 0, device=dev)
+        cu, qp = cu.numpy(), qp.numpy()
+        P, D = w.page_size, w.head_dim
+        pages = sum(n // P + 2 for n in w.seq_lens) * w.hkv + 8
+        kp = torch.empty((pages, P, D), dtype=torch.bfloat16, device=dev)
+        h = S.SegKV(1, w.hq, w.hkv, D, w.head_class, w.window, P, len(w.seq_lens),
+                    max(w.seq_lens), kp, torch.empty_like(kp))
+        ids = list(range(len(w.seq_lens)))
+        h.append(0, k, v, cu, ids, stream)
+        o = torch.empty((int(cu[-1]), w.hq, D), dtype=torch.bfloat16, device=dev)
+        for _ in range(3):
+            h.prefill_attn(0, q, cu, qp, ids, o, None, stream)
+        reps = 10
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            h.prefill_attn(0, q, cu, qp, ids, o, None, stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if h.status() != 0:
+            raise RuntimeError("device status after prefill: " + S.segkv_last_error(h.handle))
+        ms = e0.elapsed_time(e1) / reps
+        fl = sum(useful_flops_layer(w, 0, n) for n in w.seq_lens)
+        tf = fl / (ms * 1e-3) / 1e12
+        out[w.name] = {"seq_lens": list(w.seq_lens), "prefill_ms": round(ms, 3),
+                       "tokens_per_s": round(int(cu[-1]) / (ms * 1e-3)),
+                       "useful_tflop": round(fl / 1e12, 3), "useful_tflops": round(tf, 1),
+                       "frac_of_burst": round(tf / bf16_burst, 4)}
+        h.close()
+        del q, k, v, o, kp
+        torch.cuda.empty_cache()
+    out["peak_kind"] = f"bf16 burst ({peak_src}); one layer timed alone, inputs larger than L2"
+    return out
 
 
 def run_routing(dev, stream, bf16_burst, peak_src):
@@ -810,6 +858,11 @@ def run_case(args):
         print(json.dumps({"case": args.case, **run_transfer(dev, stream, measured_peaks()[0])}),
               flush=True)
         return
+    if args.case == "configs":
+        hbm, burst, _, src = measured_peaks()
+        print(json.dumps({"case": args.case, **run_prefill_configs(dev, stream, burst, src)}),
+              flush=True)
+        return
     if args.case == "routing":
         hbm, burst, _, src = measured_peaks()
         print(json.dumps({"case": args.case, **run_routing(dev, stream, burst, src)}), flush=True)
@@ -863,7 +916,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--case", default=None,
                     choices=["prefill-32k", "dense-32k", "decode", "prefill-128k-layers", "rope",
-                             "transfer", "routing"],
+                             "transfer", "routing", "configs"],
                     help="run one kernel's profiling case instead of the benchmark")
     args = ap.parse_args()
     if args.case:

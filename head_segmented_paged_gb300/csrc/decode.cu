@@ -450,7 +450,7 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
         // them are issued together, so a pair of n slices costs about n / CH
         // dependent L2 round trips instead of n / 4 per element.
         constexpr int EPT = (G * D + NCONS - 1) / NCONS;
-        constexpr int CH = (24 / EPT) > 8 ? 8 : ((24 / EPT) < 1 ? 1 : 24 / EPT);
+        constexpr int CH = (16 / EPT) > 8 ? 8 : ((16 / EPT) < 1 ? 1 : 16 / EPT);
         __threadfence();
         float M[EPT], Ls[EPT], o[EPT];
 #pragma unroll
