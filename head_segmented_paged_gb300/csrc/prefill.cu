@@ -13,8 +13,8 @@
 // and per-row masks keep every row to its own key set: j <= p, and j >= p-W+1
 // for a local head.
 //
-// Warp roles (320 threads, one CTA per SM, persistent over an LPT-sorted
-// unit list):
+// Warp roles (320 threads, one CTA per SM, each CTA running its own list of
+// units from an LPT schedule):
 //   warp 0      TMA producer: Q tiles A and B, then K and V tiles (2 stages),
 //               block-table entries fetched 32 at a time by the whole warp;
 //   warp 1      TMEM owner and MMA issuer: S_X = Q_X K^T (X = A, B) into TMEM,
@@ -108,7 +108,7 @@ __device__ void producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const C
   int armed_q[2] = {-1, -1}, armed_kv[2] = {-1, -1};
   bool ok = true;
   int g = 0, ui = 0;
-  for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++ui) {
+  for (int u = p.cta_begin[blockIdx.x]; ok && u < p.cta_begin[blockIdx.x + 1]; ++u, ++ui) {
     const PrefillUnit U = p.units[u];
     for (int x = 0; x < 2; ++x) {
       if (!waitw(c.bar(B_Q_EMPTY + x), (ui & 1) ^ 1, c.wc)) { ok = false; break; }
@@ -200,7 +200,7 @@ __device__ void mma_issuer(const PrefillParams& p, const Ctx& c) {
     ok = false;
   }
   int g = 0, ui = 0;
-  for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++ui) {
+  for (int u = p.cta_begin[blockIdx.x]; ok && u < p.cta_begin[blockIdx.x + 1]; ++u, ++ui) {
     const PrefillUnit U = p.units[u];
     const int nt = U.kt1 - U.kt0 + 1;
     const uint32_t qpar = ui & 1;
@@ -257,7 +257,7 @@ __device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int x, in
   const uint32_t t_o = c.tmem + lane_off + L::TM_O + x * L::TM_O_STRIDE;
   const float scale = p.scale_log2;
   int g = 0, ui = 0;
-  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++ui) {
+  for (int u = p.cta_begin[blockIdx.x]; u < p.cta_begin[blockIdx.x + 1]; ++u, ++ui) {
     const PrefillUnit U = p.units[u];
     const int nt = U.kt1 - U.kt0 + 1;
     const int t = x * p.tpt + r / p.G, gg = r % p.G;

@@ -587,12 +587,40 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
       }
     }
   }
+  // LPT schedule: units in descending cost, each to the CTA with the least
+  // work so far; a unit costs its key tiles plus kPrefillUnitCost for filling
+  // and draining the pipeline and the output epilogue. Each CTA then runs its
+  // own list, longest first.
+  constexpr int64_t kPrefillUnitCost = 2;
   std::stable_sort(units.begin(), units.end(), [](const PrefillUnit& a, const PrefillUnit& b) {
     return (a.kt1 - a.kt0) > (b.kt1 - b.kt0);
   });
+  const int grid = static_cast<int>(std::min<int64_t>(units.size(), h->num_sms));
+  std::vector<int32_t> cta_of(units.size());
+  std::vector<int32_t> cta_begin(grid + 1, 0);
+  {
+    using Load = std::pair<int64_t, int32_t>;  // (work so far, CTA)
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
+    for (int c = 0; c < grid; ++c) least.push({0, c});
+    for (size_t x = 0; x < units.size(); ++x) {
+      Load l = least.top();
+      least.pop();
+      cta_of[x] = l.second;
+      ++cta_begin[l.second + 1];
+      l.first += units[x].kt1 - units[x].kt0 + 1 + kPrefillUnitCost;
+      least.push(l);
+    }
+  }
+  for (int c = 0; c < grid; ++c) cta_begin[c + 1] += cta_begin[c];
+  std::vector<PrefillUnit> by_cta(units.size());
+  {
+    std::vector<int32_t> fill(cta_begin.begin(), cta_begin.end() - 1);
+    for (size_t x = 0; x < units.size(); ++x) by_cta[fill[cta_of[x]]++] = units[x];
+  }
 
   Pack pk;
-  const size_t o_units = pk.add(units.data(), units.size());
+  const size_t o_units = pk.add(by_cta.data(), by_cta.size());
+  const size_t o_cta = pk.add(cta_begin.data(), cta_begin.size());
   const size_t o_pos = pk.add(q_pos, static_cast<size_t>(total));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   size_t off;
@@ -620,6 +648,7 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
   uint8_t* d = h->ring.dev + off;
   PrefillParams p{};
   p.units = reinterpret_cast<const PrefillUnit*>(d + o_units);
+  p.cta_begin = reinterpret_cast<const int32_t*>(d + o_cta);
   p.q_pos = reinterpret_cast<const int32_t*>(d + o_pos);
   p.table = h->d_table;
   p.o = o;
@@ -638,7 +667,6 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
   p.debug = h->debug;
   p.timeout_ns = kTimeoutNs;
   h->debug = 0;
-  const int grid = static_cast<int>(std::min<int64_t>(units.size(), h->num_sms));
   e = launch_prefill(p, tq, h->tm_k, h->tm_v, h->D, grid, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "prefill kernel launch");
   e = h->ring.commit(off, pk.buf.size(), s);

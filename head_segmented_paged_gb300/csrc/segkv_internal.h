@@ -67,7 +67,8 @@ struct PrefillUnit {
   int32_t pad;
 };
 struct PrefillParams {
-  const PrefillUnit* units;
+  const PrefillUnit* units;    // grouped by CTA
+  const int32_t* cta_begin;    // [grid + 1]: CTA c runs units cta_begin[c] .. cta_begin[c+1]-1
   const int32_t* q_pos;
   const int32_t* table;
   void* o;        // bf16 [total_q, Hq, D]
