@@ -13,7 +13,8 @@
 // any cross-thread reduction; a key's total is built inside one unit, in a
 // fixed order, so the result does not depend on scheduling.
 //
-// Warp roles (320 threads, persistent over an LPT-sorted unit list):
+// Warp roles (320 threads; each CTA runs its own list of units from an LPT
+// schedule):
 //   warp 0      producer: the unit's K tile through the block table, then the
 //               query tiles (TMA, 4 stages) with each row's position and
 //               log2-domain lse staged beside them;
@@ -90,7 +91,7 @@ __device__ void m_producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const
   for (int st = 0; st < NQ; ++st) armed_q[st] = -1;
   bool ok = true;
   int g = 0, ui = 0;
-  for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++ui) {
+  for (int u = p.cta_begin[blockIdx.x]; ok && u < p.cta_begin[blockIdx.x + 1]; ++u, ++ui) {
     const MassUnit U = p.units[u];
     // the unit's key tile, page by page through the block table
     if (!waitw(c.bar(M_K_EMPTY), (ui & 1) ^ 1, c.wc)) { ok = false; break; }
@@ -174,7 +175,7 @@ __device__ void m_mma(const MassParams& p, const MCtx& c) {
   constexpr uint32_t IDESC = idesc_bf16(MT, MT, 0);
   bool ok = true;
   int g = 0, ui = 0;
-  for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x, ++ui) {
+  for (int u = p.cta_begin[blockIdx.x]; ok && u < p.cta_begin[blockIdx.x + 1]; ++u, ++ui) {
     const MassUnit U = p.units[u];
     if (!wait1(c.bar(M_K_FULL), ui & 1, c.wc)) { ok = false; break; }
     for (int qt = U.qt0; qt <= U.qt1; ++qt, ++g) {
@@ -210,7 +211,7 @@ __device__ void m_consumer(const MassParams& p, const MCtx& c, int grp, int warp
   const float sc = p.scale_log2;
   int g = 0, ui = 0;
   bool ok = true;
-  for (int u = blockIdx.x; u < p.n_units; u += gridDim.x, ++ui) {
+  for (int u = p.cta_begin[blockIdx.x]; u < p.cta_begin[blockIdx.x + 1]; ++u, ++ui) {
     const MassUnit U = p.units[u];
     const int j = U.kt * MT + jl;           // this thread's key
     const int jw = U.kt * MT + wq * 32;     // the warp's first key

@@ -1354,11 +1354,33 @@ int segkv_attn_mass(segkv_t h, int layer, const void* q, const int32_t* cu_seqle
     }
   }
   units.swap(cut);
+  // LPT schedule, as for prefill: longest first, each to the least-loaded CTA
   std::stable_sort(units.begin(), units.end(), [](const MassUnit& x, const MassUnit& y) {
     return (x.qt1 - x.qt0) > (y.qt1 - y.qt0);
   });
+  const int grid = static_cast<int>(std::min<int64_t>(units.size(), h->num_sms));
+  std::vector<int32_t> cta_begin(grid + 1, 0), cta_of(units.size());
+  {
+    using Load = std::pair<int64_t, int32_t>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
+    for (int c = 0; c < grid; ++c) least.push({0, c});
+    for (size_t x = 0; x < units.size(); ++x) {
+      Load l = least.top();
+      least.pop();
+      cta_of[x] = l.second;
+      ++cta_begin[l.second + 1];
+      l.first += units[x].qt1 - units[x].qt0 + 2;  // + the unit's key-tile load and hand-off
+      least.push(l);
+    }
+    for (int c = 0; c < grid; ++c) cta_begin[c + 1] += cta_begin[c];
+    std::vector<MassUnit> by_cta(units.size());
+    std::vector<int32_t> fill(cta_begin.begin(), cta_begin.end() - 1);
+    for (size_t x = 0; x < units.size(); ++x) by_cta[fill[cta_of[x]]++] = units[x];
+    units.swap(by_cta);
+  }
   Pack pk;
   const size_t o_units = pk.add(units.data(), units.size());
+  const size_t o_cta = pk.add(cta_begin.data(), cta_begin.size());
   const std::vector<int32_t> zeros(std::max(tiles, 1), 0);
   const size_t o_cnt = pk.add(zeros.data(), zeros.size());  // counters travel as zeros
   // partial sums live after the plan in the same ring region; they are not uploaded
@@ -1388,6 +1410,7 @@ int segkv_attn_mass(segkv_t h, int layer, const void* q, const int32_t* cu_seqle
   }
   MassParams p{};
   p.units = reinterpret_cast<const MassUnit*>(h->ring.dev + off + o_units);
+  p.cta_begin = reinterpret_cast<const int32_t*>(h->ring.dev + off + o_cta);
   p.tile_cnt = reinterpret_cast<int*>(h->ring.dev + off + o_cnt);
   p.part = reinterpret_cast<float*>(h->ring.dev + off + o_part);
   p.table = h->d_table;
@@ -1405,7 +1428,6 @@ int segkv_attn_mass(segkv_t h, int layer, const void* q, const int32_t* cu_seqle
   p.scale_log2 = h->scale * 1.4426950408889634f;
   p.status = h->d_status;
   p.timeout_ns = kTimeoutNs;
-  const int grid = static_cast<int>(std::min<int64_t>(units.size(), h->num_sms));
   e = launch_mass(p, tq, h->tm_k, h->D, grid, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "mass kernel launch");
   e = h->ring.commit(off, region, s);

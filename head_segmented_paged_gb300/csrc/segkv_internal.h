@@ -177,7 +177,8 @@ struct MassUnit {
   int32_t tile_id;     // counter of the key tile's finished pieces
 };
 struct MassParams {
-  const MassUnit* units;
+  const MassUnit* units;       // grouped by CTA
+  const int32_t* cta_begin;    // [grid + 1]: CTA c runs units cta_begin[c] .. cta_begin[c+1]-1
   float* part;         // [slots][128] partial sums of split key tiles
   int* tile_cnt;       // [tiles] finished pieces, zero at launch
   const int32_t* table;
