@@ -20,10 +20,11 @@
 //               log2-domain lse staged beside them;
 //   warp 1      TMEM owner (256 columns) and MMA issuer: S^T of query tile g
 //               into TMEM buffer g % 2;
-//   warps 2..5  consumer group 0 (even query tiles), warps 6..9 group 1
-//               (odd tiles): one thread per key, p = 2^(s c - lse2) over the
-//               visible (key, row) pairs; the groups add their sums at the end
-//               of a unit and group 0 stores them.
+//   warps 2..9  two consumer groups of four warps, group x taking the
+//               query tiles g with g % 2 == x: one thread per key,
+//               p = 2^(s c - lse2) over the visible (key, row) pairs; the
+//               groups add their sums at the end of a unit and group 0
+//               stores them.
 // A key tile seen by many query tiles (a global head's first keys) is cut
 // into pieces that run as separate units; their partial sums meet in a
 // scratch buffer and the last piece to finish adds them in piece order, so
@@ -40,7 +41,8 @@ namespace {
 
 constexpr int MT = 128;           // keys per unit, rows per query tile
 constexpr int NQ = 4;             // query-tile stages
-constexpr int kThreadsM = 320;
+constexpr int NG = 2;             // consumer groups; group x takes query tiles g with g % NG == x
+constexpr int kThreadsM = 32 * (2 + 4 * NG);
 constexpr uint32_t kAtomM = MT * 128;  // one 64-column, 128-row swizzle block
 constexpr uint64_t kDrainNsM = 200ull * 1000 * 1000;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -50,12 +52,12 @@ enum {
   M_K_EMPTY = 1,
   M_Q_FULL = 2,        // +stage
   M_Q_EMPTY = 2 + NQ,  // +stage
-  M_S_FULL = 2 + 2 * NQ,   // +buffer
-  M_S_EMPTY = 4 + 2 * NQ,  // +buffer
-  M_RED_FULL = 6 + 2 * NQ,
-  M_RED_EMPTY = 7 + 2 * NQ,
-  M_DRAIN = 8 + 2 * NQ,
-  M_NUM = 9 + 2 * NQ
+  M_S_FULL = 2 + 2 * NQ,        // +buffer (one per group)
+  M_S_EMPTY = 2 + 2 * NQ + NG,  // +buffer
+  M_RED_FULL = 2 + 2 * NQ + 2 * NG,
+  M_RED_EMPTY = 3 + 2 * NQ + 2 * NG,
+  M_DRAIN = 4 + 2 * NQ + 2 * NG,
+  M_NUM = 5 + 2 * NQ + 2 * NG
 };
 
 template <int D>
@@ -65,8 +67,8 @@ struct MLayout {
   static constexpr uint32_t OFF_Q = TILE;                 // NQ stages
   static constexpr uint32_t OFF_ROW = OFF_Q + NQ * TILE;  // per stage: lse2[128], pos[128], meta[4]
   static constexpr uint32_t ROW_BYTES = MT * 8 + 16;
-  static constexpr uint32_t OFF_RED = OFF_ROW + NQ * ROW_BYTES;  // float [128]
-  static constexpr uint32_t OFF_BAR = (OFF_RED + MT * 4 + 7) & ~7u;
+  static constexpr uint32_t OFF_RED = OFF_ROW + NQ * ROW_BYTES;  // float [NG - 1][128]
+  static constexpr uint32_t OFF_BAR = (OFF_RED + (NG - 1) * MT * 4 + 7) & ~7u;
   static constexpr uint32_t OFF_MISC = OFF_BAR + M_NUM * 8;
   static constexpr uint32_t BYTES = OFF_MISC + 16 + 1024;  // + slack to align to 1 KB
 };
@@ -179,8 +181,8 @@ __device__ void m_mma(const MassParams& p, const MCtx& c) {
     const MassUnit U = p.units[u];
     if (!wait1(c.bar(M_K_FULL), ui & 1, c.wc)) { ok = false; break; }
     for (int qt = U.qt0; qt <= U.qt1; ++qt, ++g) {
-      const int sb = g & 1, qs = g % NQ;
-      if (!wait1(c.bar(M_S_EMPTY + sb), ((g >> 1) & 1) ^ 1, c.wc)) { ok = false; break; }
+      const int sb = g % NG, qs = g % NQ;
+      if (!wait1(c.bar(M_S_EMPTY + sb), ((g / NG) & 1) ^ 1, c.wc)) { ok = false; break; }
       if (!wait1(c.bar(M_Q_FULL + qs), (g / NQ) & 1, c.wc)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
@@ -217,10 +219,10 @@ __device__ void m_consumer(const MassParams& p, const MCtx& c, int grp, int warp
     const int jw = U.kt * MT + wq * 32;     // the warp's first key
     float acc = 0.f;
     for (int qt = U.qt0; ok && qt <= U.qt1; ++qt, ++g) {
-      if ((g & 1) != grp) continue;
+      if (g % NG != grp) continue;
       const int qs = g % NQ;
       if (!waitw(c.bar(M_Q_FULL + qs), (g / NQ) & 1, c.wc) ||
-          !waitw(c.bar(M_S_FULL + grp), (g >> 1) & 1, c.wc)) {
+          !waitw(c.bar(M_S_FULL + grp), (g / NG) & 1, c.wc)) {
         ok = false;
         break;
       }
@@ -232,50 +234,60 @@ __device__ void m_consumer(const MassParams& p, const MCtx& c, int grp, int warp
       const bool whole = meta[2] && jw + 31 <= meta[0] &&
                          (!U.local || meta[1] - p.window + 1 <= jw);
       float part[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {  // 64 columns at a time keeps s in registers
-        float s[MT / 2];
-        tmem_ld32(t_s + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-        tmem_ld32(t_s + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-        tmem_wait_ld();
-        if (half == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(c.bar(M_S_EMPTY + grp));
-        }
-        const int e0 = half * 64;
+      // 32 columns at a time; the next quarter's TMEM load is in flight while
+      // this one is summed
+      auto quarter = [&](const uint32_t (&b)[32], int e0) {
         if (whole) {
 #pragma unroll
-          for (int e = 0; e < MT / 2; e += 2) {
+          for (int e = 0; e < 32; e += 2) {
             const float2 l2 = *reinterpret_cast<const float2*>(lse2 + e0 + e);
-            const float2 x = __ffma2_rn(make_float2(s[e], s[e + 1]), make_float2(sc, sc),
-                                        make_float2(-l2.x, -l2.y));
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(b[e]), __uint_as_float(b[e + 1])),
+                                        make_float2(sc, sc), make_float2(-l2.x, -l2.y));
             part[(e >> 1) & 3] += ex2(x.x) + ex2(x.y);
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < MT / 2; ++e) {
+          for (int e = 0; e < 32; ++e) {
             const int pe = rpos[e0 + e];
             const bool vis = j <= pe && (!U.local || j >= pe - p.window + 1);
-            const float x = fmaf(s[e], sc, -lse2[e0 + e]);
+            const float x = fmaf(__uint_as_float(b[e]), sc, -lse2[e0 + e]);
             part[e & 3] += vis ? ex2(x) : 0.f;
           }
         }
-      }
+      };
+      uint32_t bA[32], bB[32];
+      tmem_ld32(t_s, bA);
+      tmem_wait_ld_dep(bA);
+      tmem_ld32(t_s + 32, bB);
+      quarter(bA, 0);
+      tmem_wait_ld_dep(bB);
+      tmem_ld32(t_s + 64, bA);
+      quarter(bB, 32);
+      tmem_wait_ld_dep(bA);
+      tmem_ld32(t_s + 96, bB);
+      quarter(bA, 64);
+      tmem_wait_ld_dep(bB);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(M_S_EMPTY + grp));  // the S buffer is read
+      quarter(bB, 96);
       acc += (part[0] + part[1]) + (part[2] + part[3]);
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bar(M_Q_EMPTY + qs));
     }
     if (!ok) break;
-    // group 1 hands its sums to group 0, which adds them and stores
-    if (grp == 1) {
+    // the other groups hand their sums to group 0, which adds them in group
+    // order and stores
+    if (grp > 0) {
       if (!waitw(c.bar(M_RED_EMPTY), (ui & 1) ^ 1, c.wc)) break;
-      red[jl] = acc;
+      red[(grp - 1) * MT + jl] = acc;
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bar(M_RED_FULL));
     } else {
       if (!waitw(c.bar(M_RED_FULL), ui & 1, c.wc)) break;
-      const float tot = acc + red[jl];
+      float tot = acc;
+#pragma unroll
+      for (int x = 0; x < NG - 1; ++x) tot += red[x * MT + jl];
       __syncwarp();
       if (lane == 0) mbar_arrive(c.bar(M_RED_EMPTY));
       if (U.n_pieces == 1) {
@@ -329,11 +341,11 @@ __global__ void __launch_bounds__(kThreadsM, 1)
       mbar_init(c.bar(M_Q_FULL + x), 1 + 32);  // the copy's arrival + every producer lane
       mbar_init(c.bar(M_Q_EMPTY + x), 1 + 4);  // the MMA commit + the reading group's four warps
     }
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < NG; ++x) {
       mbar_init(c.bar(M_S_FULL + x), 1);
       mbar_init(c.bar(M_S_EMPTY + x), 4);
     }
-    mbar_init(c.bar(M_RED_FULL), 4);
+    mbar_init(c.bar(M_RED_FULL), 4 * (NG - 1));
     mbar_init(c.bar(M_RED_EMPTY), 4);
     mbar_init(c.bar(M_DRAIN), 1);
     *abort_flag = 0;
@@ -342,7 +354,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     prefetch_tmap(&tmk);
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(tmem_slot), 2 * MT);
+    tmem_alloc(smem_addr(tmem_slot), NG * MT);  // NG S buffers of 128 columns
     tmem_relinquish();
   }
   tc_fence_before();
@@ -365,7 +377,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(c.tmem, 2 * MT);
+    tmem_dealloc(c.tmem, NG * MT);
   }
 }
 

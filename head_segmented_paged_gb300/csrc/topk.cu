@@ -17,6 +17,7 @@ namespace skv {
 namespace {
 
 constexpr int kTopkThreads = 1024;
+constexpr int kTopkSmemValues = 11 * 1024;  // scores staged in shared memory up to this length
 
 __global__ void score_sum_kernel(const float* __restrict__ mass, float* __restrict__ score,
                                  int64_t total, int hkv) {
@@ -62,11 +63,18 @@ __global__ void __launch_bounds__(kTopkThreads)
                     : p.seqs;
   const TopkSeq S = seqs[blockIdx.x];
   if (S.k <= 0) return;
-  const uint32_t* bits = reinterpret_cast<const uint32_t*>(score + S.tok0);
   const int n = S.ntok, tid = threadIdx.x;
   __shared__ int hist[256];
   __shared__ int warp_tot[32];
   __shared__ int sel_digit, sel_need;
+  __shared__ uint32_t staged[kTopkSmemValues];
+  // the four passes read the scores from shared memory when they fit
+  const uint32_t* bits = reinterpret_cast<const uint32_t*>(score + S.tok0);
+  if (n <= kTopkSmemValues) {
+    for (int t = tid; t < n; t += kTopkThreads) staged[t] = bits[t];
+    __syncthreads();
+    bits = staged;
+  }
   // k-th largest bit pattern, 8 bits at a time from the top
   uint32_t prefix = 0, mask = 0;
   int need = S.k;  // how many to take from the bucket that matches prefix
@@ -78,14 +86,31 @@ __global__ void __launch_bounds__(kTopkThreads)
       if ((b & mask) == prefix) atomicAdd(&hist[(b >> shift) & 255u], 1);
     }
     __syncthreads();
-    if (tid == 0) {
-      int above = 0, d = 255;
-      for (; d > 0; --d) {
-        if (above + hist[d] >= need) break;
-        above += hist[d];
+    if (tid < 32) {
+      // digits from the top: lane l holds digits 255-8l .. 248-8l; the lane
+      // whose bins cross `need` picks the digit
+      int c[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = hist[255 - 8 * tid - i];
+        sum += c[i];
       }
-      sel_digit = d;
-      sel_need = need - above;
+      int before = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, before, o);
+        if (tid >= o) before += y;
+      }
+      before -= sum;  // count of patterns in higher lanes' digits
+      if (before < need && before + sum >= need) {
+        int above = before, i = 0;
+        for (; i < 7; ++i) {
+          if (above + c[i] >= need) break;
+          above += c[i];
+        }
+        sel_digit = 255 - 8 * tid - i;
+        sel_need = need - above;
+      }
     }
     __syncthreads();
     prefix |= static_cast<uint32_t>(sel_digit) << shift;
