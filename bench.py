@@ -232,7 +232,10 @@ def run_ours(args, rank, world):
            "prefill_ms": round(prefill_ms, 3), "append_ms": round(append_ms, 3),
            "useful_tflop_per_step": round(step_flops / 1e12, 3),
            "prefill_useful_tflops": round(achieved, 2),
-           "roofline": roofline, "clocks": clocks, "gpu_launches": 2 * L * args.steps}
+           "roofline": roofline, "clocks": clocks,
+           # per layer: append and prefill, each after a plan-copy kernel (both plans
+           # travel through the upload ring at this size)
+           "gpu_launches": 4 * L * args.steps}
 
     del h
     torch.cuda.synchronize()

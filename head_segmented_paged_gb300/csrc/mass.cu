@@ -161,7 +161,8 @@ __device__ void m_producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const
         meta[1] = U.a + last;            // largest
         meta[2] = tq0 + p.tpt <= U.ntok;  // every row is a token
       }
-      mbar_arrive(c.bar(M_Q_FULL + st));  // every lane: its rows are written
+      __syncwarp();  // every lane's rows are written
+      if (lane == 0) mbar_arrive(c.bar(M_Q_FULL + st));
     }
   }
   if (!ok && lane == 0) {  // aborting: let our own copies land before the block exits
@@ -338,7 +339,7 @@ __global__ void __launch_bounds__(kThreadsM, 1)
     mbar_init(c.bar(M_K_FULL), 1);
     mbar_init(c.bar(M_K_EMPTY), 1);
     for (int x = 0; x < NQ; ++x) {
-      mbar_init(c.bar(M_Q_FULL + x), 1 + 32);  // the copy's arrival + every producer lane
+      mbar_init(c.bar(M_Q_FULL + x), 2);  // the copy's arrival + the rows written
       mbar_init(c.bar(M_Q_EMPTY + x), 1 + 4);  // the MMA commit + the reading group's four warps
     }
     for (int x = 0; x < NG; ++x) {

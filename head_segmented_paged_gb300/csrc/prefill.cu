@@ -354,7 +354,8 @@ __device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int x, in
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(c.bar(B_P_FULL + x));
+      __syncwarp();  // one arrival per warp: the barrier is on the softmax -> P V path
+      if (lane == 0) mbar_arrive(c.bar(B_P_FULL + x));
       m_used = m_tgt;
     }
     if (!ok) break;
@@ -386,7 +387,8 @@ __device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int x, in
       p.lse[static_cast<int64_t>(U.head * p.G + gg) * p.total_q + tok] =
           (m_used + log2f(l)) * 0.69314718055994530942f;
     tc_fence_before();
-    mbar_arrive(c.bar(B_O_EMPTY + x));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.bar(B_O_EMPTY + x));
     g += nt;
   }
 }
@@ -413,9 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(c.bar(B_Q_FULL + x), 1);
       mbar_init(c.bar(B_Q_EMPTY + x), 1);
       mbar_init(c.bar(B_S_FULL + x), 1);
-      mbar_init(c.bar(B_P_FULL + x), 128);
+      mbar_init(c.bar(B_P_FULL + x), 4);  // one arrival per softmax warp
       mbar_init(c.bar(B_O_FULL + x), 1);
-      mbar_init(c.bar(B_O_EMPTY + x), 128);
+      mbar_init(c.bar(B_O_EMPTY + x), 4);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(c.bar(B_K_FULL + s), 1);
