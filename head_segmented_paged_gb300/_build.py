@@ -13,7 +13,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsegkv.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CU_SOURCES = ["append.cu", "prefill.cu", "decode.cu", "decode_noalloc.cu", "rope.cu", "transfer.cu",
+CU_SOURCES = ["append.cu", "prefill.cu", "decode.cu", "decode_mma.cu", "decode_noalloc.cu", "rope.cu",
+              "transfer.cu",
               "ffn.cu", "mass.cu", "topk.cu"]
 CPP_SOURCES = ["segkv_host.cpp"]
 

@@ -1,0 +1,463 @@
+// Decode attention on the 5th-generation tensor core for 8 or 16 query rows
+// per KV head: several query tokens per sequence (T tokens x Gm heads, as in
+// speculative or chunked decoding) or wide GQA groups (RedKnot summary page,
+// section "SegPagedAttention（存储与执行底座）": attention over the per-head
+// segments; online softmax merge from the KV-cache architecture page, section
+// 5.2). On the CUDA cores these rows make decode FMA-bound; here both
+// contractions run on tcgen05 and the kernel stays bound by the K/V stream.
+//
+// Keys go to the TMEM lanes. Per stage of 128 keys the tensor core forms
+// S^T = K Q^T (M = 128 keys, N = 16 rows, K = D = 128). Each softmax thread
+// owns one key; a row's maximum over the stage comes from a warp redux and an
+// exchange among the four softmax warps. P^T (16 rows x 128 keys, bf16) is
+// written to shared memory in the 128-byte swizzled layout and the tensor core
+// accumulates O^T += V^T P^T (M = 128 dimensions, N = 16 rows, K = 128 keys)
+// in TMEM, with V read as an MN-major operand straight from its TMA tile. O is
+// rescaled only when a row's maximum grows by more than 2^8, which is exact.
+//
+// Work comes from the split-KV decode's stream-K plan. A unit whose (sequence,
+// KV head) pair lies in one unit writes O directly; otherwise it writes fp32
+// partials and decode_combine_kernel merges each split pair afterwards, one
+// CTA per (pair, row), with the running-maximum rule.
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0      producer: the unit's query rows (TMA), then K and V tiles of
+//               128 keys, page by page through the block table (3 stages);
+//   warp 1      TMEM owner (64 columns: S^T at 0, O^T at 32) and MMA issuer;
+//   warps 2..5  softmax and epilogue: thread t holds key t of a stage and
+//               dimension t of O^T.
+// Ordering: S of stage i is issued after P V of stage i-1 and a thread's
+// tcgen05 operations complete in order, so when S(i) is complete O is stable
+// (for a rescale) and P's buffer is free.
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+#include "segkv_internal.h"
+
+namespace skv {
+using namespace ptx;
+
+namespace {
+
+constexpr int KT = 128;  // keys per stage
+constexpr int NST = 3;   // K/V stages
+constexpr int MN = 16;   // MMA N: query rows (8 or 16 used)
+constexpr int kThreadsMD = 192;
+constexpr uint32_t kAtomKV = KT * 128;     // 64 dims x 128 keys: 16 KB
+constexpr uint32_t KV_TILE = 2 * kAtomKV;  // D = 128
+constexpr uint32_t kAtomR = MN * 128;      // 64 columns x 16 rows: 2 KB
+constexpr uint32_t OFF_K = 0;
+constexpr uint32_t OFF_V = NST * KV_TILE;
+constexpr uint32_t OFF_Q = 2 * NST * KV_TILE;          // Q: 2 atoms (dims 0..63, 64..127)
+constexpr uint32_t OFF_P = OFF_Q + 2 * kAtomR;         // P^T: 2 atoms (keys 0..63, 64..127)
+constexpr uint32_t OFF_XCH = OFF_P + 2 * kAtomR;       // int [2][4][16]: per-warp row maxima
+constexpr uint32_t OFF_LS = OFF_XCH + 2 * 4 * MN * 4;  // float [2][4][16]: per-warp row sums
+constexpr uint32_t OFF_BAR = OFF_LS + 2 * 4 * MN * 4;
+enum {
+  Y_Q_FULL = 0,
+  Y_Q_EMPTY = 1,
+  Y_K_FULL = 2,                 // +stage
+  Y_V_FULL = 2 + NST,           // +stage
+  Y_KV_EMPTY = 2 + 2 * NST,     // +stage
+  Y_S_FULL = 2 + 3 * NST,
+  Y_P_FULL = Y_S_FULL + 1,
+  Y_O_FULL = Y_S_FULL + 2,
+  Y_O_EMPTY = Y_S_FULL + 3,
+  Y_MX = Y_S_FULL + 4,          // +stage parity
+  Y_LS = Y_S_FULL + 6,          // +unit parity
+  Y_DRAIN = Y_S_FULL + 8,
+  Y_NUM = Y_S_FULL + 9
+};
+constexpr uint32_t OFF_MISC = OFF_BAR + Y_NUM * 8;
+constexpr uint32_t MD_BYTES = OFF_MISC + 16 + 1024;  // + slack to align to 1 KB
+constexpr uint32_t TM_S = 0, TM_O = 32, TM_COLS = 64;
+constexpr uint64_t kDrainNsMD = 200ull * 1000 * 1000;
+static_assert(MD_BYTES <= 227 * 1024, "decode_mma shared memory");
+
+struct MdCtx {
+  uint8_t* smem;
+  uint32_t sbase;
+  uint32_t tmem;
+  WaitCtx wc;
+  __device__ uint32_t bar(int i) const { return sbase + OFF_BAR + 8u * i; }
+};
+
+template <typename T>
+__device__ __forceinline__ const T* plan_ptr(const T* p, const PlanBlob& blob, int inl) {
+  return inl ? reinterpret_cast<const T*>(blob.data + reinterpret_cast<uintptr_t>(p)) : p;
+}
+
+__device__ void md_producer(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                            const DecodeMmaParams& p, const DecodeUnit* units,
+                            const int32_t* cta_begin, const MdCtx& c, int lane) {
+  const int box_rows = p.page_size <= KT ? p.page_size : KT;
+  const int boxes = KT / box_rows;
+  int armed_q = -1, armed_kv[NST];
+  for (int s = 0; s < NST; ++s) armed_kv[s] = -1;
+  bool ok = true;
+  int g = 0, ui = 0;
+  for (int u = cta_begin[blockIdx.x]; ok && u < cta_begin[blockIdx.x + 1]; ++u, ++ui) {
+    const DecodeUnit U = units[u];
+    // the unit's query rows: token t of the sequence, heads head*Gm .. +Gm-1 -> row t*Gm + j
+    if (!waitw(c.bar(Y_Q_EMPTY), (ui & 1) ^ 1, c.wc)) { ok = false; break; }
+    if (lane == 0) {
+      mbar_expect_tx(c.bar(Y_Q_FULL), 2u * p.R_rows * 128);
+      for (int cc = 0; cc < 2; ++cc)
+        tma_load_3d(c.sbase + OFF_Q + cc * kAtomR, tq, cc * 64, U.head * p.Gm, U.req * p.T,
+                    c.bar(Y_Q_FULL));
+    }
+    armed_q = ui & 1;
+    const int32_t* trow = p.table + static_cast<int64_t>(U.table_row) * p.R;
+    const int kfirst = U.k0 / p.page_size, klast = (U.k1 - 1) / p.page_size;
+    int kbase = -(1 << 30), my_id = 0;
+    for (int kt = U.k0 / KT; kt <= (U.k1 - 1) / KT; ++kt, ++g) {
+      const int st = g % NST;
+      const uint32_t ph = (g / NST) & 1;
+      if (!waitw(c.bar(Y_KV_EMPTY + st), ph ^ 1, c.wc)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_expect_tx(c.bar(Y_K_FULL + st), KV_TILE);
+        mbar_expect_tx(c.bar(Y_V_FULL + st), KV_TILE);
+      }
+      armed_kv[st] = static_cast<int>(ph);
+      for (int bi = 0; bi < boxes; ++bi) {
+        const int pos = kt * KT + bi * box_rows;
+        const int k = pos / p.page_size;
+        int y = p.oob_row;  // a page the unit does not use: zero fill
+        if (k >= kfirst && k <= klast) {
+          if (k >= kbase + 32) {
+            kbase = k;
+            my_id = (k + lane < p.R) ? trow[k + lane] : 0;
+          }
+          y = __shfl_sync(0xffffffffu, my_id, k - kbase) * p.page_size + (pos - k * p.page_size);
+        }
+        if (lane == 0) {
+          const uint32_t off = st * KV_TILE + bi * box_rows * 128;
+          for (int cc = 0; cc < 2; ++cc) {
+            tma_load_2d(c.sbase + OFF_K + off + cc * kAtomKV, tk, cc * 64, y, c.bar(Y_K_FULL + st));
+            tma_load_2d(c.sbase + OFF_V + off + cc * kAtomKV, tv, cc * 64, y, c.bar(Y_V_FULL + st));
+          }
+        }
+      }
+    }
+  }
+  if (!ok && lane == 0) {  // aborting: let our own copies land before the block exits
+    if (armed_q >= 0) wait_drain(c.bar(Y_Q_FULL), armed_q, kDrainNsMD);
+    for (int s = 0; s < NST; ++s)
+      if (armed_kv[s] >= 0) {
+        wait_drain(c.bar(Y_K_FULL + s), armed_kv[s], kDrainNsMD);
+        wait_drain(c.bar(Y_V_FULL + s), armed_kv[s], kDrainNsMD);
+      }
+  }
+}
+
+__device__ void md_mma(const DecodeMmaParams& p, const DecodeUnit* units, const int32_t* cta_begin,
+                       const MdCtx& c) {
+  constexpr uint32_t IDESC_S = idesc_bf16_ab(KT, MN, 0, 0);   // K (keys x D) . Q^T
+  constexpr uint32_t IDESC_PV = idesc_bf16_ab(128, MN, 1, 0); // V^T (D x keys, MN-major) . P^T
+  bool ok = true;
+  int g = 0, ui = 0;
+  for (int u = cta_begin[blockIdx.x]; ok && u < cta_begin[blockIdx.x + 1]; ++u, ++ui) {
+    const DecodeUnit U = units[u];
+    const int kt0 = U.k0 / KT, kt1 = (U.k1 - 1) / KT;
+    if (!wait1(c.bar(Y_Q_FULL), ui & 1, c.wc)) { ok = false; break; }
+    for (int kt = kt0; kt <= kt1; ++kt, ++g) {
+      const int st = g % NST;
+      const uint32_t ph = (g / NST) & 1;
+      if (!wait1(c.bar(Y_K_FULL + st), ph, c.wc)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t a = c.sbase + OFF_K + st * KV_TILE + (kk >> 2) * kAtomKV + (kk & 3) * 32;
+        const uint32_t b = c.sbase + OFF_Q + (kk >> 2) * kAtomR + (kk & 3) * 32;
+        mma_bf16(c.tmem + TM_S, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, 16, 1024), IDESC_S,
+                 kk > 0 ? 1u : 0u);
+      }
+      mma_commit(c.bar(Y_S_FULL));
+      if (kt == kt1) mma_commit(c.bar(Y_Q_EMPTY));
+      if (!wait1(c.bar(Y_P_FULL), g & 1, c.wc)) { ok = false; break; }
+      if (!wait1(c.bar(Y_V_FULL + st), ph, c.wc)) { ok = false; break; }
+      if (kt == kt0 && !wait1(c.bar(Y_O_EMPTY), (ui & 1) ^ 1, c.wc)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < KT / 16; ++kk) {
+        const uint32_t a = c.sbase + OFF_V + st * KV_TILE + kk * 2048;
+        const uint32_t b = c.sbase + OFF_P + (kk >> 2) * kAtomR + (kk & 3) * 32;
+        mma_bf16(c.tmem + TM_O, sdesc_sw128(a, kAtomKV, 1024), sdesc_sw128(b, 16, 1024), IDESC_PV,
+                 (kt > kt0 || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(c.bar(Y_KV_EMPTY + st));
+      if (kt == kt1) mma_commit(c.bar(Y_O_FULL));
+    }
+  }
+  if (!ok) {  // aborting: let issued MMAs finish before TMEM is freed
+    mma_commit(c.bar(Y_DRAIN));
+    wait_drain(c.bar(Y_DRAIN), 0, kDrainNsMD);
+  }
+}
+
+__device__ void md_softmax(const DecodeMmaParams& p, const DecodeUnit* units,
+                           const int32_t* cta_begin, const MdCtx& c, int warp, int lane) {
+  const int wq = warp & 3;  // the TMEM lane quarter this warp may access
+  const int t = wq * 32 + lane;
+  const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+  const float sc = p.scale_log2;
+  const bool multi = p.T > 1;
+  int g = 0, ui = 0;
+  for (int u = cta_begin[blockIdx.x]; u < cta_begin[blockIdx.x + 1]; ++u, ++ui) {
+    const DecodeUnit U = units[u];
+    const int kt0 = U.k0 / KT, kt1 = (U.k1 - 1) / KT;
+    float m_ref[MN], l_part[MN];
+#pragma unroll
+    for (int r = 0; r < MN; ++r) {
+      m_ref[r] = -INFINITY;
+      l_part[r] = 0.f;
+    }
+    bool ok = true;
+    for (int kt = kt0; kt <= kt1; ++kt, ++g) {
+      if (!waitw(c.bar(Y_S_FULL), g & 1, c.wc)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sv[MN];
+      tmem_ld16(c.tmem + lane_off + TM_S, sv);
+      tmem_wait_ld();
+      const int j = kt * KT + t;  // this thread's key
+      const bool in_unit = j >= U.k0 && j < U.k1;
+      float s[MN];
+#pragma unroll
+      for (int r = 0; r < MN; ++r) {
+        bool vis = in_unit && r < p.R_rows;
+        if (multi) {  // row r = token r / Gm sees keys up to its own position (and its window)
+          const int pr = U.q_last - (p.T - 1) + r / p.Gm;
+          vis = vis && j <= pr && (!U.local || j >= pr - p.window + 1);
+        }
+        s[r] = vis ? __uint_as_float(sv[r]) * sc : -INFINITY;
+      }
+      // each row's maximum over the stage's 128 keys
+      int* xch = reinterpret_cast<int*>(c.smem + OFF_XCH) + (g & 1) * 4 * MN;
+#pragma unroll
+      for (int r = 0; r < MN; ++r) {
+        const int wm = warp_max_s32(f32_ordered(s[r]));
+        if (lane == 0) xch[wq * MN + r] = wm;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(Y_MX + (g & 1)));
+      if (!waitw(c.bar(Y_MX + (g & 1)), (g >> 1) & 1, c.wc)) { ok = false; break; }
+      bool resc = false;
+      float alpha[MN];
+#pragma unroll
+      for (int r = 0; r < MN; ++r) {
+        float mst = f32_from_ordered(xch[r]);
+#pragma unroll
+        for (int w = 1; w < 4; ++w) mst = fmaxf(mst, f32_from_ordered(xch[w * MN + r]));
+        alpha[r] = 1.f;
+        if (mst > m_ref[r] + 8.0f) {  // the same decision in every thread
+          alpha[r] = ex2(m_ref[r] - mst);
+          m_ref[r] = mst;
+          resc = true;
+        }
+      }
+      if (resc) {
+#pragma unroll
+        for (int r = 0; r < MN; ++r) l_part[r] *= alpha[r];
+        if (kt > kt0) {  // O^T holds earlier stages: scale its columns (this thread's dimension)
+          uint32_t ov[MN];
+          tmem_ld16(c.tmem + lane_off + TM_O, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int r = 0; r < MN; ++r) ov[r] = __float_as_uint(__uint_as_float(ov[r]) * alpha[r]);
+          tmem_st16(c.tmem + lane_off + TM_O, ov);
+          tmem_wait_st();
+        }
+      }
+      // P^T[r][t] in bf16, 128-byte swizzled: atom t / 64, 16-byte chunk ((t % 64) / 8) ^ (r % 8)
+      uint8_t* pb = c.smem + OFF_P + (t >> 6) * kAtomR + (t & 7) * 2;
+      const int chunk = (t & 63) >> 3;
+#pragma unroll
+      for (int r = 0; r < MN; ++r) {
+        const float mu = (m_ref[r] == -INFINITY) ? 0.f : m_ref[r];
+        const float pr = ex2(s[r] - mu);
+        l_part[r] += pr;
+        const __nv_bfloat16 hb = __float2bfloat16_rn(pr);
+        *reinterpret_cast<__nv_bfloat16*>(pb + r * 128 + ((chunk ^ (r & 7)) << 4)) = hb;
+      }
+      if (kt == kt0 || kt == kt1) {
+        // edge stage: zero the V rows of keys outside the unit (stale or
+        // unwritten slots), once their tile has landed, so P = 0 never meets NaN
+        const int st = g % NST;
+        if (!waitw(c.bar(Y_V_FULL + st), (g / NST) & 1, c.wc)) { ok = false; break; }
+        if (!in_unit) {
+          uint8_t* vrow = c.smem + OFF_V + st * KV_TILE + t * 128;
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              *reinterpret_cast<uint4*>(vrow + cc * kAtomKV + q * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async_smem();  // P (and zeroed V rows) are read by the tensor core
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(c.bar(Y_P_FULL));
+    }
+    if (!ok) break;
+
+    // epilogue: O^T (thread t = dimension t) and the rows' sums over all keys
+    if (!waitw(c.bar(Y_O_FULL), ui & 1, c.wc)) break;
+    tc_fence_after();
+    uint32_t ov[MN];
+    tmem_ld16(c.tmem + lane_off + TM_O, ov);
+    tmem_wait_ld();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.bar(Y_O_EMPTY));
+    float* ls = reinterpret_cast<float*>(c.smem + OFF_LS) + (ui & 1) * 4 * MN;
+#pragma unroll
+    for (int r = 0; r < MN; ++r) {
+      float v = l_part[r];
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) ls[wq * MN + r] = v;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.bar(Y_LS + (ui & 1)));
+    if (!waitw(c.bar(Y_LS + (ui & 1)), (ui >> 1) & 1, c.wc)) break;
+    const bool single = U.pair_units == 1;
+#pragma unroll
+    for (int r = 0; r < MN; ++r) {
+      if (r >= p.R_rows) break;
+      const float L = ((ls[r] + ls[MN + r]) + ls[2 * MN + r]) + ls[3 * MN + r];
+      const float o = __uint_as_float(ov[r]);
+      if (single) {
+        const int tk = r / p.Gm, gm = r - tk * p.Gm;
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) +
+                              (static_cast<int64_t>(U.req * p.T + tk) * p.hq + U.head * p.Gm + gm) * 128;
+        orow[t] = __float2bfloat16_rn(o / L);
+        if (p.lse != nullptr && t == 0)
+          p.lse[static_cast<int64_t>(U.head * p.Gm + gm) * p.n_rows + U.req * p.T + tk] =
+              (m_ref[r] + log2f(L)) * 0.6931471805599453f;
+      } else {
+        p.part_acc[(static_cast<int64_t>(u) * p.R_rows + r) * 128 + t] = o;
+        if (t == 0) {
+          p.part_ml[(static_cast<int64_t>(u) * p.R_rows + r) * 2] = m_ref[r];
+          p.part_ml[(static_cast<int64_t>(u) * p.R_rows + r) * 2 + 1] = L;
+        }
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreadsMD, 1)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                      const __grid_constant__ CUtensorMap tmv, const DecodeMmaParams p,
+                      const __grid_constant__ PlanBlob blob) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  MdCtx c;
+  c.smem = smem;
+  c.sbase = smem_addr(smem);
+  const DecodeUnit* units = plan_ptr(p.units, blob, p.plan_inline);
+  const int32_t* cta_begin = plan_ptr(p.cta_begin, blob, p.plan_inline);
+  if (threadIdx.x == 0) {
+    mbar_init(c.bar(Y_Q_FULL), 1);
+    mbar_init(c.bar(Y_Q_EMPTY), 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(c.bar(Y_K_FULL + s), 1);
+      mbar_init(c.bar(Y_V_FULL + s), 1);
+      mbar_init(c.bar(Y_KV_EMPTY + s), 1);
+    }
+    mbar_init(c.bar(Y_S_FULL), 1);
+    mbar_init(c.bar(Y_P_FULL), 4);  // one arrival per softmax warp
+    mbar_init(c.bar(Y_O_FULL), 1);
+    mbar_init(c.bar(Y_O_EMPTY), 4);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(c.bar(Y_MX + x), 4);
+      mbar_init(c.bar(Y_LS + x), 4);
+    }
+    mbar_init(c.bar(Y_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tmq);
+    prefetch_tmap(&tmk);
+    prefetch_tmap(&tmv);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  c.tmem = *tmem_slot;
+  c.wc.abort = abort_flag;
+  c.wc.status = p.status;
+  c.wc.limit_ns = p.timeout_ns;
+  if (warp == 0) {
+    md_producer(&tmq, &tmk, &tmv, p, units, cta_begin, c, lane);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) md_mma(p, units, cta_begin, c);
+    __syncwarp();
+  } else {
+    md_softmax(p, units, cta_begin, c, warp, lane);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(c.tmem, TM_COLS);
+  }
+}
+
+// Merge the partials of split pairs: block (pair, row), thread = dimension.
+__global__ void __launch_bounds__(128)
+    decode_combine_kernel(const DecodeMmaParams p, const __grid_constant__ PlanBlob blob) {
+  const DecodeCombine* cmb = plan_ptr(p.combine, blob, p.plan_inline);
+  const DecodeCombine C = cmb[blockIdx.x / p.R_rows];
+  const int r = blockIdx.x % p.R_rows;
+  const int d = threadIdx.x;
+  float M = -INFINITY;
+  for (int x = 0; x < C.units; ++x)
+    M = fmaxf(M, __ldg(p.part_ml + (static_cast<int64_t>(C.unit0 + x) * p.R_rows + r) * 2));
+  const float Mr = (M == -INFINITY) ? 0.f : M;  // a slice that sees no key has weight 0
+  float Ls = 0.f, o = 0.f;
+  for (int x = 0; x < C.units; ++x) {
+    const int64_t ur = static_cast<int64_t>(C.unit0 + x) * p.R_rows + r;
+    const float wgt = ex2(__ldg(p.part_ml + ur * 2) - Mr);
+    Ls = fmaf(wgt, __ldg(p.part_ml + ur * 2 + 1), Ls);
+    o = fmaf(wgt, __ldg(p.part_acc + ur * 128 + d), o);
+  }
+  const int tk = r / p.Gm, gm = r - tk * p.Gm;
+  static_cast<__nv_bfloat16*>(p.o)[(static_cast<int64_t>(C.req * p.T + tk) * p.hq + C.head * p.Gm + gm) * 128 + d] =
+      __float2bfloat16_rn(o / Ls);
+  if (p.lse != nullptr && d == 0)
+    p.lse[static_cast<int64_t>(C.head * p.Gm + gm) * p.n_rows + C.req * p.T + tk] =
+        (M + log2f(Ls)) * 0.6931471805599453f;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_mma(const DecodeMmaParams& p, const PlanBlob* blob, const CUtensorMap& tq,
+                              const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                              cudaStream_t s) {
+  static const PlanBlob empty_blob{};
+  static bool attr_set[kMaxDevices] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= kMaxDevices || !attr_set[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MD_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev < kMaxDevices) attr_set[dev] = true;
+  }
+  const PlanBlob& b = blob ? *blob : empty_blob;
+  decode_mma_kernel<<<grid, kThreadsMD, MD_BYTES, s>>>(tq, tk, tv, p, b);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || p.n_combine == 0) return e;
+  decode_combine_kernel<<<p.n_combine * p.R_rows, 128, 0, s>>>(p, b);
+  return cudaGetLastError();
+}
+
+}  // namespace skv

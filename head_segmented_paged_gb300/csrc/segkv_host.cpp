@@ -712,6 +712,80 @@ int segkv_workspace_size(segkv_t h, int kind, int64_t n_tokens, int n_seqs, size
   return SEGKV_OK;
 }
 
+// Tensor-core decode (8 or 16 query rows per KV head, D = 128) of a plan made
+// by decode_core, plus the merge of split pairs.
+static int decode_mma_launch(segkv* h, int layer, const void* q, int T, int n, void* o, float* lse,
+                             const std::vector<DecodeUnit>& units,
+                             const std::vector<int32_t>& cta_begin,
+                             const std::vector<DecodeCombine>& comb, void* workspace,
+                             size_t acc_bytes, int grid, cudaStream_t s) {
+  Pack pk;
+  const size_t o_units = pk.add(units.data(), units.size());
+  const size_t o_cta = pk.add(cta_begin.data(), cta_begin.size());
+  const size_t o_comb = pk.add(comb.data(), comb.size());
+  const bool inl = pk.buf.size() <= sizeof(PlanBlob);
+  size_t off_ring = 0;
+  uintptr_t d = 0;  // device address of the plan; 0 (offsets alone) when it is inline
+  cudaError_t e;
+  if (inl) {
+    std::memcpy(h->blob.data, pk.buf.data(), pk.buf.size());
+  } else {
+    e = h->ring.reserve(pk.buf.size(), &off_ring);
+    if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
+    std::memcpy(h->ring.host + off_ring, pk.buf.data(), pk.buf.size());
+    e = h->ring.upload(off_ring, pk.buf.size(), s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "plan upload (decode)");
+    d = reinterpret_cast<uintptr_t>(h->ring.dev + off_ring);
+  }
+  h->upload_bytes += static_cast<int64_t>(pk.buf.size());
+  const int rows = T * h->G;
+  CUtensorMap tq;  // the T tokens x Gm heads of one (sequence, KV head): box {64, Gm, T}
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(h->D), static_cast<cuuint64_t>(h->Hq),
+                          static_cast<cuuint64_t>(n) * T};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(h->D) * 2,
+                             static_cast<cuuint64_t>(h->Hq) * h->D * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(h->G), static_cast<cuuint32_t>(T)};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (encode_fn()(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return fail(h, SEGKV_ERR_CUDA, "tensor map encode failed for q");
+  }
+  DecodeMmaParams p{};
+  p.units = reinterpret_cast<const DecodeUnit*>(d + o_units);
+  p.cta_begin = reinterpret_cast<const int32_t*>(d + o_cta);
+  p.combine = reinterpret_cast<const DecodeCombine*>(d + o_comb);
+  p.plan_inline = inl ? 1 : 0;
+  p.n_combine = static_cast<int>(comb.size());
+  p.o = o;
+  p.lse = lse;
+  p.table = h->d_table;
+  p.part_acc = static_cast<float*>(workspace);
+  p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + acc_bytes);
+  p.n_rows = n * T;
+  p.R = h->R;
+  p.hq = h->Hq;
+  p.hkv = h->Hkv;
+  p.page_size = h->P;
+  p.R_rows = rows;
+  p.T = T;
+  p.Gm = h->G;
+  p.window = h->win[layer];
+  p.oob_row = static_cast<int>(h->num_pages * h->P);
+  p.scale_log2 = h->scale * 1.4426950408889634f;
+  p.status = h->d_status;
+  p.timeout_ns = kTimeoutNs;
+  e = launch_decode_mma(p, inl ? &h->blob : nullptr, tq, h->tm_k, h->tm_v, grid, s);
+  if (e != cudaSuccess) return cuda_fail(h, e, "decode kernel launch");
+  if (!inl) {
+    e = h->ring.commit(off_ring, pk.buf.size(), s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "event record");
+  }
+  return SEGKV_OK;
+}
+
 // Split-KV decode of the T newest tokens of n sequences: T * G query rows per
 // KV head, each with its own causal (and window) limit.
 static int decode_core(segkv* h, int layer, const void* q, int T, const int32_t* seq_lens,
@@ -747,9 +821,13 @@ static int decode_core(segkv* h, int layer, const void* q, int T, const int32_t*
   // 128 keys in. The smallest per-CTA budget whose greedy cut fits the grid is
   // found by bisection.
   constexpr int64_t kDecodeUnitCost = 128;
-  const int64_t sk = decode_stage_keys(rows);
-  const int64_t ctas = h->num_sms > 0 ? int64_t(h->num_sms) * decode_ctas_per_sm(h->D, rows)
-                                      : decode_max_grid(h);
+  // 8 or 16 query rows of 128 dims run on the tensor-core decode kernel
+  // (128-key stages, one CTA per SM); the rest on the CUDA-core kernel
+  const bool mma = h->D == 128 && (rows == 8 || rows == 16);
+  const int64_t sk = mma ? 128 : decode_stage_keys(rows);
+  const int64_t ctas = h->num_sms <= 0 ? decode_max_grid(h)
+                       : mma ? int64_t(h->num_sms)
+                             : int64_t(h->num_sms) * decode_ctas_per_sm(h->D, rows);
   const int max_grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(
       std::min<int64_t>(ctas, decode_max_grid(h)), (total + sk - 1) / sk)));
   std::vector<DecodeUnit> units;
@@ -822,6 +900,13 @@ static int decode_core(segkv* h, int layer, const void* q, int T, const int32_t*
     return fail(h, SEGKV_ERR_INVALID_ARG, "workspace needs %zu bytes (256-aligned), got %zu", need,
                 workspace_bytes);
 
+  if (mma) {
+    std::vector<DecodeCombine> comb;  // pairs split over several units
+    for (size_t r = 0; r < ranges.size(); ++r)
+      if (pair_units[r] > 1) comb.push_back({pair_unit0[r], pair_units[r], ranges[r].req, ranges[r].head});
+    return decode_mma_launch(h, layer, q, T, n, o, lse, units, cta_begin, comb, workspace, acc_bytes,
+                             grid, s);
+  }
   Pack pk;
   const size_t o_units = pk.add(units.data(), units.size());
   const size_t o_cta = pk.add(cta_begin.data(), cta_begin.size());

@@ -240,6 +240,35 @@ int prefill_smem_bytes(int head_dim);
 int prefill_unit_tokens(int G);  // query tokens per prefill work unit
 cudaError_t launch_decode(const DecodeParams& p, const PlanBlob* blob, int head_dim, int grid,
                           cudaStream_t s);
+
+// Tensor-core decode for 8 or 16 query rows per KV head (D = 128).
+struct DecodeCombine {  // one (sequence, KV head) pair split over several units
+  int32_t unit0, units;
+  int32_t req, head;
+};
+struct DecodeMmaParams {
+  const DecodeUnit* units;     // grouped by CTA (offsets into the PlanBlob when plan_inline)
+  const int32_t* cta_begin;    // [grid + 1]
+  const DecodeCombine* combine;
+  int plan_inline;
+  int n_combine;
+  void* o;                     // bf16 [n * T, Hq, D]
+  float* lse;                  // fp32 [Hq, n_rows] or null
+  const int32_t* table;
+  float* part_acc;             // [units, R, D]
+  float* part_ml;              // [units, R, 2]
+  int n_rows;
+  int R, hq, hkv, page_size;
+  int R_rows;                  // query rows per KV head: T * Gm (8 or 16)
+  int T, Gm, window;
+  int oob_row;                 // a K/V row coordinate past the end of the pools
+  float scale_log2;
+  int* status;
+  unsigned long long timeout_ns;
+};
+cudaError_t launch_decode_mma(const DecodeMmaParams& p, const PlanBlob* blob, const CUtensorMap& tq,
+                              const CUtensorMap& tk, const CUtensorMap& tv, int grid,
+                              cudaStream_t s);
 int decode_stage_keys(int G);  // keys per decode pipeline stage
 int decode_ctas_per_sm(int head_dim, int G);  // resident decode CTAs per SM
 

@@ -11,10 +11,11 @@ from harness import Cache, check_close
 pytestmark = pytest.mark.gpu
 
 
-# T * G in {1, 2, 4, 8, 16} runs on the split-KV decode kernel, the rest on
-# the prefill kernel
+# T * G in {1, 2, 4, 8, 16} runs on a decode kernel (8 or 16 rows of 128 dims
+# on the tensor-core one, fewer on the CUDA-core one), the rest on the prefill
+# kernel
 @pytest.mark.parametrize("T,G", [(1, 4), (4, 4), (2, 8), (4, 2), (16, 1), (2, 1),
-                                 (3, 4), (7, 8), (16, 2)])
+                                 (1, 8), (1, 16), (8, 1), (3, 4), (7, 8), (16, 2)])
 def test_multi_query_decode_matches_oracle(T, G):
     hkv, d, P, W = 4, 128, 64, 200
     hc = [[I.GLOBAL, I.LOCAL, I.LOCAL, I.LOCAL]]
