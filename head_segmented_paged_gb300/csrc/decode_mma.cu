@@ -26,9 +26,11 @@
 //   warp 1      TMEM owner (64 columns: S^T at 0, O^T at 32) and MMA issuer;
 //   warps 2..5  softmax and epilogue: thread t holds key t of a stage and
 //               dimension t of O^T.
-// Ordering: S of stage i is issued after P V of stage i-1 and a thread's
-// tcgen05 operations complete in order, so when S(i) is complete O is stable
-// (for a rescale) and P's buffer is free.
+// Ordering: S and P are double-buffered. S of stage i+1 is issued before P V
+// of stage i, so the tensor core forms it while the softmax warps work on
+// stage i. A thread's tcgen05 operations complete in order: when S(i) is
+// complete, P V(i-2) is too, so P buffer i % 2 is free; a rescale of O at
+// stage i first waits for P V(i-1) on its own barrier.
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -49,8 +51,8 @@ constexpr uint32_t kAtomR = MN * 128;      // 64 columns x 16 rows: 2 KB
 constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_V = NST * KV_TILE;
 constexpr uint32_t OFF_Q = 2 * NST * KV_TILE;          // Q: 2 atoms (dims 0..63, 64..127)
-constexpr uint32_t OFF_P = OFF_Q + 2 * kAtomR;         // P^T: 2 atoms (keys 0..63, 64..127)
-constexpr uint32_t OFF_XCH = OFF_P + 2 * kAtomR;       // int [2][4][16]: per-warp row maxima
+constexpr uint32_t OFF_P = OFF_Q + 2 * kAtomR;         // P^T [2 buffers]: 2 atoms (keys 0..63, 64..127)
+constexpr uint32_t OFF_XCH = OFF_P + 4 * kAtomR;       // int [2][4][16]: per-warp row maxima
 constexpr uint32_t OFF_LS = OFF_XCH + 2 * 4 * MN * 4;  // float [2][4][16]: per-warp row sums
 constexpr uint32_t OFF_BAR = OFF_LS + 2 * 4 * MN * 4;
 enum {
@@ -59,18 +61,19 @@ enum {
   Y_K_FULL = 2,                 // +stage
   Y_V_FULL = 2 + NST,           // +stage
   Y_KV_EMPTY = 2 + 2 * NST,     // +stage
-  Y_S_FULL = 2 + 3 * NST,
-  Y_P_FULL = Y_S_FULL + 1,
-  Y_O_FULL = Y_S_FULL + 2,
-  Y_O_EMPTY = Y_S_FULL + 3,
-  Y_MX = Y_S_FULL + 4,          // +stage parity
-  Y_LS = Y_S_FULL + 6,          // +unit parity
-  Y_DRAIN = Y_S_FULL + 8,
-  Y_NUM = Y_S_FULL + 9
+  Y_S_FULL = 2 + 3 * NST,       // +stage parity (S buffer)
+  Y_P_FULL = Y_S_FULL + 2,      // +stage parity (P buffer)
+  Y_PV_DONE = Y_S_FULL + 4,
+  Y_O_FULL = Y_S_FULL + 5,
+  Y_O_EMPTY = Y_S_FULL + 6,
+  Y_MX = Y_S_FULL + 7,          // +stage parity
+  Y_LS = Y_S_FULL + 9,          // +unit parity
+  Y_DRAIN = Y_S_FULL + 11,
+  Y_NUM = Y_S_FULL + 12
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + Y_NUM * 8;
 constexpr uint32_t MD_BYTES = OFF_MISC + 16 + 1024;  // + slack to align to 1 KB
-constexpr uint32_t TM_S = 0, TM_O = 32, TM_COLS = 64;
+constexpr uint32_t TM_S = 0, TM_O = 32, TM_COLS = 64;  // S^T buffers at 0 and 16
 constexpr uint64_t kDrainNsMD = 200ull * 1000 * 1000;
 static_assert(MD_BYTES <= 227 * 1024, "decode_mma shared memory");
 
@@ -154,38 +157,50 @@ __device__ void md_mma(const DecodeMmaParams& p, const DecodeUnit* units, const 
                        const MdCtx& c) {
   constexpr uint32_t IDESC_S = idesc_bf16_ab(KT, MN, 0, 0);   // K (keys x D) . Q^T
   constexpr uint32_t IDESC_PV = idesc_bf16_ab(128, MN, 1, 0); // V^T (D x keys, MN-major) . P^T
+  // S(g) = K(g) Q^T into S buffer g % 2
+  auto issue_s = [&](int g) -> bool {
+    const int st = g % NST;
+    if (!wait1(c.bar(Y_K_FULL + st), (g / NST) & 1, c.wc)) return false;
+    tc_fence_after();
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t a = c.sbase + OFF_K + st * KV_TILE + (kk >> 2) * kAtomKV + (kk & 3) * 32;
+      const uint32_t b = c.sbase + OFF_Q + (kk >> 2) * kAtomR + (kk & 3) * 32;
+      mma_bf16(c.tmem + TM_S + (g & 1) * MN, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, 16, 1024),
+               IDESC_S, kk > 0 ? 1u : 0u);
+    }
+    mma_commit(c.bar(Y_S_FULL + (g & 1)));
+    return true;
+  };
   bool ok = true;
   int g = 0, ui = 0;
   for (int u = cta_begin[blockIdx.x]; ok && u < cta_begin[blockIdx.x + 1]; ++u, ++ui) {
     const DecodeUnit U = units[u];
     const int kt0 = U.k0 / KT, kt1 = (U.k1 - 1) / KT;
     if (!wait1(c.bar(Y_Q_FULL), ui & 1, c.wc)) { ok = false; break; }
+    // S of the next stage is issued before P V of this one, so the tensor core
+    // works on it while the softmax warps handle this stage
+    if (!issue_s(g)) { ok = false; break; }
+    if (kt0 == kt1) mma_commit(c.bar(Y_Q_EMPTY));
     for (int kt = kt0; kt <= kt1; ++kt, ++g) {
       const int st = g % NST;
-      const uint32_t ph = (g / NST) & 1;
-      if (!wait1(c.bar(Y_K_FULL + st), ph, c.wc)) { ok = false; break; }
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t a = c.sbase + OFF_K + st * KV_TILE + (kk >> 2) * kAtomKV + (kk & 3) * 32;
-        const uint32_t b = c.sbase + OFF_Q + (kk >> 2) * kAtomR + (kk & 3) * 32;
-        mma_bf16(c.tmem + TM_S, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, 16, 1024), IDESC_S,
-                 kk > 0 ? 1u : 0u);
+      if (kt < kt1) {
+        if (!issue_s(g + 1)) { ok = false; break; }
+        if (kt + 1 == kt1) mma_commit(c.bar(Y_Q_EMPTY));
       }
-      mma_commit(c.bar(Y_S_FULL));
-      if (kt == kt1) mma_commit(c.bar(Y_Q_EMPTY));
-      if (!wait1(c.bar(Y_P_FULL), g & 1, c.wc)) { ok = false; break; }
-      if (!wait1(c.bar(Y_V_FULL + st), ph, c.wc)) { ok = false; break; }
+      if (!wait1(c.bar(Y_P_FULL + (g & 1)), (g >> 1) & 1, c.wc)) { ok = false; break; }
+      if (!wait1(c.bar(Y_V_FULL + st), (g / NST) & 1, c.wc)) { ok = false; break; }
       if (kt == kt0 && !wait1(c.bar(Y_O_EMPTY), (ui & 1) ^ 1, c.wc)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < KT / 16; ++kk) {
         const uint32_t a = c.sbase + OFF_V + st * KV_TILE + kk * 2048;
-        const uint32_t b = c.sbase + OFF_P + (kk >> 2) * kAtomR + (kk & 3) * 32;
+        const uint32_t b = c.sbase + OFF_P + (g & 1) * 2 * kAtomR + (kk >> 2) * kAtomR + (kk & 3) * 32;
         mma_bf16(c.tmem + TM_O, sdesc_sw128(a, kAtomKV, 1024), sdesc_sw128(b, 16, 1024), IDESC_PV,
                  (kt > kt0 || kk > 0) ? 1u : 0u);
       }
       mma_commit(c.bar(Y_KV_EMPTY + st));
+      mma_commit(c.bar(Y_PV_DONE));
       if (kt == kt1) mma_commit(c.bar(Y_O_FULL));
     }
   }
@@ -214,10 +229,10 @@ __device__ void md_softmax(const DecodeMmaParams& p, const DecodeUnit* units,
     }
     bool ok = true;
     for (int kt = kt0; kt <= kt1; ++kt, ++g) {
-      if (!waitw(c.bar(Y_S_FULL), g & 1, c.wc)) { ok = false; break; }
+      if (!waitw(c.bar(Y_S_FULL + (g & 1)), (g >> 1) & 1, c.wc)) { ok = false; break; }
       tc_fence_after();
       uint32_t sv[MN];
-      tmem_ld16(c.tmem + lane_off + TM_S, sv);
+      tmem_ld16(c.tmem + lane_off + TM_S + (g & 1) * MN, sv);
       tmem_wait_ld();
       const int j = kt * KT + t;  // this thread's key
       const bool in_unit = j >= U.k0 && j < U.k1;
@@ -259,6 +274,9 @@ __device__ void md_softmax(const DecodeMmaParams& p, const DecodeUnit* units,
 #pragma unroll
         for (int r = 0; r < MN; ++r) l_part[r] *= alpha[r];
         if (kt > kt0) {  // O^T holds earlier stages: scale its columns (this thread's dimension)
+          // S(g) may complete before P V(g-1): wait for that one first
+          if (!waitw(c.bar(Y_PV_DONE), (g - 1) & 1, c.wc)) { ok = false; break; }
+          tc_fence_after();
           uint32_t ov[MN];
           tmem_ld16(c.tmem + lane_off + TM_O, ov);
           tmem_wait_ld();
@@ -269,7 +287,8 @@ __device__ void md_softmax(const DecodeMmaParams& p, const DecodeUnit* units,
         }
       }
       // P^T[r][t] in bf16, 128-byte swizzled: atom t / 64, 16-byte chunk ((t % 64) / 8) ^ (r % 8)
-      uint8_t* pb = c.smem + OFF_P + (t >> 6) * kAtomR + (t & 7) * 2;
+      // (S(g) was issued after P V(g-2), so buffer g % 2 is free once S(g) is complete)
+      uint8_t* pb = c.smem + OFF_P + (g & 1) * 2 * kAtomR + (t >> 6) * kAtomR + (t & 7) * 2;
       const int chunk = (t & 63) >> 3;
 #pragma unroll
       for (int r = 0; r < MN; ++r) {
@@ -296,7 +315,7 @@ __device__ void md_softmax(const DecodeMmaParams& p, const DecodeUnit* units,
       fence_proxy_async_smem();  // P (and zeroed V rows) are read by the tensor core
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(Y_P_FULL));
+      if (lane == 0) mbar_arrive(c.bar(Y_P_FULL + (g & 1)));
     }
     if (!ok) break;
 
@@ -368,8 +387,11 @@ __global__ void __launch_bounds__(kThreadsMD, 1)
       mbar_init(c.bar(Y_V_FULL + s), 1);
       mbar_init(c.bar(Y_KV_EMPTY + s), 1);
     }
-    mbar_init(c.bar(Y_S_FULL), 1);
-    mbar_init(c.bar(Y_P_FULL), 4);  // one arrival per softmax warp
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(c.bar(Y_S_FULL + x), 1);
+      mbar_init(c.bar(Y_P_FULL + x), 4);  // one arrival per softmax warp
+    }
+    mbar_init(c.bar(Y_PV_DONE), 1);
     mbar_init(c.bar(Y_O_FULL), 1);
     mbar_init(c.bar(Y_O_EMPTY), 4);
     for (int x = 0; x < 2; ++x) {
