@@ -20,17 +20,19 @@
 // partials and decode_combine_kernel merges each split pair afterwards, one
 // CTA per (pair, row), with the running-maximum rule.
 //
-// Warp roles (192 threads, one CTA per SM):
+// Warp roles (320 threads, one CTA per SM):
 //   warp 0      producer: the unit's query rows (TMA), then K and V tiles of
 //               128 keys, page by page through the block table (3 stages);
-//   warp 1      TMEM owner (64 columns: S^T at 0, O^T at 32) and MMA issuer;
-//   warps 2..5  softmax and epilogue: thread t holds key t of a stage and
-//               dimension t of O^T.
-// Ordering: S and P are double-buffered. S of stage i+1 is issued before P V
-// of stage i, so the tensor core forms it while the softmax warps work on
-// stage i. A thread's tcgen05 operations complete in order: when S(i) is
-// complete, P V(i-2) is too, so P buffer i % 2 is free; a rescale of O at
-// stage i first waits for P V(i-1) on its own barrier.
+//   warp 1      TMEM owner (64 columns: S^T and O^T per group) and MMA issuer;
+//   warps 2..5, 6..9  two softmax groups taking alternate stages, each with
+//               its own running maxima, row sums and O^T accumulator; thread
+//               t holds key t of a stage and dimension t of O^T. At the end
+//               of a unit group 0 combines both groups' states and writes.
+// Ordering: S, P and O are per group (stage parity). S of stage i+1 is
+// issued before P V of stage i, so the tensor core forms it while a group
+// works on stage i. A thread's tcgen05 operations complete in order: when
+// S(i) is complete, P V(i-2) is too, so the group's P buffer is free and its
+// O^T is stable for a rescale.
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -44,7 +46,7 @@ namespace {
 constexpr int KT = 128;  // keys per stage
 constexpr int NST = 3;   // K/V stages
 constexpr int MN = 16;   // MMA N: query rows (8 or 16 used)
-constexpr int kThreadsMD = 192;
+constexpr int kThreadsMD = 320;
 constexpr uint32_t kAtomKV = KT * 128;     // 64 dims x 128 keys: 16 KB
 constexpr uint32_t KV_TILE = 2 * kAtomKV;  // D = 128
 constexpr uint32_t kAtomR = MN * 128;      // 64 columns x 16 rows: 2 KB
@@ -52,28 +54,29 @@ constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_V = NST * KV_TILE;
 constexpr uint32_t OFF_Q = 2 * NST * KV_TILE;          // Q: 2 atoms (dims 0..63, 64..127)
 constexpr uint32_t OFF_P = OFF_Q + 2 * kAtomR;         // P^T [2 buffers]: 2 atoms (keys 0..63, 64..127)
-constexpr uint32_t OFF_XCH = OFF_P + 4 * kAtomR;       // int [2][4][16]: per-warp row maxima
-constexpr uint32_t OFF_LS = OFF_XCH + 2 * 4 * MN * 4;  // float [2][4][16]: per-warp row sums
-constexpr uint32_t OFF_BAR = OFF_LS + 2 * 4 * MN * 4;
+constexpr uint32_t OFF_XCH = OFF_P + 4 * kAtomR;          // int [group][2][4][16]: per-warp row maxima
+constexpr uint32_t OFF_LS = OFF_XCH + 2 * 2 * 4 * MN * 4;  // float [group][2][4][16]: per-warp row sums
+constexpr uint32_t OFF_GX = OFF_LS + 2 * 2 * 4 * MN * 4;   // float [2][2][16]: group 1's row max and sum
+constexpr uint32_t OFF_BAR = OFF_GX + 2 * 2 * MN * 4;
 enum {
   Y_Q_FULL = 0,
   Y_Q_EMPTY = 1,
   Y_K_FULL = 2,                 // +stage
   Y_V_FULL = 2 + NST,           // +stage
   Y_KV_EMPTY = 2 + 2 * NST,     // +stage
-  Y_S_FULL = 2 + 3 * NST,       // +stage parity (S buffer)
-  Y_P_FULL = Y_S_FULL + 2,      // +stage parity (P buffer)
-  Y_PV_DONE = Y_S_FULL + 4,
-  Y_O_FULL = Y_S_FULL + 5,
-  Y_O_EMPTY = Y_S_FULL + 6,
-  Y_MX = Y_S_FULL + 7,          // +stage parity
-  Y_LS = Y_S_FULL + 9,          // +unit parity
-  Y_DRAIN = Y_S_FULL + 11,
-  Y_NUM = Y_S_FULL + 12
+  Y_S_FULL = 2 + 3 * NST,       // +group (= stage parity): S buffer
+  Y_P_FULL = Y_S_FULL + 2,      // +group: P buffer
+  Y_O_FULL = Y_S_FULL + 4,
+  Y_O_EMPTY = Y_S_FULL + 5,
+  Y_MX = Y_S_FULL + 6,          // +group * 2 + the group's stage parity
+  Y_LS = Y_S_FULL + 10,         // +group * 2 + unit parity
+  Y_GX = Y_S_FULL + 14,         // +unit parity
+  Y_DRAIN = Y_S_FULL + 16,
+  Y_NUM = Y_S_FULL + 17
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + Y_NUM * 8;
 constexpr uint32_t MD_BYTES = OFF_MISC + 16 + 1024;  // + slack to align to 1 KB
-constexpr uint32_t TM_S = 0, TM_O = 32, TM_COLS = 64;  // S^T buffers at 0 and 16
+constexpr uint32_t TM_S = 0, TM_O = 32, TM_COLS = 64;  // S^T at 0 and 16, O^T at 32 and 48 (per group)
 constexpr uint64_t kDrainNsMD = 200ull * 1000 * 1000;
 static_assert(MD_BYTES <= 227 * 1024, "decode_mma shared memory");
 
@@ -182,6 +185,7 @@ __device__ void md_mma(const DecodeMmaParams& p, const DecodeUnit* units, const 
     // works on it while the softmax warps handle this stage
     if (!issue_s(g)) { ok = false; break; }
     if (kt0 == kt1) mma_commit(c.bar(Y_Q_EMPTY));
+    const int g0 = g;
     for (int kt = kt0; kt <= kt1; ++kt, ++g) {
       const int st = g % NST;
       if (kt < kt1) {
@@ -196,11 +200,11 @@ __device__ void md_mma(const DecodeMmaParams& p, const DecodeUnit* units, const 
       for (int kk = 0; kk < KT / 16; ++kk) {
         const uint32_t a = c.sbase + OFF_V + st * KV_TILE + kk * 2048;
         const uint32_t b = c.sbase + OFF_P + (g & 1) * 2 * kAtomR + (kk >> 2) * kAtomR + (kk & 3) * 32;
-        mma_bf16(c.tmem + TM_O, sdesc_sw128(a, kAtomKV, 1024), sdesc_sw128(b, 16, 1024), IDESC_PV,
-                 (kt > kt0 || kk > 0) ? 1u : 0u);
+        // O of group g % 2; that group's first stage of the unit starts it afresh
+        mma_bf16(c.tmem + TM_O + (g & 1) * MN, sdesc_sw128(a, kAtomKV, 1024), sdesc_sw128(b, 16, 1024),
+                 IDESC_PV, (g - g0 >= 2 || kk > 0) ? 1u : 0u);
       }
       mma_commit(c.bar(Y_KV_EMPTY + st));
-      mma_commit(c.bar(Y_PV_DONE));
       if (kt == kt1) mma_commit(c.bar(Y_O_FULL));
     }
   }
@@ -211,28 +215,30 @@ __device__ void md_mma(const DecodeMmaParams& p, const DecodeUnit* units, const 
 }
 
 __device__ void md_softmax(const DecodeMmaParams& p, const DecodeUnit* units,
-                           const int32_t* cta_begin, const MdCtx& c, int warp, int lane) {
+                           const int32_t* cta_begin, const MdCtx& c, int grp, int warp, int lane) {
   const int wq = warp & 3;  // the TMEM lane quarter this warp may access
   const int t = wq * 32 + lane;
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
   const float sc = p.scale_log2;
   const bool multi = p.T > 1;
-  int g = 0, ui = 0;
+  int g = 0, ui = 0, js = 0;  // js: stages this group has handled (its exchange buffer index)
   for (int u = cta_begin[blockIdx.x]; u < cta_begin[blockIdx.x + 1]; ++u, ++ui) {
     const DecodeUnit U = units[u];
     const int kt0 = U.k0 / KT, kt1 = (U.k1 - 1) / KT;
+    const int g0 = g;
     float m_ref[MN], l_part[MN];
 #pragma unroll
     for (int r = 0; r < MN; ++r) {
       m_ref[r] = -INFINITY;
       l_part[r] = 0.f;
     }
-    bool ok = true;
+    bool ok = true, had = false;  // had: this group handled a stage of the unit
     for (int kt = kt0; kt <= kt1; ++kt, ++g) {
-      if (!waitw(c.bar(Y_S_FULL + (g & 1)), (g >> 1) & 1, c.wc)) { ok = false; break; }
+      if ((g & 1) != grp) continue;  // stages alternate between the two groups
+      if (!waitw(c.bar(Y_S_FULL + grp), (g >> 1) & 1, c.wc)) { ok = false; break; }
       tc_fence_after();
       uint32_t sv[MN];
-      tmem_ld16(c.tmem + lane_off + TM_S + (g & 1) * MN, sv);
+      tmem_ld16(c.tmem + lane_off + TM_S + grp * MN, sv);
       tmem_wait_ld();
       const int j = kt * KT + t;  // this thread's key
       const bool in_unit = j >= U.k0 && j < U.k1;
@@ -246,16 +252,16 @@ __device__ void md_softmax(const DecodeMmaParams& p, const DecodeUnit* units,
         }
         s[r] = vis ? __uint_as_float(sv[r]) * sc : -INFINITY;
       }
-      // each row's maximum over the stage's 128 keys
-      int* xch = reinterpret_cast<int*>(c.smem + OFF_XCH) + (g & 1) * 4 * MN;
+      // each row's maximum over the stage's 128 keys, shared by the group's warps
+      int* xch = reinterpret_cast<int*>(c.smem + OFF_XCH) + (grp * 2 + (js & 1)) * 4 * MN;
 #pragma unroll
       for (int r = 0; r < MN; ++r) {
         const int wm = warp_max_s32(f32_ordered(s[r]));
         if (lane == 0) xch[wq * MN + r] = wm;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(Y_MX + (g & 1)));
-      if (!waitw(c.bar(Y_MX + (g & 1)), (g >> 1) & 1, c.wc)) { ok = false; break; }
+      if (lane == 0) mbar_arrive(c.bar(Y_MX + grp * 2 + (js & 1)));
+      if (!waitw(c.bar(Y_MX + grp * 2 + (js & 1)), (js >> 1) & 1, c.wc)) { ok = false; break; }
       bool resc = false;
       float alpha[MN];
 #pragma unroll
@@ -264,7 +270,7 @@ __device__ void md_softmax(const DecodeMmaParams& p, const DecodeUnit* units,
 #pragma unroll
         for (int w = 1; w < 4; ++w) mst = fmaxf(mst, f32_from_ordered(xch[w * MN + r]));
         alpha[r] = 1.f;
-        if (mst > m_ref[r] + 8.0f) {  // the same decision in every thread
+        if (mst > m_ref[r] + 8.0f) {  // the same decision in every thread of the group
           alpha[r] = ex2(m_ref[r] - mst);
           m_ref[r] = mst;
           resc = true;
@@ -273,22 +279,19 @@ __device__ void md_softmax(const DecodeMmaParams& p, const DecodeUnit* units,
       if (resc) {
 #pragma unroll
         for (int r = 0; r < MN; ++r) l_part[r] *= alpha[r];
-        if (kt > kt0) {  // O^T holds earlier stages: scale its columns (this thread's dimension)
-          // S(g) may complete before P V(g-1): wait for that one first
-          if (!waitw(c.bar(Y_PV_DONE), (g - 1) & 1, c.wc)) { ok = false; break; }
-          tc_fence_after();
+        if (had) {  // this group's O^T holds earlier stages (their P V was issued before S(g)): scale it
           uint32_t ov[MN];
-          tmem_ld16(c.tmem + lane_off + TM_O, ov);
+          tmem_ld16(c.tmem + lane_off + TM_O + grp * MN, ov);
           tmem_wait_ld();
 #pragma unroll
           for (int r = 0; r < MN; ++r) ov[r] = __float_as_uint(__uint_as_float(ov[r]) * alpha[r]);
-          tmem_st16(c.tmem + lane_off + TM_O, ov);
+          tmem_st16(c.tmem + lane_off + TM_O + grp * MN, ov);
           tmem_wait_st();
         }
       }
-      // P^T[r][t] in bf16, 128-byte swizzled: atom t / 64, 16-byte chunk ((t % 64) / 8) ^ (r % 8)
-      // (S(g) was issued after P V(g-2), so buffer g % 2 is free once S(g) is complete)
-      uint8_t* pb = c.smem + OFF_P + (g & 1) * 2 * kAtomR + (t >> 6) * kAtomR + (t & 7) * 2;
+      // P^T[r][t] in bf16, 128-byte swizzled: atom t / 64, 16-byte chunk ((t % 64) / 8) ^ (r % 8).
+      // S(g) was issued after P V(g-2), so this group's P buffer is free once S(g) is complete.
+      uint8_t* pb = c.smem + OFF_P + grp * 2 * kAtomR + (t >> 6) * kAtomR + (t & 7) * 2;
       const int chunk = (t & 63) >> 3;
 #pragma unroll
       for (int r = 0; r < MN; ++r) {
@@ -315,20 +318,14 @@ __device__ void md_softmax(const DecodeMmaParams& p, const DecodeUnit* units,
       fence_proxy_async_smem();  // P (and zeroed V rows) are read by the tensor core
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(Y_P_FULL + (g & 1)));
+      if (lane == 0) mbar_arrive(c.bar(Y_P_FULL + grp));
+      had = true;
+      ++js;
     }
     if (!ok) break;
 
-    // epilogue: O^T (thread t = dimension t) and the rows' sums over all keys
-    if (!waitw(c.bar(Y_O_FULL), ui & 1, c.wc)) break;
-    tc_fence_after();
-    uint32_t ov[MN];
-    tmem_ld16(c.tmem + lane_off + TM_O, ov);
-    tmem_wait_ld();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(c.bar(Y_O_EMPTY));
-    float* ls = reinterpret_cast<float*>(c.smem + OFF_LS) + (ui & 1) * 4 * MN;
+    // the group's row sums over its keys
+    float* ls = reinterpret_cast<float*>(c.smem + OFF_LS) + (grp * 2 + (ui & 1)) * 4 * MN;
 #pragma unroll
     for (int r = 0; r < MN; ++r) {
       float v = l_part[r];
@@ -337,27 +334,60 @@ __device__ void md_softmax(const DecodeMmaParams& p, const DecodeUnit* units,
       if (lane == 0) ls[wq * MN + r] = v;
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(c.bar(Y_LS + (ui & 1)));
-    if (!waitw(c.bar(Y_LS + (ui & 1)), (ui >> 1) & 1, c.wc)) break;
+    if (lane == 0) mbar_arrive(c.bar(Y_LS + grp * 2 + (ui & 1)));
+    if (!waitw(c.bar(Y_LS + grp * 2 + (ui & 1)), (ui >> 1) & 1, c.wc)) break;
+    float L[MN];
+#pragma unroll
+    for (int r = 0; r < MN; ++r) L[r] = ((ls[r] + ls[MN + r]) + ls[2 * MN + r]) + ls[3 * MN + r];
+    float* gx = reinterpret_cast<float*>(c.smem + OFF_GX) + (ui & 1) * 2 * MN;
+    if (grp == 1) {  // hand this group's row maxima and sums to group 0
+      if (t == 0) {
+#pragma unroll
+        for (int r = 0; r < MN; ++r) {
+          gx[r] = m_ref[r];
+          gx[MN + r] = L[r];
+        }
+        mbar_arrive(c.bar(Y_GX + (ui & 1)));
+      }
+      continue;
+    }
+
+    // group 0: combine both groups' states and write (thread t = dimension t)
+    if (!waitw(c.bar(Y_GX + (ui & 1)), (ui >> 1) & 1, c.wc)) break;
+    if (!waitw(c.bar(Y_O_FULL), ui & 1, c.wc)) break;
+    tc_fence_after();
+    uint32_t o0[MN], o1[MN];
+    tmem_ld16(c.tmem + lane_off + TM_O, o0);
+    tmem_ld16(c.tmem + lane_off + TM_O + MN, o1);
+    tmem_wait_ld();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.bar(Y_O_EMPTY));
+    const int n_st = kt1 - kt0 + 1;
+    const bool had1 = n_st >= 2 || (g0 & 1) == 1;  // group 1 handled a stage of the unit
     const bool single = U.pair_units == 1;
 #pragma unroll
     for (int r = 0; r < MN; ++r) {
       if (r >= p.R_rows) break;
-      const float L = ((ls[r] + ls[MN + r]) + ls[2 * MN + r]) + ls[3 * MN + r];
-      const float o = __uint_as_float(ov[r]);
+      const float m1 = gx[r], L1 = gx[MN + r];
+      const float M = fmaxf(m_ref[r], m1);
+      const float Mr = (M == -INFINITY) ? 0.f : M;
+      const float w0 = ex2(m_ref[r] - Mr), w1 = ex2(m1 - Mr);
+      const float o = (had ? __uint_as_float(o0[r]) * w0 : 0.f) + (had1 ? __uint_as_float(o1[r]) * w1 : 0.f);
+      const float Lt = L[r] * w0 + L1 * w1;
       if (single) {
         const int tk = r / p.Gm, gm = r - tk * p.Gm;
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) +
                               (static_cast<int64_t>(U.req * p.T + tk) * p.hq + U.head * p.Gm + gm) * 128;
-        orow[t] = __float2bfloat16_rn(o / L);
+        orow[t] = __float2bfloat16_rn(o / Lt);
         if (p.lse != nullptr && t == 0)
           p.lse[static_cast<int64_t>(U.head * p.Gm + gm) * p.n_rows + U.req * p.T + tk] =
-              (m_ref[r] + log2f(L)) * 0.6931471805599453f;
+              (M + log2f(Lt)) * 0.6931471805599453f;
       } else {
         p.part_acc[(static_cast<int64_t>(u) * p.R_rows + r) * 128 + t] = o;
         if (t == 0) {
-          p.part_ml[(static_cast<int64_t>(u) * p.R_rows + r) * 2] = m_ref[r];
-          p.part_ml[(static_cast<int64_t>(u) * p.R_rows + r) * 2 + 1] = L;
+          p.part_ml[(static_cast<int64_t>(u) * p.R_rows + r) * 2] = M;
+          p.part_ml[(static_cast<int64_t>(u) * p.R_rows + r) * 2 + 1] = Lt;
         }
       }
     }
@@ -389,12 +419,12 @@ __global__ void __launch_bounds__(kThreadsMD, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(c.bar(Y_S_FULL + x), 1);
-      mbar_init(c.bar(Y_P_FULL + x), 4);  // one arrival per softmax warp
+      mbar_init(c.bar(Y_P_FULL + x), 4);  // one arrival per warp of the group
+      mbar_init(c.bar(Y_GX + x), 1);
     }
-    mbar_init(c.bar(Y_PV_DONE), 1);
     mbar_init(c.bar(Y_O_FULL), 1);
-    mbar_init(c.bar(Y_O_EMPTY), 4);
-    for (int x = 0; x < 2; ++x) {
+    mbar_init(c.bar(Y_O_EMPTY), 4);  // group 0's warps read both O^T
+    for (int x = 0; x < 4; ++x) {
       mbar_init(c.bar(Y_MX + x), 4);
       mbar_init(c.bar(Y_LS + x), 4);
     }
@@ -423,7 +453,7 @@ __global__ void __launch_bounds__(kThreadsMD, 1)
     if (lane == 0) md_mma(p, units, cta_begin, c);
     __syncwarp();
   } else {
-    md_softmax(p, units, cta_begin, c, warp, lane);
+    md_softmax(p, units, cta_begin, c, (warp - 2) >> 2, warp, lane);
   }
   tc_fence_before();
   __syncthreads();
