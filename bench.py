@@ -370,8 +370,11 @@ def run_decode(args, dev, stream, hbm, peak_src):
     b1.record(stream)
     torch.cuda.synchronize()
     multi_us = 1e3 * b0.elapsed_time(b1) / reps
-    multi_kernel = ("decode_split_kernel<128,%d> (T*G query rows per KV head)"
-                    % (T * w.hq // w.hkv)) if wst_bytes else "prefill_kernel<128>"
+    rows_t = T * w.hq // w.hkv
+    multi_kernel = ("prefill_kernel<128>" if not wst_bytes else
+                    "decode_mma_kernel + decode_combine_kernel (%d query rows per KV head)" % rows_t
+                    if rows_t in (8, 16) else
+                    "decode_split_kernel<128,%d> (T*G query rows per KV head)" % rows_t)
     multi_bytes = decode_bytes(w, lens_t) + sum(
         (T - 1) * w.head_dim * 4 for n in lens_t for hh in range(w.hkv) if w.head_class[0][hh])
     warm = 8
