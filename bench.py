@@ -106,6 +106,23 @@ class Clocks:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(value, world, device=None):
+    """The largest of every rank's value (one all-reduce; the value itself on
+    one rank). The step time of N replicas is the slowest rank's."""
+    if world <= 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replicas_value(units_per_rank, world, ms_per_step):
+    """Whole-job throughput of N independent replicas: all ranks' units over
+    the slowest rank's time, in units per microsecond (TFLOP/s for FLOPs)."""
+    return world * units_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -197,17 +214,13 @@ def run_ours(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     clocks = clk.stop()
-    total_ms = t0.elapsed_time(t1)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     if h.status() != 0:
         raise RuntimeError("device status after timed steps: " + S.segkv_last_error(h.handle))
     ms_step = total_ms / args.steps
     prefill_ms = statistics.median(pf_ms)
     append_ms = statistics.median(ap_ms)
-    value = world * step_flops / (ms_step * 1e-3) / 1e12
+    value = replicas_value(step_flops, world, ms_step)
 
     hbm, bf16_burst, bf16_sus, peak_src = measured_peaks()
     achieved = step_flops / (prefill_ms * 1e-3) / 1e12
