@@ -43,8 +43,8 @@ def test_tiny_256_tables_pages_and_attention():
     np.testing.assert_allclose(lse.cpu().numpy().T, ref_lse, atol=1e-3, rtol=0)
 
 
-@pytest.mark.parametrize("P", [16, 64, 128, 256])
-@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("P", [8, 16, 64, 128, 256])
+@pytest.mark.parametrize("G", [1, 4, 8, 16])
 def test_ragged_varlen_page_sizes(P, G):
     hkv = 2
     w = I.Workload("ragged", 1, G * hkv, hkv, 128, P, [[I.GLOBAL, I.LOCAL]], [100],

@@ -88,3 +88,35 @@ def test_fa_window_convention_prefill_and_decode():
     rc, ref, _ = c.oracle_attention(0, qd, [0], np.zeros(1, np.int32), np.array([256], np.int32))
     assert rc == 0
     check_close(od, ref, "FA-window decode")
+
+
+@pytest.mark.parametrize("P", [8, 16, 128, 256])
+@pytest.mark.parametrize("d", [64, 128])
+def test_single_token_decode_page_sizes(P, d):
+    """Single-token split-KV decode after a prefill append, a trim and one
+    decode append, for the smallest and largest page sizes the library takes."""
+    hkv, G, W = 2, 4, 150
+    hc = [[I.GLOBAL, I.LOCAL]]
+    lens0 = [1000, 9, 300, 257]
+    c = Cache(1, hkv * G, hkv, d, hc, [W], P, len(lens0), 2048, 2048 // P * 2 * len(lens0) + 64)
+    ids = list(range(len(lens0)))
+    for b, n in enumerate(lens0):
+        k = I.normal_bf16(61, 10 + b, (n, hkv, d))
+        v = I.normal_bf16(61, 20 + b, (n, hkv, d))
+        assert c.append(0, k.cuda(), v.cuda(), [0, n], [b]) == 0
+    c.trim(0, ids)
+    B = len(ids)
+    kd = I.normal_bf16(62, 1, (B, hkv, d))
+    vd = I.normal_bf16(62, 2, (B, hkv, d))
+    assert c.append(0, kd.cuda(), vd.cuda(), list(range(B + 1)), ids) == 0
+    c.check_tables(0)
+    lens = [c.m.seq_len(0, b) for b in ids]
+    q = I.normal_bf16(62, 3, (B, hkv * G, d))
+    o = torch.full((B, hkv * G, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(c.h.workspace_size(S.SEGKV_WS_DECODE, B, B) // 4 + 64, device="cuda")
+    c.h.decode_attn(0, q.cuda(), lens, ids, o, ws)
+    assert c.h.status() == 0
+    rc, ref, _ = c.oracle_attention(0, q, ids, np.arange(B, dtype=np.int32),
+                                    np.array([n - 1 for n in lens], np.int32))
+    assert rc == 0
+    check_close(o, ref, f"decode P={P} d={d}")
