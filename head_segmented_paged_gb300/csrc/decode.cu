@@ -32,12 +32,21 @@ using namespace ptx;
 
 namespace {
 
-constexpr int NS = 4;
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;
 
+// One CTA per SM. With two smaller CTAs per SM, measured per-CTA timestamps
+// showed the pair sharing the SM's memory stream unevenly: on 96 % of the SMs
+// one CTA of the two (nearly always the higher block index) finished about
+// 8 us later than the other, after about 4x longer waits for data, although
+// both streamed the same bytes. A static plan cannot balance that. One CTA
+// with twice the consumer warps streams a single slice per SM instead
+// (ragged decode, G = 4: 66.9 -> 62.6 us per call).
 template <int D, int G>
 struct DCfg {
-  static constexpr int NW = G == 4 ? 6 : 4;               // consumer warps
+  // consumer warps: 12 for G = 4; 8 for G = 2, and for 8 or 16 rows of 64
+  // dims; 4 for G = 1 (32 keys per warp and stage) and for 8 or 16 rows of
+  // 128 dims (register-heavy, and run on the tensor-core kernel instead)
+  static constexpr int NW = G == 4 ? 12 : (G == 2 || (D == 64 && G >= 8)) ? 8 : 4;
   static constexpr int THREADS = 32 * (NW + 1);            // + one producer warp
   static constexpr int LG = G > 8 ? G : 8;                 // lanes per score group
   static constexpr int KPG = LG / G;                       // keys per group per round
@@ -49,6 +58,9 @@ struct DCfg {
   static constexpr int DPV = D / 32;                       // P V dims per lane
   static constexpr int ROW = D * 2;
   static constexpr int STAGE = SK * ROW;                   // bytes of K (or V) per stage
+  // stages: as many K + V stages as fit in 192 KB, between 2 and 8
+  static constexpr int NS_FIT = 192 * 1024 / (2 * STAGE);
+  static constexpr int NS = NS_FIT < 2 ? 2 : (NS_FIT > 8 ? 8 : NS_FIT);
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NS * STAGE;
   static constexpr int OFF_P = OFF_V + NS * STAGE;         // float [NW][KW][G]
@@ -60,10 +72,8 @@ struct DCfg {
   static constexpr int OFF_BAR = (OFF_QB + NS * G * D * 2 + 15) & ~15;
   static constexpr int OFF_MISC = OFF_BAR + 2 * NS * 8;
   static constexpr int BYTES = OFF_MISC + 16;
-  // two CTAs per SM when their shared memory fits and the query rows leave
-  // registers for two; 8 or more rows of 128 dims take one CTA and 255
-  // registers (two would spill the per-lane query and accumulator rows)
-  static constexpr int MIN_BLOCKS = (BYTES <= 110 * 1024 && !(D == 128 && G >= 8)) ? 2 : 1;
+  static_assert(BYTES <= 227 * 1024, "decode shared memory");
+  static constexpr int MIN_BLOCKS = 1;
 };
 
 template <int N>
@@ -111,6 +121,7 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + C::OFF_MISC);
   int* last_flag = reinterpret_cast<int*>(sm + C::OFF_MISC + 4);
   auto full = [&](int s) { return sbase + C::OFF_BAR + 8u * s; };
+  constexpr int NS = C::NS;
   auto empty = [&](int s) { return sbase + C::OFF_BAR + 8u * (NS + s); };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

@@ -15,9 +15,20 @@ pytestmark = pytest.mark.gpu
 # on the tensor-core one, fewer on the CUDA-core one), the rest on the prefill
 # kernel
 @pytest.mark.parametrize("T,G", [(1, 4), (4, 4), (2, 8), (4, 2), (16, 1), (2, 1),
-                                 (1, 8), (1, 16), (8, 1), (3, 4), (7, 8), (16, 2)])
+                                 (1, 8), (1, 16), (8, 1), (3, 4), (7, 8), (16, 2),
+                                 (1, 1), (1, 2)])
 def test_multi_query_decode_matches_oracle(T, G):
-    hkv, d, P, W = 4, 128, 64, 200
+    multi_query_case(T, G, 128)
+
+
+# at 64 dims every T * G of 1 to 16 runs on the CUDA-core decode kernel
+@pytest.mark.parametrize("T,G", [(1, 1), (1, 2), (2, 2), (1, 8), (1, 16), (4, 4)])
+def test_multi_query_decode_head_dim_64(T, G):
+    multi_query_case(T, G, 64)
+
+
+def multi_query_case(T, G, d):
+    hkv, P, W = 4, 64, 200
     hc = [[I.GLOBAL, I.LOCAL, I.LOCAL, I.LOCAL]]
     lens0 = [3000, 64, 700, 1500, 20]
     c = Cache(1, hkv * G, hkv, d, hc, [W], P, len(lens0), 4096, 600)
