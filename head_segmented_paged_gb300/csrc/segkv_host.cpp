@@ -814,13 +814,17 @@ static int decode_core(segkv* h, int layer, const void* q, int T, const int32_t*
     }
   }
   // Stream-K split with a cost model: the concatenated key ranges are cut into
-  // one slice per CTA so that keys + kDecodeUnitCost per unit is the same for
-  // every CTA. A unit's epilogue (the warps' merge, the output or partials)
-  // pauses its CTA's memory stream; measured on the ragged-decode workload, a
-  // CTA finished about 3 us later per extra unit, the time it streams about
-  // 128 keys in. The smallest per-CTA budget whose greedy cut fits the grid is
-  // found by bisection.
+  // one slice per CTA so that keys + kDecodeUnitCost per unit (+
+  // kDecodeSplitCost per piece of a split pair) is the same for every CTA. A
+  // unit's epilogue (the warps' merge, the output or partials) pauses its
+  // CTA's memory stream; a piece of a split pair also writes partials, takes
+  // a ticket and may merge. Per-CTA timestamps on the ragged-decode workload
+  // priced a unit at about the time a CTA streams 128 keys in; the split
+  // surcharge was tuned on the same workload (0 -> 256 keys: 62.4 -> 61.6 us).
+  // The smallest per-CTA budget whose greedy cut fits the grid is found by
+  // bisection.
   constexpr int64_t kDecodeUnitCost = 128;
+  constexpr int64_t kDecodeSplitCost = 256;
   // 8 or 16 query rows of 128 dims run on the tensor-core decode kernel
   // (128-key stages, one CTA per SM); the rest on the CUDA-core kernel
   const bool mma = h->D == 128 && (rows == 8 || rows == 16);
@@ -847,7 +851,14 @@ static int decode_core(segkv* h, int layer, const void* q, int T, const int32_t*
       while (r < ranges.size()) {
         const Range& R = ranges[r];
         const int64_t avail = R.n - R.lo - off;
-        const int64_t room = T - cost - kDecodeUnitCost;
+        int64_t room = T - cost - kDecodeUnitCost;
+        if (room < 1) {
+          if (!any) return INT32_MAX;
+          break;
+        }
+        // a piece of a split pair also writes partials and may merge
+        const bool whole = off == 0 && avail <= room;
+        if (!whole) room -= kDecodeSplitCost;
         if (room < 1) {
           if (!any) return INT32_MAX;
           break;
@@ -867,7 +878,7 @@ static int decode_core(segkv* h, int layer, const void* q, int T, const int32_t*
           unit_pair.push_back(static_cast<int32_t>(r));
           ++pair_units[r];
         }
-        cost += kDecodeUnitCost + take;
+        cost += kDecodeUnitCost + (whole ? 0 : kDecodeSplitCost) + take;
         any = true;
         off += take;
         if (take == avail) {
