@@ -892,7 +892,15 @@ static int decode_core(segkv* h, int layer, const void* q, int T, const int32_t*
     }
     return used;
   };
-  int64_t lo = 1, hi = total + kDecodeUnitCost * (static_cast<int64_t>(ranges.size()) + 1);
+  // Every CTA costs at most the budget, so the budget is at least the total
+  // cost over the grid; the greedy cut leaves each CTA short of the budget by
+  // less than a unit and a split surcharge, so a budget a little above that
+  // bound usually fits. Probing it first narrows the bisection to a few steps.
+  const int64_t nr = static_cast<int64_t>(ranges.size());
+  int64_t lo = std::max<int64_t>(1, (total + kDecodeUnitCost * nr) / max_grid);
+  int64_t hi = total + kDecodeUnitCost * (nr + 1);  // one CTA holds everything
+  const int64_t probe = lo + lo / 8 + 2 * (kDecodeUnitCost + kDecodeSplitCost);
+  if (probe < hi && cut(probe, false) <= max_grid) hi = probe;
   while (lo < hi) {  // smallest budget that fits max_grid CTAs
     const int64_t mid = lo + (hi - lo) / 2;
     if (cut(mid, false) <= max_grid) hi = mid;
