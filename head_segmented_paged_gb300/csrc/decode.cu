@@ -6,12 +6,12 @@
 // the pieces (KV-cache architecture page, section 5.2).
 //
 // HBM bound. Work is split stream-K style: the (sequence, KV head, key)
-// sequence is cut into equal slices, one per CTA, so every CTA streams the
-// same number of K/V bytes; a slice may hold the tail of one (sequence, head)
-// pair and the head of the next. In each CTA a producer lane streams page
-// runs into a 4-stage shared-memory ring with bulk copies. Six consumer
-// warps (four when G != 4) each own a fixed share of every stage and keep their
-// own online softmax state, so a stage needs no block-wide synchronisation:
+// sequence is cut into slices of equal cost, one per CTA and one CTA per SM;
+// a slice may hold the tail of one (sequence, head) pair and the head of the
+// next. In each CTA a producer lane streams page runs into a shared-memory
+// ring with bulk copies. Twelve consumer warps at G = 4 (eight or four
+// otherwise) each own a fixed share of every stage and keep their own online
+// softmax state, so a stage needs no block-wide synchronisation:
 //   scores: 16-byte K chunk reads (lane i of a group of 8 takes chunks i and
 //           i+8 of a row, so every read is free of bank conflicts), packed
 //           f32x2 FMAs for the G query heads that share the KV head, an
