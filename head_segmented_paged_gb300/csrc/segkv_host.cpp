@@ -821,13 +821,17 @@ static int decode_core(segkv* h, int layer, const void* q, int T, const int32_t*
   // a ticket and may merge. Per-CTA timestamps on the ragged-decode workload
   // priced a unit at about the time a CTA streams 128 keys in; the split
   // surcharge was tuned on the same workload (0 -> 256 keys: 62.4 -> 61.6 us).
+  // On the tensor-core kernel a unit also waits for its query rows and its
+  // first S, and ends with a merge of two softmax groups; a sweep on the
+  // four-token ragged decode priced it at 512 keys (128: 112 us, 384: 108.7,
+  // 512: 101.4-103.0, 768: 103.3-104.3).
   // The smallest per-CTA budget whose greedy cut fits the grid is found by
   // bisection.
-  constexpr int64_t kDecodeUnitCost = 128;
-  constexpr int64_t kDecodeSplitCost = 256;
   // 8 or 16 query rows of 128 dims run on the tensor-core decode kernel
   // (128-key stages, one CTA per SM); the rest on the CUDA-core kernel
   const bool mma = h->D == 128 && (rows == 8 || rows == 16);
+  const int64_t kDecodeUnitCost = mma ? 512 : 128;
+  const int64_t kDecodeSplitCost = 256;
   const int64_t sk = mma ? 128 : decode_stage_keys(rows);
   const int64_t ctas = h->num_sms <= 0 ? decode_max_grid(h)
                        : mma ? int64_t(h->num_sms)
