@@ -52,19 +52,19 @@ constexpr uint32_t KV_TILE = 2 * kAtomKV;  // D = 128
 constexpr uint32_t kAtomR = MN * 128;      // 64 columns x 16 rows: 2 KB
 constexpr uint32_t OFF_K = 0;
 constexpr uint32_t OFF_V = NST * KV_TILE;
-constexpr uint32_t OFF_Q = 2 * NST * KV_TILE;          // Q: 2 atoms (dims 0..63, 64..127)
-constexpr uint32_t OFF_P = OFF_Q + 2 * kAtomR;         // P^T [2 buffers]: 2 atoms (keys 0..63, 64..127)
+constexpr uint32_t OFF_Q = 2 * NST * KV_TILE;          // Q [2 buffers, by unit parity]: 2 atoms (dims 0..63, 64..127)
+constexpr uint32_t OFF_P = OFF_Q + 4 * kAtomR;         // P^T [2 buffers]: 2 atoms (keys 0..63, 64..127)
 constexpr uint32_t OFF_XCH = OFF_P + 4 * kAtomR;          // int [group][2][4][16]: per-warp row maxima
 constexpr uint32_t OFF_LS = OFF_XCH + 2 * 2 * 4 * MN * 4;  // float [group][2][4][16]: per-warp row sums
 constexpr uint32_t OFF_GX = OFF_LS + 2 * 2 * 4 * MN * 4;   // float [2][2][16]: group 1's row max and sum
 constexpr uint32_t OFF_BAR = OFF_GX + 2 * 2 * MN * 4;
 enum {
-  Y_Q_FULL = 0,
-  Y_Q_EMPTY = 1,
-  Y_K_FULL = 2,                 // +stage
-  Y_V_FULL = 2 + NST,           // +stage
-  Y_KV_EMPTY = 2 + 2 * NST,     // +stage
-  Y_S_FULL = 2 + 3 * NST,       // +group (= stage parity): S buffer
+  Y_Q_FULL = 0,                 // +Q buffer (unit parity)
+  Y_Q_EMPTY = 2,                // +Q buffer
+  Y_K_FULL = 4,                 // +stage
+  Y_V_FULL = 4 + NST,           // +stage
+  Y_KV_EMPTY = 4 + 2 * NST,     // +stage
+  Y_S_FULL = 4 + 3 * NST,       // +group (= stage parity): S buffer
   Y_P_FULL = Y_S_FULL + 2,      // +group: P buffer
   Y_O_FULL = Y_S_FULL + 4,
   Y_O_EMPTY = Y_S_FULL + 5,
@@ -98,21 +98,24 @@ __device__ void md_producer(const CUtensorMap* tq, const CUtensorMap* tk, const 
                             const int32_t* cta_begin, const MdCtx& c, int lane) {
   const int box_rows = p.page_size <= KT ? p.page_size : KT;
   const int boxes = KT / box_rows;
-  int armed_q = -1, armed_kv[NST];
+  int armed_q[2] = {-1, -1}, armed_kv[NST];
   for (int s = 0; s < NST; ++s) armed_kv[s] = -1;
   bool ok = true;
   int g = 0, ui = 0;
   for (int u = cta_begin[blockIdx.x]; ok && u < cta_begin[blockIdx.x + 1]; ++u, ++ui) {
     const DecodeUnit U = units[u];
-    // the unit's query rows: token t of the sequence, heads head*Gm .. +Gm-1 -> row t*Gm + j
-    if (!waitw(c.bar(Y_Q_EMPTY), (ui & 1) ^ 1, c.wc)) { ok = false; break; }
+    // the unit's query rows: token t of the sequence, heads head*Gm .. +Gm-1 -> row t*Gm + j.
+    // Two buffers by unit parity, so they load while the previous unit runs.
+    const int qb = ui & 1;
+    const uint32_t qph = (ui >> 1) & 1;
+    if (!waitw(c.bar(Y_Q_EMPTY + qb), qph ^ 1, c.wc)) { ok = false; break; }
     if (lane == 0) {
-      mbar_expect_tx(c.bar(Y_Q_FULL), 2u * p.R_rows * 128);
+      mbar_expect_tx(c.bar(Y_Q_FULL + qb), 2u * p.R_rows * 128);
       for (int cc = 0; cc < 2; ++cc)
-        tma_load_3d(c.sbase + OFF_Q + cc * kAtomR, tq, cc * 64, U.head * p.Gm, U.req * p.T,
-                    c.bar(Y_Q_FULL));
+        tma_load_3d(c.sbase + OFF_Q + (qb * 2 + cc) * kAtomR, tq, cc * 64, U.head * p.Gm,
+                    U.req * p.T, c.bar(Y_Q_FULL + qb));
     }
-    armed_q = ui & 1;
+    armed_q[qb] = static_cast<int>(qph);
     const int32_t* trow = p.table + static_cast<int64_t>(U.table_row) * p.R;
     const int kfirst = U.k0 / p.page_size, klast = (U.k1 - 1) / p.page_size;
     int kbase = -(1 << 30), my_id = 0;
@@ -147,7 +150,8 @@ __device__ void md_producer(const CUtensorMap* tq, const CUtensorMap* tk, const 
     }
   }
   if (!ok && lane == 0) {  // aborting: let our own copies land before the block exits
-    if (armed_q >= 0) wait_drain(c.bar(Y_Q_FULL), armed_q, kDrainNsMD);
+    for (int b = 0; b < 2; ++b)
+      if (armed_q[b] >= 0) wait_drain(c.bar(Y_Q_FULL + b), armed_q[b], kDrainNsMD);
     for (int s = 0; s < NST; ++s)
       if (armed_kv[s] >= 0) {
         wait_drain(c.bar(Y_K_FULL + s), armed_kv[s], kDrainNsMD);
@@ -160,15 +164,15 @@ __device__ void md_mma(const DecodeMmaParams& p, const DecodeUnit* units, const 
                        const MdCtx& c) {
   constexpr uint32_t IDESC_S = idesc_bf16_ab(KT, MN, 0, 0);   // K (keys x D) . Q^T
   constexpr uint32_t IDESC_PV = idesc_bf16_ab(128, MN, 1, 0); // V^T (D x keys, MN-major) . P^T
-  // S(g) = K(g) Q^T into S buffer g % 2
-  auto issue_s = [&](int g) -> bool {
+  // S(g) = K(g) Q^T into S buffer g % 2, with Q buffer qb
+  auto issue_s = [&](int g, int qb) -> bool {
     const int st = g % NST;
     if (!wait1(c.bar(Y_K_FULL + st), (g / NST) & 1, c.wc)) return false;
     tc_fence_after();
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const uint32_t a = c.sbase + OFF_K + st * KV_TILE + (kk >> 2) * kAtomKV + (kk & 3) * 32;
-      const uint32_t b = c.sbase + OFF_Q + (kk >> 2) * kAtomR + (kk & 3) * 32;
+      const uint32_t b = c.sbase + OFF_Q + (qb * 2 + (kk >> 2)) * kAtomR + (kk & 3) * 32;
       mma_bf16(c.tmem + TM_S + (g & 1) * MN, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, 16, 1024),
                IDESC_S, kk > 0 ? 1u : 0u);
     }
@@ -180,17 +184,18 @@ __device__ void md_mma(const DecodeMmaParams& p, const DecodeUnit* units, const 
   for (int u = cta_begin[blockIdx.x]; ok && u < cta_begin[blockIdx.x + 1]; ++u, ++ui) {
     const DecodeUnit U = units[u];
     const int kt0 = U.k0 / KT, kt1 = (U.k1 - 1) / KT;
-    if (!wait1(c.bar(Y_Q_FULL), ui & 1, c.wc)) { ok = false; break; }
+    const int qb = ui & 1;
+    if (!wait1(c.bar(Y_Q_FULL + qb), (ui >> 1) & 1, c.wc)) { ok = false; break; }
     // S of the next stage is issued before P V of this one, so the tensor core
     // works on it while the softmax warps handle this stage
-    if (!issue_s(g)) { ok = false; break; }
-    if (kt0 == kt1) mma_commit(c.bar(Y_Q_EMPTY));
+    if (!issue_s(g, qb)) { ok = false; break; }
+    if (kt0 == kt1) mma_commit(c.bar(Y_Q_EMPTY + qb));
     const int g0 = g;
     for (int kt = kt0; kt <= kt1; ++kt, ++g) {
       const int st = g % NST;
       if (kt < kt1) {
-        if (!issue_s(g + 1)) { ok = false; break; }
-        if (kt + 1 == kt1) mma_commit(c.bar(Y_Q_EMPTY));
+        if (!issue_s(g + 1, qb)) { ok = false; break; }
+        if (kt + 1 == kt1) mma_commit(c.bar(Y_Q_EMPTY + qb));
       }
       if (!wait1(c.bar(Y_P_FULL + (g & 1)), (g >> 1) & 1, c.wc)) { ok = false; break; }
       if (!wait1(c.bar(Y_V_FULL + st), (g / NST) & 1, c.wc)) { ok = false; break; }
@@ -410,8 +415,10 @@ __global__ void __launch_bounds__(kThreadsMD, 1)
   const DecodeUnit* units = plan_ptr(p.units, blob, p.plan_inline);
   const int32_t* cta_begin = plan_ptr(p.cta_begin, blob, p.plan_inline);
   if (threadIdx.x == 0) {
-    mbar_init(c.bar(Y_Q_FULL), 1);
-    mbar_init(c.bar(Y_Q_EMPTY), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(c.bar(Y_Q_FULL + b), 1);
+      mbar_init(c.bar(Y_Q_EMPTY + b), 1);
+    }
     for (int s = 0; s < NST; ++s) {
       mbar_init(c.bar(Y_K_FULL + s), 1);
       mbar_init(c.bar(Y_V_FULL + s), 1);
