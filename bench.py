@@ -683,6 +683,17 @@ def run_e2e(args, dev, stream, w, sets, cu, q_pos, step_flops, num_pages):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    # the host->device rate alone on this machine (one layer's Q, K, V, twice),
+    # to tell a copy-bound step from a compute-bound one
+    with torch.cuda.stream(copy_stream):
+        t0.record(copy_stream)
+        for _ in range(2):
+            for dst, src in zip(dbuf[0], host[0]):
+                dst.copy_(src, non_blocking=True)
+        t1.record(copy_stream)
+    torch.cuda.synchronize()
+    layer_bytes = sum(t.numel() * t.element_size() for t in host[0])
+    h2d_gbs = 2 * layer_bytes / (t0.elapsed_time(t1) * 1e-3) / 1e9
     ks = max(1, min(args.steps, 2))
     t0.record(stream)
     for _ in range(ks):
@@ -693,6 +704,8 @@ def run_e2e(args, dev, stream, w, sets, cu, q_pos, step_flops, num_pages):
     return {"value": round(step_flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
             "ms_per_step": round(ms, 2), "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": o.numel() * o.element_size(),
+            "h2d_gbs_copy_alone": round(h2d_gbs, 1),
+            "h2d_ms_per_step_at_that_rate": round(h2d / (h2d_gbs * 1e9) * 1e3, 1),
             "note": "pinned host Q/K/V per layer copied in the timed region on a side stream "
                     "(three rotating device buffers); last layer's O copied back"}
 
