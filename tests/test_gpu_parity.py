@@ -203,3 +203,32 @@ def test_decode_subset_of_sequences_and_free_reuse():
     assert c.append(0, k.cuda(), k.cuda(), [0, 700], [1]) == 0
     c.check_tables(0)
     decode_run(c, 0, [0, 1, 2, 3], steps=3, seed=3)
+
+
+@pytest.mark.parametrize("d,P", [(128, 16), (64, 64)])
+def test_window_one_local_heads_return_their_own_value(d, P):
+    """A local head with W = 1 sees only its own key, so its softmax weight is
+    1 and its output is that key's V row exactly. Prefill, then trim (which
+    leaves the local segments with no key), then decode steps that append and
+    read a single key per local segment."""
+    hkv, G, n = 2, 4, 300
+    w = I.Workload("w1", 1, G * hkv, hkv, d, P, [[I.GLOBAL, I.LOCAL]], [1], [n], seed=21)
+    c, q, cu, qp, ids = prefill_case(w, num_pages=200, max_seq_len=512)
+    o, lse = run_prefill(c, 0, q, cu, qp, ids)
+    rc, ref, _ = c.oracle_attention(0, q, ids, q_index(cu), qp.numpy())
+    assert rc == 0
+    check_close(o, ref, "prefill W=1")
+    v_local = c.v_log[(0, ids[0])][:, 1]  # [n, d] bf16
+    for g in range(G):
+        assert torch.equal(o[:, G + g].cpu().contiguous().view(torch.int16),
+                           v_local.contiguous().view(torch.int16))
+    np.testing.assert_allclose(lse[G:].cpu().numpy(),  # one key: LSE = its scaled score
+                               (q[:, G:].double() * c.k_log[(0, ids[0])][:, 1:2].double()).sum(-1).T.numpy()
+                               / np.sqrt(d), atol=1e-3, rtol=1e-4)
+    c.trim(0, ids)
+    s, ln, _, pages = c.m.segment(0, 1, ids[0])
+    # no key kept (the next query needs only its own); only the page that will
+    # receive the next key stays held when position n falls inside it
+    assert (s, ln) == (n, 0) and len(pages) == (1 if n % P else 0)
+    c.check_tables(0)
+    decode_run(c, 0, ids, steps=3, seed=22)
