@@ -140,11 +140,15 @@ def test_empty_calls_are_noops():
     assert c.h.status() == 0
 
 
-def test_device_timeout_path_reports_status_and_context_survives():
-    w = I.tiny_256()
+# 64 dims run the single-SM prefill kernel, 128 the SM-pair kernel (whose
+# second CTA gives up on its own bounded waits once the leader has stopped)
+@pytest.mark.parametrize("d", [64, 128])
+def test_device_timeout_path_reports_status_and_context_survives(d):
+    w = I.tiny_256() if d == 64 else I.Workload("tiny128", 1, 8, 2, 128, 16, [[I.GLOBAL, I.LOCAL]],
+                                                 [32], [256], seed=0)
     c, q, cu, qp, ids = prefill_case(w)
     c.h.set_debug(1)
-    o = torch.empty((256, 8, 64), dtype=torch.bfloat16, device="cuda")
+    o = torch.empty((256, 8, d), dtype=torch.bfloat16, device="cuda")
     assert S.segkv_prefill_attn(c.h.handle, 0, q.cuda(), cu, qp, ids, o) == 0
     assert c.h.status() == S.SEGKV_ERR_DEVICE_TIMEOUT
     assert c.h.status() == 0  # cleared
