@@ -36,7 +36,7 @@ SYMBOLS = ["segkv_create", "segkv_destroy", "segkv_append", "segkv_prefill_attn"
            "segkv_last_error", "segkv_set_debug", "segkv_decode_attn_noalloc", "segkv_rope_shift",
            "segkv_export_size", "segkv_export", "segkv_import", "segkv_set_window_convention",
            "segkv_decode_attn_multi", "segkv_sparse_ffn", "segkv_ffn_workspace_size", "segkv_attn_mass",
-           "segkv_topk_tokens"]
+           "segkv_topk_tokens", "segkv_plan_decode"]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -77,6 +77,7 @@ def _load():
         "segkv_ffn_workspace_size": [I, I, I, P],
         "segkv_export": [P, I, I, P, SZ, P, P],
         "segkv_import": [P, I, I, P, SZ, P, P],
+        "segkv_plan_decode": [P, I, I, P, P, I, I, P, I, P, I, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -282,6 +283,25 @@ def segkv_status(h, stream=None):
 def segkv_last_error(h=None):
     m = _lib.segkv_last_error(h)
     return m.decode() if m else ""
+
+
+def segkv_plan_decode(h, layer, T, seq_lens, seq_ids, num_ctas=0):
+    """The decode work plan (host only). Returns (rc, units [n_units, 8] int32,
+    cta_begin [n_ctas + 1] int32); unit columns: sequence index, KV head,
+    local, k0, k1, first unit of its pair, units of its pair, newest query
+    position."""
+    sl, ids = _host_i32(seq_lens), _host_i32(seq_ids)
+    nu, nc = ctypes.c_int(0), ctypes.c_int(0)
+    rc = _lib.segkv_plan_decode(h, layer, T, sl.ctypes.data, ids.ctypes.data, len(ids), num_ctas, None,
+                                0, None, 0, ctypes.byref(nu), ctypes.byref(nc))
+    if len(ids) == 0 or (rc != 0 and nu.value == 0):
+        return rc, np.zeros((0, 8), np.int32), np.zeros(1, np.int32)
+    units = np.zeros((nu.value, 8), np.int32)
+    cta = np.zeros(nc.value + 1, np.int32)
+    rc = _lib.segkv_plan_decode(h, layer, T, sl.ctypes.data, ids.ctypes.data, len(ids), num_ctas,
+                                units.ctypes.data, nu.value, cta.ctypes.data, nc.value, ctypes.byref(nu),
+                                ctypes.byref(nc))
+    return rc, units, cta
 
 
 def segkv_set_debug(h, flags):

@@ -786,16 +786,27 @@ static int decode_mma_launch(segkv* h, int layer, const void* q, int T, int n, v
   return SEGKV_OK;
 }
 
-// Split-KV decode of the T newest tokens of n sequences: T * G query rows per
-// KV head, each with its own causal (and window) limit.
-static int decode_core(segkv* h, int layer, const void* q, int T, const int32_t* seq_lens,
-                       const int32_t* seq_ids, int n, void* o, float* lse, void* workspace,
-                       size_t workspace_bytes, cudaStream_t s) {
+// One (sequence, KV head) key range of a decode call, and the plan cut from them.
+struct DecodeRange { int32_t req, head, lo, n, row, local; };
+struct DecodePlan {
+  std::vector<DecodeRange> ranges;
+  std::vector<DecodeUnit> units;
+  std::vector<int32_t> cta_begin;
+  std::vector<int32_t> pair_unit0, pair_units;  // per range
+  int grid = 0, rows = 0;
+  bool mma = false;
+};
+
+// The split-KV decode plan of the T newest tokens of n sequences (host only):
+// the (sequence, KV head) key ranges cut into units, grouped by CTA. ctas > 0
+// plans for that many CTAs instead of the device's.
+static int decode_plan(segkv* h, int layer, int T, const int32_t* seq_lens, const int32_t* seq_ids,
+                       int n, int64_t ctas_override, DecodePlan& P) {
   const int W = h->win[layer];
   const int rows = T * h->G;
   // pairs (req, head) with their key ranges [lo, n)
-  struct Range { int32_t req, head, lo, n, row, local; };
-  std::vector<Range> ranges;
+  std::vector<DecodeRange>& ranges = P.ranges;
+  ranges.clear();
   int64_t total = 0;
   for (int i = 0; i < n; ++i) {
     const int b = seq_ids[i];
@@ -833,14 +844,21 @@ static int decode_core(segkv* h, int layer, const void* q, int T, const int32_t*
   const int64_t kDecodeUnitCost = mma ? 512 : 128;
   const int64_t kDecodeSplitCost = 256;
   const int64_t sk = mma ? 128 : decode_stage_keys(rows);
-  const int64_t ctas = h->num_sms <= 0 ? decode_max_grid(h)
+  const int64_t ctas = ctas_override > 0 ? ctas_override
+                       : h->num_sms <= 0 ? decode_max_grid(h)
                        : mma ? int64_t(h->num_sms)
                              : int64_t(h->num_sms) * decode_ctas_per_sm(h->D, rows);
   const int max_grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(
-      std::min<int64_t>(ctas, decode_max_grid(h)), (total + sk - 1) / sk)));
-  std::vector<DecodeUnit> units;
-  std::vector<int32_t> pair_unit0(ranges.size()), pair_units(ranges.size(), 0);
-  std::vector<int32_t> cta_begin;
+      std::min<int64_t>(ctas, ctas_override > 0 ? ctas_override : decode_max_grid(h)),
+      (total + sk - 1) / sk)));
+  std::vector<DecodeUnit>& units = P.units;
+  std::vector<int32_t>& pair_unit0 = P.pair_unit0;
+  std::vector<int32_t>& pair_units = P.pair_units;
+  std::vector<int32_t>& cta_begin = P.cta_begin;
+  units.clear();
+  cta_begin.clear();
+  pair_unit0.assign(ranges.size(), 0);
+  pair_units.assign(ranges.size(), 0);
   std::vector<int32_t> unit_pair;  // ranges are pushed per (req, head): pair r = req * Hkv + head
   // Greedy cut with budget T per CTA; returns the CTAs used (INT32_MAX if T is
   // too small to hold even one key), emitting the units when asked.
@@ -853,7 +871,7 @@ static int decode_core(segkv* h, int layer, const void* q, int T, const int32_t*
       int64_t cost = 0;
       bool any = false;
       while (r < ranges.size()) {
-        const Range& R = ranges[r];
+        const DecodeRange& R = ranges[r];
         const int64_t avail = R.n - R.lo - off;
         int64_t room = T - cost - kDecodeUnitCost;
         if (room < 1) {
@@ -916,6 +934,28 @@ static int decode_core(segkv* h, int layer, const void* q, int T, const int32_t*
     units[x].pair_unit0 = pair_unit0[unit_pair[x]];
     units[x].pair_units = pair_units[unit_pair[x]];
   }
+  P.grid = grid;
+  P.rows = rows;
+  P.mma = mma;
+  return SEGKV_OK;
+}
+
+// Split-KV decode of the T newest tokens of n sequences: T * G query rows per
+// KV head, each with its own causal (and window) limit.
+static int decode_core(segkv* h, int layer, const void* q, int T, const int32_t* seq_lens,
+                       const int32_t* seq_ids, int n, void* o, float* lse, void* workspace,
+                       size_t workspace_bytes, cudaStream_t s) {
+  const int W = h->win[layer];
+  DecodePlan P;
+  const int prc = decode_plan(h, layer, T, seq_lens, seq_ids, n, 0, P);
+  if (prc != SEGKV_OK) return prc;
+  const std::vector<DecodeRange>& ranges = P.ranges;
+  const std::vector<DecodeUnit>& units = P.units;
+  const std::vector<int32_t>& cta_begin = P.cta_begin;
+  const std::vector<int32_t>& pair_unit0 = P.pair_unit0;
+  const std::vector<int32_t>& pair_units = P.pair_units;
+  const int rows = P.rows, grid = P.grid;
+  const bool mma = P.mma;
   size_t acc_bytes, ml_bytes;
   const size_t need =
       decode_ws_bytes(h, static_cast<int64_t>(units.size()), rows, &acc_bytes, &ml_bytes);
@@ -1078,6 +1118,42 @@ int segkv_set_window_convention(segkv_t h, int convention) {
   const int add = (convention == SEGKV_WINDOW_FA) - (h->window_fa ? 1 : 0);
   for (int32_t& w : h->win) w += add;
   h->window_fa = convention == SEGKV_WINDOW_FA;
+  return SEGKV_OK;
+}
+
+int segkv_plan_decode(segkv_t h, int layer, int T, const int32_t* seq_lens, const int32_t* seq_ids,
+                      int n, int num_ctas, int32_t* units_out, int max_units, int32_t* cta_begin_out,
+                      int max_ctas, int* n_units, int* n_ctas) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= h->L) return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer %d", layer);
+  if (T < 1 || n < 0 || max_units < 0 || max_ctas < 0 || !n_units || !n_ctas)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "bad T, n or output sizes");
+  if (!ids_valid(h, seq_ids, n)) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq_ids");
+  *n_units = 0;
+  *n_ctas = 0;
+  if (n == 0) return SEGKV_OK;
+  if (!seq_lens) return fail(h, SEGKV_ERR_INVALID_ARG, "seq_lens NULL");
+  DecodePlan P;
+  const int rc = decode_plan(h, layer, T, seq_lens, seq_ids, n, num_ctas, P);
+  if (rc != SEGKV_OK) return rc;
+  *n_units = static_cast<int>(P.units.size());
+  *n_ctas = P.grid;
+  if (static_cast<int>(P.units.size()) > max_units || P.grid > max_ctas || (max_units && !units_out) ||
+      !cta_begin_out)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "plan needs %d units and %d CTAs", *n_units, *n_ctas);
+  for (size_t x = 0; x < P.units.size(); ++x) {
+    const DecodeUnit& u = P.units[x];
+    int32_t* o = units_out + 8 * x;
+    o[0] = u.req;
+    o[1] = u.head;
+    o[2] = u.local;
+    o[3] = u.k0;
+    o[4] = u.k1;
+    o[5] = u.pair_unit0;
+    o[6] = u.pair_units;
+    o[7] = u.q_last;
+  }
+  for (int c = 0; c <= P.grid; ++c) cta_begin_out[c] = P.cta_begin[c];
   return SEGKV_OK;
 }
 

@@ -372,6 +372,25 @@ const char* segkv_last_error(segkv_t h);
 int segkv_decode_attn_noalloc(segkv_t h, int layer, const void* q, const int32_t* seq_lens,
                               const int32_t* seq_ids, int n, void* o, segkv_stream_t stream);
 
+/* segkv_plan_decode — the work plan that segkv_decode_attn (T = 1) or
+ * segkv_decode_attn_multi would use for the T newest tokens of n sequences,
+ * computed on the host only (no device work; host-only handles work too), for
+ * tests and tools. The plan is the stream-K cut of the (sequence, KV head) key
+ * ranges into units, grouped by CTA.
+ *   num_ctas    > 0: plan for that many CTAs; otherwise for the device's grid.
+ *   units       host int32 [max_units][8], out: sequence index i of the call,
+ *               KV head, 1 if local, keys [k0, k1), first unit of the unit's
+ *               (sequence, head) pair, units of that pair, position of the
+ *               sequence's newest query token.
+ *   cta_begin   host int32 [max_ctas + 1], out: CTA c runs units
+ *               cta_begin[c] .. cta_begin[c + 1] - 1.
+ *   n_units, n_ctas  out: the plan's sizes, written even when an output
+ *               array is too small (then SEGKV_ERR_INVALID_ARG).
+ * Errors: those of segkv_decode_attn_multi for the same arguments. */
+int segkv_plan_decode(segkv_t h, int layer, int T, const int32_t* seq_lens, const int32_t* seq_ids,
+                      int n, int num_ctas, int32_t* units, int max_units, int32_t* cta_begin,
+                      int max_ctas, int* n_units, int* n_ctas);
+
 /* segkv_set_debug — test hook. Bit 0: the next prefill launch makes one wait
  * on a barrier that nothing signals, with a short limit, so the timeout path
  * runs (status becomes SEGKV_ERR_DEVICE_TIMEOUT). Bits are cleared on use. */

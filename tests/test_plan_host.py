@@ -1,0 +1,144 @@
+"""Decode work plans on the host, without a GPU.
+
+`segkv_plan_decode` returns the plan a decode call would launch: the
+(sequence, KV head) key ranges cut stream-K style into units, grouped by CTA.
+The checks here pin what the plan must be for the kernels to be right and
+balanced:
+- every kept key a query row needs is in exactly one unit;
+- a pair's units are consecutive and in key order, and carry the pair's
+  bookkeeping;
+- each CTA's cost (keys + a charge per unit + a charge per split piece) stays
+  within one unit's charges of the most loaded CTA.
+"""
+import numpy as np
+import pytest
+
+import head_segmented_paged_gb300 as S
+import oracle
+
+GLOBAL, LOCAL = 0, 1
+SPLIT_COST = 256
+
+
+def unit_cost(d, rows):
+    # the tensor-core decode kernel (8 or 16 rows of 128 dims) pays more per unit
+    return 512 if d == 128 and rows in (8, 16) else 128
+
+
+def host_handle(hq, hkv, d, hc, W, P, max_seqs, max_len, pages):
+    return S.SegKV(1, hq, hkv, d, [hc], [W], P, max_seqs, max_len, num_pages=pages)
+
+
+def fill(h, lens):
+    for b, n in enumerate(lens):
+        rc = S.segkv_append(h.handle, 0, None, None, np.array([0, n], np.int32),
+                            np.array([b], np.int32))
+        assert rc == 0
+
+
+def check_plan(units, cta, lens, hc, W, T, d, G, num_ctas):
+    rows = T * G
+    n_units = units.shape[0]
+    assert cta[0] == 0 and cta[-1] == n_units and (np.diff(cta) >= 1).all()
+    assert len(cta) - 1 <= num_ctas
+    hkv = len(hc)
+    # coverage, order and bookkeeping per (sequence index, head)
+    for i, n in enumerate(lens):
+        for hd in range(hkv):
+            sel = np.nonzero((units[:, 0] == i) & (units[:, 1] == hd))[0]
+            assert len(sel) >= 1
+            assert (np.diff(sel) == 1).all(), "a pair's units are consecutive"
+            lo = max(0, n - T - W + 1) if hc[hd] == LOCAL else 0
+            assert units[sel[0], 3] == lo and units[sel[-1], 4] == n
+            assert (units[sel[1:], 3] == units[sel[:-1], 4]).all(), "pieces tile the range"
+            assert (units[sel, 4] > units[sel, 3]).all()
+            assert (units[sel, 5] == sel[0]).all() and (units[sel, 6] == len(sel)).all()
+            assert (units[sel, 2] == hc[hd]).all() and (units[sel, 7] == n - 1).all()
+    # balance: a CTA closes only when the next unit's charges no longer fit
+    U = unit_cost(d, rows)
+    costs = []
+    for c in range(len(cta) - 1):
+        us = units[cta[c]:cta[c + 1]]
+        split = us[:, 6] > 1
+        costs.append(int((us[:, 4] - us[:, 3]).sum()) + U * len(us) + SPLIT_COST * int(split.sum()))
+    costs = np.array(costs)
+    assert (costs[:-1] >= costs.max() - U - SPLIT_COST - 1).all(), costs
+
+
+@pytest.mark.parametrize("hq,hkv,d,T", [(32, 8, 128, 1), (32, 8, 128, 4), (64, 8, 128, 2),
+                                        (8, 2, 64, 1), (16, 2, 64, 3)])
+@pytest.mark.parametrize("num_ctas", [152, 16, 1])
+def test_decode_plan_covers_each_needed_key_once_and_balances(hq, hkv, d, T, num_ctas):
+    G = hq // hkv
+    hc = [GLOBAL] + [LOCAL] * (hkv - 1)
+    W, P = 300, 64
+    rng = np.random.default_rng(hq * 7 + T)
+    lens = [int(x) for x in rng.integers(T, 6000, size=24)] + [T, T + 1, 4097]
+    h = host_handle(hq, hkv, d, hc, W, P, len(lens), 8192, 16 * 1024)
+    fill(h, lens)
+    ids = list(range(len(lens)))
+    rc, units, cta = S.segkv_plan_decode(h.handle, 0, T, lens, ids, num_ctas)
+    assert rc == 0, S.segkv_last_error(h.handle)
+    check_plan(units, cta, lens, hc, W, T, d, G, num_ctas)
+
+
+def test_decode_plan_after_trim_and_on_a_subset_of_sequences():
+    hq, hkv, d = 32, 8, 128
+    hc = [LOCAL, GLOBAL, LOCAL, LOCAL, LOCAL, LOCAL, LOCAL, LOCAL]
+    W, P = 1024, 64
+    lens = [2048, 32768, 5000, 1, 1023, 1024, 1025]
+    h = host_handle(hq, hkv, d, hc, W, P, len(lens), 40000, 12000)
+    fill(h, lens)
+    assert h.trim(0, list(range(len(lens)))) == 0
+    # one new token each, then plan for a subset in a shuffled order
+    for b in range(len(lens)):
+        assert S.segkv_append(h.handle, 0, None, None, np.array([0, 1], np.int32),
+                              np.array([b], np.int32)) == 0
+    ids = [5, 1, 3, 0]
+    sub = [lens[b] + 1 for b in ids]
+    rc, units, cta = S.segkv_plan_decode(h.handle, 0, 1, sub, ids, 152)
+    assert rc == 0, S.segkv_last_error(h.handle)
+    check_plan(units, cta, sub, hc, W, 1, d, hq // hkv, 152)
+
+
+def test_decode_plan_matches_the_oracle_page_model_key_sets():
+    """The keys a plan streams for each (sequence, head) are those the oracle's
+    page model keeps and the query sees."""
+    hq, hkv, d, W, P = 16, 2, 64, 40, 16
+    hc = [GLOBAL, LOCAL]
+    lens = [10, 100, 333]
+    h = host_handle(hq, hkv, d, hc, W, P, len(lens), 1024, 512)
+    m = oracle.PageModel(1, hkv, [hc], [W], P, len(lens), 1024, 512)
+    for b, n in enumerate(lens):
+        cu = np.array([0, n], np.int32)
+        assert S.segkv_append(h.handle, 0, None, None, cu, np.array([b], np.int32)) == 0
+        assert m.append(0, cu, [b]) == 0
+    assert h.trim(0, [0, 1, 2]) == 0 and m.trim(0, [0, 1, 2]) == 0
+    # the next token of each sequence, then its decode
+    one = np.array([0, 1, 2, 3], np.int32)
+    assert S.segkv_append(h.handle, 0, None, None, one, np.array([0, 1, 2], np.int32)) == 0
+    assert m.append(0, one, [0, 1, 2]) == 0
+    lens = [n + 1 for n in lens]
+    rc, units, cta = S.segkv_plan_decode(h.handle, 0, 1, lens, [0, 1, 2], 4)
+    assert rc == 0, S.segkv_last_error(h.handle)
+    for i, n in enumerate(lens):
+        for hd in range(hkv):
+            s, ln, _, _ = m.segment(0, hd, i)
+            sel = (units[:, 0] == i) & (units[:, 1] == hd)
+            k0, k1 = units[sel, 3].min(), units[sel, 4].max()
+            # the query at n - 1 sees [max(0, n - W), n) on a local head, all keys on a global one
+            want = max(0, n - W) if hc[hd] == LOCAL else 0
+            assert (k0, k1) == (want, n)
+            assert s <= k0 and s + ln == n  # every streamed key is kept
+
+
+def test_decode_plan_errors():
+    h = host_handle(8, 2, 64, [GLOBAL, LOCAL], 16, 16, 2, 512, 64)
+    fill(h, [100, 5])
+    assert S.segkv_plan_decode(h.handle, 0, 1, [99, 5], [0, 1], 8)[0] == S.SEGKV_ERR_INVALID_ARG
+    assert S.segkv_plan_decode(h.handle, 0, 6, [100, 5], [0, 1], 8)[0] == S.SEGKV_ERR_INVALID_ARG
+    assert S.segkv_plan_decode(h.handle, 1, 1, [100, 5], [0, 1], 8)[0] == S.SEGKV_ERR_INVALID_ARG
+    assert h.trim(0, [0]) == 0  # the local head keeps only what position 100 needs
+    assert S.segkv_plan_decode(h.handle, 0, 3, [100], [0], 8)[0] == S.SEGKV_ERR_EVICTED
+    rc, units, cta = S.segkv_plan_decode(h.handle, 0, 1, [], [], 8)
+    assert rc == 0 and units.shape == (0, 8)
