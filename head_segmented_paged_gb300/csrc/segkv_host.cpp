@@ -520,25 +520,10 @@ int segkv_append(segkv_t h, int layer, const void* k, const void* v, const int32
 }
 
 // ---------------------------------------------------------------- prefill
-int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_seqlens,
-                       const int32_t* q_pos, const int32_t* seq_ids, int n, void* o, float* lse,
-                       void* workspace, size_t workspace_bytes, segkv_stream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
-  if (!h) return SEGKV_ERR_INVALID_ARG;
-  if (h->host_only) return fail(h, SEGKV_ERR_INVALID_ARG, "host-only handle has no pools");
-  if (layer < 0 || layer >= h->L) return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer %d", layer);
-  if (!ids_valid(h, seq_ids, n)) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq_ids");
-  if (n == 0) return SEGKV_OK;
-  if (!cu_seqlens || cu_seqlens[0] != 0) return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens[0] != 0");
-  for (int i = 0; i < n; ++i)
-    if (cu_seqlens[i + 1] < cu_seqlens[i])
-      return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens decreases at %d", i);
-  const int64_t total = cu_seqlens[n];
-  if (total == 0) return SEGKV_OK;
-  if (!q || !o || !q_pos) return fail(h, SEGKV_ERR_INVALID_ARG, "q/o/q_pos NULL");
-  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(o)) & 15)
-    return fail(h, SEGKV_ERR_INVALID_ARG, "q and o must be 16-byte aligned");
+// Positions and kept keys of a prefill call (host): every query position lies
+// in its sequence, and every key it sees is still kept.
+static int prefill_validate(segkv* h, int layer, const int32_t* cu_seqlens, const int32_t* q_pos,
+                            const int32_t* seq_ids, int n) {
   const int W = h->win[layer];
   // validate positions and kept keys
   for (int i = 0; i < n; ++i) {
@@ -555,8 +540,16 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
       }
     }
   }
+  return SEGKV_OK;
+}
+
+// The prefill work plan (host): units of one KV head x the Q tiles of a
+// chunk of tokens, scheduled onto `ctas` lists by LPT and grouped by list.
+static void prefill_plan(segkv* h, int layer, const int32_t* cu_seqlens, const int32_t* q_pos,
+                         const int32_t* seq_ids, int n, int ctas, std::vector<PrefillUnit>& by_cta,
+                         std::vector<int32_t>& cta_begin) {
+  const int W = h->win[layer];
   // units: (KV head, two Q tiles of 128/G tokens each), LPT order
-  const int tpt = kRowsPerTile / h->G;
   const int unit_tok = prefill_unit_tokens(h->G);
   std::vector<PrefillUnit> units;
   for (int i = 0; i < n; ++i) {
@@ -595,9 +588,9 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
   std::stable_sort(units.begin(), units.end(), [](const PrefillUnit& a, const PrefillUnit& b) {
     return (a.kt1 - a.kt0) > (b.kt1 - b.kt0);
   });
-  const int grid = static_cast<int>(std::min<int64_t>(units.size(), h->num_sms));
+  const int grid = static_cast<int>(std::min<int64_t>(units.size(), ctas));
   std::vector<int32_t> cta_of(units.size());
-  std::vector<int32_t> cta_begin(grid + 1, 0);
+  cta_begin.assign(grid + 1, 0);
   {
     using Load = std::pair<int64_t, int32_t>;  // (work so far, CTA)
     std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
@@ -612,11 +605,44 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
     }
   }
   for (int c = 0; c < grid; ++c) cta_begin[c + 1] += cta_begin[c];
-  std::vector<PrefillUnit> by_cta(units.size());
+  by_cta.assign(units.size(), PrefillUnit{});
   {
     std::vector<int32_t> fill(cta_begin.begin(), cta_begin.end() - 1);
     for (size_t x = 0; x < units.size(); ++x) by_cta[fill[cta_of[x]]++] = units[x];
   }
+
+}
+
+int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_seqlens,
+                       const int32_t* q_pos, const int32_t* seq_ids, int n, void* o, float* lse,
+                       void* workspace, size_t workspace_bytes, segkv_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (h->host_only) return fail(h, SEGKV_ERR_INVALID_ARG, "host-only handle has no pools");
+  if (layer < 0 || layer >= h->L) return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer %d", layer);
+  if (!ids_valid(h, seq_ids, n)) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq_ids");
+  if (n == 0) return SEGKV_OK;
+  if (!cu_seqlens || cu_seqlens[0] != 0) return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens[0] != 0");
+  for (int i = 0; i < n; ++i)
+    if (cu_seqlens[i + 1] < cu_seqlens[i])
+      return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens decreases at %d", i);
+  const int64_t total = cu_seqlens[n];
+  if (total == 0) return SEGKV_OK;
+  if (!q || !o || !q_pos) return fail(h, SEGKV_ERR_INVALID_ARG, "q/o/q_pos NULL");
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(o)) & 15)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "q and o must be 16-byte aligned");
+  {
+    const int vrc = prefill_validate(h, layer, cu_seqlens, q_pos, seq_ids, n);
+    if (vrc != SEGKV_OK) return vrc;
+  }
+  const int W = h->win[layer];
+  const int tpt = kRowsPerTile / h->G;
+  std::vector<PrefillUnit> by_cta;
+  std::vector<int32_t> cta_begin;
+  prefill_plan(h, layer, cu_seqlens, q_pos, seq_ids, n, h->num_sms, by_cta, cta_begin);
+  const int grid = static_cast<int>(cta_begin.size()) - 1;
+  const size_t n_units = by_cta.size();
 
   Pack pk;
   const size_t o_units = pk.add(by_cta.data(), by_cta.size());
@@ -654,7 +680,7 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
   p.o = o;
   p.lse = lse;
   p.total_q = total;
-  p.n_units = static_cast<int>(units.size());
+  p.n_units = static_cast<int>(n_units);
   p.R = h->R;
   p.hq = h->Hq;
   p.G = h->G;
@@ -671,6 +697,49 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
   if (e != cudaSuccess) return cuda_fail(h, e, "prefill kernel launch");
   e = h->ring.commit(off, pk.buf.size(), s);
   if (e != cudaSuccess) return cuda_fail(h, e, "event record");
+  return SEGKV_OK;
+}
+
+int segkv_plan_prefill(segkv_t h, int layer, const int32_t* cu_seqlens, const int32_t* q_pos,
+                       const int32_t* seq_ids, int n, int num_ctas, int32_t* units_out, int max_units,
+                       int32_t* cta_begin_out, int max_ctas, int* n_units, int* n_ctas) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= h->L) return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer %d", layer);
+  if (n < 0 || max_units < 0 || max_ctas < 0 || !n_units || !n_ctas)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "bad n or output sizes");
+  if (!ids_valid(h, seq_ids, n)) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq_ids");
+  *n_units = 0;
+  *n_ctas = 0;
+  if (n == 0) return SEGKV_OK;
+  if (!cu_seqlens || cu_seqlens[0] != 0) return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens[0] != 0");
+  for (int i = 0; i < n; ++i)
+    if (cu_seqlens[i + 1] < cu_seqlens[i])
+      return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens decreases at %d", i);
+  if (cu_seqlens[n] == 0) return SEGKV_OK;
+  if (!q_pos) return fail(h, SEGKV_ERR_INVALID_ARG, "q_pos NULL");
+  const int vrc = prefill_validate(h, layer, cu_seqlens, q_pos, seq_ids, n);
+  if (vrc != SEGKV_OK) return vrc;
+  std::vector<PrefillUnit> by_cta;
+  std::vector<int32_t> cta_begin;
+  const int ctas = num_ctas > 0 ? num_ctas : (h->num_sms > 0 ? h->num_sms : 1);
+  prefill_plan(h, layer, cu_seqlens, q_pos, seq_ids, n, ctas, by_cta, cta_begin);
+  *n_units = static_cast<int>(by_cta.size());
+  *n_ctas = static_cast<int>(cta_begin.size()) - 1;
+  if (*n_units > max_units || *n_ctas > max_ctas || (max_units && !units_out) || !cta_begin_out)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "plan needs %d units and %d CTAs", *n_units, *n_ctas);
+  for (size_t x = 0; x < by_cta.size(); ++x) {
+    const PrefillUnit& u = by_cta[x];
+    int32_t* o = units_out + 8 * x;
+    o[0] = u.tok0;
+    o[1] = u.ntok;
+    o[2] = u.head;
+    o[3] = u.local;
+    o[4] = u.kt0;
+    o[5] = u.kt1;
+    o[6] = u.klo;
+    o[7] = u.khi;
+  }
+  for (int c = 0; c <= *n_ctas; ++c) cta_begin_out[c] = cta_begin[c];
   return SEGKV_OK;
 }
 

@@ -372,6 +372,25 @@ const char* segkv_last_error(segkv_t h);
 int segkv_decode_attn_noalloc(segkv_t h, int layer, const void* q, const int32_t* seq_lens,
                               const int32_t* seq_ids, int n, void* o, segkv_stream_t stream);
 
+/* segkv_plan_prefill — the work plan that segkv_prefill_attn would use,
+ * computed on the host only (no device work; host-only handles work too), for
+ * tests and tools. A unit is one KV head x the query rows of two 128-row tiles
+ * (2 x 128 / G tokens of one sequence); units are dealt to num_ctas lists by
+ * longest-processing-time-first and grouped by list.
+ *   num_ctas    > 0: plan for that many CTAs; otherwise one per SM.
+ *   units       host int32 [max_units][8], out: first token (index into the
+ *               call's packed tokens), tokens, KV head, 1 if local, key tiles
+ *               kt0 .. kt1 (128 keys each), lowest and highest key any of
+ *               its rows sees.
+ *   cta_begin   host int32 [max_ctas + 1], out: list c holds units
+ *               cta_begin[c] .. cta_begin[c + 1] - 1.
+ *   n_units, n_ctas  out: the plan's sizes, written even when an output
+ *               array is too small (then SEGKV_ERR_INVALID_ARG).
+ * Errors: those of segkv_prefill_attn for the same arguments. */
+int segkv_plan_prefill(segkv_t h, int layer, const int32_t* cu_seqlens, const int32_t* q_pos,
+                       const int32_t* seq_ids, int n, int num_ctas, int32_t* units, int max_units,
+                       int32_t* cta_begin, int max_ctas, int* n_units, int* n_ctas);
+
 /* segkv_plan_decode — the work plan that segkv_decode_attn (T = 1) or
  * segkv_decode_attn_multi would use for the T newest tokens of n sequences,
  * computed on the host only (no device work; host-only handles work too), for

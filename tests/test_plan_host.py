@@ -1,14 +1,19 @@
-"""Decode work plans on the host, without a GPU.
+"""Work plans on the host, without a GPU.
 
 `segkv_plan_decode` returns the plan a decode call would launch: the
 (sequence, KV head) key ranges cut stream-K style into units, grouped by CTA.
-The checks here pin what the plan must be for the kernels to be right and
+The checks pin what the plan must be for the kernels to be right and
 balanced:
 - every kept key a query row needs is in exactly one unit;
 - a pair's units are consecutive and in key order, and carry the pair's
   bookkeeping;
 - each CTA's cost (keys + a charge per unit + a charge per split piece) stays
   within one unit's charges of the most loaded CTA.
+
+`segkv_plan_prefill` returns the prefill plan: one unit per (KV head, chunk of
+two Q tiles' tokens), with the chunk's key range, dealt to CTA lists by LPT.
+The checks pin that every (chunk, head) appears once with the right key
+range, and the LPT bound on the lists' loads.
 """
 import numpy as np
 import pytest
@@ -141,4 +146,71 @@ def test_decode_plan_errors():
     assert h.trim(0, [0]) == 0  # the local head keeps only what position 100 needs
     assert S.segkv_plan_decode(h.handle, 0, 3, [100], [0], 8)[0] == S.SEGKV_ERR_EVICTED
     rc, units, cta = S.segkv_plan_decode(h.handle, 0, 1, [], [], 8)
+    assert rc == 0 and units.shape == (0, 8)
+
+
+# ---------------------------------------------------------------- prefill
+def prefill_cost(u):
+    return int(u[5] - u[4] + 1) + 2  # key tiles + the per-unit surcharge
+
+
+@pytest.mark.parametrize("G,hkv", [(1, 2), (4, 8), (8, 8), (16, 2)])
+@pytest.mark.parametrize("num_ctas", [152, 7])
+def test_prefill_plan_tiles_every_token_and_head_once_and_is_lpt(G, hkv, num_ctas):
+    hq, d, P = G * hkv, 128, 64
+    hc = [GLOBAL if hd % 4 == 1 else LOCAL for hd in range(hkv)]
+    W = 700
+    rng = np.random.default_rng(G * 31 + num_ctas)
+    lens = [int(x) for x in rng.integers(1, 3000, size=6)] + [1, 4096]
+    h = host_handle(hq, hkv, d, hc, W, P, len(lens), 8192, 4 * 8192)
+    fill(h, lens)
+    # chunked queries: the second half of each sequence, positions shuffled within it
+    cu, qp = [0], []
+    for n in lens:
+        pos = np.arange(n // 2, n, dtype=np.int32)
+        rng.shuffle(pos)
+        qp.extend(pos.tolist())
+        cu.append(cu[-1] + len(pos))
+    ids = list(range(len(lens)))
+    rc, units, cta = S.segkv_plan_prefill(h.handle, 0, cu, qp, ids, num_ctas)
+    assert rc == 0, S.segkv_last_error(h.handle)
+    assert cta[0] == 0 and cta[-1] == units.shape[0] and (np.diff(cta) >= 1).all()
+    assert len(cta) - 1 == min(num_ctas, units.shape[0])
+    unit_tok = 2 * (128 // G)
+    qp = np.array(qp)
+    # every (token chunk, head) exactly once, with the chunk's key range
+    seen = set()
+    for u in units:
+        tok0, ntok, hd, local, kt0, kt1, klo, khi = (int(v) for v in u)
+        i = int(np.searchsorted(cu, tok0, side="right")) - 1
+        assert (tok0 - cu[i]) % unit_tok == 0 and ntok == min(unit_tok, cu[i + 1] - tok0)
+        pos = qp[tok0:tok0 + ntok]
+        assert local == (hc[hd] == LOCAL)
+        assert khi == pos.max() and klo == (max(0, pos.min() - W + 1) if local else 0)
+        assert (kt0, kt1) == (klo // 128, khi // 128)
+        assert (tok0, hd) not in seen
+        seen.add((tok0, hd))
+    want = {(t0, hd) for i in range(len(lens)) for t0 in range(cu[i], cu[i + 1], unit_tok)
+            for hd in range(hkv)}
+    assert seen == want
+    # LPT: each list runs longest first, and the most loaded list exceeds the
+    # least loaded by at most the cost of the last unit it was given
+    loads = []
+    for c in range(len(cta) - 1):
+        costs = [prefill_cost(u) for u in units[cta[c]:cta[c + 1]]]
+        assert costs == sorted(costs, reverse=True)
+        loads.append(sum(costs))
+    worst = int(np.argmax(loads))
+    last = prefill_cost(units[cta[worst + 1] - 1])
+    assert max(loads) - last <= min(loads)
+
+
+def test_prefill_plan_errors():
+    h = host_handle(8, 2, 64, [GLOBAL, LOCAL], 16, 16, 2, 512, 64)
+    fill(h, [100, 5])
+    assert S.segkv_plan_prefill(h.handle, 0, [0, 2], [99, 100], [0], 8)[0] == S.SEGKV_ERR_INVALID_ARG
+    assert S.segkv_plan_prefill(h.handle, 0, [0, 1], [0], [3], 8)[0] == S.SEGKV_ERR_INVALID_ARG
+    assert h.trim(0, [0]) == 0
+    assert S.segkv_plan_prefill(h.handle, 0, [0, 1], [50], [0], 8)[0] == S.SEGKV_ERR_EVICTED
+    rc, units, cta = S.segkv_plan_prefill(h.handle, 0, [0], [], [], 8)
     assert rc == 0 and units.shape == (0, 8)
