@@ -525,19 +525,27 @@ int segkv_append(segkv_t h, int layer, const void* k, const void* v, const int32
 static int prefill_validate(segkv* h, int layer, const int32_t* cu_seqlens, const int32_t* q_pos,
                             const int32_t* seq_ids, int n) {
   const int W = h->win[layer];
-  // validate positions and kept keys
   for (int i = 0; i < n; ++i) {
     const int b = seq_ids[i];
     const int32_t nlen = h->len[h->lidx(layer, b)];
+    if (cu_seqlens[i + 1] == cu_seqlens[i]) continue;
+    // positions in range; the lowest one needs the oldest keys
+    int32_t pmin = q_pos[cu_seqlens[i]];
+    int32_t tmin = cu_seqlens[i];
     for (int32_t t = cu_seqlens[i]; t < cu_seqlens[i + 1]; ++t) {
       const int32_t p = q_pos[t];
       if (p < 0 || p >= nlen)
         return fail(h, SEGKV_ERR_INVALID_ARG, "q_pos[%d]=%d outside [0,%d) of seq %d", t, p, nlen, b);
-      for (int hd = 0; hd < h->Hkv; ++hd) {
-        const int32_t need = h->local(layer, hd) ? std::max(0, p - W + 1) : 0;
-        if (need < h->start[h->seg(layer, hd, b)])
-          return fail(h, SEGKV_ERR_EVICTED, "seq %d head %d: key %d already evicted", b, hd, need);
+      if (p < pmin) {
+        pmin = p;
+        tmin = t;
       }
+    }
+    (void)tmin;
+    for (int hd = 0; hd < h->Hkv; ++hd) {
+      const int32_t need = h->local(layer, hd) ? std::max(0, pmin - W + 1) : 0;
+      if (need < h->start[h->seg(layer, hd, b)])
+        return fail(h, SEGKV_ERR_EVICTED, "seq %d head %d: key %d already evicted", b, hd, need);
     }
   }
   return SEGKV_OK;
@@ -552,6 +560,11 @@ static void prefill_plan(segkv* h, int layer, const int32_t* cu_seqlens, const i
   // units: (KV head, two Q tiles of 128/G tokens each), LPT order
   const int unit_tok = prefill_unit_tokens(h->G);
   std::vector<PrefillUnit> units;
+  {
+    int64_t count = 0;
+    for (int i = 0; i < n; ++i) count += (cu_seqlens[i + 1] - cu_seqlens[i] + unit_tok - 1) / unit_tok;
+    units.reserve(static_cast<size_t>(count) * h->Hkv);
+  }
   for (int i = 0; i < n; ++i) {
     const int b = seq_ids[i];
     const int32_t nlen = h->len[h->lidx(layer, b)];
@@ -585,30 +598,45 @@ static void prefill_plan(segkv* h, int layer, const int32_t* cu_seqlens, const i
   // and draining the pipeline and the output epilogue. Each CTA then runs its
   // own list, longest first.
   constexpr int64_t kPrefillUnitCost = 2;
-  std::stable_sort(units.begin(), units.end(), [](const PrefillUnit& a, const PrefillUnit& b) {
-    return (a.kt1 - a.kt0) > (b.kt1 - b.kt0);
-  });
+  // descending key tiles, stable: a counting sort on the tile count
+  int32_t max_tiles = 0;
+  for (const PrefillUnit& u : units) max_tiles = std::max(max_tiles, u.kt1 - u.kt0);
+  std::vector<int32_t> order(units.size()), start(static_cast<size_t>(max_tiles) + 2, 0);
+  for (const PrefillUnit& u : units) ++start[max_tiles - (u.kt1 - u.kt0) + 1];
+  for (size_t c = 1; c < start.size(); ++c) start[c] += start[c - 1];
+  for (size_t x = 0; x < units.size(); ++x)
+    order[start[max_tiles - (units[x].kt1 - units[x].kt0)]++] = static_cast<int32_t>(x);
   const int grid = static_cast<int>(std::min<int64_t>(units.size(), ctas));
   std::vector<int32_t> cta_of(units.size());
   cta_begin.assign(grid + 1, 0);
   {
-    using Load = std::pair<int64_t, int32_t>;  // (work so far, CTA)
-    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
-    for (int c = 0; c < grid; ++c) least.push({0, c});
-    for (size_t x = 0; x < units.size(); ++x) {
-      Load l = least.top();
-      least.pop();
-      cta_of[x] = l.second;
-      ++cta_begin[l.second + 1];
-      l.first += units[x].kt1 - units[x].kt0 + 1 + kPrefillUnitCost;
-      least.push(l);
+    // min-heap of (work so far << 16 | CTA): the root is the least loaded CTA
+    // (lowest index on ties); each unit replaces the root and sifts it down
+    std::vector<uint64_t> heap(static_cast<size_t>(grid));
+    for (int c = 0; c < grid; ++c) heap[c] = static_cast<uint64_t>(c);
+    for (size_t r = 0; r < order.size(); ++r) {
+      const PrefillUnit& u = units[order[r]];
+      const int c = static_cast<int>(heap[0] & 0xffffu);
+      cta_of[r] = c;
+      ++cta_begin[c + 1];
+      const uint64_t key = heap[0] + (static_cast<uint64_t>(u.kt1 - u.kt0 + 1 + kPrefillUnitCost) << 16);
+      size_t i = 0;
+      for (;;) {
+        size_t m = 2 * i + 1;
+        if (m >= heap.size()) break;
+        if (m + 1 < heap.size() && heap[m + 1] < heap[m]) ++m;
+        if (heap[m] >= key) break;
+        heap[i] = heap[m];
+        i = m;
+      }
+      heap[i] = key;
     }
   }
   for (int c = 0; c < grid; ++c) cta_begin[c + 1] += cta_begin[c];
-  by_cta.assign(units.size(), PrefillUnit{});
+  by_cta.resize(units.size());
   {
     std::vector<int32_t> fill(cta_begin.begin(), cta_begin.end() - 1);
-    for (size_t x = 0; x < units.size(); ++x) by_cta[fill[cta_of[x]]++] = units[x];
+    for (size_t r = 0; r < order.size(); ++r) by_cta[fill[cta_of[r]]++] = units[order[r]];
   }
 
 }
