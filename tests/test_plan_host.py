@@ -47,6 +47,9 @@ def check_plan(units, cta, lens, hc, W, T, d, G, num_ctas):
     assert cta[0] == 0 and cta[-1] == n_units and (np.diff(cta) >= 1).all()
     assert len(cta) - 1 <= num_ctas
     hkv = len(hc)
+    # each CTA boundary splits at most one range, so the workspace bound
+    # (one partial slot per pair plus one per CTA) always holds
+    assert n_units <= len(lens) * hkv + (len(cta) - 1) - 1
     # coverage, order and bookkeeping per (sequence index, head)
     for i, n in enumerate(lens):
         for hd in range(hkv):
