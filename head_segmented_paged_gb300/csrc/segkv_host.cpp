@@ -164,6 +164,20 @@ struct Pack {
 
 }  // namespace
 
+// One (sequence, KV head) key range of a decode call, and the plan cut from
+// them. A handle keeps one plan and reuses its storage from call to call.
+struct DecodeRange { int32_t req, head, lo, n, row, local; };
+struct DecodePlan {
+  std::vector<DecodeRange> ranges;
+  std::vector<int64_t> keys;  // per range: its key count, n - lo
+  std::vector<DecodeUnit> units;
+  std::vector<int32_t> unit_pair;  // per unit: its range
+  std::vector<int32_t> cta_begin;
+  std::vector<int32_t> pair_unit0, pair_units;  // per range
+  int grid = 0, rows = 0;
+  bool mma = false;
+};
+
 struct segkv {
   int L = 0, Hq = 0, Hkv = 0, D = 0, G = 0, P = 0, S = 0, max_len = 0, R = 0;
   int64_t num_pages = 0;
@@ -191,6 +205,7 @@ struct segkv {
   int debug = 0;
   bool window_fa = false;  // win[] holds W+1 for the FlashAttention convention
   int64_t upload_bytes = 0;
+  DecodePlan dplan;  // the last decode plan (storage reused)
   std::string err;
 
   size_t seg(int l, int h, int b) const { return (static_cast<size_t>(l) * Hkv + h) * S + b; }
@@ -883,16 +898,39 @@ static int decode_mma_launch(segkv* h, int layer, const void* q, int T, int n, v
   return SEGKV_OK;
 }
 
-// One (sequence, KV head) key range of a decode call, and the plan cut from them.
-struct DecodeRange { int32_t req, head, lo, n, row, local; };
-struct DecodePlan {
-  std::vector<DecodeRange> ranges;
-  std::vector<DecodeUnit> units;
-  std::vector<int32_t> cta_begin;
-  std::vector<int32_t> pair_unit0, pair_units;  // per range
-  int grid = 0, rows = 0;
-  bool mma = false;
-};
+// Whether the greedy stream-K cut of decode_plan, with per-CTA budget B, fits
+// in max_grid CTAs. The same walk as the cut that emits the units, over the
+// ranges' key counts alone, given up as soon as the grid is full.
+static bool decode_cut_fits(const int64_t* keys, int64_t nr, int64_t B, int64_t unit_cost,
+                            int64_t split_cost, int64_t max_grid) {
+  int64_t used = 0, r = 0, off = 0;
+  while (r < nr) {
+    if (++used > max_grid) return false;
+    int64_t cost = 0;
+    bool any = false;
+    while (r < nr) {
+      const int64_t avail = keys[r] - off;  // >= 1
+      int64_t room = B - cost - unit_cost;
+      const bool whole = off == 0 && avail <= room;
+      if (!whole) room -= split_cost;
+      if (room < 1) {
+        if (!any) return false;  // B cannot hold even one key
+        break;
+      }
+      const int64_t take = avail < room ? avail : room;
+      cost += unit_cost + (whole ? 0 : split_cost) + take;
+      any = true;
+      if (take == avail) {
+        ++r;
+        off = 0;
+      } else {
+        off += take;
+        break;  // this CTA's budget is spent
+      }
+    }
+  }
+  return true;
+}
 
 // The split-KV decode plan of the T newest tokens of n sequences (host only):
 // the (sequence, KV head) key ranges cut into units, grouped by CTA. ctas > 0
@@ -903,7 +941,11 @@ static int decode_plan(segkv* h, int layer, int T, const int32_t* seq_lens, cons
   const int rows = T * h->G;
   // pairs (req, head) with their key ranges [lo, n)
   std::vector<DecodeRange>& ranges = P.ranges;
+  std::vector<int64_t>& keys = P.keys;
   ranges.clear();
+  keys.clear();
+  ranges.reserve(static_cast<size_t>(n) * h->Hkv);
+  keys.reserve(static_cast<size_t>(n) * h->Hkv);
   int64_t total = 0;
   for (int i = 0; i < n; ++i) {
     const int b = seq_ids[i];
@@ -918,6 +960,7 @@ static int decode_plan(segkv* h, int layer, int T, const int32_t* seq_lens, cons
       if (lo < h->start[h->seg(layer, hd, b)])
         return fail(h, SEGKV_ERR_EVICTED, "seq %d head %d: key %d already evicted", b, hd, lo);
       ranges.push_back({i, hd, lo, nlen, static_cast<int32_t>(h->seg(layer, hd, b)), local});
+      keys.push_back(nlen - lo);
       total += nlen - lo;
     }
   }
@@ -949,83 +992,81 @@ static int decode_plan(segkv* h, int layer, int T, const int32_t* seq_lens, cons
       std::min<int64_t>(ctas, ctas_override > 0 ? ctas_override : decode_max_grid(h)),
       (total + sk - 1) / sk)));
   std::vector<DecodeUnit>& units = P.units;
+  std::vector<int32_t>& unit_pair = P.unit_pair;
   std::vector<int32_t>& pair_unit0 = P.pair_unit0;
   std::vector<int32_t>& pair_units = P.pair_units;
   std::vector<int32_t>& cta_begin = P.cta_begin;
-  units.clear();
-  cta_begin.clear();
-  pair_unit0.assign(ranges.size(), 0);
-  pair_units.assign(ranges.size(), 0);
-  std::vector<int32_t> unit_pair;  // ranges are pushed per (req, head): pair r = req * Hkv + head
-  // Greedy cut with budget T per CTA; returns the CTAs used (INT32_MAX if T is
-  // too small to hold even one key), emitting the units when asked.
-  auto cut = [&](int64_t T, bool emit) -> int64_t {
-    int64_t used = 0;
-    size_t r = 0;
-    int64_t off = 0;
-    while (r < ranges.size()) {
-      if (emit) cta_begin.push_back(static_cast<int32_t>(units.size()));
-      int64_t cost = 0;
-      bool any = false;
-      while (r < ranges.size()) {
-        const DecodeRange& R = ranges[r];
-        const int64_t avail = R.n - R.lo - off;
-        int64_t room = T - cost - kDecodeUnitCost;
-        if (room < 1) {
-          if (!any) return INT32_MAX;
-          break;
-        }
-        // a piece of a split pair also writes partials and may merge
-        const bool whole = off == 0 && avail <= room;
-        if (!whole) room -= kDecodeSplitCost;
-        if (room < 1) {
-          if (!any) return INT32_MAX;
-          break;
-        }
-        const int64_t take = std::min(avail, room);
-        if (emit) {
-          if (off == 0) pair_unit0[r] = static_cast<int32_t>(units.size());
-          DecodeUnit u{};
-          u.req = R.req;
-          u.head = static_cast<int16_t>(R.head);
-          u.local = static_cast<int16_t>(R.local);
-          u.k0 = static_cast<int32_t>(R.lo + off);
-          u.k1 = static_cast<int32_t>(R.lo + off + take);
-          u.table_row = R.row;
-          u.q_last = R.n - 1;
-          units.push_back(u);
-          unit_pair.push_back(static_cast<int32_t>(r));
-          ++pair_units[r];
-        }
-        cost += kDecodeUnitCost + (whole ? 0 : kDecodeSplitCost) + take;
-        any = true;
-        off += take;
-        if (take == avail) {
-          ++r;
-          off = 0;
-        } else {
-          break;  // this CTA's budget is spent
-        }
-      }
-      ++used;
-    }
-    return used;
-  };
+  const int64_t nr = static_cast<int64_t>(ranges.size());
   // Every CTA costs at most the budget, so the budget is at least the total
   // cost over the grid; the greedy cut leaves each CTA short of the budget by
   // less than a unit and a split surcharge, so a budget a little above that
   // bound usually fits. Probing it first narrows the bisection to a few steps.
-  const int64_t nr = static_cast<int64_t>(ranges.size());
   int64_t lo = std::max<int64_t>(1, (total + kDecodeUnitCost * nr) / max_grid);
   int64_t hi = total + kDecodeUnitCost * (nr + 1);  // one CTA holds everything
+  auto fits = [&](int64_t B) {
+    return decode_cut_fits(keys.data(), nr, B, kDecodeUnitCost, kDecodeSplitCost, max_grid);
+  };
   const int64_t probe = lo + lo / 8 + 2 * (kDecodeUnitCost + kDecodeSplitCost);
-  if (probe < hi && cut(probe, false) <= max_grid) hi = probe;
+  if (probe < hi && fits(probe)) hi = probe;
   while (lo < hi) {  // smallest budget that fits max_grid CTAs
     const int64_t mid = lo + (hi - lo) / 2;
-    if (cut(mid, false) <= max_grid) hi = mid;
+    if (fits(mid)) hi = mid;
     else lo = mid + 1;
   }
-  const int grid = static_cast<int>(cut(lo, true));
+  // The greedy cut with that budget, emitting the units. A CTA takes whole
+  // ranges while they fit, then a piece of the next one, which pays the split
+  // surcharge (a piece also writes partials and may merge).
+  units.clear();
+  unit_pair.clear();
+  cta_begin.clear();
+  units.reserve(static_cast<size_t>(nr + max_grid));
+  unit_pair.reserve(static_cast<size_t>(nr + max_grid));
+  cta_begin.reserve(static_cast<size_t>(max_grid) + 1);
+  pair_unit0.assign(static_cast<size_t>(nr), 0);
+  pair_units.assign(static_cast<size_t>(nr), 0);
+  {
+    const int64_t B = lo;
+    int64_t r = 0, off = 0;
+    while (r < nr) {
+      cta_begin.push_back(static_cast<int32_t>(units.size()));
+      int64_t cost = 0;
+      while (r < nr) {
+        const DecodeRange& R = ranges[r];
+        const int64_t avail = keys[r] - off;
+        int64_t room = B - cost - kDecodeUnitCost;
+        const bool whole = off == 0 && avail <= room;
+        if (!whole) room -= kDecodeSplitCost;
+        if (room < 1) {
+          if (cost == 0)  // cannot happen: B was found to fit
+            return fail(h, SEGKV_ERR_INVALID_ARG, "decode plan: budget %lld holds no key",
+                        static_cast<long long>(B));
+          break;
+        }
+        const int64_t take = std::min(avail, room);
+        if (off == 0) pair_unit0[r] = static_cast<int32_t>(units.size());
+        DecodeUnit u{};
+        u.req = R.req;
+        u.head = static_cast<int16_t>(R.head);
+        u.local = static_cast<int16_t>(R.local);
+        u.k0 = static_cast<int32_t>(R.lo + off);
+        u.k1 = static_cast<int32_t>(R.lo + off + take);
+        u.table_row = R.row;
+        u.q_last = R.n - 1;
+        units.push_back(u);
+        unit_pair.push_back(static_cast<int32_t>(r));
+        ++pair_units[r];
+        cost += kDecodeUnitCost + (whole ? 0 : kDecodeSplitCost) + take;
+        if (take == avail) {
+          ++r;
+          off = 0;
+        } else {
+          off += take;
+          break;  // this CTA's budget is spent
+        }
+      }
+    }
+  }
+  const int grid = static_cast<int>(cta_begin.size());
   cta_begin.push_back(static_cast<int32_t>(units.size()));
   for (size_t x = 0; x < units.size(); ++x) {
     units[x].pair_unit0 = pair_unit0[unit_pair[x]];
@@ -1043,7 +1084,7 @@ static int decode_core(segkv* h, int layer, const void* q, int T, const int32_t*
                        const int32_t* seq_ids, int n, void* o, float* lse, void* workspace,
                        size_t workspace_bytes, cudaStream_t s) {
   const int W = h->win[layer];
-  DecodePlan P;
+  DecodePlan& P = h->dplan;
   const int prc = decode_plan(h, layer, T, seq_lens, seq_ids, n, 0, P);
   if (prc != SEGKV_OK) return prc;
   const std::vector<DecodeRange>& ranges = P.ranges;
@@ -1230,7 +1271,7 @@ int segkv_plan_decode(segkv_t h, int layer, int T, const int32_t* seq_lens, cons
   *n_ctas = 0;
   if (n == 0) return SEGKV_OK;
   if (!seq_lens) return fail(h, SEGKV_ERR_INVALID_ARG, "seq_lens NULL");
-  DecodePlan P;
+  DecodePlan& P = h->dplan;
   const int rc = decode_plan(h, layer, T, seq_lens, seq_ids, n, num_ctas, P);
   if (rc != SEGKV_OK) return rc;
   *n_units = static_cast<int>(P.units.size());
