@@ -171,7 +171,6 @@ struct DecodePlan {
   std::vector<DecodeRange> ranges;
   std::vector<int64_t> keys;  // per range: its key count, n - lo
   std::vector<DecodeUnit> units;
-  std::vector<int32_t> unit_pair;  // per unit: its range
   std::vector<int32_t> cta_begin;
   std::vector<int32_t> pair_unit0, pair_units;  // per range
   int grid = 0, rows = 0;
@@ -992,7 +991,6 @@ static int decode_plan(segkv* h, int layer, int T, const int32_t* seq_lens, cons
       std::min<int64_t>(ctas, ctas_override > 0 ? ctas_override : decode_max_grid(h)),
       (total + sk - 1) / sk)));
   std::vector<DecodeUnit>& units = P.units;
-  std::vector<int32_t>& unit_pair = P.unit_pair;
   std::vector<int32_t>& pair_unit0 = P.pair_unit0;
   std::vector<int32_t>& pair_units = P.pair_units;
   std::vector<int32_t>& cta_begin = P.cta_begin;
@@ -1017,13 +1015,11 @@ static int decode_plan(segkv* h, int layer, int T, const int32_t* seq_lens, cons
   // ranges while they fit, then a piece of the next one, which pays the split
   // surcharge (a piece also writes partials and may merge).
   units.clear();
-  unit_pair.clear();
   cta_begin.clear();
   units.reserve(static_cast<size_t>(nr + max_grid));
-  unit_pair.reserve(static_cast<size_t>(nr + max_grid));
   cta_begin.reserve(static_cast<size_t>(max_grid) + 1);
-  pair_unit0.assign(static_cast<size_t>(nr), 0);
-  pair_units.assign(static_cast<size_t>(nr), 0);
+  pair_unit0.resize(static_cast<size_t>(nr));
+  pair_units.resize(static_cast<size_t>(nr));
   {
     const int64_t B = lo;
     int64_t r = 0, off = 0;
@@ -1053,10 +1049,14 @@ static int decode_plan(segkv* h, int layer, int T, const int32_t* seq_lens, cons
         u.table_row = R.row;
         u.q_last = R.n - 1;
         units.push_back(u);
-        unit_pair.push_back(static_cast<int32_t>(r));
-        ++pair_units[r];
         cost += kDecodeUnitCost + (whole ? 0 : kDecodeSplitCost) + take;
-        if (take == avail) {
+        if (take == avail) {  // the pair is complete: its units learn their count
+          const int32_t u0 = pair_unit0[r], cnt = static_cast<int32_t>(units.size()) - u0;
+          pair_units[r] = cnt;
+          for (int32_t x = u0; x < u0 + cnt; ++x) {
+            units[x].pair_unit0 = u0;
+            units[x].pair_units = cnt;
+          }
           ++r;
           off = 0;
         } else {
@@ -1068,10 +1068,6 @@ static int decode_plan(segkv* h, int layer, int T, const int32_t* seq_lens, cons
   }
   const int grid = static_cast<int>(cta_begin.size());
   cta_begin.push_back(static_cast<int32_t>(units.size()));
-  for (size_t x = 0; x < units.size(); ++x) {
-    units[x].pair_unit0 = pair_unit0[unit_pair[x]];
-    units[x].pair_units = pair_units[unit_pair[x]];
-  }
   P.grid = grid;
   P.rows = rows;
   P.mma = mma;
