@@ -177,6 +177,15 @@ struct DecodePlan {
   bool mma = false;
 };
 
+// The prefill plan and its scratch; a handle keeps one and reuses its storage.
+struct PrefillPlan {
+  std::vector<PrefillUnit> units;   // in building order
+  std::vector<PrefillUnit> by_cta;  // the plan: grouped by CTA, each list longest first
+  std::vector<int32_t> cta_begin;   // [grid + 1]
+  std::vector<int32_t> order, count, cta_of, fill;
+  std::vector<uint64_t> tree;       // LPT: winner tree over the CTAs' (load << 16 | CTA)
+};
+
 struct segkv {
   int L = 0, Hq = 0, Hkv = 0, D = 0, G = 0, P = 0, S = 0, max_len = 0, R = 0;
   int64_t num_pages = 0;
@@ -204,7 +213,9 @@ struct segkv {
   int debug = 0;
   bool window_fa = false;  // win[] holds W+1 for the FlashAttention convention
   int64_t upload_bytes = 0;
-  DecodePlan dplan;  // the last decode plan (storage reused)
+  DecodePlan dplan;   // the last decode plan (storage reused)
+  PrefillPlan pplan;  // the last prefill plan (storage reused)
+  Pack pack;          // staging of a plan upload (storage reused)
   std::string err;
 
   size_t seg(int l, int h, int b) const { return (static_cast<size_t>(l) * Hkv + h) * S + b; }
@@ -566,14 +577,16 @@ static int prefill_validate(segkv* h, int layer, const int32_t* cu_seqlens, cons
 }
 
 // The prefill work plan (host): units of one KV head x the Q tiles of a
-// chunk of tokens, scheduled onto `ctas` lists by LPT and grouped by list.
+// chunk of tokens, scheduled onto `ctas` lists by LPT and grouped by list,
+// into h->pplan (by_cta, cta_begin).
 static void prefill_plan(segkv* h, int layer, const int32_t* cu_seqlens, const int32_t* q_pos,
-                         const int32_t* seq_ids, int n, int ctas, std::vector<PrefillUnit>& by_cta,
-                         std::vector<int32_t>& cta_begin) {
+                         const int32_t* seq_ids, int n, int ctas) {
+  PrefillPlan& P = h->pplan;
   const int W = h->win[layer];
   // units: (KV head, two Q tiles of 128/G tokens each), LPT order
   const int unit_tok = prefill_unit_tokens(h->G);
-  std::vector<PrefillUnit> units;
+  std::vector<PrefillUnit>& units = P.units;
+  units.clear();
   {
     int64_t count = 0;
     for (int i = 0; i < n; ++i) count += (cu_seqlens[i + 1] - cu_seqlens[i] + unit_tok - 1) / unit_tok;
@@ -607,6 +620,7 @@ static void prefill_plan(segkv* h, int layer, const int32_t* cu_seqlens, const i
       }
     }
   }
+  const size_t nu = units.size();
   // LPT schedule: units in descending cost, each to the CTA with the least
   // work so far; a unit costs its key tiles plus kPrefillUnitCost for filling
   // and draining the pipeline and the output epilogue. Each CTA then runs its
@@ -615,44 +629,52 @@ static void prefill_plan(segkv* h, int layer, const int32_t* cu_seqlens, const i
   // descending key tiles, stable: a counting sort on the tile count
   int32_t max_tiles = 0;
   for (const PrefillUnit& u : units) max_tiles = std::max(max_tiles, u.kt1 - u.kt0);
-  std::vector<int32_t> order(units.size()), start(static_cast<size_t>(max_tiles) + 2, 0);
+  std::vector<int32_t>& order = P.order;
+  std::vector<int32_t>& start = P.count;
+  order.resize(nu);
+  start.assign(static_cast<size_t>(max_tiles) + 2, 0);
   for (const PrefillUnit& u : units) ++start[max_tiles - (u.kt1 - u.kt0) + 1];
   for (size_t c = 1; c < start.size(); ++c) start[c] += start[c - 1];
-  for (size_t x = 0; x < units.size(); ++x)
+  for (size_t x = 0; x < nu; ++x)
     order[start[max_tiles - (units[x].kt1 - units[x].kt0)]++] = static_cast<int32_t>(x);
-  const int grid = static_cast<int>(std::min<int64_t>(units.size(), ctas));
-  std::vector<int32_t> cta_of(units.size());
+  const int grid = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(nu), ctas));
+  std::vector<int32_t>& cta_of = P.cta_of;
+  std::vector<int32_t>& cta_begin = P.cta_begin;
+  cta_of.resize(nu);
   cta_begin.assign(grid + 1, 0);
   {
-    // min-heap of (work so far << 16 | CTA): the root is the least loaded CTA
-    // (lowest index on ties); each unit replaces the root and sifts it down
-    std::vector<uint64_t> heap(static_cast<size_t>(grid));
-    for (int c = 0; c < grid; ++c) heap[c] = static_cast<uint64_t>(c);
-    for (size_t r = 0; r < order.size(); ++r) {
+    // winner tree over (work so far << 16 | CTA), leaves padded to a power of
+    // two with the largest key: the root is the least loaded CTA (lowest index
+    // on ties); each unit raises its CTA's leaf and the path above it is redone
+    size_t leaves = 1;
+    while (leaves < static_cast<size_t>(grid)) leaves <<= 1;
+    std::vector<uint64_t>& tree = P.tree;
+    tree.assign(2 * leaves, ~0ull);
+    for (int c = 0; c < grid; ++c) tree[leaves + c] = static_cast<uint64_t>(c);
+    for (size_t i = leaves - 1; i >= 1; --i) tree[i] = std::min(tree[2 * i], tree[2 * i + 1]);
+    for (size_t r = 0; r < nu; ++r) {
       const PrefillUnit& u = units[order[r]];
-      const int c = static_cast<int>(heap[0] & 0xffffu);
+      const uint64_t root = tree[1];
+      const int c = static_cast<int>(root & 0xffffu);
       cta_of[r] = c;
       ++cta_begin[c + 1];
-      const uint64_t key = heap[0] + (static_cast<uint64_t>(u.kt1 - u.kt0 + 1 + kPrefillUnitCost) << 16);
-      size_t i = 0;
-      for (;;) {
-        size_t m = 2 * i + 1;
-        if (m >= heap.size()) break;
-        if (m + 1 < heap.size() && heap[m + 1] < heap[m]) ++m;
-        if (heap[m] >= key) break;
-        heap[i] = heap[m];
-        i = m;
+      size_t i = leaves + static_cast<size_t>(c);
+      uint64_t v = root + (static_cast<uint64_t>(u.kt1 - u.kt0 + 1 + kPrefillUnitCost) << 16);
+      tree[i] = v;
+      for (; i > 1; i >>= 1) {  // each node on the path: the smaller of its two children
+        v = std::min(v, tree[i ^ 1]);
+        tree[i >> 1] = v;
       }
-      heap[i] = key;
     }
   }
   for (int c = 0; c < grid; ++c) cta_begin[c + 1] += cta_begin[c];
-  by_cta.resize(units.size());
+  std::vector<PrefillUnit>& by_cta = P.by_cta;
+  by_cta.resize(nu);
   {
-    std::vector<int32_t> fill(cta_begin.begin(), cta_begin.end() - 1);
-    for (size_t r = 0; r < order.size(); ++r) by_cta[fill[cta_of[r]]++] = units[order[r]];
+    std::vector<int32_t>& fill = P.fill;
+    fill.assign(cta_begin.begin(), cta_begin.end() - 1);
+    for (size_t r = 0; r < nu; ++r) by_cta[fill[cta_of[r]]++] = units[order[r]];
   }
-
 }
 
 int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_seqlens,
@@ -680,13 +702,14 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
   }
   const int W = h->win[layer];
   const int tpt = kRowsPerTile / h->G;
-  std::vector<PrefillUnit> by_cta;
-  std::vector<int32_t> cta_begin;
-  prefill_plan(h, layer, cu_seqlens, q_pos, seq_ids, n, h->num_sms, by_cta, cta_begin);
+  prefill_plan(h, layer, cu_seqlens, q_pos, seq_ids, n, h->num_sms);
+  const std::vector<PrefillUnit>& by_cta = h->pplan.by_cta;
+  const std::vector<int32_t>& cta_begin = h->pplan.cta_begin;
   const int grid = static_cast<int>(cta_begin.size()) - 1;
   const size_t n_units = by_cta.size();
 
-  Pack pk;
+  Pack& pk = h->pack;
+  pk.buf.clear();
   const size_t o_units = pk.add(by_cta.data(), by_cta.size());
   const size_t o_cta = pk.add(cta_begin.data(), cta_begin.size());
   const size_t o_pos = pk.add(q_pos, static_cast<size_t>(total));
@@ -761,10 +784,10 @@ int segkv_plan_prefill(segkv_t h, int layer, const int32_t* cu_seqlens, const in
   if (!q_pos) return fail(h, SEGKV_ERR_INVALID_ARG, "q_pos NULL");
   const int vrc = prefill_validate(h, layer, cu_seqlens, q_pos, seq_ids, n);
   if (vrc != SEGKV_OK) return vrc;
-  std::vector<PrefillUnit> by_cta;
-  std::vector<int32_t> cta_begin;
   const int ctas = num_ctas > 0 ? num_ctas : (h->num_sms > 0 ? h->num_sms : 1);
-  prefill_plan(h, layer, cu_seqlens, q_pos, seq_ids, n, ctas, by_cta, cta_begin);
+  prefill_plan(h, layer, cu_seqlens, q_pos, seq_ids, n, ctas);
+  const std::vector<PrefillUnit>& by_cta = h->pplan.by_cta;
+  const std::vector<int32_t>& cta_begin = h->pplan.cta_begin;
   *n_units = static_cast<int>(by_cta.size());
   *n_ctas = static_cast<int>(cta_begin.size()) - 1;
   if (*n_units > max_units || *n_ctas > max_ctas || (max_units && !units_out) || !cta_begin_out)
