@@ -217,3 +217,77 @@ def test_prefill_plan_errors():
     assert S.segkv_plan_prefill(h.handle, 0, [0, 1], [50], [0], 8)[0] == S.SEGKV_ERR_EVICTED
     rc, units, cta = S.segkv_plan_prefill(h.handle, 0, [0], [], [], 8)
     assert rc == 0 and units.shape == (0, 8)
+
+
+def replay_lpt(units, num_ctas):
+    """The LPT schedule replayed from its definition: units in building order
+    (token chunk, then KV head), stably sorted by key tiles, longest first;
+    each goes to the least loaded list, the lowest index on ties."""
+    build = sorted(range(len(units)), key=lambda x: (int(units[x][0]), int(units[x][2])))
+    order = sorted(build, key=lambda x: -int(units[x][5] - units[x][4]))
+    grid = min(num_ctas, len(units))
+    loads = np.zeros(grid, np.int64)
+    lists = [[] for _ in range(grid)]
+    for x in order:
+        c = int(np.argmin(loads))  # first minimum: the lowest index on ties
+        lists[c].append(x)
+        loads[c] += prefill_cost(units[x])
+    return lists
+
+
+@pytest.mark.parametrize("G,hkv,num_ctas", [(4, 8, 152), (8, 8, 7), (1, 2, 3)])
+def test_prefill_plan_is_exactly_the_lpt_schedule(G, hkv, num_ctas):
+    hq, d, P, W = G * hkv, 128, 64, 500
+    hc = [GLOBAL] + [LOCAL] * (hkv - 1)
+    rng = np.random.default_rng(G + 5 * hkv + num_ctas)
+    lens = [int(x) for x in rng.integers(1, 5000, size=5)]
+    h = host_handle(hq, hkv, d, hc, W, P, len(lens), 8192, 4 * 8192)
+    fill(h, lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    qp = np.concatenate([np.arange(n) for n in lens]).astype(np.int32)
+    rc, units, cta = S.segkv_plan_prefill(h.handle, 0, cu, qp, list(range(len(lens))), num_ctas)
+    assert rc == 0, S.segkv_last_error(h.handle)
+    lists = replay_lpt(units, num_ctas)
+    assert len(cta) - 1 == len(lists)
+    for c, want in enumerate(lists):
+        got = units[cta[c]:cta[c + 1]]
+        assert got.shape[0] == len(want)
+        assert (got == units[want]).all(), c
+
+
+def test_plans_on_a_reused_handle_match_fresh_handles():
+    """A handle keeps its plan storage from call to call: a large plan, then a
+    small one, then the large one again must each equal the plan a fresh
+    handle makes."""
+    hq, hkv, d, W, P = 32, 8, 128, 1024, 64
+    hc = [GLOBAL] + [LOCAL] * 7
+    rng = np.random.default_rng(99)
+    lens = [int(x) for x in rng.integers(2048, 20000, size=12)]
+    small = [0, 5]
+
+    def make():
+        h = host_handle(hq, hkv, d, hc, W, P, len(lens), 20480, 80000)
+        fill(h, lens)
+        return h
+
+    def dec(h, ids, T):
+        rc, u, c = S.segkv_plan_decode(h.handle, 0, T, [lens[b] for b in ids], ids, 152)
+        assert rc == 0
+        return u, c
+
+    def pre(h, ids):
+        cu = np.concatenate([[0], np.cumsum([256 for _ in ids])]).astype(np.int32)
+        qp = np.concatenate([np.arange(lens[b] - 256, lens[b]) for b in ids]).astype(np.int32)
+        rc, u, c = S.segkv_plan_prefill(h.handle, 0, cu, qp, ids, 152)
+        assert rc == 0
+        return u, c
+
+    every = list(range(len(lens)))
+    calls = [(dec, every, 1), (dec, small, 4), (dec, every, 4), (pre, every, None), (pre, small, None),
+             (pre, every, None), (dec, every, 1)]
+    reused = make()
+    for fn, ids, T in calls:
+        args = (ids,) if T is None else (ids, T)
+        u1, c1 = fn(reused, *args)
+        u2, c2 = fn(make(), *args)
+        assert np.array_equal(u1, u2) and np.array_equal(c1, c2)
