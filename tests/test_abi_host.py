@@ -194,3 +194,23 @@ def test_fa_window_convention_equals_inclusive_window_plus_one():
     assert S.segkv_set_window_convention(fa.handle, S.SEGKV_WINDOW_INCLUSIVE) == \
         S.SEGKV_ERR_INVALID_ARG
     assert S.segkv_set_window_convention(fa.handle, 7) == S.SEGKV_ERR_INVALID_ARG
+
+
+def test_plain_c_caller_compiles_against_the_header_and_runs(tmp_path):
+    """`tests/c/abi_host_check.c` includes `include/segkv.h` from C99 (strict,
+    warnings as errors), links the library and drives a host-only handle:
+    append, trim, segment and page counts, a decode plan's key coverage, and
+    refused calls that change nothing."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    exe = str(tmp_path / "abi_host_check")
+    lib_dir = os.path.dirname(S.LIB_PATH)
+    cmd = [cc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+           os.path.join(ROOT, "tests", "c", "abi_host_check.c"), S.LIB_PATH, f"-Wl,-rpath,{lib_dir}", "-o", exe]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
