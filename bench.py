@@ -706,8 +706,12 @@ def run_e2e(args, dev, stream, w, sets, cu, q_pos, step_flops, num_pages):
             "d2h_bytes_per_step": o.numel() * o.element_size(),
             "h2d_gbs_copy_alone": round(h2d_gbs, 1),
             "h2d_ms_per_step_at_that_rate": round(h2d / (h2d_gbs * 1e9) * 1e3, 1),
+            "h2d_gbs_in_step": round(h2d / (ms * 1e-3) / 1e9, 1),
             "note": "pinned host Q/K/V per layer copied in the timed region on a side stream "
-                    "(three rotating device buffers); last layer's O copied back"}
+                    "(three rotating device buffers); last layer's O copied back. The copy-alone "
+                    "rate is one short sample (a layer's Q, K, V twice) taken before the timed "
+                    "steps; on a shared host it can differ from the rate the copies reach inside "
+                    "the step (h2d_gbs_in_step, a lower bound: the copies overlap compute)"}
 
 
 # ------------------------------------------------------------------ oracle (CPU) arm
