@@ -162,6 +162,37 @@ struct Pack {
   }
 };
 
+// The least-loaded list of an LPT schedule: a winner tree over the lists'
+// keys (load << 16 | list), its leaves padded to a power of two with the
+// largest key, so the root is the least loaded list (the lowest index on
+// ties). add() raises one list's load and redoes the path above its leaf,
+// keeping the running minimum in a register. Lists < 65,536, loads < 2^47.
+class LeastLoaded {
+ public:
+  void reset(int lists) {
+    leaves_ = 1;
+    while (leaves_ < static_cast<size_t>(lists)) leaves_ <<= 1;
+    tree_.assign(2 * leaves_, ~0ull);
+    for (int c = 0; c < lists; ++c) tree_[leaves_ + c] = static_cast<uint64_t>(c);
+    for (size_t i = leaves_ - 1; i >= 1; --i) tree_[i] = std::min(tree_[2 * i], tree_[2 * i + 1]);
+  }
+  int least() const { return static_cast<int>(tree_[1] & 0xffffu); }
+  void add(int c, int64_t load) {
+    uint64_t* t = tree_.data();
+    size_t i = leaves_ + static_cast<size_t>(c);
+    uint64_t v = t[i] + (static_cast<uint64_t>(load) << 16);
+    t[i] = v;
+    for (; i > 1; i >>= 1) {  // each node on the path: the smaller of its two children
+      v = std::min(v, t[i ^ 1]);
+      t[i >> 1] = v;
+    }
+  }
+
+ private:
+  std::vector<uint64_t> tree_;
+  size_t leaves_ = 1;
+};
+
 }  // namespace
 
 // One (sequence, KV head) key range of a decode call, and the plan cut from
@@ -183,7 +214,7 @@ struct PrefillPlan {
   std::vector<PrefillUnit> by_cta;  // the plan: grouped by CTA, each list longest first
   std::vector<int32_t> cta_begin;   // [grid + 1]
   std::vector<int32_t> order, count, cta_of, fill;
-  std::vector<uint64_t> tree;       // LPT: winner tree over the CTAs' (load << 16 | CTA)
+  LeastLoaded lpt;
 };
 
 struct segkv {
@@ -643,28 +674,14 @@ static void prefill_plan(segkv* h, int layer, const int32_t* cu_seqlens, const i
   cta_of.resize(nu);
   cta_begin.assign(grid + 1, 0);
   {
-    // winner tree over (work so far << 16 | CTA), leaves padded to a power of
-    // two with the largest key: the root is the least loaded CTA (lowest index
-    // on ties); each unit raises its CTA's leaf and the path above it is redone
-    size_t leaves = 1;
-    while (leaves < static_cast<size_t>(grid)) leaves <<= 1;
-    std::vector<uint64_t>& tree = P.tree;
-    tree.assign(2 * leaves, ~0ull);
-    for (int c = 0; c < grid; ++c) tree[leaves + c] = static_cast<uint64_t>(c);
-    for (size_t i = leaves - 1; i >= 1; --i) tree[i] = std::min(tree[2 * i], tree[2 * i + 1]);
+    LeastLoaded& lpt = P.lpt;
+    lpt.reset(grid);
     for (size_t r = 0; r < nu; ++r) {
       const PrefillUnit& u = units[order[r]];
-      const uint64_t root = tree[1];
-      const int c = static_cast<int>(root & 0xffffu);
+      const int c = lpt.least();
       cta_of[r] = c;
       ++cta_begin[c + 1];
-      size_t i = leaves + static_cast<size_t>(c);
-      uint64_t v = root + (static_cast<uint64_t>(u.kt1 - u.kt0 + 1 + kPrefillUnitCost) << 16);
-      tree[i] = v;
-      for (; i > 1; i >>= 1) {  // each node on the path: the smaller of its two children
-        v = std::min(v, tree[i ^ 1]);
-        tree[i >> 1] = v;
-      }
+      lpt.add(c, u.kt1 - u.kt0 + 1 + kPrefillUnitCost);
     }
   }
   for (int c = 0; c < grid; ++c) cta_begin[c + 1] += cta_begin[c];
@@ -1702,16 +1719,13 @@ int segkv_attn_mass(segkv_t h, int layer, const void* q, const int32_t* cu_seqle
   const int grid = static_cast<int>(std::min<int64_t>(units.size(), h->num_sms));
   std::vector<int32_t> cta_begin(grid + 1, 0), cta_of(units.size());
   {
-    using Load = std::pair<int64_t, int32_t>;
-    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> least;
-    for (int c = 0; c < grid; ++c) least.push({0, c});
+    LeastLoaded lpt;
+    lpt.reset(grid);
     for (size_t x = 0; x < units.size(); ++x) {
-      Load l = least.top();
-      least.pop();
-      cta_of[x] = l.second;
-      ++cta_begin[l.second + 1];
-      l.first += units[x].qt1 - units[x].qt0 + 2;  // + the unit's key-tile load and hand-off
-      least.push(l);
+      const int c = lpt.least();
+      cta_of[x] = c;
+      ++cta_begin[c + 1];
+      lpt.add(c, units[x].qt1 - units[x].qt0 + 2);  // + the unit's key-tile load and hand-off
     }
     for (int c = 0; c < grid; ++c) cta_begin[c + 1] += cta_begin[c];
     std::vector<MassUnit> by_cta(units.size());
