@@ -36,7 +36,7 @@ SYMBOLS = ["segkv_create", "segkv_destroy", "segkv_append", "segkv_prefill_attn"
            "segkv_last_error", "segkv_set_debug", "segkv_decode_attn_noalloc", "segkv_rope_shift",
            "segkv_export_size", "segkv_export", "segkv_import", "segkv_set_window_convention",
            "segkv_decode_attn_multi", "segkv_sparse_ffn", "segkv_ffn_workspace_size", "segkv_attn_mass",
-           "segkv_topk_tokens", "segkv_plan_decode", "segkv_plan_prefill"]
+           "segkv_topk_tokens", "segkv_plan_decode", "segkv_plan_prefill", "segkv_plan_mass"]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -79,6 +79,7 @@ def _load():
         "segkv_import": [P, I, I, P, SZ, P, P],
         "segkv_plan_decode": [P, I, I, P, P, I, I, P, I, P, I, P, P],
         "segkv_plan_prefill": [P, I, P, P, P, I, I, P, I, P, I, P, P],
+        "segkv_plan_mass": [P, I, P, P, P, I, I, P, I, P, I, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -320,6 +321,25 @@ def segkv_plan_prefill(h, layer, cu_seqlens, q_pos, seq_ids, num_ctas=0):
     rc = _lib.segkv_plan_prefill(h, layer, cu.ctypes.data, qp.ctypes.data, ids.ctypes.data, len(ids),
                                  num_ctas, units.ctypes.data, nu.value, cta.ctypes.data, nc.value,
                                  ctypes.byref(nu), ctypes.byref(nc))
+    return rc, units, cta
+
+
+def segkv_plan_mass(h, layer, cu_seqlens, q_pos, seq_ids, num_ctas=0):
+    """The attention-mass work plan (host only). Returns (rc, units [n_units, 12]
+    int32, cta_begin [n_ctas + 1] int32); unit columns: first token, chunk
+    length, first position, KV head, local, key tile, qt0, qt1, piece, pieces,
+    first partial slot, key-tile counter."""
+    cu, qp, ids = _host_i32(cu_seqlens), _host_i32(q_pos), _host_i32(seq_ids)
+    nu, nc = ctypes.c_int(0), ctypes.c_int(0)
+    rc = _lib.segkv_plan_mass(h, layer, cu.ctypes.data, qp.ctypes.data, ids.ctypes.data, len(ids),
+                              num_ctas, None, 0, None, 0, ctypes.byref(nu), ctypes.byref(nc))
+    if len(ids) == 0 or (rc != 0 and nu.value == 0):
+        return rc, np.zeros((0, 12), np.int32), np.zeros(1, np.int32)
+    units = np.zeros((nu.value, 12), np.int32)
+    cta = np.zeros(nc.value + 1, np.int32)
+    rc = _lib.segkv_plan_mass(h, layer, cu.ctypes.data, qp.ctypes.data, ids.ctypes.data, len(ids),
+                              num_ctas, units.ctypes.data, nu.value, cta.ctypes.data, nc.value,
+                              ctypes.byref(nu), ctypes.byref(nc))
     return rc, units, cta
 
 

@@ -1624,26 +1624,27 @@ int segkv_stats(segkv_t h, segkv_stats_t* out) {
 }
 
 // ---------------------------------------------------------------- attention mass
-int segkv_attn_mass(segkv_t h, int layer, const void* q, const int32_t* cu_seqlens,
-                    const int32_t* q_pos, const int32_t* seq_ids, int n, const float* lse,
-                    float* mass, segkv_stream_t stream) {
-  if (!h) return SEGKV_ERR_INVALID_ARG;
-  if (h->host_only) return fail(h, SEGKV_ERR_INVALID_ARG, "host-only handle has no pools");
-  if (layer < 0 || layer >= h->L) return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer %d", layer);
-  if (!ids_valid(h, seq_ids, n)) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq_ids");
-  if (n == 0) return SEGKV_OK;
-  if (!cu_seqlens || cu_seqlens[0] != 0) return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens[0] != 0");
-  for (int i = 0; i < n; ++i)
-    if (cu_seqlens[i + 1] < cu_seqlens[i])
-      return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens decreases at %d", i);
-  const int64_t total = cu_seqlens[n];
-  if (total == 0) return SEGKV_OK;
-  if (!q || !lse || !mass || !q_pos) return fail(h, SEGKV_ERR_INVALID_ARG, "q/lse/mass/q_pos NULL");
-  if (reinterpret_cast<uintptr_t>(q) & 15)
-    return fail(h, SEGKV_ERR_INVALID_ARG, "q must be 16-byte aligned");
+// One prefill chunk per sequence, its attention mass per key: the work plan
+// (host). A unit is one KV head x one key tile of 128 positions, over the
+// query tiles that see some of its keys; a key tile seen by many query tiles
+// is cut into pieces (partial sums in slots part0 .. part0 + n_pieces - 1, a
+// finished-piece counter tile_id). Units are dealt to `ctas` lists by LPT.
+struct MassPlan {
+  std::vector<MassUnit> units;     // grouped by CTA
+  std::vector<int32_t> cta_begin;  // [grid + 1]
+  int32_t slots = 0, tiles = 0;
+  int grid = 0;
+};
+
+static int mass_plan(segkv* h, int layer, const int32_t* cu_seqlens, const int32_t* q_pos,
+                     const int32_t* seq_ids, int n, int ctas, MassPlan& M) {
   const int W = h->win[layer];
   const int tpt = kRowsPerTile / h->G;
-  std::vector<MassUnit> units;
+  std::vector<MassUnit>& units = M.units;
+  units.clear();
+  M.cta_begin.assign(1, 0);
+  M.slots = M.tiles = 0;
+  M.grid = 0;
   for (int i = 0; i < n; ++i) {
     const int b = seq_ids[i];
     const int32_t nlen = h->len[h->lidx(layer, b)];
@@ -1689,7 +1690,6 @@ int segkv_attn_mass(segkv_t h, int layer, const void* q, const int32_t* cu_seqle
   // query tiles, so that no unit is much longer than a CTA's fair share.
   int64_t steps = 0;
   for (const MassUnit& u : units) steps += u.qt1 - u.qt0 + 1;
-  const int ctas = std::max(1, h->num_sms);
   const int32_t cap = static_cast<int32_t>(std::max<int64_t>(8, (steps + 2 * ctas - 1) / (2 * ctas)));
   std::vector<MassUnit> cut;
   int32_t slots = 0, tiles = 0;
@@ -1716,8 +1716,10 @@ int segkv_attn_mass(segkv_t h, int layer, const void* q, const int32_t* cu_seqle
   std::stable_sort(units.begin(), units.end(), [](const MassUnit& x, const MassUnit& y) {
     return (x.qt1 - x.qt0) > (y.qt1 - y.qt0);
   });
-  const int grid = static_cast<int>(std::min<int64_t>(units.size(), h->num_sms));
-  std::vector<int32_t> cta_begin(grid + 1, 0), cta_of(units.size());
+  const int grid = static_cast<int>(std::min<int64_t>(units.size(), ctas));
+  std::vector<int32_t>& cta_begin = M.cta_begin;
+  cta_begin.assign(grid + 1, 0);
+  std::vector<int32_t> cta_of(units.size());
   {
     LeastLoaded lpt;
     lpt.reset(grid);
@@ -1733,6 +1735,41 @@ int segkv_attn_mass(segkv_t h, int layer, const void* q, const int32_t* cu_seqle
     for (size_t x = 0; x < units.size(); ++x) by_cta[fill[cta_of[x]]++] = units[x];
     units.swap(by_cta);
   }
+  M.slots = slots;
+  M.tiles = tiles;
+  M.grid = grid;
+  return SEGKV_OK;
+}
+
+int segkv_attn_mass(segkv_t h, int layer, const void* q, const int32_t* cu_seqlens,
+                    const int32_t* q_pos, const int32_t* seq_ids, int n, const float* lse,
+                    float* mass, segkv_stream_t stream) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (h->host_only) return fail(h, SEGKV_ERR_INVALID_ARG, "host-only handle has no pools");
+  if (layer < 0 || layer >= h->L) return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer %d", layer);
+  if (!ids_valid(h, seq_ids, n)) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq_ids");
+  if (n == 0) return SEGKV_OK;
+  if (!cu_seqlens || cu_seqlens[0] != 0) return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens[0] != 0");
+  for (int i = 0; i < n; ++i)
+    if (cu_seqlens[i + 1] < cu_seqlens[i])
+      return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens decreases at %d", i);
+  const int64_t total = cu_seqlens[n];
+  if (total == 0) return SEGKV_OK;
+  if (!q || !lse || !mass || !q_pos) return fail(h, SEGKV_ERR_INVALID_ARG, "q/lse/mass/q_pos NULL");
+  if (reinterpret_cast<uintptr_t>(q) & 15)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  const int W = h->win[layer];
+  const int tpt = kRowsPerTile / h->G;
+  MassPlan M;
+  {
+    const int prc = mass_plan(h, layer, cu_seqlens, q_pos, seq_ids, n, std::max(1, h->num_sms), M);
+    if (prc != SEGKV_OK) return prc;
+  }
+  if (M.units.empty()) return SEGKV_OK;
+  const std::vector<MassUnit>& units = M.units;
+  const std::vector<int32_t>& cta_begin = M.cta_begin;
+  const int32_t slots = M.slots, tiles = M.tiles;
+  const int grid = M.grid;
   Pack pk;
   const size_t o_units = pk.add(units.data(), units.size());
   const size_t o_cta = pk.add(cta_begin.data(), cta_begin.size());
@@ -1787,6 +1824,52 @@ int segkv_attn_mass(segkv_t h, int layer, const void* q, const int32_t* cu_seqle
   if (e != cudaSuccess) return cuda_fail(h, e, "mass kernel launch");
   e = h->ring.commit(off, region, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "event record");
+  return SEGKV_OK;
+}
+
+int segkv_plan_mass(segkv_t h, int layer, const int32_t* cu_seqlens, const int32_t* q_pos,
+                    const int32_t* seq_ids, int n, int num_ctas, int32_t* units_out, int max_units,
+                    int32_t* cta_begin_out, int max_ctas, int* n_units, int* n_ctas) {
+  if (!h) return SEGKV_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= h->L) return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer %d", layer);
+  if (n < 0 || max_units < 0 || max_ctas < 0 || !n_units || !n_ctas)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "bad n or output sizes");
+  if (!ids_valid(h, seq_ids, n)) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq_ids");
+  *n_units = 0;
+  *n_ctas = 0;
+  if (n == 0) return SEGKV_OK;
+  if (!cu_seqlens || cu_seqlens[0] != 0) return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens[0] != 0");
+  for (int i = 0; i < n; ++i)
+    if (cu_seqlens[i + 1] < cu_seqlens[i])
+      return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens decreases at %d", i);
+  if (cu_seqlens[n] == 0) return SEGKV_OK;
+  if (!q_pos) return fail(h, SEGKV_ERR_INVALID_ARG, "q_pos NULL");
+  const int ctas = num_ctas > 0 ? num_ctas : std::max(1, h->num_sms);
+  MassPlan M;
+  const int rc = mass_plan(h, layer, cu_seqlens, q_pos, seq_ids, n, ctas, M);
+  if (rc != SEGKV_OK) return rc;
+  if (M.units.empty()) return SEGKV_OK;
+  *n_units = static_cast<int>(M.units.size());
+  *n_ctas = M.grid;
+  if (*n_units > max_units || *n_ctas > max_ctas || (max_units && !units_out) || !cta_begin_out)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "plan needs %d units and %d CTAs", *n_units, *n_ctas);
+  for (size_t x = 0; x < M.units.size(); ++x) {
+    const MassUnit& u = M.units[x];
+    int32_t* o = units_out + 12 * x;
+    o[0] = u.tok0;
+    o[1] = u.ntok;
+    o[2] = u.a;
+    o[3] = u.head;
+    o[4] = u.local;
+    o[5] = u.kt;
+    o[6] = u.qt0;
+    o[7] = u.qt1;
+    o[8] = u.piece;
+    o[9] = u.n_pieces;
+    o[10] = u.part0;
+    o[11] = u.tile_id;
+  }
+  for (int c = 0; c <= M.grid; ++c) cta_begin_out[c] = M.cta_begin[c];
   return SEGKV_OK;
 }
 

@@ -391,6 +391,28 @@ int segkv_plan_prefill(segkv_t h, int layer, const int32_t* cu_seqlens, const in
                        const int32_t* seq_ids, int n, int num_ctas, int32_t* units, int max_units,
                        int32_t* cta_begin, int max_ctas, int* n_units, int* n_ctas);
 
+/* segkv_plan_mass — the work plan that segkv_attn_mass would use for the same
+ * chunks, computed on the host only (host-only handles work too), for tests
+ * and tools. A unit is one KV head x one key tile of 128 positions of one
+ * chunk, over the query tiles (128 / G tokens each, chunk-relative) that see
+ * some of its keys; a key tile seen by many query tiles is cut into pieces.
+ * Units are dealt to num_ctas lists by longest-processing-time-first.
+ *   num_ctas    > 0: plan for that many CTAs; otherwise one per SM.
+ *   units       host int32 [max_units][12], out: first token of the chunk
+ *               (index into the call's packed tokens), chunk length, position
+ *               of its first token, KV head, 1 if local, key tile, query
+ *               tiles qt0 .. qt1, piece, pieces of its key tile, first
+ *               partial-sum slot of the key tile, the key tile's counter
+ *               (the last two 0 for a key tile in one piece).
+ *   cta_begin   host int32 [max_ctas + 1], out: list c holds units
+ *               cta_begin[c] .. cta_begin[c + 1] - 1.
+ *   n_units, n_ctas  out: the plan's sizes, written even when an output
+ *               array is too small (then SEGKV_ERR_INVALID_ARG).
+ * Errors: those of segkv_attn_mass for the same arguments. */
+int segkv_plan_mass(segkv_t h, int layer, const int32_t* cu_seqlens, const int32_t* q_pos,
+                    const int32_t* seq_ids, int n, int num_ctas, int32_t* units, int max_units,
+                    int32_t* cta_begin, int max_ctas, int* n_units, int* n_ctas);
+
 /* segkv_plan_decode — the work plan that segkv_decode_attn (T = 1) or
  * segkv_decode_attn_multi would use for the T newest tokens of n sequences,
  * computed on the host only (no device work; host-only handles work too), for

@@ -14,6 +14,12 @@ balanced:
 two Q tiles' tokens), with the chunk's key range, dealt to CTA lists by LPT.
 The checks pin that every (chunk, head) appears once with the right key
 range, and the LPT bound on the lists' loads.
+
+`segkv_plan_mass` returns the attention-mass plan: one unit per (KV head, key
+tile of a chunk) over the query tiles that see its keys, long ones cut into
+pieces with their own partial-sum slots, dealt by LPT. The checks pin the
+query-tile ranges against the visibility rule, the pieces and slots, and the
+exact LPT order.
 """
 import numpy as np
 import pytest
@@ -291,3 +297,105 @@ def test_plans_on_a_reused_handle_match_fresh_handles():
         u1, c1 = fn(reused, *args)
         u2, c2 = fn(make(), *args)
         assert np.array_equal(u1, u2) and np.array_equal(c1, c2)
+
+
+# ---------------------------------------------------------------- attention mass
+def mass_case(G, hkv, W, chunks, prior, num_ctas, seed):
+    """Host-only handle; sequence b holds prior[b] tokens, then its chunk of
+    chunks[b] tokens is appended and planned."""
+    hq, d, P = G * hkv, 128, 64
+    hc = [GLOBAL if hd % 3 == 0 else LOCAL for hd in range(hkv)]
+    n = len(chunks)
+    h = host_handle(hq, hkv, d, hc, W, P, n, 16384, 8 * 16384)
+    for b in range(n):
+        if prior[b]:
+            fill_one = np.array([0, prior[b]], np.int32)
+            assert S.segkv_append(h.handle, 0, None, None, fill_one, np.array([b], np.int32)) == 0
+    rng = np.random.default_rng(seed)
+    ids = rng.permutation(n).astype(np.int32)
+    cu = np.concatenate([[0], np.cumsum([chunks[b] for b in ids])]).astype(np.int32)
+    assert S.segkv_append(h.handle, 0, None, None, cu, ids) == 0
+    qp = np.concatenate([np.arange(prior[b], prior[b] + chunks[b]) for b in ids]).astype(np.int32)
+    rc, units, cta = S.segkv_plan_mass(h.handle, 0, cu, qp, ids, num_ctas)
+    assert rc == 0, S.segkv_last_error(h.handle)
+    return h, hc, ids, cu, units, cta
+
+
+@pytest.mark.parametrize("G,hkv,W,num_ctas", [(4, 8, 300, 152), (8, 4, 1024, 16), (1, 2, 64, 5),
+                                              (16, 2, 5000, 152)])
+def test_mass_plan_covers_every_seeing_query_tile_once(G, hkv, W, num_ctas):
+    chunks, prior = [700, 4096, 1, 129, 2500], [0, 1000, 37, 5000, 300]
+    h, hc, ids, cu, units, cta = mass_case(G, hkv, W, chunks, prior, num_ctas, G + hkv)
+    tpt = 128 // G
+    assert cta[0] == 0 and cta[-1] == units.shape[0] and (np.diff(cta) >= 1).all()
+    assert len(cta) - 1 == min(num_ctas, units.shape[0])
+    # group the pieces by (chunk, head, key tile)
+    tiles = {}
+    for u in units:
+        tok0, ntok, a, hd, local, kt, qt0, qt1, piece, npc, part0, tid = (int(v) for v in u)
+        tiles.setdefault((tok0, hd, kt), []).append((piece, npc, qt0, qt1, part0, tid))
+        assert local == (hc[hd] == LOCAL)
+    slots, counters = [], []
+    for i, b in enumerate(ids):
+        a, T = prior[b], chunks[b]
+        for hd in range(hkv):
+            for kt in range(a // 128, (a + T - 1) // 128 + 1):
+                ps = sorted(tiles.pop((int(cu[i]), hd, kt)))
+                npc = len(ps)
+                assert [p[0] for p in ps] == list(range(npc)) and all(p[1] == npc for p in ps)
+                # pieces tile a contiguous run of query tiles
+                assert all(ps[x][3] + 1 == ps[x + 1][2] for x in range(npc - 1))
+                lens = [p[3] - p[2] + 1 for p in ps]
+                assert min(lens) >= 1 and max(lens) - min(lens) <= 1
+                # from the definition: query p (a <= p < a+T) sees key j iff
+                # j <= p, and j >= p - W + 1 on a local head
+                j = np.arange(max(a, 128 * kt), min(a + T, 128 * (kt + 1)))[:, None]
+                p = np.arange(a, a + T)[None, :]
+                vis = (j <= p) & ((hc[hd] == GLOBAL) | (j >= p - W + 1))
+                seeing = np.nonzero(vis.any(axis=0))[0]  # chunk-relative query tokens
+                assert ps[0][2] == seeing[0] // tpt and ps[-1][3] == seeing[-1] // tpt
+                if npc > 1:
+                    assert len({p[4] for p in ps}) == 1 and len({p[5] for p in ps}) == 1
+                    slots.append((ps[0][4], npc))
+                    counters.append(ps[0][5])
+                else:
+                    assert ps[0][4] == 0 and ps[0][5] == 0
+    assert not tiles, "no unit outside the chunks' key tiles"
+    # split key tiles own disjoint runs of partial slots and distinct counters
+    slots.sort()
+    assert all(slots[x][0] + slots[x][1] == slots[x + 1][0] for x in range(len(slots) - 1))
+    assert (not slots or slots[0][0] == 0) and sorted(counters) == list(range(len(counters)))
+
+
+@pytest.mark.parametrize("num_ctas", [152, 7])
+def test_mass_plan_is_exactly_the_lpt_schedule(num_ctas):
+    chunks, prior = [3000, 640, 9000], [100, 0, 2000]
+    h, hc, ids, cu, units, cta = mass_case(4, 8, 700, chunks, prior, num_ctas, 3)
+    # building order: chunk (call order), KV head, key tile, piece; then a
+    # stable sort on query tiles, longest first; least loaded list, lowest
+    # index on ties; a unit costs its query tiles + 1
+    build = sorted(range(len(units)), key=lambda x: tuple(int(v) for v in units[x][[0, 3, 5, 8]]))
+    order = sorted(build, key=lambda x: -int(units[x][7] - units[x][6]))
+    grid = min(num_ctas, len(units))
+    loads = np.zeros(grid, np.int64)
+    lists = [[] for _ in range(grid)]
+    for x in order:
+        c = int(np.argmin(loads))
+        lists[c].append(x)
+        loads[c] += int(units[x][7] - units[x][6]) + 2
+    assert len(cta) - 1 == grid
+    for c in range(grid):
+        assert (units[cta[c]:cta[c + 1]] == units[lists[c]]).all(), c
+
+
+def test_mass_plan_errors():
+    h = host_handle(8, 2, 64, [GLOBAL, LOCAL], 16, 16, 2, 512, 64)
+    fill(h, [100, 5])
+    # positions of a chunk must be consecutive and inside the sequence
+    assert S.segkv_plan_mass(h.handle, 0, [0, 2], [10, 12], [0], 8)[0] == S.SEGKV_ERR_INVALID_ARG
+    assert S.segkv_plan_mass(h.handle, 0, [0, 2], [99, 100], [0], 8)[0] == S.SEGKV_ERR_INVALID_ARG
+    assert S.segkv_plan_mass(h.handle, 0, [0, 1], [0], [3], 8)[0] == S.SEGKV_ERR_INVALID_ARG
+    assert h.trim(0, [0]) == 0
+    assert S.segkv_plan_mass(h.handle, 0, [0, 1], [50], [0], 8)[0] == S.SEGKV_ERR_EVICTED
+    rc, units, cta = S.segkv_plan_mass(h.handle, 0, [0], [], [], 8)
+    assert rc == 0 and units.shape == (0, 12)
