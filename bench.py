@@ -252,19 +252,68 @@ def run_ours(args, rank, world):
 
     del h
     torch.cuda.synchronize()
+    cpu = rank == 0 and not args.no_cpu
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(args, dev, stream, w, sets, cu, q_pos, step_flops, num_pages)
+    if cpu:
+        out["cpu_baseline"] = cpu_baseline(sets, w, budget_s=args.cpu_seconds)
     if not args.no_decode:
-        out["decode"] = run_decode(args, dev, stream, hbm, peak_src)
         out["rope_shift"] = run_rope(dev, stream, hbm)
         out["pd_transfer"] = run_transfer(dev, stream, hbm)
         out["sparse_ffn_routing"] = run_routing(dev, stream, bf16_burst, peak_src)
-        out["prefill_configs"] = run_prefill_configs(dev, stream, bf16_burst, peak_src)
+        out["prefill_configs"] = run_prefill_configs(dev, stream, bf16_burst, peak_src, cpu=cpu)
     if not args.no_dense:
         out["dense"] = run_dense(args, dev, stream, sets, cu, q_pos, o, prefill_ms)
-    if not args.no_e2e:
-        out["e2e"] = run_e2e(args, dev, stream, w, sets, cu, q_pos, step_flops, num_pages)
-    if rank == 0 and not args.no_cpu:
-        out["cpu_baseline"] = cpu_baseline(sets, w, budget_s=args.cpu_seconds)
+        out["context_sweep"] = run_context_sweep(dev, stream, sets)
+    if not args.no_decode:
+        out["decode"] = run_decode(args, dev, stream, hbm, peak_src, cpu=cpu)
+    out["summary"] = summary(out, bf16_burst, bf16_sus, hbm)
     return out
+
+
+def summary(out, bf16_burst, bf16_sus, hbm):
+    """The headline figures of every workload in one short object, printed
+    last in the JSON line."""
+    r = out["roofline"]
+    sm = {"128k_64layer": {"prefill_s": round(out["prefill_ms"] / 1e3, 4),
+                           "tflops": r["achieved"], "frac_sustained": r["frac"],
+                           "frac_burst": r["frac_of_burst"]}}
+    if "cpu_baseline" in out:
+        sm["128k_64layer"]["cpu_oracle_tflops"] = round(out["cpu_baseline"]["value"], 4)
+        sm["cpu_cores"] = out["cpu_baseline"]["cores"]
+    for name, d in out.get("prefill_configs", {}).items():
+        if not isinstance(d, dict):
+            continue
+        e = {"ms": d["prefill_ms"], "tflops": d["useful_tflops"], "frac_burst": d["frac_of_burst"]}
+        if "cpu_oracle" in d:
+            e["cpu_oracle_ms"] = d["cpu_oracle"]["ms_full_layer"]
+            e["cpu_oracle_tflops"] = d["cpu_oracle"]["tflops"]
+        sm[name] = e
+    if "decode" in out:
+        d = out["decode"]
+        sm["ragged_decode"] = {"us": d["decode_us_median"], "gbs": d["gbs_median"],
+                               "frac_hbm": d["frac"], "back_to_back_gbs": d["back_to_back_gbs"],
+                               "back_to_back_frac": d["back_to_back_frac"],
+                               "step_us_with_append": d["step_us_median"],
+                               "tokens_per_s": d["tokens_per_s"],
+                               "multi_query_t4_frac": d["multi_query_t4"]["frac"]}
+        if "cpu_oracle" in d:
+            sm["ragged_decode"]["cpu_oracle_gbs"] = d["cpu_oracle"]["gbs"]
+    if "dense" in out:
+        sm["dense_speedup_128k_64layer"] = out["dense"]["speedup_segpaged_vs_dense"]
+    if "context_sweep" in out:
+        c = out["context_sweep"]
+        sm["speedup_vs_context"] = {"n": c["n"], "shallow": c["shallow"]["speedup_vs_dense"],
+                                    "deep_g1": c["deep_g1"]["speedup_vs_dense"],
+                                    "monotone": c["shallow"]["monotone"] and c["deep_g1"]["monotone"]}
+    if "e2e" in out:
+        sm["e2e_tflops"] = out["e2e"]["value"]
+    if "rope_shift" in out:
+        sm["rope_frac_hbm"] = out["rope_shift"]["frac_hbm"]
+        sm["transfer_gbs"] = {"export": out["pd_transfer"]["export_gbs"],
+                              "import": out["pd_transfer"]["import_gbs"]}
+        sm["sparse_ffn_frac_burst"] = out["sparse_ffn_routing"]["roofline_ffn"]["frac"]
+    return sm
 
 
 def run_dense(args, dev, stream, sets, cu, q_pos, o, sparse_prefill_ms):
@@ -307,7 +356,98 @@ def run_dense(args, dev, stream, sets, cu, q_pos, o, sparse_prefill_ms):
             "note": "all heads global, full causal; 4 identical layers timed, x16"}
 
 
-def run_decode(args, dev, stream, hbm, peak_src):
+def oracle_decode_timing(w, k, v, cu, step0):
+    """Time the fp64 oracle on one whole decode step of the ragged-decode
+    workload (every request and query head: step 0's token attending to its
+    context plus itself) and report it in the GPU path's unit, GB/s of
+    algorithmic K/V bytes."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    qq, kk, vv = (t.cpu() for t in step0)
+    B = len(w.seq_lens)
+    cu = np.asarray(cu, np.int64)
+    ks, vs = [], []
+    for b in range(B):
+        ks += [k[cu[b]:cu[b + 1]].cpu(), kk[b:b + 1]]
+        vs += [v[cu[b]:cu[b + 1]].cpu(), vv[b:b + 1]]
+    lens = np.array(w.seq_lens, np.int64) + 1
+    offs = np.concatenate([[0], np.cumsum(lens)[:-1]])
+    W = w.window[0]
+    start = np.array([[0 if w.head_class[0][hh] == 0 else max(0, int(n) - W) for hh in range(w.hkv)]
+                      for n in lens], np.int32)
+    kc, vc = torch.cat(ks), torch.cat(vs)
+    t0 = time.perf_counter()
+    rc, _, _ = oracle.attention(qq, kc, vc, np.arange(B, dtype=np.int32),
+                                (lens - 1).astype(np.int32), offs, lens, w.head_class[0], W, start)
+    secs = time.perf_counter() - t0
+    assert rc == 0
+    nbytes = decode_bytes(w, lens.tolist())
+    return {"gbs": round(nbytes / secs / 1e9, 4), "us_per_step": round(1e6 * secs, 1),
+            "sample": "one whole decode step (32 requests x 32 query heads)", "cores": host_cores()}
+
+
+def run_context_sweep(dev, stream, sets, contexts=(8192, 16384, 32768, 65536, 131072)):
+    """Speed-up of segmented over dense prefill against context length, on
+    the 128K workload's layer shape (64/8 heads, D=128, pages of 128): a
+    shallow layer (all 8 KV heads local, window 4096), a deep layer (KV head
+    0 global, 7 local with window 1024) and the dense layer of the same
+    library (all 8 heads global, full causal), each timed alone on the first
+    n tokens of the same inputs."""
+    import numpy as np
+    import torch
+
+    import head_segmented_paged_gb300 as S
+    from head_segmented_paged_gb300 import inputs as I
+
+    q, k, v = sets[0]
+    hq, hkv, D, P = q.shape[1], k.shape[1], q.shape[2], 128
+    kinds = {"shallow": ([1] * hkv, 4096), "deep_g1": ([0] + [1] * (hkv - 1), 1024),
+             "dense": ([0] * hkv, 1 << 30)}
+    out = {"n": list(contexts)}
+    res = {kk: [] for kk in kinds}
+    for n in contexts:
+        cu = np.array([0, n], np.int32)
+        qp = np.arange(n, dtype=np.int32)
+        o = torch.empty((n, hq, D), dtype=torch.bfloat16, device=dev)
+        for kind, (hc, W) in kinds.items():
+            kp = torch.empty((hkv * (n // P) + 8, P, D), dtype=torch.bfloat16, device=dev)
+            h = S.SegKV(1, hq, hkv, D, [hc], [min(W, n)], P, 1, n, kp, torch.empty_like(kp))
+            h.append(0, k[:n], v[:n], cu, [0], stream)
+            reps = 3 if n >= 65536 else 10
+            h.prefill_attn(0, q[:n], cu, qp, [0], o, None, stream)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                h.prefill_attn(0, q[:n], cu, qp, [0], o, None, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if h.status() != 0:
+                raise RuntimeError("device status in the context sweep: " +
+                                   S.segkv_last_error(h.handle))
+            ms = e0.elapsed_time(e1) / reps
+            wl = I.Workload(kind, 1, hq, hkv, D, P, [hc], [min(W, n)], [n])
+            res[kind].append((ms, useful_flops_layer(wl, 0, n)))
+            h.close()
+            del kp
+        del o
+    torch.cuda.empty_cache()
+    dense = [ms for ms, _ in res["dense"]]
+    for kind in ("shallow", "deep_g1"):
+        sp = [d / ms for (ms, _), d in zip(res[kind], dense)]
+        out[kind] = {"seg_ms": [round(ms, 3) for ms, _ in res[kind]],
+                     "useful_tflops": [round(f / (ms * 1e-3) / 1e12, 1) for ms, f in res[kind]],
+                     "speedup_vs_dense": [round(x, 2) for x in sp],
+                     "monotone": all(b > a for a, b in zip(sp, sp[1:]))}
+    out["dense"] = {"ms": [round(x, 3) for x in dense],
+                    "useful_tflops": [round(f / (ms * 1e-3) / 1e12, 1) for ms, f in res["dense"]]}
+    return out
+
+
+def run_decode(args, dev, stream, hbm, peak_src, cpu=False):
     import numpy as np
     import torch
 
@@ -328,6 +468,8 @@ def run_decode(args, dev, stream, hbm, peak_src):
     h.trim(0, ids)
     del q
     qd = [I.decode_step_tensors(w, s, device=dev) for s in range(steps)]
+    cpu_oracle = oracle_decode_timing(w, k, v, cu, qd[0]) if cpu else None
+    del k, v
     ws = torch.empty(h.workspace_size(S.SEGKV_WS_DECODE, B, B) // 4 + 64, dtype=torch.float32,
                      device=dev)
     o = torch.empty((B, w.hq, D), dtype=torch.bfloat16, device=dev)
@@ -412,7 +554,8 @@ def run_decode(args, dev, stream, hbm, peak_src):
             "bytes_per_step_mean": int(statistics.mean(bytes_step)),
             "host_issue_us_per_step": round(1e6 * t_host / steps, 2),
             "steps_timed": steps - warm,
-            "kernels": ["decode_split_kernel<128,4> (split-KV with the merge fused in)"]}
+            "kernels": ["decode_split_kernel<128,4> (split-KV with the merge fused in)"],
+            **({"cpu_oracle": cpu_oracle} if cpu_oracle else {})}
 
 
 def run_rope(dev, stream, hbm):
@@ -450,10 +593,12 @@ def run_rope(dev, stream, hbm):
             "kernel": "rope_kernel"}
 
 
-def run_prefill_configs(dev, stream, bf16_burst, peak_src):
+def run_prefill_configs(dev, stream, bf16_burst, peak_src, cpu=False):
     """Single-layer prefill of the Mistral-shaped 8K sequence and of the
     Llama-70B-shaped varlen batch (4 sequences of 16K-32K, window 2048, key
-    sinks): prefill kernel time, tokens/s and useful TFLOP/s."""
+    sinks): prefill kernel time, tokens/s and useful TFLOP/s; with cpu=True
+    also the fp64 oracle on the host cores (the 8K layer in full, the varlen
+    batch on sampled query tokens)."""
     import torch
 
     import head_segmented_paged_gb300 as S
@@ -490,6 +635,10 @@ def run_prefill_configs(dev, stream, bf16_burst, peak_src):
                        "tokens_per_s": round(int(cu[-1]) / (ms * 1e-3)),
                        "useful_tflop": round(fl / 1e12, 3), "useful_tflops": round(tf, 1),
                        "frac_of_burst": round(tf / bf16_burst, 4)}
+        if cpu:
+            out[w.name]["cpu_oracle"] = oracle_prefill_timing(
+                w, q.cpu(), k.cpu(), v.cpu(), cu, qp,
+                sample_rows=None if w.name == "mistral-8k" else 384)
         h.close()
         del q, k, v, o, kp
         torch.cuda.empty_cache()
@@ -653,6 +802,11 @@ def run_e2e(args, dev, stream, w, sets, cu, q_pos, step_flops, num_pages):
     done = [torch.cuda.Event() for _ in range(NB)]
     free = [torch.cuda.Event() for _ in range(NB)]
     h2d = 0
+    # per layer: its copies' start and end on the copy stream, and the start
+    # and end of its kernels on the compute stream (after the wait on its copy)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    cp_ev = [(ev(), ev()) for _ in range(L)]
+    k_ev = [(ev(), ev()) for _ in range(L)]
 
     def step():
         nonlocal h2d
@@ -663,17 +817,21 @@ def run_e2e(args, dev, stream, w, sets, cu, q_pos, step_flops, num_pages):
                 b = l % NB
                 copy_stream.wait_event(free[b])
                 with torch.cuda.stream(copy_stream):
+                    cp_ev[l][0].record(copy_stream)
                     for dst, src in zip(dbuf[b], host[l % N_INPUT_SETS]):
                         dst.copy_(src, non_blocking=True)
                         h2d += src.numel() * src.element_size()
+                    cp_ev[l][1].record(copy_stream)
                 done[b].record(copy_stream)
             if l >= 1:  # compute layer l-1
                 lb = (l - 1) % NB
                 stream.wait_event(done[lb])
+                k_ev[l - 1][0].record(stream)
                 qd, kd, vd = dbuf[lb]
                 h.append(l - 1, kd, vd, cu, [0], stream)
                 h.prefill_attn(l - 1, qd, cu, q_pos, [0], o, None, stream)
                 h.trim(l - 1, [0])
+                k_ev[l - 1][1].record(stream)
                 free[lb].record(stream)
         o_host.copy_(o, non_blocking=True)
 
@@ -694,24 +852,74 @@ def run_e2e(args, dev, stream, w, sets, cu, q_pos, step_flops, num_pages):
     torch.cuda.synchronize()
     layer_bytes = sum(t.numel() * t.element_size() for t in host[0])
     h2d_gbs = 2 * layer_bytes / (t0.elapsed_time(t1) * 1e-3) / 1e9
-    ks = max(1, min(args.steps, 2))
+    ks = 5
+    rates, waits = [], []
     t0.record(stream)
     for _ in range(ks):
         step()
+        torch.cuda.synchronize()
+        # each layer's copy rate, and how long the kernels waited for copies
+        rates += [layer_bytes / (a.elapsed_time(b) * 1e-3) / 1e9 for a, b in cp_ev]
+        waits.append(sum(max(0.0, k_ev[l][1].elapsed_time(k_ev[l + 1][0]))
+                         for l in range(L - 1)))
     t1.record(stream)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / ks
+    rates.sort()
     return {"value": round(step_flops / (ms * 1e-3) / 1e12, 2), "unit": UNIT,
-            "ms_per_step": round(ms, 2), "h2d_bytes_per_step": h2d,
+            "ms_per_step": round(ms, 2), "steps_timed": ks, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": o.numel() * o.element_size(),
             "h2d_gbs_copy_alone": round(h2d_gbs, 1),
-            "h2d_ms_per_step_at_that_rate": round(h2d / (h2d_gbs * 1e9) * 1e3, 1),
-            "h2d_gbs_in_step": round(h2d / (ms * 1e-3) / 1e9, 1),
-            "note": "pinned host Q/K/V per layer copied in the timed region on a side stream "
-                    "(three rotating device buffers); last layer's O copied back. The copy-alone "
-                    "rate is one short sample (a layer's Q, K, V twice) taken before the timed "
-                    "steps; on a shared host it can differ from the rate the copies reach inside "
-                    "the step (h2d_gbs_in_step, a lower bound: the copies overlap compute)"}
+            "h2d_gbs_per_layer_in_step": {"median": round(statistics.median(rates), 1),
+                                          "p10": round(rates[len(rates) // 10], 1),
+                                          "min": round(rates[0], 1)},
+            "kernels_waiting_for_copies_ms_per_step": round(statistics.median(waits), 1),
+            "note": "pinned host Q/K/V per layer copied inside the timed region on a side stream "
+                    "into three rotating device buffers; the last layer's O copied back"}
+
+
+# ------------------------------------------------------------------ oracle timings per config
+def visible_keys(head_class, window, p):
+    """Keys a query at position p sees in a head: p+1 (global) or min(p+1, W)."""
+    return p + 1 if head_class == 0 else min(p + 1, window)
+
+
+def rows_flops(w, layer, pos):
+    """Useful FLOPs of the query tokens at positions pos (all query heads)."""
+    pos = [int(x) for x in pos]
+    return sum(4 * w.head_dim * w.group * visible_keys(w.head_class[layer][hh], w.window[layer], p)
+               for p in pos for hh in range(w.hkv))
+
+
+def oracle_prefill_timing(w, q, k, v, cu, qp, sample_rows=None, seed=0):
+    """Time the fp64 oracle on a prefill layer (CPU tensors): every query
+    token, or sample_rows random tokens spread over the sequences, and
+    extrapolate by useful FLOPs to the whole layer."""
+    import numpy as np
+
+    import oracle
+
+    cu = np.asarray(cu, np.int64)
+    qp = np.asarray(qp, np.int32)
+    nseq = len(w.seq_lens)
+    row_seq = np.repeat(np.arange(nseq), np.diff(cu)).astype(np.int32)
+    tot = int(cu[-1])
+    rows = None
+    if sample_rows is not None and sample_rows < tot:
+        rows = np.sort(np.random.default_rng(seed).choice(tot, sample_rows, replace=False))
+    t0 = time.perf_counter()
+    rc, _, _ = oracle.attention(q, k, v, row_seq, qp, cu[:-1], np.diff(cu), w.head_class[0],
+                                w.window[0], np.zeros((nseq, w.hkv), np.int32), rows=rows)
+    secs = time.perf_counter() - t0
+    assert rc == 0
+    full = sum(useful_flops_layer(w, 0, n) for n in w.seq_lens)
+    done = full if rows is None else rows_flops(w, 0, qp[rows])
+    rate = done / secs
+    return {"tflops": round(rate / 1e12, 5), "seconds": round(secs, 2),
+            "ms_full_layer": round(1e3 * full / rate, 1),
+            "sample": ("every query token" if rows is None else
+                       f"{len(rows)} random query tokens of {tot}, extrapolated by useful FLOPs"),
+            "cores": host_cores()}
 
 
 # ------------------------------------------------------------------ oracle (CPU) arm
@@ -787,11 +995,17 @@ def cpu_baseline(sets, w, budget_s=20.0):
 def run_reference(args, rank, world):
     """The oracle, as it stands, on the host cores, on bounded samples of the
     same 128K workload; each step is one sample."""
-    import torch
+    import importlib.util
 
-    from head_segmented_paged_gb300 import inputs as I
     import oracle
 
+    # the seeded generators only, loaded by path: importing the package would
+    # map the CUDA library into a process that runs none of it
+    spec = importlib.util.spec_from_file_location(
+        "segkv_inputs", os.path.join(ROOT, "head_segmented_paged_gb300", "inputs.py"))
+    I = importlib.util.module_from_spec(spec)
+    sys.modules["segkv_inputs"] = I  # dataclasses resolve annotations through it
+    spec.loader.exec_module(I)
     oracle.build()
     w = I.long_128k_64layer(seed=0)
     n = w.seq_lens[0]

@@ -36,7 +36,8 @@ SYMBOLS = ["segkv_create", "segkv_destroy", "segkv_append", "segkv_prefill_attn"
            "segkv_last_error", "segkv_set_debug", "segkv_decode_attn_noalloc", "segkv_rope_shift",
            "segkv_export_size", "segkv_export", "segkv_import", "segkv_set_window_convention",
            "segkv_decode_attn_multi", "segkv_sparse_ffn", "segkv_ffn_workspace_size", "segkv_attn_mass",
-           "segkv_topk_tokens", "segkv_plan_decode", "segkv_plan_prefill", "segkv_plan_mass"]
+           "segkv_topk_tokens", "segkv_plan_decode", "segkv_plan_prefill", "segkv_plan_mass",
+           "segkv_exp2_check"]
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -80,6 +81,7 @@ def _load():
         "segkv_plan_decode": [P, I, I, P, P, I, I, P, I, P, I, P, P],
         "segkv_plan_prefill": [P, I, P, P, P, I, I, P, I, P, I, P, P],
         "segkv_plan_mass": [P, I, P, P, P, I, I, P, I, P, I, P, P],
+        "segkv_exp2_check": [P, P, P, I, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -285,6 +287,13 @@ def segkv_status(h, stream=None):
 def segkv_last_error(h=None):
     m = _lib.segkv_last_error(h)
     return m.decode() if m else ""
+
+
+def segkv_exp2_check(x, y_poly, y_mufu, stream=None):
+    """The softmax's two base-2 exponentials over device fp32 x (test hook):
+    the FMA-pipe cubic into y_poly, the hardware ex2 into y_mufu."""
+    return _lib.segkv_exp2_check(_ptr(x), _ptr(y_poly), _ptr(y_mufu), int(x.numel()),
+                                 _stream_ptr(stream))
 
 
 def segkv_plan_decode(h, layer, T, seq_lens, seq_ids, num_ctas=0):

@@ -461,6 +461,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The two base-2 exponentials of the softmax, elementwise over an array, so
+// that they can be checked against 2^x outside any attention call.
+__global__ void exp2_check_kernel(const float* x, float* y_poly, float* y_mufu, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) {
+    y_poly[i] = exp2_poly(x[i]);
+    y_mufu[i] = ex2(x[i]);
+  }
+}
+
+cudaError_t launch_exp2_check(const float* x, float* y_poly, float* y_mufu, int n, cudaStream_t s) {
+  exp2_check_kernel<<<(n + 255) / 256, 256, 0, s>>>(x, y_poly, y_mufu, n);
+  return cudaGetLastError();
+}
+
 int prefill_smem_bytes(int head_dim) {
   return head_dim == 64 ? static_cast<int>(Layout<64>::BYTES) : static_cast<int>(Layout<128>::BYTES);
 }

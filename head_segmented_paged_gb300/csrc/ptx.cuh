@@ -306,11 +306,14 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 
 // 2^x on the FMA/ALU pipes, to relieve the MUFU unit. x is split as
 // i + f with i = nearest integer (by adding 1.5 * 2^23, whose ulp is 1) and
-// f in [-1/2, 1/2]; 2^f is a cubic fitted to minimise the maximum relative
-// error on [-1/2, 1/2] (Remez exchange on the relative error, fitted for this
-// library: max relative error 7.5e-5, well below bf16's 2^-9); 2^i is added
-// to the exponent field. Inputs below -125 are clamped (the result is then
-// 2^-125 instead of 0); callers use it only where every input is a live key.
+// f in [-1/2, 1/2]; 2^f is the cubic that minimises the maximum relative
+// error on [-1/2, 1/2] (Remez exchange on the relative error: max relative
+// error 7.48e-5, well below bf16's 2^-9); 2^i is added to the exponent
+// field. Inputs below -125 are clamped, so the result is 2^-125, not 0.
+// The prefill softmax passes -inf for masked columns: such a column then
+// weighs 2^-125 (about 2.4e-38) in the row sum and in P V, where the row's
+// largest term weighs at least 1, and a row that has seen no key yet drops
+// it when its running maximum first becomes finite (rescale by 2^-inf = 0).
 __device__ __forceinline__ float exp2_poly(float x) {
   constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
   constexpr float c3 = 0.0551716685f, c2 = 0.2426111251f, c1 = 0.6932609677f,

@@ -10,6 +10,7 @@
 // an id; evictions before allocations, in (seq_ids order, head, page) order.
 // All planning is host-only and never waits on the device.
 #include <algorithm>
+#include <cassert>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -167,9 +168,12 @@ struct Pack {
 // largest key, so the root is the least loaded list (the lowest index on
 // ties). add() raises one list's load and redoes the path above its leaf,
 // keeping the running minimum in a register. Lists < 65,536, loads < 2^47.
+constexpr int kMaxPlanCtas = 65535;  // LeastLoaded packs a list index into 16 bits
+
 class LeastLoaded {
  public:
   void reset(int lists) {
+    assert(lists >= 1 && lists <= kMaxPlanCtas);
     leaves_ = 1;
     while (leaves_ < static_cast<size_t>(lists)) leaves_ <<= 1;
     tree_.assign(2 * leaves_, ~0ull);
@@ -437,6 +441,13 @@ int segkv_destroy(segkv_t h) {
 
 const char* segkv_last_error(segkv_t h) {
   return h ? h->err.c_str() : g_create_error.c_str();
+}
+
+int segkv_exp2_check(const float* x, float* y_poly, float* y_mufu, int n, segkv_stream_t stream) {
+  if (n < 0 || (n > 0 && (!x || !y_poly || !y_mufu))) return SEGKV_ERR_INVALID_ARG;
+  if (n == 0) return SEGKV_OK;
+  const cudaError_t e = skv::launch_exp2_check(x, y_poly, y_mufu, n, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SEGKV_OK : SEGKV_ERR_CUDA;
 }
 
 int segkv_set_debug(segkv_t h, int flags) {
@@ -801,6 +812,8 @@ int segkv_plan_prefill(segkv_t h, int layer, const int32_t* cu_seqlens, const in
   if (!q_pos) return fail(h, SEGKV_ERR_INVALID_ARG, "q_pos NULL");
   const int vrc = prefill_validate(h, layer, cu_seqlens, q_pos, seq_ids, n);
   if (vrc != SEGKV_OK) return vrc;
+  if (num_ctas > kMaxPlanCtas)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "num_ctas %d above %d", num_ctas, kMaxPlanCtas);
   const int ctas = num_ctas > 0 ? num_ctas : (h->num_sms > 0 ? h->num_sms : 1);
   prefill_plan(h, layer, cu_seqlens, q_pos, seq_ids, n, ctas);
   const std::vector<PrefillUnit>& by_cta = h->pplan.by_cta;
@@ -1844,6 +1857,8 @@ int segkv_plan_mass(segkv_t h, int layer, const int32_t* cu_seqlens, const int32
       return fail(h, SEGKV_ERR_INVALID_ARG, "cu_seqlens decreases at %d", i);
   if (cu_seqlens[n] == 0) return SEGKV_OK;
   if (!q_pos) return fail(h, SEGKV_ERR_INVALID_ARG, "q_pos NULL");
+  if (num_ctas > kMaxPlanCtas)
+    return fail(h, SEGKV_ERR_INVALID_ARG, "num_ctas %d above %d", num_ctas, kMaxPlanCtas);
   const int ctas = num_ctas > 0 ? num_ctas : std::max(1, h->num_sms);
   MassPlan M;
   const int rc = mass_plan(h, layer, cu_seqlens, q_pos, seq_ids, n, ctas, M);

@@ -237,6 +237,7 @@ cudaError_t launch_plan_copy(const void* src, void* dst, size_t bytes, cudaStrea
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, int head_dim, int grid, cudaStream_t s);
 int prefill_smem_bytes(int head_dim);
+cudaError_t launch_exp2_check(const float* x, float* y_poly, float* y_mufu, int n, cudaStream_t s);
 int prefill_unit_tokens(int G);  // query tokens per prefill work unit
 cudaError_t launch_decode(const DecodeParams& p, const PlanBlob* blob, int head_dim, int grid,
                           cudaStream_t s);

@@ -361,7 +361,10 @@ const char* segkv_last_error(segkv_t h);
  *   SEGKV_ERR_INVALID_ARG with a message; use segkv_decode_attn then.
  *   The call allocates no memory. Its first call on a device looks up the
  *   array's device address (cudaGetSymbolAddress) with the handle's device
- *   current, so make that first call before any stream capture.
+ *   current, so make that first call before any stream capture. The address
+ *   is kept for the life of the process: after a cudaDeviceReset (which also
+ *   invalidates every handle on that device) this entry point may not be
+ *   used again in the same process.
  *   Every call shares the one array: calls that overlap on the GPU (other
  *   streams, other handles) race. The caller clears nothing: each call
  *   resets, on its stream, the counters it keeps there.
@@ -377,7 +380,8 @@ int segkv_decode_attn_noalloc(segkv_t h, int layer, const void* q, const int32_t
  * tests and tools. A unit is one KV head x the query rows of two 128-row tiles
  * (2 x 128 / G tokens of one sequence); units are dealt to num_ctas lists by
  * longest-processing-time-first and grouped by list.
- *   num_ctas    > 0: plan for that many CTAs; otherwise one per SM.
+ *   num_ctas    > 0: plan for that many CTAs (at most 65,535, else
+ *               SEGKV_ERR_INVALID_ARG); otherwise one per SM.
  *   units       host int32 [max_units][8], out: first token (index into the
  *               call's packed tokens), tokens, KV head, 1 if local, key tiles
  *               kt0 .. kt1 (128 keys each), lowest and highest key any of
@@ -397,7 +401,8 @@ int segkv_plan_prefill(segkv_t h, int layer, const int32_t* cu_seqlens, const in
  * chunk, over the query tiles (128 / G tokens each, chunk-relative) that see
  * some of its keys; a key tile seen by many query tiles is cut into pieces.
  * Units are dealt to num_ctas lists by longest-processing-time-first.
- *   num_ctas    > 0: plan for that many CTAs; otherwise one per SM.
+ *   num_ctas    > 0: plan for that many CTAs (at most 65,535, else
+ *               SEGKV_ERR_INVALID_ARG); otherwise one per SM.
  *   units       host int32 [max_units][12], out: first token of the chunk
  *               (index into the call's packed tokens), chunk length, position
  *               of its first token, KV head, 1 if local, key tile, query
@@ -431,6 +436,18 @@ int segkv_plan_mass(segkv_t h, int layer, const int32_t* cu_seqlens, const int32
 int segkv_plan_decode(segkv_t h, int layer, int T, const int32_t* seq_lens, const int32_t* seq_ids,
                       int n, int num_ctas, int32_t* units, int max_units, int32_t* cta_begin,
                       int max_ctas, int* n_units, int* n_ctas);
+
+/* segkv_exp2_check — test hook for the two base-2 exponentials that the
+ * prefill softmax uses to form p = 2^(s*scale*log2(e) - m) (online softmax
+ * with the running maximum kept as an offset: KV-cache architecture page,
+ * section 5.2). For i < n it writes
+ *   y_poly[i] = the cubic on the FMA pipe (2^x = 2^i * 2^f, f in [-1/2, 1/2],
+ *               2^f by the minimax cubic on relative error, max 7.48e-5;
+ *               inputs below -125, -inf included, give 2^-125),
+ *   y_mufu[i] = the hardware ex2.approx.ftz (2^-inf = 0).
+ * x, y_poly, y_mufu are device fp32 [n]; stream-ordered on stream.
+ * Errors: SEGKV_ERR_INVALID_ARG (n < 0 or a NULL array), SEGKV_ERR_CUDA. */
+int segkv_exp2_check(const float* x, float* y_poly, float* y_mufu, int n, segkv_stream_t stream);
 
 /* segkv_set_debug — test hook. Bit 0: the next prefill launch makes one wait
  * on a barrier that nothing signals, with a short limit, so the timeout path

@@ -26,3 +26,20 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The flat max-abs / mean-abs of every parity comparison that ran."""
+    try:
+        import harness
+    except ImportError:
+        return
+    if not harness.RECORDS:
+        return
+    tr = terminalreporter
+    tr.section("parity against the fp64 oracle (flat max-abs bar 1e-2, mean-abs 1e-3)")
+    worst = max(r[1] for r in harness.RECORDS)
+    for what, mx, mean, size, rounding in harness.RECORDS:
+        tag = "  [bf16 output-rounding allowance]" if rounding else ""
+        tr.write_line(f"{mx:.3e}  {mean:.3e}  {size:>10d}  {what}{tag}")
+    tr.write_line(f"{len(harness.RECORDS)} comparisons; largest flat max-abs {worst:.3e}")

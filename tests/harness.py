@@ -10,24 +10,43 @@ import head_segmented_paged_gb300 as S
 import oracle
 from head_segmented_paged_gb300 import inputs as I
 
-# Output bar: the stated 1e-2 max-abs / 1e-3 mean-abs, plus the half-ulp of
-# the bf16 output rounding (2^-8 |o| bounds it), since O is returned in bf16.
+# Output bar, as stated for the method: max-abs <= 1e-2 and mean-abs <= 1e-3
+# of the bf16 GPU output against the fp64 oracle, element by element.
 MAX_ABS = 1e-2
 MEAN_ABS = 1e-3
-BF16_HALF_ULP_REL = 2.0 ** -8
+
+# Every comparison's flat max-abs and mean-abs, in call order; the test
+# session prints them at its end (tests/conftest.py).
+RECORDS: list = []
 
 
-def check_close(o_gpu, o_ref, what=""):
-    g = o_gpu.detach().to("cpu", torch.float64).numpy()
+def bf16_half_ulp(x):
+    """Half a unit in the last place of bf16 (8 significant bits) at |x|:
+    2^(floor(log2 |x|) - 8) for normal values."""
+    a = np.maximum(np.abs(np.asarray(x, np.float64)), 2.0 ** -126)
+    return np.ldexp(1.0, np.floor(np.log2(a)).astype(np.int64) - 8)
+
+
+def check_close(o_gpu, o_ref, what="", output_rounding=False):
+    """Assert the flat bar: max |o_gpu - o_ref| <= 1e-2, mean <= 1e-3.
+
+    output_rounding=True is for a named case whose outputs reach |o| >= 4,
+    where the bf16 half-ulp of the returned value alone (2^-6 from 4 on)
+    exceeds 1e-2: each element may then also carry exactly the bf16
+    half-ulp of its oracle value. No case uses it unless it names it."""
+    g = o_gpu.detach().to("cpu", torch.float64).numpy() if torch.is_tensor(o_gpu) else \
+        np.asarray(o_gpu, np.float64)
     assert np.isfinite(g).all(), f"{what}: non-finite output"
     err = np.abs(g - o_ref)
-    bound = MAX_ABS + BF16_HALF_ULP_REL * np.abs(o_ref)
+    bound = MAX_ABS + (bf16_half_ulp(o_ref) if output_rounding else 0.0)
+    mx, mean = float(err.max()), float(err.mean())
+    RECORDS.append((what, mx, mean, err.size, output_rounding))
     worst = np.argmax(err - bound)
-    assert (err <= bound).all(), (f"{what}: max err {err.max():.3e} "
+    assert (err <= bound).all(), (f"{what}: max err {mx:.3e} "
                                   f"at {np.unravel_index(worst, err.shape)}, ref "
                                   f"{o_ref.reshape(-1)[worst]:.4f}")
-    assert err.mean() <= MEAN_ABS, f"{what}: mean err {err.mean():.3e}"
-    return float(err.max()), float(err.mean())
+    assert mean <= MEAN_ABS, f"{what}: mean err {mean:.3e}"
+    return mx, mean
 
 
 class Cache:

@@ -140,8 +140,8 @@ def test_empty_calls_are_noops():
     assert c.h.status() == 0
 
 
-# 64 dims run the single-SM prefill kernel, 128 the SM-pair kernel (whose
-# second CTA gives up on its own bounded waits once the leader has stopped)
+# both head dims of the prefill kernel: the MMA issuer's wait expires, then
+# every other warp's bounded wait sees the block's abort flag and returns
 @pytest.mark.parametrize("d", [64, 128])
 def test_device_timeout_path_reports_status_and_context_survives(d):
     w = I.tiny_256() if d == 64 else I.Workload("tiny128", 1, 8, 2, 128, 16, [[I.GLOBAL, I.LOCAL]],

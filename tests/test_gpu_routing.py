@@ -16,6 +16,7 @@ import torch
 
 import head_segmented_paged_gb300 as S
 from head_segmented_paged_gb300 import inputs as I
+import oracle
 from harness import Cache, oracle_mass
 from oracle import sparse_ffn as F
 
@@ -146,6 +147,29 @@ def test_topk_matches_oracle_bit_for_bit(lens, ks, levels):
         off += kk
 
 
+def score_tolerance(ref_mass):
+    """Per-token bound on |GPU score - fp64 score|: the per-head mass bound
+    summed over the KV heads, plus fp32 rounding of that sum."""
+    return (RTOL * np.abs(ref_mass) + ATOL).sum(axis=0) + 2.0 ** -22 * ref_mass.sum(axis=0)
+
+
+def check_valid_topk(idx, ref_score, tol, k):
+    """idx must be a valid top-k of the fp64 scores within the tolerance:
+    k distinct positions, and no unchosen token's score exceeds a chosen
+    token's by more than both tolerances (several sets are correct where
+    scores sit within the tolerance of the k-th largest)."""
+    n = ref_score.shape[0]
+    assert idx.shape == (k,) and len(np.unique(idx)) == k
+    assert ((0 <= idx) & (idx < n)).all() and (np.diff(idx) > 0).all()
+    chosen = np.zeros(n, bool)
+    chosen[idx] = True
+    if 0 < k < n:
+        lo = (ref_score[chosen] + tol[chosen]).min()
+        hi = (ref_score[~chosen] - tol[~chosen]).max()
+        assert lo >= hi, (lo, hi)
+    return chosen
+
+
 def test_routing_end_to_end():
     # chunk -> prefill (LSE) -> mass -> top-k -> FFN on the chosen rows
     hkv, G, d, P, W = 2, 4, 128, 64, 128
@@ -159,20 +183,38 @@ def test_routing_end_to_end():
     mass = chunk_mass(c, 0, q, cu, qp, [0])
     check_mass(c, 0, q, cu, qp, [0], mass)
     score, idx = run_topk(c.h, mass, cu, [kk])
+    # stage check: the choice on the GPU's own fp32 scores, bit for bit
     assert np.array_equal(idx, F.topk_tokens(fp32_score(mass).astype(np.float64), kk))
+    # end to end: the choice is a valid top-k of the oracle's fp64 scores
+    rc, ref_mass, _ = oracle_mass(c, 0, q, [0], np.zeros(n, np.int32), qp)
+    assert rc == 0
+    ref_score = ref_mass.sum(axis=0)
+    check_valid_topk(idx, ref_score, score_tolerance(ref_mass), kk)
+    sel_ref = F.topk_tokens(ref_score, kk)  # the oracle's own choice
     w = I.FfnWorkload("t", n, dm, dff, kk, 5)
     x, r, wg, wu, wd = I.ffn_tensors(w, device="cuda")
     out = r.clone()
     c.h.sparse_ffn(x, out, torch.tensor(idx, dtype=torch.int32, device="cuda"), wg, wu, wd)
     assert c.h.status() == 0
-    ref, hh = F.sparse_ffn(*(t.to(torch.float64).cpu().numpy() for t in (x, r)), idx,
-                           *(t.to(torch.float64).cpu().numpy() for t in (wg, wu, wd)))
+    host = [t.to(torch.float64).cpu().numpy() for t in (x, r, wg, wu, wd)]
     got = out.to(torch.float64).cpu().numpy()
-    sig = 2.0 ** -8 / np.sqrt(3) * np.sqrt((hh ** 2) @ (wd.to(torch.float64).cpu().numpy() ** 2).T)
-    err = np.abs(got[idx] - ref[idx])
-    assert (err <= 2.0 ** -8 * np.abs(ref[idx]) + 6 * sig + 1e-3).all()
+    sig_w = host[4] ** 2
+
+    def check_rows(rows, ref, hh_rows):
+        sig = 2.0 ** -8 / np.sqrt(3) * np.sqrt((hh_rows ** 2) @ sig_w.T)
+        err = np.abs(got[rows] - ref[rows])
+        assert (err <= 2.0 ** -8 * np.abs(ref[rows]) + 6 * sig + 1e-3).all()
+
+    # the oracle FFN on the oracle's own choice, on every row both choose
+    ref_o, hh_o = F.sparse_ffn(host[0], host[1], sel_ref, *host[2:])
+    both = np.intersect1d(idx, sel_ref)
+    check_rows(both, ref_o, hh_o[np.searchsorted(sel_ref, both)])
+    # rows where the two valid choices differ: the oracle FFN on the GPU's set
+    ref_g, hh_g = F.sparse_ffn(host[0], host[1], idx, *host[2:])
+    only = np.setdiff1d(idx, sel_ref)
+    check_rows(only, ref_g, hh_g[np.searchsorted(idx, only)])
     rest = np.setdiff1d(np.arange(n), idx)
-    assert np.array_equal(got[rest], ref[rest])
+    assert np.array_equal(got[rest], host[1][rest])  # residual identity, bit for bit
 
 
 def test_mass_mistral_8k_conserves_probability():
@@ -196,3 +238,16 @@ def test_mass_mistral_8k_conserves_probability():
     m = mass.cpu().numpy().astype(np.float64)
     assert (m >= 0).all()
     np.testing.assert_allclose(m.sum(axis=1), w.group * n, rtol=1e-4)
+    # element by element against the oracle's fp64 mass, every key
+    rc, ref = oracle.attn_mass(q.cpu(), k.cpu(), np.zeros(n, np.int32), qp.numpy(), [0], [n],
+                               w.head_class[0], w.window[0], np.zeros((1, w.hkv), np.int32))
+    assert rc == 0
+    bad = np.abs(m - ref) > RTOL * np.abs(ref) + ATOL
+    assert not bad.any(), (np.argwhere(bad)[:5], m[bad][:5], ref[bad][:5])
+    # the top-k of a quarter of the chunk is a valid top-k of the fp64 scores
+    kk = n // 4
+    score = torch.empty((n,), device="cuda")
+    idx = torch.empty((kk,), dtype=torch.int32, device="cuda")
+    h.topk_tokens(mass, cu, [kk], score, idx)
+    assert h.status() == 0
+    check_valid_topk(idx.cpu().numpy().astype(np.int64), ref.sum(axis=0), score_tolerance(ref), kk)

@@ -2,10 +2,13 @@
 
 segkv_decode_attn_noalloc serves callers that cannot allocate device memory
 when they decode (no per-call workspace): it keeps its split partials in a
-fixed array inside the library. Its outputs must match segkv_decode_attn's
-on the same cache, on consecutive calls, and it must refuse a call whose
+fixed array inside the library. It runs the same plan and kernels as
+segkv_decode_attn, only with another partials buffer, so its outputs must
+equal that call's bit for bit on the same cache, on consecutive calls, and
+match the fp64 oracle within the output bar; it must refuse a call whose
 partials do not fit. This file is collected last.
 """
+import numpy as np
 import pytest
 import torch
 
@@ -40,7 +43,11 @@ def test_noalloc_decode_matches_workspace_decode_on_consecutive_calls():
         rc = S.segkv_decode_attn_noalloc(c.h.handle, 0, qd, cur, ids, o_na)
         assert rc == 0, S.segkv_last_error(c.h.handle)
         assert c.h.status() == 0
-        check_close(o_na, o_ref.to(torch.float64).cpu().numpy(), f"no-alloc step {step}")
+        assert torch.equal(o_na.view(torch.int16), o_ref.view(torch.int16)), f"step {step}"
+        rc, ref, _ = c.oracle_attention(0, qd.cpu(), ids, np.arange(B, dtype=np.int32),
+                                        np.array(cur, np.int32) - 1)
+        assert rc == 0
+        check_close(o_na, ref, f"no-alloc decode step {step}")
 
 
 def test_noalloc_decode_refuses_plans_beyond_its_scratch():
