@@ -18,12 +18,17 @@
 //   warp 0      TMA producer: Q tiles A and B, then K and V tiles (2 stages),
 //               block-table entries fetched 32 at a time by the whole warp;
 //   warp 1      TMEM owner and MMA issuer: S_X = Q_X K^T (X = A, B) into TMEM,
-//               then O_X += P_X V with P_X read back from TMEM;
+//               then O_X += P_X V with P_X read back from TMEM, as one stream
+//               across the CTA's units; every MMA is issued from descriptors
+//               computed once, because the issuing thread shares its
+//               sub-partition with two softmax warps and the tensor pipe
+//               drains whenever it is starved of issue slots;
 //   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B (one thread
 //               per row): read S from TMEM, mask only on edge tiles, update
 //               the running max (O is rescaled in TMEM only when the max grows
 //               by more than 2^8, which is exact), write P as bf16 over S; at
-//               the end of a unit, normalise O and store it.
+//               the end of a unit, normalise O and store it. Unit descriptors
+//               come from the producer through a shared-memory ring.
 // TMEM columns: S_A [0,128), S_B [128,256) (P_X aliases the first 64 columns
 // of S_X), O_A [256, 256+D), O_B [384, 384+D).
 //
@@ -65,8 +70,14 @@ enum {
   B_O_EMPTY = 16,  // +X
   B_NEVER = 18,
   B_DRAIN = 19,
-  NUM_BARS = 20
+  B_DESC = 20,     // +slot: the producer has written that slot's unit descriptor
+  NUM_BARS = 24
 };
+// Unit descriptors reach the softmax warps through a ring of kDescSlots
+// shared-memory slots written by the producer. The producer starts unit u
+// only after the softmax of unit u-2's tiles is done in every softmax warp,
+// so it runs at most three units ahead and no slot is overwritten unread.
+constexpr int kDescSlots = 4;
 
 template <int D>
 struct Layout {
@@ -76,7 +87,8 @@ struct Layout {
   static constexpr uint32_t OFF_K = OFF_Q + 2 * Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + 2 * KV_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_V + 2 * KV_BYTES;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr uint32_t OFF_DESC = OFF_BAR + NUM_BARS * 8;
+  static constexpr uint32_t OFF_MISC = OFF_DESC + kDescSlots * sizeof(PrefillUnit);
   // + slack to align to 1 KB; at least 116 KB so that one CTA holds an SM (and
   // its 512 TMEM columns) alone
   static constexpr uint32_t RAW = OFF_MISC + 16 + 1024;
@@ -110,6 +122,10 @@ __device__ void producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const C
   int g = 0, ui = 0;
   for (int u = p.cta_begin[blockIdx.x]; ok && u < p.cta_begin[blockIdx.x + 1]; ++u, ++ui) {
     const PrefillUnit U = p.units[u];
+    if (lane == 0) {  // publish the descriptor to the softmax warps (arrive = release)
+      reinterpret_cast<PrefillUnit*>(c.smem + L::OFF_DESC)[ui % kDescSlots] = U;
+      mbar_arrive(c.bar(B_DESC + ui % kDescSlots));
+    }
     for (int x = 0; x < 2; ++x) {
       if (!waitw(c.bar(B_Q_EMPTY + x), (ui & 1) ^ 1, c.wc)) { ok = false; break; }
       if (lane == 0) {
@@ -165,33 +181,60 @@ __device__ void producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const C
 }
 
 // ---------------------------------------------------------------- MMA issuer
+// The issuing thread shares its sub-partition with a softmax warp, so each
+// MMA is issued from precomputed descriptors: the descriptors of the six
+// shared-memory operands (Q tiles A and B, K and V of both stages) are built
+// once, and an MMA's own descriptor adds its compile-time offset (in 16-byte
+// units, which never carries out of the 14-bit address field) to the low
+// word.
+struct MmaDescs {
+  uint64_t q[2], k[2], v[2];
+};
+
+__device__ __forceinline__ uint64_t desc_add(uint64_t base, uint32_t off16) {
+  return base + off16;  // the address field is the low 14 bits; no carry out
+}
+
 template <int D>
-__device__ __forceinline__ void issue_s(const Ctx& c, int x, int st) {
+__device__ __forceinline__ MmaDescs mma_descs(const Ctx& c) {
   using L = Layout<D>;
+  MmaDescs m;
+  for (int i = 0; i < 2; ++i) {
+    m.q[i] = sdesc_sw128(c.sbase + L::OFF_Q + i * L::Q_BYTES, 16, 1024);
+    m.k[i] = sdesc_sw128(c.sbase + L::OFF_K + i * L::KV_BYTES, 16, 1024);
+    m.v[i] = sdesc_sw128(c.sbase + L::OFF_V + i * L::KV_BYTES, kAtom, 1024);
+  }
+  return m;
+}
+
+template <int D>
+__device__ __forceinline__ void issue_s(const Ctx& c, const MmaDescs& m, int x, int st) {
   constexpr uint32_t IDESC_QK = idesc_bf16(BM, BN, 0);
+  const uint64_t qa = x ? m.q[1] : m.q[0], kb = st ? m.k[1] : m.k[0];
+  const uint32_t d = c.tmem + x * BN;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t a = c.sbase + L::OFF_Q + x * L::Q_BYTES + (kk >> 2) * kAtom + (kk & 3) * 32;
-    const uint32_t b = c.sbase + L::OFF_K + st * L::KV_BYTES + (kk >> 2) * kAtom + (kk & 3) * 32;
-    mma_bf16(c.tmem + x * BN, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, 16, 1024), IDESC_QK,
-             kk > 0 ? 1u : 0u);
+    const uint32_t off16 = ((kk >> 2) * kAtom + (kk & 3) * 32) >> 4;
+    mma_bf16(d, desc_add(qa, off16), desc_add(kb, off16), IDESC_QK, kk > 0 ? 1u : 0u);
   }
 }
 
 template <int D>
-__device__ __forceinline__ void issue_pv(const Ctx& c, int x, int st, bool first) {
+__device__ __forceinline__ void issue_pv(const Ctx& c, const MmaDescs& m, int x, int st,
+                                         bool first) {
   using L = Layout<D>;
   constexpr uint32_t IDESC_PV = idesc_bf16(BM, D, 1);
+  const uint64_t vb = st ? m.v[1] : m.v[0];
+  const uint32_t d = c.tmem + L::TM_O + x * L::TM_O_STRIDE, a = c.tmem + x * BN;
 #pragma unroll
-  for (int kk = 0; kk < BN / 16; ++kk) {
-    const uint32_t b = c.sbase + L::OFF_V + st * L::KV_BYTES + kk * 2048;
-    mma_bf16_ts(c.tmem + L::TM_O + x * L::TM_O_STRIDE, c.tmem + x * BN + kk * 8,
-                sdesc_sw128(b, kAtom, 1024), IDESC_PV, (first && kk == 0) ? 0u : 1u);
-  }
+  for (int kk = 0; kk < BN / 16; ++kk)
+    mma_bf16_ts(d, a + kk * 8, desc_add(vb, kk * 2048 / 16), IDESC_PV,
+                (first && kk == 0) ? 0u : 1u);
 }
 
 template <int D>
 __device__ void mma_issuer(const PrefillParams& p, const Ctx& c) {
+  const MmaDescs md = mma_descs<D>(c);
   bool ok = true;
   if (p.debug & 1) {  // test hook: one wait on a barrier nothing signals
     WaitCtx w = c.wc;
@@ -199,23 +242,31 @@ __device__ void mma_issuer(const PrefillParams& p, const Ctx& c) {
     wait1(c.bar(B_NEVER), 0, w);
     ok = false;
   }
-  int g = 0, ui = 0;
-  for (int u = p.cta_begin[blockIdx.x]; ok && u < p.cta_begin[blockIdx.x + 1]; ++u, ++ui) {
-    const PrefillUnit U = p.units[u];
-    const int nt = U.kt1 - U.kt0 + 1;
-    const uint32_t qpar = ui & 1;
-    // prologue: S_A and S_B of the first key tile
-    if (!wait1(c.bar(B_K_FULL + (g & 1)), (g >> 1) & 1, c.wc)) { ok = false; break; }
-    for (int x = 0; x < 2; ++x) {
-      if (!wait1(c.bar(B_Q_FULL + x), qpar, c.wc)) { ok = false; break; }
+  // The MMAs run as one stream across the CTA's units: S_A and S_B of the
+  // next unit's first key tile follow this unit's last P V MMAs directly,
+  // with no descriptor load in between. The next unit's key-tile range is
+  // read one unit ahead.
+  const int u0 = p.cta_begin[blockIdx.x], n_units = p.cta_begin[blockIdx.x + 1] - u0;
+  int g = 0;
+  int nt_next = n_units > 0 ? p.units[u0].kt1 - p.units[u0].kt0 + 1 : 0;
+  // S_A and S_B of the first unit's first key tile
+  if (ok && n_units > 0) {
+    if (!wait1(c.bar(B_K_FULL + 0), 0, c.wc)) ok = false;
+    for (int x = 0; ok && x < 2; ++x) {
+      if (!wait1(c.bar(B_Q_FULL + x), 0, c.wc)) { ok = false; break; }
       tc_fence_after();
-      issue_s<D>(c, x, g & 1);
+      issue_s<D>(c, md, x, 0);
       mma_commit(c.bar(B_S_FULL + x));
-      if (nt == 1) mma_commit(c.bar(B_Q_EMPTY + x));
+      if (nt_next == 1) mma_commit(c.bar(B_Q_EMPTY + x));
     }
-    if (!ok) break;
+  }
+  for (int ui = 0; ok && ui < n_units; ++ui) {
+    const int nt = nt_next;
+    const bool more = ui + 1 < n_units;
+    if (more) nt_next = p.units[u0 + ui + 1].kt1 - p.units[u0 + ui + 1].kt0 + 1;
+    const uint32_t qpar = ui & 1;
     for (int i = 0; i < nt && ok; ++i) {
-      const int gi = g + i, st = gi & 1;
+      const int gi = g + i, st = gi & 1, gn = gi + 1;
       const uint32_t ph = (gi >> 1) & 1;
       const bool last = (i + 1 == nt);
       for (int x = 0; x < 2; ++x) {
@@ -223,18 +274,30 @@ __device__ void mma_issuer(const PrefillParams& p, const Ctx& c) {
         if (!wait1(c.bar(B_P_FULL + x), gi & 1, c.wc)) { ok = false; break; }
         if (x == 0 && !wait1(c.bar(B_V_FULL + st), ph, c.wc)) { ok = false; break; }
         tc_fence_after();
-        issue_pv<D>(c, x, st, i == 0);
+        issue_pv<D>(c, md, x, st, i == 0);
         if (x == 1) mma_commit(c.bar(B_KV_EMPTY + st));
-        if (!last) {
-          const int gn = gi + 1;
-          if (x == 0 && !wait1(c.bar(B_K_FULL + (gn & 1)), (gn >> 1) & 1, c.wc)) { ok = false; break; }
-          tc_fence_after();
-          issue_s<D>(c, x, gn & 1);
-          mma_commit(c.bar(B_S_FULL + x));
-          if (i + 2 == nt) mma_commit(c.bar(B_Q_EMPTY + x));
-        } else {
+        if (last) {
           mma_commit(c.bar(B_O_FULL + x));
+          continue;
         }
+        if (x == 0 && !wait1(c.bar(B_K_FULL + (gn & 1)), (gn >> 1) & 1, c.wc)) { ok = false; break; }
+        tc_fence_after();
+        issue_s<D>(c, md, x, gn & 1);
+        mma_commit(c.bar(B_S_FULL + x));
+        if (i + 2 == nt) mma_commit(c.bar(B_Q_EMPTY + x));  // the unit's last S MMAs
+      }
+    }
+    // S_A and S_B of the next unit's first key tile, issued behind this
+    // unit's last P V MMAs without waiting on anything else
+    if (ok && more) {
+      const int gn = g + nt;
+      if (!wait1(c.bar(B_K_FULL + (gn & 1)), (gn >> 1) & 1, c.wc)) { ok = false; break; }
+      for (int x = 0; x < 2; ++x) {
+        if (!wait1(c.bar(B_Q_FULL + x), qpar ^ 1, c.wc)) { ok = false; break; }
+        tc_fence_after();
+        issue_s<D>(c, md, x, gn & 1);
+        mma_commit(c.bar(B_S_FULL + x));
+        if (nt_next == 1) mma_commit(c.bar(B_Q_EMPTY + x));
       }
     }
     g += nt;
@@ -257,18 +320,22 @@ __device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int x, in
   const uint32_t t_o = c.tmem + lane_off + L::TM_O + x * L::TM_O_STRIDE;
   const float scale = p.scale_log2;
   int g = 0, ui = 0;
-  for (int u = p.cta_begin[blockIdx.x]; u < p.cta_begin[blockIdx.x + 1]; ++u, ++ui) {
-    const PrefillUnit U = p.units[u];
+  const int n_units = p.cta_begin[blockIdx.x + 1] - p.cta_begin[blockIdx.x];
+  for (; ui < n_units; ++ui) {
+    // the unit's descriptor, from the producer's ring; consecutive query
+    // positions come with it (pos0), so no per-row load of q_pos is needed
+    if (!waitw(c.bar(B_DESC + ui % kDescSlots), (ui / kDescSlots) & 1, c.wc)) break;
+    const PrefillUnit U = reinterpret_cast<const PrefillUnit*>(c.smem + L::OFF_DESC)[ui % kDescSlots];
     const int nt = U.kt1 - U.kt0 + 1;
     const int t = x * p.tpt + r / p.G, gg = r % p.G;
     const bool row_ok = t < U.ntok;
     const int tok = U.tok0 + t;
     int hi = -1, lo = 1 << 30;  // an invalid row sees no key
     if (row_ok) {
-      hi = p.q_pos[tok];
+      hi = U.pos0 >= 0 ? U.pos0 + t : p.q_pos[tok];
       lo = U.local ? max(0, hi - p.window + 1) : 0;
     }
-    float m_used = -INFINITY, l = 0.f;
+    float m_used = -INFINITY, l = 0.f, lc = 0.f;
     bool ok = true;
     for (int i = 0; i < nt; ++i) {
       const int gi = g + i, st = gi & 1;
@@ -297,7 +364,8 @@ __device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int x, in
         m4[2] = max3(m4[2], s[e + 4], s[e + 5]);
         m4[3] = max3(m4[3], s[e + 6], s[e + 7]);
       }
-      const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale;
+      const float smax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      const float mx = smax * scale;
       const float m_new = fmaxf(m_used, mx);
       const bool resc = m_new > m_used + kRescaleLog2;
       const float m_tgt = resc ? m_new : m_used;
@@ -305,6 +373,7 @@ __device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int x, in
       const float neg_m = (m_tgt == -INFINITY) ? 0.f : -m_tgt;
 
       l *= alpha;
+      lc *= alpha;
 
       // p = 2^(s * scale - m), two columns per packed FMA/add
       const float2 sc2 = make_float2(scale, scale), nm2 = make_float2(neg_m, neg_m);
@@ -324,6 +393,15 @@ __device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int x, in
         tmem_st16(t_s + q * 16, pk);
       }
       l += (rs[0].x + rs[0].y) + (rs[1].x + rs[1].y);
+      {
+        // P is rounded to bf16 for the P V MMA while l sums the fp32 values.
+        // Where attention concentrates on a few keys, the rounding of the
+        // largest P dominates the error of O, so O's normaliser also adds the
+        // rounding error of each tile's largest P (same FMA and ex2 as its
+        // column above); the LSE keeps the exact sum.
+        const float pm = ex2(fmaf(smax, scale, neg_m));
+        lc += __bfloat162float(__float2bfloat16_rn(pm)) - pm;
+      }
 
       if (i > 0 && __any_sync(0xffffffffu, resc)) {  // O_X is stable: P V of tile i-1 is done
 #pragma unroll
@@ -362,7 +440,7 @@ __device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int x, in
 
     if (!waitw(c.bar(B_O_FULL + x), ui & 1, c.wc)) break;
     tc_fence_after();
-    const float inv_l = row_ok ? 1.f / l : 0.f;
+    const float inv_l = row_ok ? 1.f / (l + lc) : 0.f;
     __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) +
                           (static_cast<int64_t>(tok) * p.hq + U.head * p.G + gg) * D;
 #pragma unroll
@@ -426,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(c.bar(B_NEVER), 1);
     mbar_init(c.bar(B_DRAIN), 1);
+    for (int d = 0; d < kDescSlots; ++d) mbar_init(c.bar(B_DESC + d), 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tmq);

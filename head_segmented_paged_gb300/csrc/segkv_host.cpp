@@ -640,9 +640,11 @@ static void prefill_plan(segkv* h, int layer, const int32_t* cu_seqlens, const i
     for (int32_t t0 = cu_seqlens[i]; t0 < cu_seqlens[i + 1]; t0 += unit_tok) {
       const int32_t t1 = std::min<int32_t>(t0 + unit_tok, cu_seqlens[i + 1]);
       int32_t pmin = q_pos[t0], pmax = q_pos[t0];
+      bool consecutive = true;
       for (int32_t t = t0; t < t1; ++t) {
         pmin = std::min(pmin, q_pos[t]);
         pmax = std::max(pmax, q_pos[t]);
+        consecutive = consecutive && q_pos[t] == q_pos[t0] + (t - t0);
       }
       for (int hd = 0; hd < h->Hkv; ++hd) {
         PrefillUnit u{};
@@ -658,6 +660,7 @@ static void prefill_plan(segkv* h, int layer, const int32_t* cu_seqlens, const i
         u.first_page = s0 / h->P;
         u.last_page = (nlen - 1) / h->P;
         u.table_row = static_cast<int32_t>(h->seg(layer, hd, b));
+        u.pos0 = consecutive ? q_pos[t0] : -1;
         units.push_back(u);
       }
     }

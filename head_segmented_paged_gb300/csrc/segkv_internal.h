@@ -64,8 +64,9 @@ struct PrefillUnit {
   int32_t first_page;  // first held logical page of the segment
   int32_t last_page;   // last held logical page
   int32_t table_row;   // (layer * Hkv + head) * max_seqs + seq
-  int32_t pad;
+  int32_t pos0;        // position of token tok0 + t is pos0 + t; -1: read q_pos
 };
+static_assert(sizeof(PrefillUnit) == 48, "prefill units are staged in 48-byte slots");
 struct PrefillParams {
   const PrefillUnit* units;    // grouped by CTA
   const int32_t* cta_begin;    // [grid + 1]: CTA c runs units cta_begin[c] .. cta_begin[c+1]-1

@@ -443,7 +443,10 @@ int segkv_plan_decode(segkv_t h, int layer, int T, const int32_t* seq_lens, cons
  * section 5.2). For i < n it writes
  *   y_poly[i] = the cubic on the FMA pipe (2^x = 2^i * 2^f, f in [-1/2, 1/2],
  *               2^f by the minimax cubic on relative error, max 7.48e-5;
- *               inputs below -125, -inf included, give 2^-125),
+ *               inputs below -125, -inf included, are clamped to -125, so
+ *               they give 2^-125 within the same bound; the softmax never
+ *               passes more than 8, and inputs above 127 are outside the
+ *               domain),
  *   y_mufu[i] = the hardware ex2.approx.ftz (2^-inf = 0).
  * x, y_poly, y_mufu are device fp32 [n]; stream-ordered on stream.
  * Errors: SEGKV_ERR_INVALID_ARG (n < 0 or a NULL array), SEGKV_ERR_CUDA. */

@@ -41,7 +41,8 @@ def gen_layer(w, layer_set, lens, device="cuda"):
     return q, k, v
 
 
-def run_prefill_case(w, head_class, window, q, k, v, lens, rows_per_seq, edge_stride=1):
+def run_prefill_case(w, head_class, window, q, k, v, lens, rows_per_seq, edge_stride=1,
+                     output_rounding=False):
     P, D = w.page_size, w.head_dim
     pages = sum((n + P - 1) // P for n in lens) * w.hkv + 8
     kp = torch.full((pages, P, D), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -64,7 +65,8 @@ def run_prefill_case(w, head_class, window, q, k, v, lens, rows_per_seq, edge_st
                                       np.zeros(len(pos), np.int32), pos.astype(np.int32), [0], [n],
                                       head_class, window, np.zeros((1, w.hkv), np.int32))
         assert rc == 0
-        check_close(o[torch.as_tensor(tok, device="cuda")], ref, f"{w.name} seq {b}")
+        check_close(o[torch.as_tensor(tok, device="cuda")], ref, f"{w.name} seq {b}",
+                    output_rounding=output_rounding)
     h.close()
 
 
@@ -76,6 +78,9 @@ def test_mistral_8k_prefill_sampled():
 
 
 def test_llama70b_varlen_with_sinks_sampled():
+    # Named output-rounding case: key rows scaled x8 concentrate attention on
+    # single keys, so outputs reach |o| >= 4 (one sampled element is -4.40),
+    # where the bf16 half-ulp of the returned value is 2^-6 = 0.0156 > 1e-2.
     w = I.llama70b_varlen()
     q, k, v = gen_layer(w, 0, w.seq_lens)
     off = 0
@@ -84,7 +89,8 @@ def test_llama70b_varlen_with_sinks_sampled():
         k[idx] = k[idx] * 8
         off += n
     run_prefill_case(w, w.head_class[0], w.window[0], q, k, v, w.seq_lens,
-                     lambda n: sample_positions(n, w.window[0], w.page_size, edge_stride=8))
+                     lambda n: sample_positions(n, w.window[0], w.page_size, edge_stride=8),
+                     output_rounding=True)
 
 
 @pytest.mark.parametrize("kind", ["shallow", "deep_g1", "deep_g0", "dense"])
