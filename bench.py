@@ -744,26 +744,31 @@ def run_transfer(dev, stream, hbm):
     vp2 = torch.empty_like(kp)
     dst = S.SegKV(1, 32, hkv, D, hc, [W], P, 1, n + 8, kp2, vp2)
 
-    def timed(fn, reps=20):
+    host_us = {}
+
+    def timed(name, fn, reps=20):
         for _ in range(3):
             fn()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
         e0.record(stream)
         for _ in range(reps):
             fn()
         e1.record(stream)
+        host_us[name] = round(1e6 * (time.perf_counter() - t0) / reps, 2)  # issue cost per call
         torch.cuda.synchronize()
         return 1e3 * e0.elapsed_time(e1) / reps
 
     hnd = src.handle
     header = np.zeros(1 + hkv, np.int32)
-    exp_us = timed(lambda: S.segkv_export(hnd, 0, 0, buf, header, stream))
+    exp_us = timed("export", lambda: S.segkv_export(hnd, 0, 0, buf, header, stream))
 
     def imp():
         dst.free_seq(0)
         dst.import_segment(0, 0, buf, hdr, stream)
-    imp_us = timed(imp)
+    imp_us = timed("import", imp)
     assert src.status() == 0 and dst.status() == 0
     seg_bytes = buf.numel() * 2
     dense_bytes = n * hkv * D * 2 * 2
@@ -777,6 +782,7 @@ def run_transfer(dev, stream, hbm):
             "import_gbs": round(2 * seg_bytes / (imp_us * 1e-6) / 1e9, 1),
             "kv_sessions_per_gb": {"segmented": round(1e9 / seg_bytes, 2),
                                    "dense": round(1e9 / dense_bytes, 2)},
+            "host_issue_us_per_call": host_us,
             "kernels": ["transfer_kernel"]}
 
 

@@ -89,9 +89,12 @@ struct Layout {
   static constexpr uint32_t OFF_BAR = OFF_V + 2 * KV_BYTES;
   static constexpr uint32_t OFF_DESC = OFF_BAR + NUM_BARS * 8;
   static constexpr uint32_t OFF_MISC = OFF_DESC + kDescSlots * sizeof(PrefillUnit);
+  // O staging for the bulk tensor stores: 32 rows x 64 columns per softmax warp
+  static constexpr uint32_t OFF_STAGE = (OFF_MISC + 16 + 1023) / 1024 * 1024;
+  static constexpr uint32_t STAGE_WARP = 32 * 128;
   // + slack to align to 1 KB; at least 116 KB so that one CTA holds an SM (and
   // its 512 TMEM columns) alone
-  static constexpr uint32_t RAW = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t RAW = OFF_STAGE + 8 * STAGE_WARP + 1024;
   static constexpr uint32_t BYTES = RAW > 116u * 1024 ? RAW : 116u * 1024;
   static constexpr uint32_t TM_O = 256;             // TMEM column of O_A
   static constexpr uint32_t TM_O_STRIDE = 128;      // O_B = O_A + this
@@ -122,6 +125,9 @@ __device__ void producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const C
   int g = 0, ui = 0;
   for (int u = p.cta_begin[blockIdx.x]; ok && u < p.cta_begin[blockIdx.x + 1]; ++u, ++ui) {
     const PrefillUnit U = p.units[u];
+    const bool has_next = u + 1 < p.cta_begin[blockIdx.x + 1];
+    PrefillUnit Un{};
+    if (has_next) Un = p.units[u + 1];
     if (lane == 0) {  // publish the descriptor to the softmax warps (arrive = release)
       reinterpret_cast<PrefillUnit*>(c.smem + L::OFF_DESC)[ui % kDescSlots] = U;
       mbar_arrive(c.bar(B_DESC + ui % kDescSlots));
@@ -137,6 +143,10 @@ __device__ void producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const C
       armed_q[x] = ui & 1;
     }
     if (!ok) break;
+    if (has_next && lane == 0)  // the next unit's Q into L2, so that its loads hit there
+      for (int x = 0; x < 2; ++x)
+        for (int cc = 0; cc < NC; ++cc)
+          tma_prefetch_3d(tmq, cc * 64, Un.head * p.G, Un.tok0 + x * p.tpt);
     const int32_t* trow = p.table + static_cast<int64_t>(U.table_row) * p.R;
     int kbase = -(1 << 30), my_id = 0;
     for (int kt = U.kt0; kt <= U.kt1; ++kt, ++g) {
@@ -310,7 +320,8 @@ __device__ void mma_issuer(const PrefillParams& p, const Ctx& c) {
 
 // ---------------------------------------------------------------- softmax
 template <int D>
-__device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int x, int warp, int lane) {
+__device__ void softmax_epilogue(const CUtensorMap* tmo, const PrefillParams& p, const Ctx& c, int x,
+                                 int warp, int lane) {
   using L = Layout<D>;
   constexpr int NC = D / 64;
   const int wq = warp & 3;  // TMEM lane quarter this warp may access
@@ -441,34 +452,62 @@ __device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int x, in
     if (!waitw(c.bar(B_O_FULL + x), ui & 1, c.wc)) break;
     tc_fence_after();
     const float inv_l = row_ok ? 1.f / (l + lc) : 0.f;
-    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) +
-                          (static_cast<int64_t>(tok) * p.hq + U.head * p.G + gg) * D;
+    // O / l as bf16 in registers; then O_X in TMEM is free for the next unit
+    if (lane == 0) bulk_wait_read();  // the last unit's stores have read the staging rows
+    uint32_t ob[D / 2];
 #pragma unroll
     for (int q = 0; q < D / 32; ++q) {
       uint32_t v[32];
       tmem_ld32(t_o + q * 32, v);
       tmem_wait_ld();
-      if (row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + q * 32);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(v[8 * e + 0]) * inv_l, __uint_as_float(v[8 * e + 1]) * inv_l);
-          w.y = pack_bf16x2(__uint_as_float(v[8 * e + 2]) * inv_l, __uint_as_float(v[8 * e + 3]) * inv_l);
-          w.z = pack_bf16x2(__uint_as_float(v[8 * e + 4]) * inv_l, __uint_as_float(v[8 * e + 5]) * inv_l);
-          w.w = pack_bf16x2(__uint_as_float(v[8 * e + 6]) * inv_l, __uint_as_float(v[8 * e + 7]) * inv_l);
-          dst[e] = w;
+      for (int e = 0; e < 16; ++e)
+        ob[q * 16 + e] =
+            pack_bf16x2(__uint_as_float(v[2 * e]) * inv_l, __uint_as_float(v[2 * e + 1]) * inv_l);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(c.bar(B_O_EMPTY + x));
+    if (U.ntok >= x * p.tpt + (wq + 1) * 32 / p.G) {
+      // The warp's 32 rows are 32 / G whole tokens: they go to the warp's
+      // 128B-swizzled staging rows, 64 columns at a time, and lane 0 writes
+      // them with one bulk tensor store each (the rows are one box of the O
+      // tensor map). Per-thread row stores would touch 32 rows per
+      // instruction and hold this SM's shared-memory and barrier operations
+      // up behind them.
+      uint8_t* stg = c.smem + L::OFF_STAGE + (x * 4 + wq) * L::STAGE_WARP;
+#pragma unroll
+      for (int cc = 0; cc < NC; ++cc) {
+        if (cc > 0) {  // the previous store has read the staging rows
+          if (lane == 0) bulk_wait_read();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+              make_uint4(ob[cc * 32 + 4 * j], ob[cc * 32 + 4 * j + 1], ob[cc * 32 + 4 * j + 2],
+                         ob[cc * 32 + 4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(tmo, smem_addr(stg), cc * 64, U.head * p.G,
+                       U.tok0 + x * p.tpt + wq * 32 / p.G);
+          bulk_commit();
         }
       }
+    } else if (row_ok) {  // rows of a sequence's last, partial tile: row stores
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
+                                            (static_cast<int64_t>(tok) * p.hq + U.head * p.G + gg) * D);
+#pragma unroll
+      for (int e = 0; e < D / 8; ++e)
+        dst[e] = make_uint4(ob[4 * e], ob[4 * e + 1], ob[4 * e + 2], ob[4 * e + 3]);
     }
     if (row_ok && p.lse != nullptr)
       p.lse[static_cast<int64_t>(U.head * p.G + gg) * p.total_q + tok] =
           (m_used + log2f(l)) * 0.69314718055994530942f;
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(c.bar(B_O_EMPTY + x));
     g += nt;
   }
+  if (lane == 0) bulk_wait();  // this warp's bulk stores are complete
 }
 
 }  // namespace
@@ -476,7 +515,8 @@ __device__ void softmax_epilogue(const PrefillParams& p, const Ctx& c, int x, in
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmo,
+                   const PrefillParams p) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -510,6 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tmq);
     prefetch_tmap(&tmk);
     prefetch_tmap(&tmv);
+    prefetch_tmap(&tmo);
   }
   if (warp == 1) {
     tmem_alloc(smem_addr(tmem_slot), 512);
@@ -530,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mma_issuer<D>(p, c);
     __syncwarp();
   } else {
-    softmax_epilogue<D>(p, c, (warp - 2) >> 2, warp, lane);
+    softmax_epilogue<D>(&tmo, p, c, (warp - 2) >> 2, warp, lane);
   }
   tc_fence_before();
   __syncthreads();
@@ -562,19 +603,20 @@ int prefill_smem_bytes(int head_dim) {
 int prefill_unit_tokens(int G) { return 2 * (kRowsPerTile / G); }
 
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, int head_dim, int grid, cudaStream_t s) {
+                           const CUtensorMap& tv, const CUtensorMap& to, int head_dim, int grid,
+                           cudaStream_t s) {
   if (head_dim == 64) {
     const int bytes = Layout<64>::BYTES;
     cudaError_t e =
         cudaFuncSetAttribute(prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    prefill_kernel<64><<<grid, kThreads, bytes, s>>>(tq, tk, tv, p);
+    prefill_kernel<64><<<grid, kThreads, bytes, s>>>(tq, tk, tv, to, p);
   } else {
     const int bytes = Layout<128>::BYTES;
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<128>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    prefill_kernel<128><<<grid, kThreads, bytes, s>>>(tq, tk, tv, p);
+    prefill_kernel<128><<<grid, kThreads, bytes, s>>>(tq, tk, tv, to, p);
   }
   return cudaGetLastError();
 }

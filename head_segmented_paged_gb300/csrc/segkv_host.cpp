@@ -753,7 +753,7 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
   if (e != cudaSuccess) return cuda_fail(h, e, "plan upload (prefill)");
   h->upload_bytes += static_cast<int64_t>(pk.buf.size());
 
-  CUtensorMap tq;
+  CUtensorMap tq, to;
   {
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(h->D), static_cast<cuuint64_t>(h->Hq),
                           static_cast<cuuint64_t>(total)};
@@ -766,6 +766,13 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return fail(h, SEGKV_ERR_CUDA, "tensor map encode failed for q");
+    // O has Q's shape; a box is one softmax warp's 32 rows (32 / G tokens)
+    cuuint32_t obox[3] = {64, static_cast<cuuint32_t>(h->G), static_cast<cuuint32_t>(32 / h->G)};
+    if (encode_fn()(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, o, dims, strides, obox, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return fail(h, SEGKV_ERR_CUDA, "tensor map encode failed for o");
   }
   uint8_t* d = h->ring.dev + off;
   PrefillParams p{};
@@ -789,7 +796,7 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
   p.debug = h->debug;
   p.timeout_ns = kTimeoutNs;
   h->debug = 0;
-  e = launch_prefill(p, tq, h->tm_k, h->tm_v, h->D, grid, s);
+  e = launch_prefill(p, tq, h->tm_k, h->tm_v, to, h->D, grid, s);
   if (e != cudaSuccess) return cuda_fail(h, e, "prefill kernel launch");
   e = h->ring.commit(off, pk.buf.size(), s);
   if (e != cudaSuccess) return cuda_fail(h, e, "event record");

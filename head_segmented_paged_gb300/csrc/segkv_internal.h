@@ -236,7 +236,8 @@ cudaError_t launch_append(const AppendParams& p, const AppendBlob* blob, int gri
 // copy a plan (16-byte aligned, size rounded up to 16) from mapped host memory to the device
 cudaError_t launch_plan_copy(const void* src, void* dst, size_t bytes, cudaStream_t s);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                           const CUtensorMap& tv, int head_dim, int grid, cudaStream_t s);
+                           const CUtensorMap& tv, const CUtensorMap& to, int head_dim, int grid,
+                           cudaStream_t s);
 int prefill_smem_bytes(int head_dim);
 cudaError_t launch_exp2_check(const float* x, float* y_poly, float* y_mufu, int n, cudaStream_t s);
 int prefill_unit_tokens(int G);  // query tokens per prefill work unit
