@@ -164,18 +164,32 @@ __device__ void md_mma(const DecodeMmaParams& p, const DecodeUnit* units, const 
                        const MdCtx& c) {
   constexpr uint32_t IDESC_S = idesc_bf16_ab(KT, MN, 0, 0);   // K (keys x D) . Q^T
   constexpr uint32_t IDESC_PV = idesc_bf16_ab(128, MN, 1, 0); // V^T (D x keys, MN-major) . P^T
+  // The issuing thread shares its sub-partition with softmax warps, so each
+  // MMA is issued from descriptors built once: one per shared-memory operand
+  // buffer (K and V stages, Q and P buffers); an MMA adds its compile-time
+  // offset, in 16-byte units, which never carries out of the 14-bit address
+  // field.
+  uint64_t dk[NST], dv[NST], dq[2], dp[2];
+  for (int i = 0; i < NST; ++i) {
+    dk[i] = sdesc_sw128(c.sbase + OFF_K + i * KV_TILE, 16, 1024);
+    dv[i] = sdesc_sw128(c.sbase + OFF_V + i * KV_TILE, kAtomKV, 1024);
+  }
+  for (int i = 0; i < 2; ++i) {
+    dq[i] = sdesc_sw128(c.sbase + OFF_Q + i * 2 * kAtomR, 16, 1024);
+    dp[i] = sdesc_sw128(c.sbase + OFF_P + i * 2 * kAtomR, 16, 1024);
+  }
   // S(g) = K(g) Q^T into S buffer g % 2, with Q buffer qb
   auto issue_s = [&](int g, int qb) -> bool {
     const int st = g % NST;
     if (!wait1(c.bar(Y_K_FULL + st), (g / NST) & 1, c.wc)) return false;
     tc_fence_after();
+    const uint64_t ka = st == 0 ? dk[0] : (st == 1 ? dk[1] : dk[2]);
+    const uint64_t qb_desc = qb ? dq[1] : dq[0];
+    const uint32_t d = c.tmem + TM_S + (g & 1) * MN;
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t a = c.sbase + OFF_K + st * KV_TILE + (kk >> 2) * kAtomKV + (kk & 3) * 32;
-      const uint32_t b = c.sbase + OFF_Q + (qb * 2 + (kk >> 2)) * kAtomR + (kk & 3) * 32;
-      mma_bf16(c.tmem + TM_S + (g & 1) * MN, sdesc_sw128(a, 16, 1024), sdesc_sw128(b, 16, 1024),
-               IDESC_S, kk > 0 ? 1u : 0u);
-    }
+    for (int kk = 0; kk < 8; ++kk)
+      mma_bf16(d, ka + (((kk >> 2) * kAtomKV + (kk & 3) * 32) >> 4),
+               qb_desc + (((kk >> 2) * kAtomR + (kk & 3) * 32) >> 4), IDESC_S, kk > 0 ? 1u : 0u);
     mma_commit(c.bar(Y_S_FULL + (g & 1)));
     return true;
   };
@@ -201,13 +215,16 @@ __device__ void md_mma(const DecodeMmaParams& p, const DecodeUnit* units, const 
       if (!wait1(c.bar(Y_V_FULL + st), (g / NST) & 1, c.wc)) { ok = false; break; }
       if (kt == kt0 && !wait1(c.bar(Y_O_EMPTY), (ui & 1) ^ 1, c.wc)) { ok = false; break; }
       tc_fence_after();
+      {
+        const uint64_t va = st == 0 ? dv[0] : (st == 1 ? dv[1] : dv[2]);
+        const uint64_t pb = (g & 1) ? dp[1] : dp[0];
+        const uint32_t d = c.tmem + TM_O + (g & 1) * MN;
+        const bool fresh = g - g0 < 2;
 #pragma unroll
-      for (int kk = 0; kk < KT / 16; ++kk) {
-        const uint32_t a = c.sbase + OFF_V + st * KV_TILE + kk * 2048;
-        const uint32_t b = c.sbase + OFF_P + (g & 1) * 2 * kAtomR + (kk >> 2) * kAtomR + (kk & 3) * 32;
-        // O of group g % 2; that group's first stage of the unit starts it afresh
-        mma_bf16(c.tmem + TM_O + (g & 1) * MN, sdesc_sw128(a, kAtomKV, 1024), sdesc_sw128(b, 16, 1024),
-                 IDESC_PV, (g - g0 >= 2 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < KT / 16; ++kk)
+          // O of group g % 2; that group's first stage of the unit starts it afresh
+          mma_bf16(d, va + kk * 2048 / 16, pb + (((kk >> 2) * kAtomR + (kk & 3) * 32) >> 4),
+                   IDESC_PV, (!fresh || kk > 0) ? 1u : 0u);
       }
       mma_commit(c.bar(Y_KV_EMPTY + st));
       if (kt == kt1) mma_commit(c.bar(Y_O_FULL));

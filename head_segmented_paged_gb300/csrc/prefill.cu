@@ -602,23 +602,22 @@ int prefill_smem_bytes(int head_dim) {
 
 int prefill_unit_tokens(int G) { return 2 * (kRowsPerTile / G); }
 
+template <class K>
+cudaError_t launch_kernel(K kernel, int smem, int grid, cudaStream_t s, const CUtensorMap& tq,
+                          const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                          const PrefillParams& p) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, kThreads, smem, s>>>(tq, tk, tv, to, p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const CUtensorMap& to, int head_dim, int grid,
                            cudaStream_t s) {
-  if (head_dim == 64) {
-    const int bytes = Layout<64>::BYTES;
-    cudaError_t e =
-        cudaFuncSetAttribute(prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    prefill_kernel<64><<<grid, kThreads, bytes, s>>>(tq, tk, tv, to, p);
-  } else {
-    const int bytes = Layout<128>::BYTES;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<128>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    prefill_kernel<128><<<grid, kThreads, bytes, s>>>(tq, tk, tv, to, p);
-  }
-  return cudaGetLastError();
+  if (head_dim == 64)
+    return launch_kernel(prefill_kernel<64>, Layout<64>::BYTES, grid, s, tq, tk, tv, to, p);
+  return launch_kernel(prefill_kernel<128>, Layout<128>::BYTES, grid, s, tq, tk, tv, to, p);
 }
 
 }  // namespace skv

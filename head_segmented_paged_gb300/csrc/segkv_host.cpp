@@ -170,6 +170,46 @@ struct Pack {
 // keeping the running minimum in a register. Lists < 65,536, loads < 2^47.
 constexpr int kMaxPlanCtas = 65535;  // LeastLoaded packs a list index into 16 bits
 
+// The free pages, handed out lowest id first. A bit per page and a bit per
+// 64-page word that has any free page: push and pop touch one or two words,
+// and the lowest free page is found from a cursor that only moves down when
+// a lower page is freed, so a run of allocations costs O(1) per page.
+class PagePool {
+ public:
+  void reset(int64_t n) {
+    bits_.assign(static_cast<size_t>((n + 63) / 64), 0);
+    sum_.assign((bits_.size() + 63) / 64, 0);
+    count_ = 0;
+    cursor_ = 0;
+    for (int64_t i = 0; i < n; ++i) push(static_cast<int32_t>(i));
+  }
+  int64_t size() const { return count_; }
+  void push(int32_t id) {
+    const size_t w = static_cast<size_t>(id) >> 6;
+    if (bits_[w] == 0) sum_[w >> 6] |= 1ull << (w & 63);
+    bits_[w] |= 1ull << (id & 63);
+    cursor_ = std::min(cursor_, w >> 6);
+    ++count_;
+  }
+  int32_t top() {  // the lowest free page; the pool must not be empty
+    while (sum_[cursor_] == 0) ++cursor_;
+    const size_t w = cursor_ * 64 + static_cast<size_t>(__builtin_ctzll(sum_[cursor_]));
+    return static_cast<int32_t>(w * 64 + static_cast<size_t>(__builtin_ctzll(bits_[w])));
+  }
+  void pop() {
+    const int32_t id = top();
+    const size_t w = static_cast<size_t>(id) >> 6;
+    bits_[w] &= bits_[w] - 1;  // clear the lowest set bit: id
+    if (bits_[w] == 0) sum_[w >> 6] &= ~(1ull << (w & 63));
+    --count_;
+  }
+
+ private:
+  std::vector<uint64_t> bits_, sum_;
+  int64_t count_ = 0;
+  size_t cursor_ = 0;
+};
+
 class LeastLoaded {
  public:
   void reset(int lists) {
@@ -235,7 +275,7 @@ struct segkv {
   std::vector<int32_t> len;    // [L][S]
   std::vector<int32_t> start;  // [L][Hkv][S]
   std::vector<int32_t> table;  // [L][Hkv][S][R], -1 = not held
-  std::priority_queue<int32_t, std::vector<int32_t>, std::greater<int32_t>> free_ids;
+  PagePool free_ids;  // lowest id first
 
   // device
   int device = 0, num_sms = 0;
@@ -251,6 +291,8 @@ struct segkv {
   DecodePlan dplan;   // the last decode plan (storage reused)
   PrefillPlan pplan;  // the last prefill plan (storage reused)
   Pack pack;          // staging of a plan upload (storage reused)
+  std::vector<XferHead> xfer_heads;  // a transfer's plan (storage reused)
+  std::vector<int32_t> xfer_pages;
   std::string err;
 
   size_t seg(int l, int h, int b) const { return (static_cast<size_t>(l) * Hkv + h) * S + b; }
@@ -378,11 +420,7 @@ int segkv_create(segkv_t* out, int num_layers, int num_q_heads, int num_kv_heads
   h->len.assign(static_cast<size_t>(num_layers) * max_seqs, 0);
   h->start.assign(static_cast<size_t>(num_layers) * num_kv_heads * max_seqs, 0);
   h->table.assign(static_cast<size_t>(entries), -1);
-  {
-    std::vector<int32_t> ids(static_cast<size_t>(num_pages));
-    for (int64_t i = 0; i < num_pages; ++i) ids[i] = static_cast<int32_t>(i);
-    h->free_ids = decltype(h->free_ids)(std::greater<int32_t>(), std::move(ids));
-  }
+  h->free_ids.reset(num_pages);
   h->host_only = (k_pool == nullptr);
   h->kpool = k_pool;
   h->vpool = v_pool;
@@ -670,7 +708,7 @@ static void prefill_plan(segkv* h, int layer, const int32_t* cu_seqlens, const i
   // work so far; a unit costs its key tiles plus kPrefillUnitCost for filling
   // and draining the pipeline and the output epilogue. Each CTA then runs its
   // own list, longest first.
-  constexpr int64_t kPrefillUnitCost = 2;
+  constexpr int64_t kPrefillUnitCost = 1;
   // descending key tiles, stable: a counting sort on the tile count
   int32_t max_tiles = 0;
   for (const PrefillUnit& u : units) max_tiles = std::max(max_tiles, u.kt1 - u.kt0);
@@ -1416,6 +1454,13 @@ static int finish_small_plan(segkv* h, const PlanPlace& pp, const Pack& pk, cuda
   return e == cudaSuccess ? SEGKV_OK : cuda_fail(h, e, "event record");
 }
 
+// Transfer grid: enough CTAs for about 4 chunks per thread, at most 8 per SM.
+static int transfer_grid(const segkv* h, int64_t rows) {
+  const int64_t chunks = rows * (h->D / 8);
+  const int64_t want = (chunks + 256 * 4 - 1) / (256 * 4);
+  return static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, int64_t(std::max(1, h->num_sms)) * 8)));
+}
+
 int segkv_export_size(segkv_t h, int layer, int seq, size_t* bytes) {
   if (!h || !bytes) return SEGKV_ERR_INVALID_ARG;
   if (layer < 0 || layer >= h->L || seq < 0 || seq >= h->S)
@@ -1441,42 +1486,55 @@ int segkv_export(segkv_t h, int layer, int seq, void* out, size_t out_bytes, int
   if (!out || out_bytes < need || (reinterpret_cast<uintptr_t>(out) & 15))
     return fail(h, SEGKV_ERR_INVALID_ARG, "export needs %zu bytes (16-aligned), got %zu", need,
                 out_bytes);
-  std::vector<TransferRun> runs;
-  int32_t row = 0;
+  std::vector<XferHead>& hv = h->xfer_heads;
+  std::vector<int32_t>& pl = h->xfer_pages;
+  hv.clear();
+  pl.clear();
+  int32_t row = 0, rows = 0;
   for (int hd = 0; hd < h->Hkv; ++hd) {
-    const int32_t s0 = h->start[h->seg(layer, hd, seq)];
-    const int32_t* r = h->table.data() + h->seg(layer, hd, seq) * h->R;
-    const int32_t len = n - s0;
-    for (int32_t pos = s0; pos < n;) {
-      const int k = pos / h->P;
-      const int32_t pend = std::min<int32_t>(n, (k + 1) * h->P);
-      runs.push_back({r[k], pos - k * h->P, pend - pos, row + (pos - s0), row + len + (pos - s0),
-                      {0, 0, 0}});
-      pos = pend;
-    }
+    const int64_t sg = h->seg(layer, hd, seq);
+    const int32_t s0 = h->start[sg], len = n - s0;
+    const int32_t* r = h->table.data() + sg * h->R;
+    XferHead H{};
+    H.s0 = s0;
+    H.len = len;
+    H.out_row = row;
+    H.first_k = s0 / h->P;
+    H.page_off = static_cast<int32_t>(pl.size());
+    H.table_row = static_cast<int32_t>(sg);
+    H.row_begin = rows;
+    if (len > 0)
+      for (int k = s0 / h->P; k <= (n - 1) / h->P; ++k) pl.push_back(r[k]);
+    hv.push_back(H);
     row += 2 * len;
+    rows += len;
   }
-  if (runs.empty()) return SEGKV_OK;
-  Pack pk;
-  const size_t o_runs = pk.add(runs.data(), runs.size());
+  if (rows == 0) return SEGKV_OK;
+  Pack& pk = h->pack;
+  pk.buf.clear();
+  const size_t o_heads = pk.add(hv.data(), hv.size());
+  const size_t o_pages = pk.add(pl.data(), pl.size());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   PlanPlace pp;
   rc = place_small_plan(h, pk, s, &pp);
   if (rc != SEGKV_OK) return rc;
   TransferParams p{};
-  p.runs = reinterpret_cast<const TransferRun*>(pp.base + o_runs);
+  p.heads = reinterpret_cast<const XferHead*>(pp.base + o_heads);
+  p.page_list = reinterpret_cast<const int32_t*>(pp.base + o_pages);
   p.kpool = static_cast<uint4*>(h->kpool);
   p.vpool = static_cast<uint4*>(h->vpool);
   p.buf_out = static_cast<uint4*>(out);
   p.table = h->d_table;
   p.plan_inline = pp.inl ? 1 : 0;
   p.to_pool = 0;
-  p.n_runs = static_cast<int>(runs.size());
+  p.n_heads = h->Hkv;
+  p.n_pages = static_cast<int>(pl.size());
   p.vec_per_row = h->D / 8;
   p.page_size = h->P;
-  const int grid = static_cast<int>(std::min<int64_t>(runs.size(), int64_t(h->num_sms) * 16));
+  p.R = h->R;
+  p.total_rows = rows;
   cudaError_t e = launch_transfer(p, pp.inl ? reinterpret_cast<const AppendBlob*>(&h->blob) : nullptr,
-                                  grid, s);
+                                  transfer_grid(h, rows), s);
   if (e != cudaSuccess) return cuda_fail(h, e, "export kernel launch");
   return finish_small_plan(h, pp, pk, s);
 }
@@ -1506,59 +1564,61 @@ int segkv_import(segkv_t h, int layer, int seq, const void* in, size_t in_bytes,
   if (static_cast<int64_t>(h->free_ids.size()) < need)
     return fail(h, SEGKV_ERR_OUT_OF_PAGES, "import needs %lld pages, %lld free",
                 static_cast<long long>(need), static_cast<long long>(h->free_ids.size()));
-  std::vector<TransferRun> runs;
-  std::vector<int32_t> plist;
-  std::vector<int64_t> tidx;
-  int32_t row = 0;
+  std::vector<XferHead>& hv = h->xfer_heads;
+  std::vector<int32_t>& pl = h->xfer_pages;
+  hv.clear();
+  pl.clear();
+  int32_t row = 0, nrows = 0;
   for (int hd = 0; hd < h->Hkv; ++hd) {
-    const int32_t s0 = header[1 + hd];
-    h->start[h->seg(layer, hd, seq)] = s0;
+    const int64_t sg = h->seg(layer, hd, seq);
+    const int32_t s0 = header[1 + hd], len = n - s0;
+    h->start[sg] = s0;
     int32_t* r = h->row(layer, hd, seq);
+    XferHead H{};
+    H.s0 = s0;
+    H.len = len;
+    H.out_row = row;
+    H.first_k = s0 / h->P;
+    H.page_off = static_cast<int32_t>(pl.size());
+    H.table_row = static_cast<int32_t>(sg);
+    H.row_begin = nrows;
     if (n > 0)
       for (int k = s0 / h->P; k <= (n - 1) / h->P; ++k) {
         r[k] = h->free_ids.top();
         h->free_ids.pop();
-        plist.push_back(r[k]);
-        tidx.push_back(static_cast<int64_t>(h->seg(layer, hd, seq)) * h->R + k);
+        pl.push_back(r[k]);
       }
-    const int32_t len = n - s0;
-    for (int32_t pos = s0; pos < n;) {
-      const int k = pos / h->P;
-      const int32_t pend = std::min<int32_t>(n, (k + 1) * h->P);
-      runs.push_back({r[k], pos - k * h->P, pend - pos, row + (pos - s0), row + len + (pos - s0),
-                      {0, 0, 0}});
-      pos = pend;
-    }
+    hv.push_back(H);
     row += 2 * len;
+    nrows += len;
   }
   h->len[h->lidx(layer, seq)] = n;
-  if (h->host_only || (runs.empty() && plist.empty())) return SEGKV_OK;
-  Pack pk;
-  const size_t o_runs = pk.add(runs.data(), runs.size());
-  const size_t o_pl = pk.add(plist.data(), plist.size());
-  const size_t o_ti = pk.add(tidx.data(), tidx.size());
+  if (h->host_only || pl.empty()) return SEGKV_OK;
+  Pack& pk = h->pack;
+  pk.buf.clear();
+  const size_t o_heads = pk.add(hv.data(), hv.size());
+  const size_t o_pages = pk.add(pl.data(), pl.size());
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   PlanPlace pp;
   int rc = place_small_plan(h, pk, s, &pp);
   if (rc != SEGKV_OK) return rc;
   TransferParams p{};
-  p.runs = reinterpret_cast<const TransferRun*>(pp.base + o_runs);
-  p.page_list = reinterpret_cast<const int32_t*>(pp.base + o_pl);
-  p.table_idx = reinterpret_cast<const int64_t*>(pp.base + o_ti);
+  p.heads = reinterpret_cast<const XferHead*>(pp.base + o_heads);
+  p.page_list = reinterpret_cast<const int32_t*>(pp.base + o_pages);
   p.kpool = static_cast<uint4*>(h->kpool);
   p.vpool = static_cast<uint4*>(h->vpool);
   p.buf = static_cast<const uint4*>(in);
   p.table = h->d_table;
   p.plan_inline = pp.inl ? 1 : 0;
   p.to_pool = 1;
-  p.n_runs = static_cast<int>(runs.size());
-  p.n_entries = static_cast<int>(plist.size());
+  p.n_heads = h->Hkv;
+  p.n_pages = static_cast<int>(pl.size());
   p.vec_per_row = h->D / 8;
   p.page_size = h->P;
-  const int grid = static_cast<int>(
-      std::max<int64_t>(1, std::min<int64_t>(runs.size(), int64_t(h->num_sms) * 16)));
+  p.R = h->R;
+  p.total_rows = nrows;
   cudaError_t e = launch_transfer(p, pp.inl ? reinterpret_cast<const AppendBlob*>(&h->blob) : nullptr,
-                                  grid, s);
+                                  transfer_grid(h, std::max<int64_t>(nrows, static_cast<int64_t>(pl.size()))), s);
   if (e != cudaSuccess) return cuda_fail(h, e, "import kernel launch");
   return finish_small_plan(h, pp, pk, s);
 }

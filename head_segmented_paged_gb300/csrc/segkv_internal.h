@@ -139,23 +139,27 @@ struct RopeParams {
 cudaError_t launch_rope(const RopeParams& p, const AppendBlob* blob, int grid, cudaStream_t s);
 
 // ---- segment transfer -------------------------------------------------------
-struct TransferRun {
-  int32_t page, slot0, nrows;  // pool rows
-  int32_t k_row, v_row;        // first buffer row of these keys / values
-  int32_t pad[3];
+// One KV head of a transferred (layer, sequence): its kept rows [s0, s0 + len)
+// in pages page_list[page_off ..] (logical pages first_k ..), and where they
+// sit in the buffer (K rows from out_row, V rows from out_row + len).
+struct XferHead {
+  int32_t s0, len, out_row, first_k;
+  int32_t page_off, table_row, row_begin;  // row_begin: sum of the earlier heads' len
+  int32_t pad;
 };
+static_assert(sizeof(XferHead) == 32, "transfer heads are staged in 32-byte slots");
 struct TransferParams {
-  const TransferRun* runs;
-  const int32_t* page_list;  // import: new block-table entries ...
-  const int64_t* table_idx;  // ... and their slots
+  const XferHead* heads;
+  const int32_t* page_list;
   uint4* kpool;
   uint4* vpool;
   const uint4* buf;          // import source
   uint4* buf_out;            // export destination
-  int32_t* table;
+  int32_t* table;            // import: the heads' block-table rows get their new pages
   int plan_inline;           // 1: the plan arrays are offsets into the AppendBlob
   int to_pool;               // 1: import (buffer -> pages), 0: export
-  int n_runs, n_entries, vec_per_row, page_size;
+  int n_heads, n_pages, vec_per_row, page_size, R;
+  int64_t total_rows;        // sum of the heads' len
 };
 cudaError_t launch_transfer(const TransferParams& p, const AppendBlob* blob, int grid,
                             cudaStream_t s);

@@ -160,7 +160,7 @@ def test_decode_plan_errors():
 
 # ---------------------------------------------------------------- prefill
 def prefill_cost(u):
-    return int(u[5] - u[4] + 1) + 2  # key tiles + the per-unit surcharge
+    return int(u[5] - u[4] + 1) + 1  # key tiles + the per-unit surcharge
 
 
 @pytest.mark.parametrize("G,hkv", [(1, 2), (4, 8), (8, 8), (16, 2)])
