@@ -1002,7 +1002,7 @@ static int decode_mma_launch(segkv* h, int layer, const void* q, int T, int n, v
 // in max_grid CTAs. The same walk as the cut that emits the units, over the
 // ranges' key counts alone, given up as soon as the grid is full.
 static bool decode_cut_fits(const int64_t* keys, int64_t nr, int64_t B, int64_t unit_cost,
-                            int64_t split_cost, int64_t max_grid) {
+                            int64_t split_cost, int64_t max_grid, int64_t quantum) {
   int64_t used = 0, r = 0, off = 0;
   while (r < nr) {
     if (++used > max_grid) return false;
@@ -1013,11 +1013,11 @@ static bool decode_cut_fits(const int64_t* keys, int64_t nr, int64_t B, int64_t 
       int64_t room = B - cost - unit_cost;
       const bool whole = off == 0 && avail <= room;
       if (!whole) room -= split_cost;
-      if (room < 1) {
-        if (!any) return false;  // B cannot hold even one key
+      if (room < quantum) {
+        if (!any) return false;  // B cannot hold even one key (or tile)
         break;
       }
-      const int64_t take = avail < room ? avail : room;
+      const int64_t take = avail <= room ? avail : room / quantum * quantum;
       cost += unit_cost + (whole ? 0 : split_cost) + take;
       any = true;
       if (take == avail) {
@@ -1039,6 +1039,9 @@ static int decode_plan(segkv* h, int layer, int T, const int32_t* seq_lens, cons
                        int n, int64_t ctas_override, DecodePlan& P) {
   const int W = h->win[layer];
   const int rows = T * h->G;
+  // 8 or 16 query rows of 128 dims run on the tensor-core decode kernel
+  // (128-key stages, one CTA per SM); the rest on the CUDA-core kernel
+  const bool mma = h->D == 128 && (rows == 8 || rows == 16);
   // pairs (req, head) with their key ranges [lo, n)
   std::vector<DecodeRange>& ranges = P.ranges;
   std::vector<int64_t>& keys = P.keys;
@@ -1060,8 +1063,10 @@ static int decode_plan(segkv* h, int layer, int T, const int32_t* seq_lens, cons
       if (lo < h->start[h->seg(layer, hd, b)])
         return fail(h, SEGKV_ERR_EVICTED, "seq %d head %d: key %d already evicted", b, hd, lo);
       ranges.push_back({i, hd, lo, nlen, static_cast<int32_t>(h->seg(layer, hd, b)), local});
-      keys.push_back(nlen - lo);
-      total += nlen - lo;
+      // the tensor-core kernel streams whole 128-key tiles: its work is priced in tiles
+      const int64_t work = mma ? (int64_t((nlen - 1) / 128) - lo / 128 + 1) * 128 : int64_t(nlen - lo);
+      keys.push_back(work);
+      total += work;
     }
   }
   // Stream-K split with a cost model: the concatenated key ranges are cut into
@@ -1078,9 +1083,9 @@ static int decode_plan(segkv* h, int layer, int T, const int32_t* seq_lens, cons
   // 512: 101.4-103.0, 768: 103.3-104.3).
   // The smallest per-CTA budget whose greedy cut fits the grid is found by
   // bisection.
-  // 8 or 16 query rows of 128 dims run on the tensor-core decode kernel
-  // (128-key stages, one CTA per SM); the rest on the CUDA-core kernel
-  const bool mma = h->D == 128 && (rows == 8 || rows == 16);
+  // On the tensor-core kernel, work and cuts are in whole 128-key tiles: a cut
+  // inside a tile would make both neighbours stream that whole tile.
+  const int64_t quantum = mma ? 128 : 1;
   const int64_t kDecodeUnitCost = mma ? 512 : 128;
   const int64_t kDecodeSplitCost = 256;
   const int64_t sk = mma ? 128 : decode_stage_keys(rows);
@@ -1103,7 +1108,7 @@ static int decode_plan(segkv* h, int layer, int T, const int32_t* seq_lens, cons
   int64_t lo = std::max<int64_t>(1, (total + kDecodeUnitCost * nr) / max_grid);
   int64_t hi = total + kDecodeUnitCost * (nr + 1);  // one CTA holds everything
   auto fits = [&](int64_t B) {
-    return decode_cut_fits(keys.data(), nr, B, kDecodeUnitCost, kDecodeSplitCost, max_grid);
+    return decode_cut_fits(keys.data(), nr, B, kDecodeUnitCost, kDecodeSplitCost, max_grid, quantum);
   };
   const int64_t probe = lo + lo / 8 + 2 * (kDecodeUnitCost + kDecodeSplitCost);
   if (probe < hi && fits(probe)) hi = probe;
@@ -1133,20 +1138,22 @@ static int decode_plan(segkv* h, int layer, int T, const int32_t* seq_lens, cons
         int64_t room = B - cost - kDecodeUnitCost;
         const bool whole = off == 0 && avail <= room;
         if (!whole) room -= kDecodeSplitCost;
-        if (room < 1) {
+        if (room < quantum) {
           if (cost == 0)  // cannot happen: B was found to fit
             return fail(h, SEGKV_ERR_INVALID_ARG, "decode plan: budget %lld holds no key",
                         static_cast<long long>(B));
           break;
         }
-        const int64_t take = std::min(avail, room);
+        const int64_t take = avail <= room ? avail : room / quantum * quantum;
         if (off == 0) pair_unit0[r] = static_cast<int32_t>(units.size());
         DecodeUnit u{};
         u.req = R.req;
         u.head = static_cast<int16_t>(R.head);
         u.local = static_cast<int16_t>(R.local);
-        u.k0 = static_cast<int32_t>(R.lo + off);
-        u.k1 = static_cast<int32_t>(R.lo + off + take);
+        // work offsets are keys from lo, or from lo's tile start when quantum = 128
+        const int64_t base = quantum > 1 ? R.lo / quantum * quantum : R.lo;
+        u.k0 = static_cast<int32_t>(std::max<int64_t>(R.lo, base + off));
+        u.k1 = static_cast<int32_t>(std::min<int64_t>(R.n, base + off + take));
         u.table_row = R.row;
         u.q_last = R.n - 1;
         units.push_back(u);
