@@ -334,7 +334,8 @@ __device__ void md_softmax(const DecodeMmaParams& p, const DecodeUnit* units,
           for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-              *reinterpret_cast<uint4*>(vrow + cc * kAtomKV + q * 16) = make_uint4(0, 0, 0, 0);
+              // chunk q ^ (t % 8): the warp's 32 rows spread over all banks
+              *reinterpret_cast<uint4*>(vrow + cc * kAtomKV + ((q ^ (t & 7)) << 4)) = make_uint4(0, 0, 0, 0);
         }
       }
       fence_proxy_async_smem();  // P (and zeroed V rows) are read by the tensor core
@@ -388,28 +389,60 @@ __device__ void md_softmax(const DecodeMmaParams& p, const DecodeUnit* units,
     const int n_st = kt1 - kt0 + 1;
     const bool had1 = n_st >= 2 || (g0 & 1) == 1;  // group 1 handled a stage of the unit
     const bool single = U.pair_units == 1;
+    // Every row's merge is computed into registers before any store, so the
+    // rows' arithmetic overlaps instead of running one row after another
+    // behind each row's global store.
+    float gm[MN], gl[MN];
 #pragma unroll
     for (int r = 0; r < MN; ++r) {
-      if (r >= p.R_rows) break;
-      const float m1 = gx[r], L1 = gx[MN + r];
-      const float M = fmaxf(m_ref[r], m1);
+      gm[r] = gx[r];
+      gl[r] = gx[MN + r];
+    }
+    float ov[MN], Mv[MN], Lv[MN];
+#pragma unroll
+    for (int r = 0; r < MN; ++r) {
+      const float M = fmaxf(m_ref[r], gm[r]);
       const float Mr = (M == -INFINITY) ? 0.f : M;
-      const float w0 = ex2(m_ref[r] - Mr), w1 = ex2(m1 - Mr);
-      const float o = (had ? __uint_as_float(o0[r]) * w0 : 0.f) + (had1 ? __uint_as_float(o1[r]) * w1 : 0.f);
-      const float Lt = L[r] * w0 + L1 * w1;
-      if (single) {
-        const int tk = r / p.Gm, gm = r - tk * p.Gm;
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) +
-                              (static_cast<int64_t>(U.req * p.T + tk) * p.hq + U.head * p.Gm + gm) * 128;
-        orow[t] = __float2bfloat16_rn(o / Lt);
-        if (p.lse != nullptr && t == 0)
-          p.lse[static_cast<int64_t>(U.head * p.Gm + gm) * p.n_rows + U.req * p.T + tk] =
-              (M + log2f(Lt)) * 0.6931471805599453f;
-      } else {
-        p.part_acc[(static_cast<int64_t>(u) * p.R_rows + r) * 128 + t] = o;
-        if (t == 0) {
-          p.part_ml[(static_cast<int64_t>(u) * p.R_rows + r) * 2] = M;
-          p.part_ml[(static_cast<int64_t>(u) * p.R_rows + r) * 2 + 1] = Lt;
+      const float w0 = ex2(m_ref[r] - Mr), w1 = ex2(gm[r] - Mr);
+      ov[r] = (had ? __uint_as_float(o0[r]) * w0 : 0.f) + (had1 ? __uint_as_float(o1[r]) * w1 : 0.f);
+      Lv[r] = L[r] * w0 + gl[r] * w1;
+      Mv[r] = M;
+    }
+    if (single) {
+      __nv_bfloat16 ob[MN];
+#pragma unroll
+      for (int r = 0; r < MN; ++r) ob[r] = __float2bfloat16_rn(ov[r] / Lv[r]);
+      __nv_bfloat16* obase = static_cast<__nv_bfloat16*>(p.o) +
+                             (static_cast<int64_t>(U.req) * p.T * p.hq + U.head * p.Gm) * 128 + t;
+#pragma unroll
+      for (int r = 0; r < MN; ++r) {
+        if (r >= p.R_rows) break;
+        const int tk = r / p.Gm, gm_ = r - tk * p.Gm;
+        obase[(static_cast<int64_t>(tk) * p.hq + gm_) * 128] = ob[r];
+      }
+      if (p.lse != nullptr && t == 0) {
+#pragma unroll
+        for (int r = 0; r < MN; ++r) {
+          if (r >= p.R_rows) break;
+          const int tk = r / p.Gm, gm_ = r - tk * p.Gm;
+          p.lse[static_cast<int64_t>(U.head * p.Gm + gm_) * p.n_rows + U.req * p.T + tk] =
+              (Mv[r] + log2f(Lv[r])) * 0.6931471805599453f;
+        }
+      }
+    } else {
+      float* acc = p.part_acc + static_cast<int64_t>(u) * p.R_rows * 128 + t;
+#pragma unroll
+      for (int r = 0; r < MN; ++r) {
+        if (r >= p.R_rows) break;
+        acc[r * 128] = ov[r];
+      }
+      if (t == 0) {
+        float* ml = p.part_ml + static_cast<int64_t>(u) * p.R_rows * 2;
+#pragma unroll
+        for (int r = 0; r < MN; ++r) {
+          if (r >= p.R_rows) break;
+          ml[2 * r] = Mv[r];
+          ml[2 * r + 1] = Lv[r];
         }
       }
     }
@@ -467,6 +500,9 @@ __global__ void __launch_bounds__(kThreadsMD, 1)
   __syncthreads();
   tc_fence_after();
   c.tmem = *tmem_slot;
+  // the merge kernel may be scheduled now: it waits for this whole grid to
+  // complete (griddepcontrol.wait) before it reads a partial
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   c.wc.abort = abort_flag;
   c.wc.status = p.status;
   c.wc.limit_ns = p.timeout_ns;
@@ -490,6 +526,9 @@ __global__ void __launch_bounds__(kThreadsMD, 1)
 // Merge the partials of split pairs: block (pair, row), thread = dimension.
 __global__ void __launch_bounds__(128)
     decode_combine_kernel(const DecodeMmaParams p, const __grid_constant__ PlanBlob blob) {
+  // launched as a programmatic dependent of decode_mma_kernel: wait until
+  // that grid is complete and its partials are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const DecodeCombine* cmb = plan_ptr(p.combine, blob, p.plan_inline);
   const DecodeCombine C = cmb[blockIdx.x / p.R_rows];
   const int r = blockIdx.x % p.R_rows;
@@ -532,8 +571,19 @@ cudaError_t launch_decode_mma(const DecodeMmaParams& p, const PlanBlob* blob, co
   decode_mma_kernel<<<grid, kThreadsMD, MD_BYTES, s>>>(tq, tk, tv, p, b);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || p.n_combine == 0) return e;
-  decode_combine_kernel<<<p.n_combine * p.R_rows, 128, 0, s>>>(p, b);
-  return cudaGetLastError();
+  // programmatic dependent launch: the merge's launch overlaps the tail of
+  // the attention kernel instead of following its completion
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_combine * p.R_rows);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel, p, b);
 }
 
 }  // namespace skv

@@ -148,6 +148,7 @@ __device__ void producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const C
         for (int cc = 0; cc < NC; ++cc)
           tma_prefetch_3d(tmq, cc * 64, Un.head * p.G, Un.tok0 + x * p.tpt);
     const int32_t* trow = p.table + static_cast<int64_t>(U.table_row) * p.R;
+    const int first_page = U.vlo / p.page_size, last_page = U.vhi / p.page_size;
     int kbase = -(1 << 30), my_id = 0;
     for (int kt = U.kt0; kt <= U.kt1; ++kt, ++g) {
       const int st = g & 1;
@@ -162,7 +163,7 @@ __device__ void producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const C
         const int pos = kt * BN + bi * box_rows;
         const int k = pos / p.page_size;
         int y = p.oob_row;  // zero fill: page not held by this segment
-        if (k >= U.first_page && k <= U.last_page) {
+        if (k >= first_page && k <= last_page) {
           if (k >= kbase + 32) {
             kbase = k;
             my_id = (k + lane < p.R) ? trow[k + lane] : 0;
@@ -426,18 +427,21 @@ __device__ void softmax_epilogue(const CUtensorMap* tmo, const PrefillParams& p,
         }
       }
 
-      if (x == 0 && (i == 0 || i == nt - 1)) {
-        // Edge tiles: zero the V rows of keys outside every row's range
-        // (stale page heads, unwritten page tails) so P never meets NaN.
+      if (x == 0 && (i == 0 || i == nt - 1) && (j0 < U.vlo || j0 + BN - 1 > U.vhi)) {
+        // An edge tile that reaches past the segment's written keys: zero
+        // those V rows (a stale page head, an unwritten page tail) so that
+        // P = 0 never meets NaN. Keys of the segment that a row does not see
+        // hold finite values and meet P = 0 as they are.
         if (!waitw(c.bar(B_V_FULL + st), ph, c.wc)) { ok = false; break; }
         const int jr = j0 + r;
-        if (jr < U.klo || jr > U.khi) {
+        if (jr < U.vlo || jr > U.vhi) {
           uint8_t* vrow = c.smem + L::OFF_V + st * L::KV_BYTES + r * 128;
 #pragma unroll
           for (int cc = 0; cc < NC; ++cc)
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-              *reinterpret_cast<uint4*>(vrow + cc * kAtom + q * 16) = make_uint4(0, 0, 0, 0);
+              // chunk q ^ (r % 8): the warp's 32 rows spread over all banks
+              *reinterpret_cast<uint4*>(vrow + cc * kAtom + ((q ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
       }

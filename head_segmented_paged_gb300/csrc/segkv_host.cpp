@@ -694,9 +694,8 @@ static void prefill_plan(segkv* h, int layer, const int32_t* cu_seqlens, const i
         u.khi = pmax;
         u.kt0 = u.klo / kKeyTile;
         u.kt1 = u.khi / kKeyTile;
-        const int32_t s0 = h->start[h->seg(layer, hd, b)];
-        u.first_page = s0 / h->P;
-        u.last_page = (nlen - 1) / h->P;
+        u.vlo = h->start[h->seg(layer, hd, b)];
+        u.vhi = nlen - 1;
         u.table_row = static_cast<int32_t>(h->seg(layer, hd, b));
         u.pos0 = consecutive ? q_pos[t0] : -1;
         units.push_back(u);
@@ -1079,14 +1078,14 @@ static int decode_plan(segkv* h, int layer, int T, const int32_t* seq_lens, cons
   // surcharge was tuned on the same workload (0 -> 256 keys: 62.4 -> 61.6 us).
   // On the tensor-core kernel a unit also waits for its query rows and its
   // first S, and ends with a merge of two softmax groups; a sweep on the
-  // four-token ragged decode priced it at 512 keys (128: 112 us, 384: 108.7,
-  // 512: 101.4-103.0, 768: 103.3-104.3).
+  // four-token ragged decode priced it at 384 keys (256: 91.6-92.0 us, 384:
+  // 89.4-89.6, 512: 92.8).
   // The smallest per-CTA budget whose greedy cut fits the grid is found by
   // bisection.
   // On the tensor-core kernel, work and cuts are in whole 128-key tiles: a cut
   // inside a tile would make both neighbours stream that whole tile.
   const int64_t quantum = mma ? 128 : 1;
-  const int64_t kDecodeUnitCost = mma ? 512 : 128;
+  const int64_t kDecodeUnitCost = mma ? 384 : 128;
   const int64_t kDecodeSplitCost = 256;
   const int64_t sk = mma ? 128 : decode_stage_keys(rows);
   const int64_t ctas = ctas_override > 0 ? ctas_override

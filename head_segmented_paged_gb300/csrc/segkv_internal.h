@@ -61,8 +61,7 @@ struct PrefillUnit {
   int32_t local;       // 1 = local head
   int32_t kt0, kt1;    // key tiles kt0 .. kt1 (inclusive), tile = 128 positions
   int32_t klo, khi;    // union of the rows' visible keys
-  int32_t first_page;  // first held logical page of the segment
-  int32_t last_page;   // last held logical page
+  int32_t vlo, vhi;    // the segment's written keys [vlo, vhi]: its start, its length - 1
   int32_t table_row;   // (layer * Hkv + head) * max_seqs + seq
   int32_t pos0;        // position of token tok0 + t is pos0 + t; -1: read q_pos
 };

@@ -33,7 +33,7 @@ SPLIT_COST = 256
 
 def unit_cost(d, rows):
     # the tensor-core decode kernel (8 or 16 rows of 128 dims) pays more per unit
-    return 512 if d == 128 and rows in (8, 16) else 128
+    return 384 if d == 128 and rows in (8, 16) else 128
 
 
 def host_handle(hq, hkv, d, hc, W, P, max_seqs, max_len, pages):
