@@ -533,16 +533,33 @@ __global__ void __launch_bounds__(128)
   const DecodeCombine C = cmb[blockIdx.x / p.R_rows];
   const int r = blockIdx.x % p.R_rows;
   const int d = threadIdx.x;
-  float M = -INFINITY;
-  for (int x = 0; x < C.units; ++x)
-    M = fmaxf(M, __ldg(p.part_ml + (static_cast<int64_t>(C.unit0 + x) * p.R_rows + r) * 2));
-  const float Mr = (M == -INFINITY) ? 0.f : M;  // a slice that sees no key has weight 0
-  float Ls = 0.f, o = 0.f;
-  for (int x = 0; x < C.units; ++x) {
-    const int64_t ur = static_cast<int64_t>(C.unit0 + x) * p.R_rows + r;
-    const float wgt = ex2(__ldg(p.part_ml + ur * 2) - Mr);
-    Ls = fmaf(wgt, __ldg(p.part_ml + ur * 2 + 1), Ls);
-    o = fmaf(wgt, __ldg(p.part_acc + ur * 128 + d), o);
+  // running-maximum merge over the pair's pieces, eight at a time with all
+  // their loads issued together: one round trip to L2 for up to eight pieces
+  constexpr int CH = 8;
+  float M = -INFINITY, Ls = 0.f, o = 0.f;
+  for (int x0 = 0; x0 < C.units; x0 += CH) {
+    float mm[CH], ll[CH], aa[CH];
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+      const int64_t ur = static_cast<int64_t>(C.unit0 + min(x0 + j, C.units - 1)) * p.R_rows + r;
+      mm[j] = x0 + j < C.units ? __ldg(p.part_ml + ur * 2) : -INFINITY;
+      ll[j] = __ldg(p.part_ml + ur * 2 + 1);
+      aa[j] = __ldg(p.part_acc + ur * 128 + d);
+    }
+    float Mn = M;
+#pragma unroll
+    for (int j = 0; j < CH; ++j) Mn = fmaxf(Mn, mm[j]);
+    const float Mr = (Mn == -INFINITY) ? 0.f : Mn;  // a piece that sees no key has weight 0
+    const float sc = ex2(M - Mr);
+    Ls *= sc;
+    o *= sc;
+#pragma unroll
+    for (int j = 0; j < CH; ++j) {
+      const float wgt = ex2(mm[j] - Mr);
+      Ls = fmaf(wgt, ll[j], Ls);
+      o = fmaf(wgt, aa[j], o);
+    }
+    M = Mn;
   }
   const int tk = r / p.Gm, gm = r - tk * p.Gm;
   static_cast<__nv_bfloat16*>(p.o)[(static_cast<int64_t>(C.req * p.T + tk) * p.hq + C.head * p.Gm + gm) * 128 + d] =
