@@ -1291,60 +1291,33 @@ int segkv_rope_shift(segkv_t h, int layer, int seq, int32_t delta, double base, 
       !(base > 1.0))
     return fail(h, SEGKV_ERR_INVALID_ARG, "bad rotary parameters");
   const int32_t nlen = h->len[h->lidx(layer, seq)];
-  std::vector<RopeRun> runs;
+  // the plan is one entry per selected KV head, passed in the kernel's
+  // parameters; the kernel walks each head's block-table row itself
+  RopeParams p{};
+  int32_t max_pages = 0;
   for (int hd = 0; hd < h->Hkv && hd < 64; ++hd) {
     if (!((head_mask >> hd) & 1u)) continue;
     const int32_t s0 = h->start[h->seg(layer, hd, seq)];
-    const int32_t* r = h->table.data() + h->seg(layer, hd, seq) * h->R;
-    for (int32_t pos = s0; pos < nlen;) {
-      const int k = pos / h->P;
-      const int32_t pend = std::min<int32_t>(nlen, (k + 1) * h->P);
-      runs.push_back({r[k], pos - k * h->P, pend - pos, 0});
-      pos = pend;
-    }
+    if (s0 >= nlen) continue;
+    p.heads[p.n_heads++] = {static_cast<int32_t>(h->seg(layer, hd, seq)), s0, nlen, 0};
+    max_pages = std::max(max_pages, (nlen - 1) / h->P - s0 / h->P + 1);
   }
-  if (runs.empty() || delta == 0) return SEGKV_OK;
-  std::vector<float2> cs(rotary_dim / 2);
+  if (p.n_heads == 0 || delta == 0) return SEGKV_OK;
   for (int i = 0; i < rotary_dim / 2; ++i) {
     const double ang = static_cast<double>(delta) * std::pow(base, -2.0 * i / rotary_dim);
-    cs[i] = make_float2(static_cast<float>(std::cos(ang)), static_cast<float>(std::sin(ang)));
+    p.cos_sin[i] = make_float2(static_cast<float>(std::cos(ang)), static_cast<float>(std::sin(ang)));
   }
-  Pack pk;
-  const size_t o_runs = pk.add(runs.data(), runs.size());
-  const size_t o_cs = pk.add(cs.data(), cs.size());
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool inl = pk.buf.size() <= sizeof(AppendBlob);
-  size_t off = 0;
-  uintptr_t d = 0;  // device address of the plan; 0 (offsets alone) when it is inline
-  cudaError_t e;
-  if (inl) {
-    std::memcpy(h->blob.data, pk.buf.data(), pk.buf.size());
-  } else {
-    e = h->ring.reserve(pk.buf.size(), &off);
-    if (e != cudaSuccess) return cuda_fail(h, e, "upload ring");
-    std::memcpy(h->ring.host + off, pk.buf.data(), pk.buf.size());
-    e = h->ring.upload(off, pk.buf.size(), s);
-    if (e != cudaSuccess) return cuda_fail(h, e, "plan upload (rope)");
-    d = reinterpret_cast<uintptr_t>(h->ring.dev + off);
-  }
-  h->upload_bytes += static_cast<int64_t>(pk.buf.size());
-  RopeParams p{};
-  p.runs = reinterpret_cast<const RopeRun*>(d + o_runs);
-  p.cos_sin = reinterpret_cast<const float2*>(d + o_cs);
+  p.table = h->d_table;
   p.kpool = h->kpool;
-  p.plan_inline = inl ? 1 : 0;
-  p.n_runs = static_cast<int>(runs.size());
+  p.R = h->R;
   p.page_size = h->P;
   p.head_dim = h->D;
   p.rotary_dim = rotary_dim;
   p.style = style;
-  const int grid = static_cast<int>(std::min<int64_t>(runs.size(), int64_t(h->num_sms) * 16));
-  e = launch_rope(p, inl ? reinterpret_cast<const AppendBlob*>(&h->blob) : nullptr, grid, s);
+  const int64_t chunks = int64_t(max_pages) * p.n_heads;
+  const int grid = static_cast<int>(std::min<int64_t>(chunks, int64_t(std::max(1, h->num_sms)) * 8));
+  cudaError_t e = launch_rope(p, max_pages, grid, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(h, e, "rope kernel launch");
-  if (!inl) {
-    e = h->ring.commit(off, pk.buf.size(), s);
-    if (e != cudaSuccess) return cuda_fail(h, e, "event record");
-  }
   return SEGKV_OK;
 }
 

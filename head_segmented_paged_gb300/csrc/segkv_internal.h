@@ -122,20 +122,21 @@ struct DecodeParams {
 };
 
 // ---- rotary re-alignment ------------------------------------------------------
-struct RopeRun {
-  int32_t page;   // physical page
-  int32_t slot0;  // first row in the page
-  int32_t nrows;  // rows to rotate
-  int32_t pad;
+// One KV head of the rotated sequence: its kept keys [s0, n), in the pages of
+// block-table row table_row.
+struct RopeHead {
+  int32_t table_row, s0, n, pad;
 };
+constexpr int kRopeMaxHeads = 64;
 struct RopeParams {
-  const RopeRun* runs;
-  const float2* cos_sin;  // [rotary_dim / 2]
+  RopeHead heads[kRopeMaxHeads];
+  float2 cos_sin[128];    // cos and sin of delta * theta_i, i < rotary_dim / 2
+  const int32_t* table;   // device block table
   void* kpool;
-  int plan_inline;        // 1: runs and cos_sin are offsets into the AppendBlob
-  int n_runs, page_size, head_dim, rotary_dim, style;
+  int n_heads, R, page_size, head_dim, rotary_dim, style;
 };
-cudaError_t launch_rope(const RopeParams& p, const AppendBlob* blob, int grid, cudaStream_t s);
+// chunks_per_head: pages spanned by the longest head's kept range
+cudaError_t launch_rope(const RopeParams& p, int chunks_per_head, int grid, cudaStream_t s);
 
 // ---- segment transfer -------------------------------------------------------
 // One KV head of a transferred (layer, sequence): its kept rows [s0, s0 + len)
