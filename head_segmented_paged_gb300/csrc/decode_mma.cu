@@ -23,16 +23,18 @@
 // Warp roles (320 threads, one CTA per SM):
 //   warp 0      producer: the unit's query rows (TMA), then K and V tiles of
 //               128 keys, page by page through the block table (3 stages);
-//   warp 1      TMEM owner (64 columns: S^T and O^T per group) and MMA issuer;
-//   warps 2..5, 6..9  two softmax groups taking alternate stages, each with
-//               its own running maxima, row sums and O^T accumulator; thread
-//               t holds key t of a stage and dimension t of O^T. At the end
-//               of a unit group 0 combines both groups' states and writes.
-// Ordering: S, P and O are per group (stage parity). S of stage i+1 is
-// issued before P V of stage i, so the tensor core forms it while a group
-// works on stage i. A thread's tcgen05 operations complete in order: when
-// S(i) is complete, P V(i-2) is too, so the group's P buffer is free and its
-// O^T is stable for a rescale.
+//   warp 1      TMEM owner (64 columns: two S^T buffers and O^T) and MMA
+//               issuer;
+//   warps 2..5, 6..9  two softmax groups working on every stage together,
+//               each on its own query rows (rows 0..7 and 8..15; with 8 rows
+//               group 0 takes them all), with their own running maxima and row
+//               sums; thread t holds key t of a stage and dimension t of O^T.
+//               At the end of a unit each group writes its own rows.
+// Ordering: S and P have two buffers by stage parity; O^T is one accumulator.
+// S of stage i+1 is issued before P V of stage i, so the tensor core forms it
+// while the groups work on stage i. A thread's tcgen05 operations complete in
+// order: when S(i) is complete, P V(i-2) is too, so P buffer i % 2 is free. A
+// group that must rescale O^T at stage i first waits for P V(i-1).
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -56,8 +58,7 @@ constexpr uint32_t OFF_Q = 2 * NST * KV_TILE;          // Q [2 buffers, by unit 
 constexpr uint32_t OFF_P = OFF_Q + 4 * kAtomR;         // P^T [2 buffers]: 2 atoms (keys 0..63, 64..127)
 constexpr uint32_t OFF_XCH = OFF_P + 4 * kAtomR;          // int [group][2][4][16]: per-warp row maxima
 constexpr uint32_t OFF_LS = OFF_XCH + 2 * 2 * 4 * MN * 4;  // float [group][2][4][16]: per-warp row sums
-constexpr uint32_t OFF_GX = OFF_LS + 2 * 2 * 4 * MN * 4;   // float [2][2][16]: group 1's row max and sum
-constexpr uint32_t OFF_BAR = OFF_GX + 2 * 2 * MN * 4;
+constexpr uint32_t OFF_BAR = OFF_LS + 2 * 2 * 4 * MN * 4;
 enum {
   Y_Q_FULL = 0,                 // +Q buffer (unit parity)
   Y_Q_EMPTY = 2,                // +Q buffer
@@ -70,13 +71,14 @@ enum {
   Y_O_EMPTY = Y_S_FULL + 5,
   Y_MX = Y_S_FULL + 6,          // +group * 2 + the group's stage parity
   Y_LS = Y_S_FULL + 10,         // +group * 2 + unit parity
-  Y_GX = Y_S_FULL + 14,         // +unit parity
+  Y_PV_DONE = Y_S_FULL + 14,    // the last P V issued is complete
   Y_DRAIN = Y_S_FULL + 16,
   Y_NUM = Y_S_FULL + 17
 };
 constexpr uint32_t OFF_MISC = OFF_BAR + Y_NUM * 8;
 constexpr uint32_t MD_BYTES = OFF_MISC + 16 + 1024;  // + slack to align to 1 KB
-constexpr uint32_t TM_S = 0, TM_O = 32, TM_COLS = 64;  // S^T at 0 and 16, O^T at 32 and 48 (per group)
+constexpr uint32_t TM_S = 0, TM_O = 32, TM_COLS = 64;  // S^T at 0 and 16 (by stage parity), O^T at 32
+constexpr int RG = 8;  // query rows per softmax group (TMEM columns 8 * group ..)
 constexpr uint64_t kDrainNsMD = 200ull * 1000 * 1000;
 static_assert(MD_BYTES <= 227 * 1024, "decode_mma shared memory");
 
@@ -87,6 +89,9 @@ struct MdCtx {
   WaitCtx wc;
   __device__ uint32_t bar(int i) const { return sbase + OFF_BAR + 8u * i; }
 };
+
+// 16 rows: each softmax group takes 8; 8 rows: group 0 takes them all
+__device__ __forceinline__ int n_groups(const DecodeMmaParams& p) { return p.R_rows > RG ? 2 : 1; }
 
 template <typename T>
 __device__ __forceinline__ const T* plan_ptr(const T* p, const PlanBlob& blob, int inl) {
@@ -218,14 +223,15 @@ __device__ void md_mma(const DecodeMmaParams& p, const DecodeUnit* units, const 
       {
         const uint64_t va = st == 0 ? dv[0] : (st == 1 ? dv[1] : dv[2]);
         const uint64_t pb = (g & 1) ? dp[1] : dp[0];
-        const uint32_t d = c.tmem + TM_O + (g & 1) * MN;
-        const bool fresh = g - g0 < 2;
+        const uint32_t d = c.tmem + TM_O;
+        const bool fresh = g == g0;
 #pragma unroll
         for (int kk = 0; kk < KT / 16; ++kk)
-          // O of group g % 2; that group's first stage of the unit starts it afresh
+          // the unit's first stage starts O^T afresh
           mma_bf16(d, va + kk * 2048 / 16, pb + (((kk >> 2) * kAtomR + (kk & 3) * 32) >> 4),
                    IDESC_PV, (!fresh || kk > 0) ? 1u : 0u);
       }
+      mma_commit(c.bar(Y_PV_DONE));
       mma_commit(c.bar(Y_KV_EMPTY + st));
       if (kt == kt1) mma_commit(c.bar(Y_O_FULL));
     }
@@ -238,56 +244,61 @@ __device__ void md_mma(const DecodeMmaParams& p, const DecodeUnit* units, const 
 
 __device__ void md_softmax(const DecodeMmaParams& p, const DecodeUnit* units,
                            const int32_t* cta_begin, const MdCtx& c, int grp, int warp, int lane) {
+  // rows of this group: with 16 rows each group takes 8 (TMEM columns
+  // 8 * grp ..); with 8 rows group 0 takes them all and group 1 has no work
+  if (grp >= n_groups(p)) return;
+  const int r0 = grp * RG;  // first row (and S^T / O^T column) of the group
+  const int nr = p.R_rows - r0 < RG ? p.R_rows - r0 : RG;
   const int wq = warp & 3;  // the TMEM lane quarter this warp may access
   const int t = wq * 32 + lane;
   const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
   const float sc = p.scale_log2;
   const bool multi = p.T > 1;
-  int g = 0, ui = 0, js = 0;  // js: stages this group has handled (its exchange buffer index)
+  int g = 0, ui = 0;
   for (int u = cta_begin[blockIdx.x]; u < cta_begin[blockIdx.x + 1]; ++u, ++ui) {
     const DecodeUnit U = units[u];
     const int kt0 = U.k0 / KT, kt1 = (U.k1 - 1) / KT;
     const int g0 = g;
-    float m_ref[MN], l_part[MN];
+    float m_ref[RG], l_part[RG];
 #pragma unroll
-    for (int r = 0; r < MN; ++r) {
+    for (int r = 0; r < RG; ++r) {
       m_ref[r] = -INFINITY;
       l_part[r] = 0.f;
     }
-    bool ok = true, had = false;  // had: this group handled a stage of the unit
+    bool ok = true;
     for (int kt = kt0; kt <= kt1; ++kt, ++g) {
-      if ((g & 1) != grp) continue;  // stages alternate between the two groups
-      if (!waitw(c.bar(Y_S_FULL + grp), (g >> 1) & 1, c.wc)) { ok = false; break; }
+      const int sb = g & 1;  // S and P buffers, exchange slot: by stage parity
+      if (!waitw(c.bar(Y_S_FULL + sb), (g >> 1) & 1, c.wc)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sv[MN];
-      tmem_ld16(c.tmem + lane_off + TM_S + grp * MN, sv);
+      uint32_t sv[RG];
+      tmem_ld8(c.tmem + lane_off + TM_S + sb * MN + r0, sv);
       tmem_wait_ld();
       const int j = kt * KT + t;  // this thread's key
       const bool in_unit = j >= U.k0 && j < U.k1;
-      float s[MN];
+      float s[RG];
 #pragma unroll
-      for (int r = 0; r < MN; ++r) {
-        bool vis = in_unit && r < p.R_rows;
-        if (multi) {  // row r = token r / Gm sees keys up to its own position (and its window)
-          const int pr = U.q_last - (p.T - 1) + r / p.Gm;
+      for (int r = 0; r < RG; ++r) {
+        bool vis = in_unit && r < nr;
+        if (multi) {  // row r0 + r = token (r0 + r) / Gm sees keys up to its own position (and its window)
+          const int pr = U.q_last - (p.T - 1) + (r0 + r) / p.Gm;
           vis = vis && j <= pr && (!U.local || j >= pr - p.window + 1);
         }
         s[r] = vis ? __uint_as_float(sv[r]) * sc : -INFINITY;
       }
       // each row's maximum over the stage's 128 keys, shared by the group's warps
-      int* xch = reinterpret_cast<int*>(c.smem + OFF_XCH) + (grp * 2 + (js & 1)) * 4 * MN;
+      int* xch = reinterpret_cast<int*>(c.smem + OFF_XCH) + (grp * 2 + sb) * 4 * MN;
 #pragma unroll
-      for (int r = 0; r < MN; ++r) {
+      for (int r = 0; r < RG; ++r) {
         const int wm = warp_max_s32(f32_ordered(s[r]));
         if (lane == 0) xch[wq * MN + r] = wm;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(Y_MX + grp * 2 + (js & 1)));
-      if (!waitw(c.bar(Y_MX + grp * 2 + (js & 1)), (js >> 1) & 1, c.wc)) { ok = false; break; }
+      if (lane == 0) mbar_arrive(c.bar(Y_MX + grp * 2 + sb));
+      if (!waitw(c.bar(Y_MX + grp * 2 + sb), (g >> 1) & 1, c.wc)) { ok = false; break; }
       bool resc = false;
-      float alpha[MN];
+      float alpha[RG];
 #pragma unroll
-      for (int r = 0; r < MN; ++r) {
+      for (int r = 0; r < RG; ++r) {
         float mst = f32_from_ordered(xch[r]);
 #pragma unroll
         for (int w = 1; w < 4; ++w) mst = fmaxf(mst, f32_from_ordered(xch[w * MN + r]));
@@ -300,30 +311,35 @@ __device__ void md_softmax(const DecodeMmaParams& p, const DecodeUnit* units,
       }
       if (resc) {
 #pragma unroll
-        for (int r = 0; r < MN; ++r) l_part[r] *= alpha[r];
-        if (had) {  // this group's O^T holds earlier stages (their P V was issued before S(g)): scale it
-          uint32_t ov[MN];
-          tmem_ld16(c.tmem + lane_off + TM_O + grp * MN, ov);
+        for (int r = 0; r < RG; ++r) l_part[r] *= alpha[r];
+        if (g > g0) {
+          // O^T holds the unit's earlier stages. S(g) was issued after P V(g-2)
+          // but before P V(g-1): wait for P V(g-1), then scale this group's rows
+          if (!waitw(c.bar(Y_PV_DONE), (g - 1) & 1, c.wc)) { ok = false; break; }
+          tc_fence_after();
+          uint32_t ov[RG];
+          tmem_ld8(c.tmem + lane_off + TM_O + r0, ov);
           tmem_wait_ld();
 #pragma unroll
-          for (int r = 0; r < MN; ++r) ov[r] = __float_as_uint(__uint_as_float(ov[r]) * alpha[r]);
-          tmem_st16(c.tmem + lane_off + TM_O + grp * MN, ov);
+          for (int r = 0; r < RG; ++r) ov[r] = __float_as_uint(__uint_as_float(ov[r]) * alpha[r]);
+          tmem_st8(c.tmem + lane_off + TM_O + r0, ov);
           tmem_wait_st();
         }
       }
       // P^T[r][t] in bf16, 128-byte swizzled: atom t / 64, 16-byte chunk ((t % 64) / 8) ^ (r % 8).
-      // S(g) was issued after P V(g-2), so this group's P buffer is free once S(g) is complete.
-      uint8_t* pb = c.smem + OFF_P + grp * 2 * kAtomR + (t >> 6) * kAtomR + (t & 7) * 2;
+      // S(g) was issued after P V(g-2), so P buffer g % 2 is free once S(g) is complete.
+      uint8_t* pb = c.smem + OFF_P + sb * 2 * kAtomR + (t >> 6) * kAtomR + (t & 7) * 2;
       const int chunk = (t & 63) >> 3;
 #pragma unroll
-      for (int r = 0; r < MN; ++r) {
+      for (int r = 0; r < RG; ++r) {
+        const int row = r0 + r;
         const float mu = (m_ref[r] == -INFINITY) ? 0.f : m_ref[r];
         const float pr = ex2(s[r] - mu);
         l_part[r] += pr;
         const __nv_bfloat16 hb = __float2bfloat16_rn(pr);
-        *reinterpret_cast<__nv_bfloat16*>(pb + r * 128 + ((chunk ^ (r & 7)) << 4)) = hb;
+        *reinterpret_cast<__nv_bfloat16*>(pb + row * 128 + ((chunk ^ (row & 7)) << 4)) = hb;
       }
-      if (kt == kt0 || kt == kt1) {
+      if (grp == 0 && (kt == kt0 || kt == kt1)) {
         // edge stage: zero the V rows of keys outside the unit (stale or
         // unwritten slots), once their tile has landed, so P = 0 never meets NaN
         const int st = g % NST;
@@ -341,16 +357,14 @@ __device__ void md_softmax(const DecodeMmaParams& p, const DecodeUnit* units,
       fence_proxy_async_smem();  // P (and zeroed V rows) are read by the tensor core
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(c.bar(Y_P_FULL + grp));
-      had = true;
-      ++js;
+      if (lane == 0) mbar_arrive(c.bar(Y_P_FULL + sb));
     }
     if (!ok) break;
 
-    // the group's row sums over its keys
+    // the group's row sums over the stage's keys
     float* ls = reinterpret_cast<float*>(c.smem + OFF_LS) + (grp * 2 + (ui & 1)) * 4 * MN;
 #pragma unroll
-    for (int r = 0; r < MN; ++r) {
+    for (int r = 0; r < RG; ++r) {
       float v = l_part[r];
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -359,90 +373,54 @@ __device__ void md_softmax(const DecodeMmaParams& p, const DecodeUnit* units,
     __syncwarp();
     if (lane == 0) mbar_arrive(c.bar(Y_LS + grp * 2 + (ui & 1)));
     if (!waitw(c.bar(Y_LS + grp * 2 + (ui & 1)), (ui >> 1) & 1, c.wc)) break;
-    float L[MN];
+    float L[RG];
 #pragma unroll
-    for (int r = 0; r < MN; ++r) L[r] = ((ls[r] + ls[MN + r]) + ls[2 * MN + r]) + ls[3 * MN + r];
-    float* gx = reinterpret_cast<float*>(c.smem + OFF_GX) + (ui & 1) * 2 * MN;
-    if (grp == 1) {  // hand this group's row maxima and sums to group 0
-      if (t == 0) {
-#pragma unroll
-        for (int r = 0; r < MN; ++r) {
-          gx[r] = m_ref[r];
-          gx[MN + r] = L[r];
-        }
-        mbar_arrive(c.bar(Y_GX + (ui & 1)));
-      }
-      continue;
-    }
+    for (int r = 0; r < RG; ++r) L[r] = ((ls[r] + ls[MN + r]) + ls[2 * MN + r]) + ls[3 * MN + r];
 
-    // group 0: combine both groups' states and write (thread t = dimension t)
-    if (!waitw(c.bar(Y_GX + (ui & 1)), (ui >> 1) & 1, c.wc)) break;
+    // this group's rows of O^T (thread t = dimension t), then its output
     if (!waitw(c.bar(Y_O_FULL), ui & 1, c.wc)) break;
     tc_fence_after();
-    uint32_t o0[MN], o1[MN];
-    tmem_ld16(c.tmem + lane_off + TM_O, o0);
-    tmem_ld16(c.tmem + lane_off + TM_O + MN, o1);
+    uint32_t ov[RG];
+    tmem_ld8(c.tmem + lane_off + TM_O + r0, ov);
     tmem_wait_ld();
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(c.bar(Y_O_EMPTY));
-    const int n_st = kt1 - kt0 + 1;
-    const bool had1 = n_st >= 2 || (g0 & 1) == 1;  // group 1 handled a stage of the unit
-    const bool single = U.pair_units == 1;
-    // Every row's merge is computed into registers before any store, so the
-    // rows' arithmetic overlaps instead of running one row after another
-    // behind each row's global store.
-    float gm[MN], gl[MN];
+    if (U.pair_units == 1) {
+      __nv_bfloat16 ob[RG];
 #pragma unroll
-    for (int r = 0; r < MN; ++r) {
-      gm[r] = gx[r];
-      gl[r] = gx[MN + r];
-    }
-    float ov[MN], Mv[MN], Lv[MN];
-#pragma unroll
-    for (int r = 0; r < MN; ++r) {
-      const float M = fmaxf(m_ref[r], gm[r]);
-      const float Mr = (M == -INFINITY) ? 0.f : M;
-      const float w0 = ex2(m_ref[r] - Mr), w1 = ex2(gm[r] - Mr);
-      ov[r] = (had ? __uint_as_float(o0[r]) * w0 : 0.f) + (had1 ? __uint_as_float(o1[r]) * w1 : 0.f);
-      Lv[r] = L[r] * w0 + gl[r] * w1;
-      Mv[r] = M;
-    }
-    if (single) {
-      __nv_bfloat16 ob[MN];
-#pragma unroll
-      for (int r = 0; r < MN; ++r) ob[r] = __float2bfloat16_rn(ov[r] / Lv[r]);
+      for (int r = 0; r < RG; ++r) ob[r] = __float2bfloat16_rn(__uint_as_float(ov[r]) / L[r]);
       __nv_bfloat16* obase = static_cast<__nv_bfloat16*>(p.o) +
                              (static_cast<int64_t>(U.req) * p.T * p.hq + U.head * p.Gm) * 128 + t;
 #pragma unroll
-      for (int r = 0; r < MN; ++r) {
-        if (r >= p.R_rows) break;
-        const int tk = r / p.Gm, gm_ = r - tk * p.Gm;
-        obase[(static_cast<int64_t>(tk) * p.hq + gm_) * 128] = ob[r];
+      for (int r = 0; r < RG; ++r) {
+        if (r >= nr) break;
+        const int tk = (r0 + r) / p.Gm, gm = (r0 + r) - tk * p.Gm;
+        obase[(static_cast<int64_t>(tk) * p.hq + gm) * 128] = ob[r];
       }
       if (p.lse != nullptr && t == 0) {
 #pragma unroll
-        for (int r = 0; r < MN; ++r) {
-          if (r >= p.R_rows) break;
-          const int tk = r / p.Gm, gm_ = r - tk * p.Gm;
-          p.lse[static_cast<int64_t>(U.head * p.Gm + gm_) * p.n_rows + U.req * p.T + tk] =
-              (Mv[r] + log2f(Lv[r])) * 0.6931471805599453f;
+        for (int r = 0; r < RG; ++r) {
+          if (r >= nr) break;
+          const int tk = (r0 + r) / p.Gm, gm = (r0 + r) - tk * p.Gm;
+          p.lse[static_cast<int64_t>(U.head * p.Gm + gm) * p.n_rows + U.req * p.T + tk] =
+              (m_ref[r] + log2f(L[r])) * 0.6931471805599453f;
         }
       }
     } else {
-      float* acc = p.part_acc + static_cast<int64_t>(u) * p.R_rows * 128 + t;
+      float* acc = p.part_acc + (static_cast<int64_t>(u) * p.R_rows + r0) * 128 + t;
 #pragma unroll
-      for (int r = 0; r < MN; ++r) {
-        if (r >= p.R_rows) break;
-        acc[r * 128] = ov[r];
+      for (int r = 0; r < RG; ++r) {
+        if (r >= nr) break;
+        acc[r * 128] = __uint_as_float(ov[r]);
       }
       if (t == 0) {
-        float* ml = p.part_ml + static_cast<int64_t>(u) * p.R_rows * 2;
+        float* ml = p.part_ml + (static_cast<int64_t>(u) * p.R_rows + r0) * 2;
 #pragma unroll
-        for (int r = 0; r < MN; ++r) {
-          if (r >= p.R_rows) break;
-          ml[2 * r] = Mv[r];
-          ml[2 * r + 1] = Lv[r];
+        for (int r = 0; r < RG; ++r) {
+          if (r >= nr) break;
+          ml[2 * r] = m_ref[r];
+          ml[2 * r + 1] = L[r];
         }
       }
     }
@@ -474,13 +452,14 @@ __global__ void __launch_bounds__(kThreadsMD, 1)
       mbar_init(c.bar(Y_V_FULL + s), 1);
       mbar_init(c.bar(Y_KV_EMPTY + s), 1);
     }
+    const uint32_t softmax_warps = 4u * n_groups(p);
     for (int x = 0; x < 2; ++x) {
       mbar_init(c.bar(Y_S_FULL + x), 1);
-      mbar_init(c.bar(Y_P_FULL + x), 4);  // one arrival per warp of the group
-      mbar_init(c.bar(Y_GX + x), 1);
+      mbar_init(c.bar(Y_P_FULL + x), softmax_warps);  // one arrival per softmax warp
     }
+    mbar_init(c.bar(Y_PV_DONE), 1);
     mbar_init(c.bar(Y_O_FULL), 1);
-    mbar_init(c.bar(Y_O_EMPTY), 4);  // group 0's warps read both O^T
+    mbar_init(c.bar(Y_O_EMPTY), softmax_warps);  // each group reads its rows of O^T
     for (int x = 0; x < 4; ++x) {
       mbar_init(c.bar(Y_MX + x), 4);
       mbar_init(c.bar(Y_LS + x), 4);
