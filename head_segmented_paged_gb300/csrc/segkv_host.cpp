@@ -1076,17 +1076,17 @@ static int decode_plan(segkv* h, int layer, int T, const int32_t* seq_lens, cons
   // a ticket and may merge. Per-CTA timestamps on the ragged-decode workload
   // priced a unit at about the time a CTA streams 128 keys in; the split
   // surcharge was tuned on the same workload (0 -> 256 keys: 62.4 -> 61.6 us).
-  // On the tensor-core kernel a unit also waits for its query rows and its
-  // first S, and ends with a merge of two softmax groups; a sweep on the
-  // four-token ragged decode priced it at 384 keys (256: 91.6-92.0 us, 384:
-  // 89.4-89.6, 512: 92.8).
+  // On the tensor-core kernel, with the rows split between its two softmax
+  // groups, a sweep on the four-token ragged decode priced a unit at 64 keys
+  // (0: 71.3-71.8 us, 64: 70.2-70.5, 128: 70.8-71.1, 384: 73.6, 512: 75.6-75.9)
+  // and a split piece at 128 (70.5 us; 512: 72.0).
   // The smallest per-CTA budget whose greedy cut fits the grid is found by
   // bisection.
   // On the tensor-core kernel, work and cuts are in whole 128-key tiles: a cut
   // inside a tile would make both neighbours stream that whole tile.
   const int64_t quantum = mma ? 128 : 1;
-  const int64_t kDecodeUnitCost = mma ? 384 : 128;
-  const int64_t kDecodeSplitCost = 256;
+  const int64_t kDecodeUnitCost = mma ? 64 : 128;
+  const int64_t kDecodeSplitCost = mma ? 128 : 256;
   const int64_t sk = mma ? 128 : decode_stage_keys(rows);
   const int64_t ctas = ctas_override > 0 ? ctas_override
                        : h->num_sms <= 0 ? decode_max_grid(h)

@@ -28,12 +28,15 @@ import head_segmented_paged_gb300 as S
 import oracle
 
 GLOBAL, LOCAL = 0, 1
-SPLIT_COST = 256
 
 
 def unit_cost(d, rows):
-    # the tensor-core decode kernel (8 or 16 rows of 128 dims) pays more per unit
-    return 384 if d == 128 and rows in (8, 16) else 128
+    # the tensor-core decode kernel (8 or 16 rows of 128 dims) is priced apart
+    return 64 if d == 128 and rows in (8, 16) else 128
+
+
+def split_cost(d, rows):
+    return 128 if d == 128 and rows in (8, 16) else 256
 
 
 def host_handle(hq, hkv, d, hc, W, P, max_seqs, max_len, pages):
@@ -79,6 +82,7 @@ def check_plan(units, cta, lens, hc, W, T, d, G, num_ctas):
     # balance: a CTA closes only when the next unit's charges and one quantum
     # of work no longer fit
     U = unit_cost(d, rows)
+    SPLIT_COST = split_cost(d, rows)
     costs = []
     for c in range(len(cta) - 1):
         us = units[cta[c]:cta[c + 1]]
