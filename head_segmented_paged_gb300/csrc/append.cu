@@ -19,6 +19,10 @@ __device__ __forceinline__ const T* plan_ptr(const T* p, const AppendBlob& blob,
 
 __global__ void __launch_bounds__(256)
     append_kernel(AppendParams p, const __grid_constant__ AppendBlob blob) {
+  // a kernel launched as a programmatic dependent of this one (decode) may
+  // start its prologue now; it waits for this grid's completion before it
+  // reads anything this grid writes
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   p.seqs = plan_ptr(p.seqs, blob, p.plan_inline);
   p.tiles = plan_ptr(p.tiles, blob, p.plan_inline);
   p.page_list = plan_ptr(p.page_list, blob, p.plan_inline);

@@ -134,6 +134,10 @@ __global__ void __launch_bounds__(DCfg<D, G>::THREADS, DCfg<D, G>::MIN_BLOCKS)
     fence_mbar_init();
   }
   __syncthreads();
+  // launched as a programmatic dependent of the previous kernel on the stream:
+  // everything above overlaps its tail; nothing the previous kernels wrote
+  // (plan, block table, q, K/V, partials, counters) is read before this wait
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const WaitCtx wc{abort_flag, p.status, p.timeout_ns};
   const DecodeUnit* units =
       p.plan_inline ? reinterpret_cast<const DecodeUnit*>(blob.data + reinterpret_cast<uintptr_t>(p.units))
@@ -533,8 +537,19 @@ static cudaError_t launch_dgm(const DecodeParams& p, const PlanBlob* blob, int g
     if (e != cudaSuccess) return e;
     if (dev < kMaxDevices) attr_set[dev] = true;
   }
-  decode_split_kernel<D, G, MQ><<<grid, C::THREADS, C::BYTES, s>>>(p, blob ? *blob : empty_blob);
-  return cudaGetLastError();
+  // programmatic dependent launch: the CTAs start while the previous kernel
+  // drains and wait in the kernel (griddepcontrol.wait) for its completion
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, MQ>, p, blob ? *blob : empty_blob);
 }
 
 template <int D, int G>

@@ -479,6 +479,10 @@ __global__ void __launch_bounds__(kThreadsMD, 1)
   __syncthreads();
   tc_fence_after();
   c.tmem = *tmem_slot;
+  // launched as a programmatic dependent of the previous kernel on the stream:
+  // the setup above overlaps its tail; nothing the previous kernels wrote is
+  // read before this wait
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // the merge kernel may be scheduled now: it waits for this whole grid to
   // complete (griddepcontrol.wait) before it reads a partial
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -564,8 +568,22 @@ cudaError_t launch_decode_mma(const DecodeMmaParams& p, const PlanBlob* blob, co
     if (dev < kMaxDevices) attr_set[dev] = true;
   }
   const PlanBlob& b = blob ? *blob : empty_blob;
-  decode_mma_kernel<<<grid, kThreadsMD, MD_BYTES, s>>>(tq, tk, tv, p, b);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  {
+    // programmatic dependent launch: the CTAs set up while the previous
+    // kernel drains and wait in the kernel for its completion
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreadsMD);
+    cfg.dynamicSmemBytes = MD_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_mma_kernel, tq, tk, tv, p, b);
+  }
   if (e != cudaSuccess || p.n_combine == 0) return e;
   // programmatic dependent launch: the merge's launch overlaps the tail of
   // the attention kernel instead of following its completion
