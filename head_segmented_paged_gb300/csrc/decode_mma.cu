@@ -65,11 +65,11 @@ enum {
   Y_K_FULL = 4,                 // +stage
   Y_V_FULL = 4 + NST,           // +stage
   Y_KV_EMPTY = 4 + 2 * NST,     // +stage
-  Y_S_FULL = 4 + 3 * NST,       // +group (= stage parity): S buffer
-  Y_P_FULL = Y_S_FULL + 2,      // +group: P buffer
+  Y_S_FULL = 4 + 3 * NST,       // +stage parity: S buffer
+  Y_P_FULL = Y_S_FULL + 2,      // +stage parity: P buffer
   Y_O_FULL = Y_S_FULL + 4,
   Y_O_EMPTY = Y_S_FULL + 5,
-  Y_MX = Y_S_FULL + 6,          // +group * 2 + the group's stage parity
+  Y_MX = Y_S_FULL + 6,          // +group * 2 + stage parity
   Y_LS = Y_S_FULL + 10,         // +group * 2 + unit parity
   Y_PV_DONE = Y_S_FULL + 14,    // the last P V issued is complete
   Y_DRAIN = Y_S_FULL + 16,
