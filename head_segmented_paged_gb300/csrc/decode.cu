@@ -537,19 +537,8 @@ static cudaError_t launch_dgm(const DecodeParams& p, const PlanBlob* blob, int g
     if (e != cudaSuccess) return e;
     if (dev < kMaxDevices) attr_set[dev] = true;
   }
-  // programmatic dependent launch: the CTAs start while the previous kernel
-  // drains and wait in the kernel (griddepcontrol.wait) for its completion
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(C::THREADS);
-  cfg.dynamicSmemBytes = C::BYTES;
-  cfg.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_split_kernel<D, G, MQ>, p, blob ? *blob : empty_blob);
+  return launch_pdl(decode_split_kernel<D, G, MQ>, dim3(grid), dim3(C::THREADS), C::BYTES, s, p,
+                    blob ? *blob : empty_blob);
 }
 
 template <int D, int G>

@@ -568,36 +568,10 @@ cudaError_t launch_decode_mma(const DecodeMmaParams& p, const PlanBlob* blob, co
     if (dev < kMaxDevices) attr_set[dev] = true;
   }
   const PlanBlob& b = blob ? *blob : empty_blob;
-  cudaError_t e;
-  {
-    // programmatic dependent launch: the CTAs set up while the previous
-    // kernel drains and wait in the kernel for its completion
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreadsMD);
-    cfg.dynamicSmemBytes = MD_BYTES;
-    cfg.stream = s;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, decode_mma_kernel, tq, tk, tv, p, b);
-  }
+  cudaError_t e = launch_pdl(decode_mma_kernel, dim3(grid), dim3(kThreadsMD), MD_BYTES, s, tq, tk, tv, p, b);
   if (e != cudaSuccess || p.n_combine == 0) return e;
-  // programmatic dependent launch: the merge's launch overlaps the tail of
-  // the attention kernel instead of following its completion
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_combine * p.R_rows);
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_combine_kernel, p, b);
+  // the merge's launch overlaps the tail of the attention kernel
+  return launch_pdl(decode_combine_kernel, dim3(p.n_combine * p.R_rows), dim3(128), 0, s, p, b);
 }
 
 }  // namespace skv

@@ -37,6 +37,9 @@ __global__ void __launch_bounds__(256) rope_kernel(const __grid_constant__ RopeP
   __shared__ float2 cs[128];
   for (int i = threadIdx.x; i < half; i += blockDim.x) cs[i] = p.cos_sin[i];
   __syncthreads();
+  // launched as a programmatic dependent of the previous kernel: the block
+  // table and the keys are read only after it has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __nv_bfloat16* kp = static_cast<__nv_bfloat16*>(p.kpool);
   const int n_chunks = chunks_per_head * p.n_heads;
   // chunk c: head c / chunks_per_head, rows [P * (c % chunks_per_head), + P) of
@@ -104,8 +107,7 @@ __global__ void __launch_bounds__(256) rope_kernel(const __grid_constant__ RopeP
 }
 
 cudaError_t launch_rope(const RopeParams& p, int chunks_per_head, int grid, cudaStream_t s) {
-  rope_kernel<<<grid, 256, 0, s>>>(p, chunks_per_head);
-  return cudaGetLastError();
+  return launch_pdl(rope_kernel, dim3(grid), dim3(256), 0, s, p, chunks_per_head);
 }
 
 }  // namespace skv

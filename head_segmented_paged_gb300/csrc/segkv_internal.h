@@ -3,11 +3,31 @@
 // buffer; one cudaMemcpyAsync per call moves them next to the kernel.
 #pragma once
 
+#include <utility>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace skv {
+
+// Launch a kernel as a programmatic dependent of the previous kernel on the
+// stream: its CTAs may start while that kernel drains. The kernel must execute
+// griddepcontrol.wait before it reads anything an earlier kernel wrote.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 constexpr int kKeyTile = 128;     // prefill: keys per tile (one MMA N)
 constexpr int kRowsPerTile = 128; // prefill: query rows per tile (MMA M)

@@ -19,6 +19,10 @@ constexpr int kXferUnroll = 4;  // 16-byte chunks of K and of V in flight per th
 __global__ void __launch_bounds__(256)
     transfer_kernel(TransferParams p, const __grid_constant__ AppendBlob blob) {
   extern __shared__ XferHead hs[];  // [n_heads]
+  // launched as a programmatic dependent of the previous kernel: the plan (it
+  // may come from the upload kernel), the tables and the pools are read only
+  // after it has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const XferHead* heads = xfer_plan_ptr(p.heads, blob, p.plan_inline);
   const int32_t* page_list = xfer_plan_ptr(p.page_list, blob, p.plan_inline);
   for (int i = threadIdx.x; i < p.n_heads; i += blockDim.x) hs[i] = heads[i];
@@ -83,8 +87,8 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_transfer(const TransferParams& p, const AppendBlob* blob, int grid,
                             cudaStream_t s) {
   static const AppendBlob empty_blob{};
-  transfer_kernel<<<grid, 256, p.n_heads * sizeof(XferHead), s>>>(p, blob ? *blob : empty_blob);
-  return cudaGetLastError();
+  return launch_pdl(transfer_kernel, dim3(grid), dim3(256), p.n_heads * sizeof(XferHead), s, p,
+                    blob ? *blob : empty_blob);
 }
 
 }  // namespace skv
