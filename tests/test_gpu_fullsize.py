@@ -157,3 +157,49 @@ def test_ragged_decode_full_steps():
         for b in ids:
             assert h.segment(0, hd, b) == m.segment(0, hd, b)
     h.close()
+
+
+def test_ragged_decode_four_tokens_full():
+    # The benchmark's four-token leg: the ragged-decode contexts, four new
+    # tokens per request appended in one call, 4 x 4 = 16 query rows per KV head
+    # on the tensor-core decode kernel (split pairs, merge kernel, LSE).
+    w = I.ragged_decode(steps=1)
+    B, P, D, T = len(w.seq_lens), w.page_size, w.head_dim, 4
+    q, k, v = gen_layer(w, 0, w.seq_lens)
+    del q
+    pages = sum((n + T + 8) // P + 2 for n in w.seq_lens) * w.hkv + 64
+    kp = torch.full((pages, P, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    vp = torch.full_like(kp, float("nan"))
+    h = S.SegKV(1, w.hq, w.hkv, D, w.head_class, w.window, P, B, max(w.seq_lens) + T + 8, kp, vp)
+    m = oracle.PageModel(1, w.hkv, w.head_class, w.window, P, B, max(w.seq_lens) + T + 8, pages)
+    cu = np.concatenate([[0], np.cumsum(w.seq_lens)]).astype(np.int32)
+    ids = list(range(B))
+    h.append(0, k, v, cu, ids)
+    assert m.append(0, cu, ids) == 0
+    h.trim(0, ids)
+    assert m.trim(0, ids) == 0
+    kt = I.normal_bf16(w.seed, I.tensor_stream(I._KD, 1, 9999), (B * T, w.hkv, D), device="cuda")
+    vt = I.normal_bf16(w.seed, I.tensor_stream(I._VD, 1, 9999), (B * T, w.hkv, D), device="cuda")
+    qt = I.normal_bf16(w.seed, I.tensor_stream(I._QD, 1, 9999), (B * T, w.hq, D), device="cuda")
+    cut = np.arange(0, B * T + 1, T, dtype=np.int32)
+    h.append(0, kt, vt, cut, ids)
+    assert m.append(0, cut, ids) == 0
+    lens = [m.seq_len(0, b) for b in ids]
+    o = torch.full((B * T, w.hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.hq, B * T), dtype=torch.float32, device="cuda")
+    ws = torch.empty(h.workspace_size(S.SEGKV_WS_DECODE, B * T, B) // 4 + 64, device="cuda")
+    h.decode_attn_multi(0, qt, T, lens, ids, o, lse, ws)
+    assert h.status() == 0
+    kc, vc, ktc, vtc = k.cpu(), v.cpu(), kt.cpu(), vt.cpu()
+    klog = torch.cat([torch.cat([kc[cu[b]:cu[b + 1]], ktc[T * b:T * b + T]]) for b in ids])
+    vlog = torch.cat([torch.cat([vc[cu[b]:cu[b + 1]], vtc[T * b:T * b + T]]) for b in ids])
+    offs = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(np.int64)
+    seg = np.array([[m.segment(0, hd, b)[0] for hd in range(w.hkv)] for b in ids], np.int32)
+    row_seq = np.repeat(np.arange(B), T).astype(np.int32)
+    row_pos = np.concatenate([np.arange(n - T, n) for n in lens]).astype(np.int32)
+    rc, ref, ref_lse = oracle.attention(qt.cpu(), klog, vlog, row_seq, row_pos, offs, lens,
+                                        w.head_class[0], w.window[0], seg)
+    assert rc == 0
+    check_close(o, ref, "four-token ragged decode")
+    np.testing.assert_allclose(lse.cpu().numpy().T, ref_lse, atol=1e-3, rtol=0)
+    h.close()
