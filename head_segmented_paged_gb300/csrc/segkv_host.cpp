@@ -191,17 +191,31 @@ class PagePool {
     cursor_ = std::min(cursor_, w >> 6);
     ++count_;
   }
-  int32_t top() {  // the lowest free page; the pool must not be empty
+  int32_t take() {  // remove and return the lowest free page; the pool must not be empty
     while (sum_[cursor_] == 0) ++cursor_;
     const size_t w = cursor_ * 64 + static_cast<size_t>(__builtin_ctzll(sum_[cursor_]));
-    return static_cast<int32_t>(w * 64 + static_cast<size_t>(__builtin_ctzll(bits_[w])));
-  }
-  void pop() {
-    const int32_t id = top();
-    const size_t w = static_cast<size_t>(id) >> 6;
-    bits_[w] &= bits_[w] - 1;  // clear the lowest set bit: id
-    if (bits_[w] == 0) sum_[w >> 6] &= ~(1ull << (w & 63));
+    const uint64_t b = bits_[w];
+    bits_[w] = b & (b - 1);  // clear the lowest set bit
+    if (bits_[w] == 0) sum_[cursor_] &= ~(1ull << (w & 63));
     --count_;
+    return static_cast<int32_t>(w * 64 + static_cast<size_t>(__builtin_ctzll(b)));
+  }
+  // the n lowest free pages into out[0..n), ascending, a bitmap word at a time;
+  // the pool must hold n pages
+  void take(int32_t* out, int64_t n) {
+    int64_t k = 0;
+    while (k < n) {
+      while (sum_[cursor_] == 0) ++cursor_;
+      const size_t w = cursor_ * 64 + static_cast<size_t>(__builtin_ctzll(sum_[cursor_]));
+      uint64_t b = bits_[w];
+      while (b != 0 && k < n) {
+        out[k++] = static_cast<int32_t>(w * 64 + static_cast<size_t>(__builtin_ctzll(b)));
+        b &= b - 1;
+      }
+      bits_[w] = b;
+      if (b == 0) sum_[cursor_] &= ~(1ull << (w & 63));
+    }
+    count_ -= n;
   }
 
  private:
@@ -557,10 +571,7 @@ int segkv_append(segkv_t h, int layer, const void* k, const void* v, const int32
     for (int hd = 0; hd < h->Hkv; ++hd) {
       int32_t* r = h->row(layer, hd, b);
       for (int kk = sq.first_k; kk < sq.first_k + sq.n_pages; ++kk) {
-        if (r[kk] < 0) {
-          r[kk] = h->free_ids.top();
-          h->free_ids.pop();
-        }
+        if (r[kk] < 0) r[kk] = h->free_ids.take();
         plist.push_back(r[kk]);
         tidx.push_back(static_cast<int64_t>(h->seg(layer, hd, b)) * h->R + kk);
       }
@@ -1561,12 +1572,11 @@ int segkv_import(segkv_t h, int layer, int seq, const void* in, size_t in_bytes,
     H.page_off = static_cast<int32_t>(pl.size());
     H.table_row = static_cast<int32_t>(sg);
     H.row_begin = nrows;
-    if (n > 0)
-      for (int k = s0 / h->P; k <= (n - 1) / h->P; ++k) {
-        r[k] = h->free_ids.top();
-        h->free_ids.pop();
-        pl.push_back(r[k]);
-      }
+    if (n > 0) {
+      const int k0 = s0 / h->P, np = (n - 1) / h->P - k0 + 1;
+      h->free_ids.take(r + k0, np);
+      pl.insert(pl.end(), r + k0, r + k0 + np);
+    }
     hv.push_back(H);
     row += 2 * len;
     nrows += len;
