@@ -79,7 +79,7 @@ def _load():
         "segkv_export": [P, I, I, P, SZ, P, P],
         "segkv_import": [P, I, I, P, SZ, P, P],
         "segkv_plan_decode": [P, I, I, P, P, I, I, P, I, P, I, P, P],
-        "segkv_plan_prefill": [P, I, P, P, P, I, I, P, I, P, I, P, P],
+        "segkv_plan_prefill": [P, I, P, P, P, I, I, P, I, P, P],
         "segkv_plan_mass": [P, I, P, P, P, I, I, P, I, P, I, P, P],
         "segkv_exp2_check": [P, P, P, I, P],
     }
@@ -316,21 +316,20 @@ def segkv_plan_decode(h, layer, T, seq_lens, seq_ids, num_ctas=0):
 
 
 def segkv_plan_prefill(h, layer, cu_seqlens, q_pos, seq_ids, num_ctas=0):
-    """The prefill work plan (host only). Returns (rc, units [n_units, 8] int32,
-    cta_begin [n_ctas + 1] int32); unit columns: first token, tokens, KV head,
-    local, kt0, kt1, lowest and highest key seen."""
+    """The prefill work plan (host only). Returns (rc, units [n_units, 8] int32
+    in claim order, n_ctas); unit columns: first token, tokens, KV head, local,
+    kt0, kt1, lowest and highest key seen. CTA c runs unit c first and then
+    claims the next unclaimed unit each time it finishes one."""
     cu, qp, ids = _host_i32(cu_seqlens), _host_i32(q_pos), _host_i32(seq_ids)
     nu, nc = ctypes.c_int(0), ctypes.c_int(0)
     rc = _lib.segkv_plan_prefill(h, layer, cu.ctypes.data, qp.ctypes.data, ids.ctypes.data, len(ids),
-                                 num_ctas, None, 0, None, 0, ctypes.byref(nu), ctypes.byref(nc))
+                                 num_ctas, None, 0, ctypes.byref(nu), ctypes.byref(nc))
     if len(ids) == 0 or (rc != 0 and nu.value == 0):
-        return rc, np.zeros((0, 8), np.int32), np.zeros(1, np.int32)
+        return rc, np.zeros((0, 8), np.int32), 0
     units = np.zeros((nu.value, 8), np.int32)
-    cta = np.zeros(nc.value + 1, np.int32)
     rc = _lib.segkv_plan_prefill(h, layer, cu.ctypes.data, qp.ctypes.data, ids.ctypes.data, len(ids),
-                                 num_ctas, units.ctypes.data, nu.value, cta.ctypes.data, nc.value,
-                                 ctypes.byref(nu), ctypes.byref(nc))
-    return rc, units, cta
+                                 num_ctas, units.ctypes.data, nu.value, ctypes.byref(nu), ctypes.byref(nc))
+    return rc, units, nc.value
 
 
 def segkv_plan_mass(h, layer, cu_seqlens, q_pos, seq_ids, num_ctas=0):

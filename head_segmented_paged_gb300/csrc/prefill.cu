@@ -13,10 +13,15 @@
 // and per-row masks keep every row to its own key set: j <= p, and j >= p-W+1
 // for a local head.
 //
-// Warp roles (320 threads, one CTA per SM, each CTA running its own list of
-// units from an LPT schedule):
-//   warp 0      TMA producer: Q tiles A and B, then K and V tiles (2 stages),
-//               block-table entries fetched 32 at a time by the whole warp;
+// Warp roles (320 threads, one CTA per SM). The units form one list in
+// descending cost; CTA c starts with unit c and then claims the next unclaimed
+// unit from a counter in global memory, so a CTA on a slower SM simply runs
+// fewer units (greedy list scheduling with the measured rather than the
+// estimated unit times):
+//   warp 0      TMA producer: claims the units (one ahead of the one it
+//               publishes), then Q tiles A and B, then K and V tiles (2
+//               stages), block-table entries fetched 32 at a time by the
+//               whole warp;
 //   warp 1      TMEM owner and MMA issuer: S_X = Q_X K^T (X = A, B) into TMEM,
 //               then O_X += P_X V with P_X read back from TMEM, as one stream
 //               across the CTA's units; every MMA is issued from descriptors
@@ -28,7 +33,9 @@
 //               the running max (O is rescaled in TMEM only when the max grows
 //               by more than 2^8, which is exact), write P as bf16 over S; at
 //               the end of a unit, normalise O and store it. Unit descriptors
-//               come from the producer through a shared-memory ring.
+//               come from the producer through a shared-memory ring, which
+//               the MMA issuer reads too; a descriptor with no key tiles ends
+//               the CTA's work.
 // TMEM columns: S_A [0,128), S_B [128,256) (P_X aliases the first 64 columns
 // of S_X), O_A [256, 256+D), O_B [384, 384+D).
 //
@@ -73,10 +80,12 @@ enum {
   B_DESC = 20,     // +slot: the producer has written that slot's unit descriptor
   NUM_BARS = 24
 };
-// Unit descriptors reach the softmax warps through a ring of kDescSlots
-// shared-memory slots written by the producer. The producer starts unit u
-// only after the softmax of unit u-2's tiles is done in every softmax warp,
-// so it runs at most three units ahead and no slot is overwritten unread.
+// Unit descriptors reach the MMA issuer and the softmax warps through a ring
+// of kDescSlots shared-memory slots written by the producer; a slot is
+// rewritten four units later. The producer publishes unit u+4 only after it
+// has loaded unit u+3's Q tiles, which waits for the last S MMAs of unit
+// u+2. The issuer issues those after it has read unit u+2's descriptor and
+// after P of a tile of unit u+1 or u+2, so every reader is past unit u.
 constexpr int kDescSlots = 4;
 
 template <int D>
@@ -123,12 +132,20 @@ __device__ void producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const C
   int armed_q[2] = {-1, -1}, armed_kv[2] = {-1, -1};
   bool ok = true;
   int g = 0, ui = 0;
-  for (int u = p.cta_begin[blockIdx.x]; ok && u < p.cta_begin[blockIdx.x + 1]; ++u, ++ui) {
-    const PrefillUnit U = p.units[u];
-    const bool has_next = u + 1 < p.cta_begin[blockIdx.x + 1];
+  // CTA c starts with unit c. Lane 0 claims every later unit one unit ahead
+  // of its use, so the atomic's round trip hides behind a unit's loads.
+  const int n = p.n_units;
+  int u = static_cast<int>(blockIdx.x), claim = 0;
+  if (lane == 0 && u < n) claim = atomicAdd(p.next_unit, 1);
+  PrefillUnit U{};
+  if (u < n) U = p.units[u];
+  for (; ok && u < n; ++ui) {
+    const int un = __shfl_sync(0xffffffffu, claim, 0) + static_cast<int>(gridDim.x);
+    const bool has_next = un < n;
     PrefillUnit Un{};
-    if (has_next) Un = p.units[u + 1];
-    if (lane == 0) {  // publish the descriptor to the softmax warps (arrive = release)
+    if (has_next) Un = p.units[un];
+    if (lane == 0 && has_next) claim = atomicAdd(p.next_unit, 1);
+    if (lane == 0) {  // publish the descriptor (arrive = release)
       reinterpret_cast<PrefillUnit*>(c.smem + L::OFF_DESC)[ui % kDescSlots] = U;
       mbar_arrive(c.bar(B_DESC + ui % kDescSlots));
     }
@@ -143,10 +160,6 @@ __device__ void producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const C
       armed_q[x] = ui & 1;
     }
     if (!ok) break;
-    if (has_next && lane == 0)  // the next unit's Q into L2, so that its loads hit there
-      for (int x = 0; x < 2; ++x)
-        for (int cc = 0; cc < NC; ++cc)
-          tma_prefetch_3d(tmq, cc * 64, Un.head * p.G, Un.tok0 + x * p.tpt);
     const int32_t* trow = p.table + static_cast<int64_t>(U.table_row) * p.R;
     const int first_page = U.vlo / p.page_size, last_page = U.vhi / p.page_size;
     int kbase = -(1 << 30), my_id = 0;
@@ -159,6 +172,7 @@ __device__ void producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const C
         mbar_expect_tx(c.bar(B_V_FULL + st), L::KV_BYTES);
       }
       armed_kv[st] = static_cast<int>(ph);
+      int yv = 0;  // lane bi keeps box bi's row
       for (int bi = 0; bi < boxes; ++bi) {
         const int pos = kt * BN + bi * box_rows;
         const int k = pos / p.page_size;
@@ -170,15 +184,32 @@ __device__ void producer(const CUtensorMap* tmq, const CUtensorMap* tmk, const C
           }
           y = __shfl_sync(0xffffffffu, my_id, k - kbase) * p.page_size + (pos - k * p.page_size);
         }
+        if (lane == bi) yv = y;
         if (lane == 0) {
           const uint32_t off = st * L::KV_BYTES + bi * box_rows * 128;
-          for (int cc = 0; cc < NC; ++cc) {
+          for (int cc = 0; cc < NC; ++cc)
             tma_load_2d(c.sbase + L::OFF_K + off + cc * kAtom, tmk, cc * 64, y, c.bar(B_K_FULL + st));
+        }
+      }
+      // V boxes after every K box: the tile's S MMAs wait for K only, and V
+      // is needed half a key tile later
+      for (int bi = 0; bi < boxes; ++bi) {
+        const int y = __shfl_sync(0xffffffffu, yv, bi);
+        if (lane == 0) {
+          const uint32_t off = st * L::KV_BYTES + bi * box_rows * 128;
+          for (int cc = 0; cc < NC; ++cc)
             tma_load_2d(c.sbase + L::OFF_V + off + cc * kAtom, tmv, cc * 64, y, c.bar(B_V_FULL + st));
-          }
         }
       }
     }
+    U = Un;
+    u = un;
+  }
+  if (ok && lane == 0) {  // no unit left: a descriptor with no key tiles ends the readers' loops
+    PrefillUnit E{};
+    E.kt1 = -1;
+    reinterpret_cast<PrefillUnit*>(c.smem + L::OFF_DESC)[ui % kDescSlots] = E;
+    mbar_arrive(c.bar(B_DESC + ui % kDescSlots));
   }
   if (!ok && lane == 0) {  // aborting: let our own copies land before the block exits
     for (int x = 0; x < 2; ++x)
@@ -254,14 +285,21 @@ __device__ void mma_issuer(const PrefillParams& p, const Ctx& c) {
     ok = false;
   }
   // The MMAs run as one stream across the CTA's units: S_A and S_B of the
-  // next unit's first key tile follow this unit's last P V MMAs directly,
-  // with no descriptor load in between. The next unit's key-tile range is
-  // read one unit ahead.
-  const int u0 = p.cta_begin[blockIdx.x], n_units = p.cta_begin[blockIdx.x + 1] - u0;
-  int g = 0;
-  int nt_next = n_units > 0 ? p.units[u0].kt1 - p.units[u0].kt0 + 1 : 0;
+  // next unit's first key tile follow this unit's last P V MMAs directly.
+  // A unit's key-tile count comes from the producer's descriptor ring, where
+  // the producer has published it a key tile or more before it is needed;
+  // zero tiles means no unit is left.
+  const PrefillUnit* ring = reinterpret_cast<const PrefillUnit*>(c.smem + Layout<D>::OFF_DESC);
+  auto tiles_of = [&](int ui, int* nt) {
+    if (!wait1(c.bar(B_DESC + ui % kDescSlots), (ui / kDescSlots) & 1, c.wc)) return false;
+    const PrefillUnit& d = ring[ui % kDescSlots];
+    *nt = max(0, d.kt1 - d.kt0 + 1);
+    return true;
+  };
+  int g = 0, nt_next = 0;
+  if (ok && !tiles_of(0, &nt_next)) ok = false;
   // S_A and S_B of the first unit's first key tile
-  if (ok && n_units > 0) {
+  if (ok && nt_next > 0) {
     if (!wait1(c.bar(B_K_FULL + 0), 0, c.wc)) ok = false;
     for (int x = 0; ok && x < 2; ++x) {
       if (!wait1(c.bar(B_Q_FULL + x), 0, c.wc)) { ok = false; break; }
@@ -271,10 +309,8 @@ __device__ void mma_issuer(const PrefillParams& p, const Ctx& c) {
       if (nt_next == 1) mma_commit(c.bar(B_Q_EMPTY + x));
     }
   }
-  for (int ui = 0; ok && ui < n_units; ++ui) {
+  for (int ui = 0; ok && nt_next > 0; ++ui) {
     const int nt = nt_next;
-    const bool more = ui + 1 < n_units;
-    if (more) nt_next = p.units[u0 + ui + 1].kt1 - p.units[u0 + ui + 1].kt0 + 1;
     const uint32_t qpar = ui & 1;
     for (int i = 0; i < nt && ok; ++i) {
       const int gi = g + i, st = gi & 1, gn = gi + 1;
@@ -299,8 +335,9 @@ __device__ void mma_issuer(const PrefillParams& p, const Ctx& c) {
       }
     }
     // S_A and S_B of the next unit's first key tile, issued behind this
-    // unit's last P V MMAs without waiting on anything else
-    if (ok && more) {
+    // unit's last P V MMAs
+    if (ok && !tiles_of(ui + 1, &nt_next)) ok = false;
+    if (ok && nt_next > 0) {
       const int gn = g + nt;
       if (!wait1(c.bar(B_K_FULL + (gn & 1)), (gn >> 1) & 1, c.wc)) { ok = false; break; }
       for (int x = 0; x < 2; ++x) {
@@ -331,14 +368,15 @@ __device__ void softmax_epilogue(const CUtensorMap* tmo, const PrefillParams& p,
   const uint32_t t_s = c.tmem + lane_off + x * BN;
   const uint32_t t_o = c.tmem + lane_off + L::TM_O + x * L::TM_O_STRIDE;
   const float scale = p.scale_log2;
-  int g = 0, ui = 0;
-  const int n_units = p.cta_begin[blockIdx.x + 1] - p.cta_begin[blockIdx.x];
-  for (; ui < n_units; ++ui) {
-    // the unit's descriptor, from the producer's ring; consecutive query
-    // positions come with it (pos0), so no per-row load of q_pos is needed
+  int g = 0;
+  for (int ui = 0;; ++ui) {
+    // the unit's descriptor, from the producer's ring (no key tiles: no unit
+    // is left); consecutive query positions come with it (pos0), so no
+    // per-row load of q_pos is needed
     if (!waitw(c.bar(B_DESC + ui % kDescSlots), (ui / kDescSlots) & 1, c.wc)) break;
     const PrefillUnit U = reinterpret_cast<const PrefillUnit*>(c.smem + L::OFF_DESC)[ui % kDescSlots];
     const int nt = U.kt1 - U.kt0 + 1;
+    if (nt <= 0) break;
     const int t = x * p.tpt + r / p.G, gg = r % p.G;
     const bool row_ok = t < U.ntok;
     const int tok = U.tok0 + t;
@@ -361,12 +399,22 @@ __device__ void softmax_epilogue(const CUtensorMap* tmo, const PrefillParams& p,
       tmem_ld32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
       tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
       tmem_wait_ld();
-      // mask only where some row of this warp does not see the whole tile
+      // mask only where some row of this warp does not see the whole tile;
+      // where every row of the warp sees one end of it (the diagonal tile of
+      // a causal row, the first tile of a window), test only the other bound
       const bool whole = (j0 >= lo) && (j0 + BN - 1 <= hi);
       if (!__all_sync(0xffffffffu, whole)) {
         const int c_lo = lo - j0, c_hi = hi - j0;
+        if (__all_sync(0xffffffffu, c_lo <= 0)) {
 #pragma unroll
-        for (int e = 0; e < BN; ++e) s[e] = (e >= c_lo && e <= c_hi) ? s[e] : -INFINITY;
+          for (int e = 0; e < BN; ++e) s[e] = e <= c_hi ? s[e] : -INFINITY;
+        } else if (__all_sync(0xffffffffu, c_hi >= BN - 1)) {
+#pragma unroll
+          for (int e = 0; e < BN; ++e) s[e] = e >= c_lo ? s[e] : -INFINITY;
+        } else {
+#pragma unroll
+          for (int e = 0; e < BN; ++e) s[e] = (e >= c_lo && e <= c_hi) ? s[e] : -INFINITY;
+        }
       }
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll

@@ -268,11 +268,10 @@ struct DecodePlan {
 
 // The prefill plan and its scratch; a handle keeps one and reuses its storage.
 struct PrefillPlan {
-  std::vector<PrefillUnit> units;   // in building order
-  std::vector<PrefillUnit> by_cta;  // the plan: grouped by CTA, each list longest first
-  std::vector<int32_t> cta_begin;   // [grid + 1]
-  std::vector<int32_t> order, count, cta_of, fill;
-  LeastLoaded lpt;
+  std::vector<PrefillUnit> units;  // in building order
+  std::vector<PrefillUnit> claim;  // the plan: the order in which the kernel's CTAs claim units
+  int grid = 0;                    // CTAs of the launch: min(units, CTAs asked for)
+  std::vector<int32_t> count;
 };
 
 struct segkv {
@@ -668,13 +667,13 @@ static int prefill_validate(segkv* h, int layer, const int32_t* cu_seqlens, cons
 }
 
 // The prefill work plan (host): units of one KV head x the Q tiles of a
-// chunk of tokens, scheduled onto `ctas` lists by LPT and grouped by list,
-// into h->pplan (by_cta, cta_begin).
+// chunk of tokens, in the order the kernel's CTAs claim them, and the grid
+// for `ctas` CTAs, into h->pplan (claim, grid).
 static void prefill_plan(segkv* h, int layer, const int32_t* cu_seqlens, const int32_t* q_pos,
                          const int32_t* seq_ids, int n, int ctas) {
   PrefillPlan& P = h->pplan;
   const int W = h->win[layer];
-  // units: (KV head, two Q tiles of 128/G tokens each), LPT order
+  // units: (KV head, two Q tiles of 128/G tokens each)
   const int unit_tok = prefill_unit_tokens(h->G);
   std::vector<PrefillUnit>& units = P.units;
   units.clear();
@@ -714,46 +713,21 @@ static void prefill_plan(segkv* h, int layer, const int32_t* cu_seqlens, const i
     }
   }
   const size_t nu = units.size();
-  // LPT schedule: units in descending cost, each to the CTA with the least
-  // work so far; a unit costs its key tiles plus kPrefillUnitCost for filling
-  // and draining the pipeline and the output epilogue. Each CTA then runs its
-  // own list, longest first.
-  constexpr int64_t kPrefillUnitCost = 1;
-  // descending key tiles, stable: a counting sort on the tile count
+  // Claim order: descending key tiles, stable (a counting sort on the tile
+  // count). The kernel's CTA c runs unit c first; each CTA that finishes a
+  // unit claims the next unit of this order, so the longest units start
+  // first and every CTA stays busy until the list runs out, whatever the
+  // speed of its SM.
   int32_t max_tiles = 0;
   for (const PrefillUnit& u : units) max_tiles = std::max(max_tiles, u.kt1 - u.kt0);
-  std::vector<int32_t>& order = P.order;
   std::vector<int32_t>& start = P.count;
-  order.resize(nu);
   start.assign(static_cast<size_t>(max_tiles) + 2, 0);
   for (const PrefillUnit& u : units) ++start[max_tiles - (u.kt1 - u.kt0) + 1];
   for (size_t c = 1; c < start.size(); ++c) start[c] += start[c - 1];
-  for (size_t x = 0; x < nu; ++x)
-    order[start[max_tiles - (units[x].kt1 - units[x].kt0)]++] = static_cast<int32_t>(x);
-  const int grid = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(nu), ctas));
-  std::vector<int32_t>& cta_of = P.cta_of;
-  std::vector<int32_t>& cta_begin = P.cta_begin;
-  cta_of.resize(nu);
-  cta_begin.assign(grid + 1, 0);
-  {
-    LeastLoaded& lpt = P.lpt;
-    lpt.reset(grid);
-    for (size_t r = 0; r < nu; ++r) {
-      const PrefillUnit& u = units[order[r]];
-      const int c = lpt.least();
-      cta_of[r] = c;
-      ++cta_begin[c + 1];
-      lpt.add(c, u.kt1 - u.kt0 + 1 + kPrefillUnitCost);
-    }
-  }
-  for (int c = 0; c < grid; ++c) cta_begin[c + 1] += cta_begin[c];
-  std::vector<PrefillUnit>& by_cta = P.by_cta;
-  by_cta.resize(nu);
-  {
-    std::vector<int32_t>& fill = P.fill;
-    fill.assign(cta_begin.begin(), cta_begin.end() - 1);
-    for (size_t r = 0; r < nu; ++r) by_cta[fill[cta_of[r]]++] = units[order[r]];
-  }
+  std::vector<PrefillUnit>& claim = P.claim;
+  claim.resize(nu);
+  for (size_t x = 0; x < nu; ++x) claim[start[max_tiles - (units[x].kt1 - units[x].kt0)]++] = units[x];
+  P.grid = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(nu), ctas));
 }
 
 int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_seqlens,
@@ -782,15 +756,15 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
   const int W = h->win[layer];
   const int tpt = kRowsPerTile / h->G;
   prefill_plan(h, layer, cu_seqlens, q_pos, seq_ids, n, h->num_sms);
-  const std::vector<PrefillUnit>& by_cta = h->pplan.by_cta;
-  const std::vector<int32_t>& cta_begin = h->pplan.cta_begin;
-  const int grid = static_cast<int>(cta_begin.size()) - 1;
-  const size_t n_units = by_cta.size();
+  const std::vector<PrefillUnit>& claim = h->pplan.claim;
+  const int grid = h->pplan.grid;
+  const size_t n_units = claim.size();
 
   Pack& pk = h->pack;
   pk.buf.clear();
-  const size_t o_units = pk.add(by_cta.data(), by_cta.size());
-  const size_t o_cta = pk.add(cta_begin.data(), cta_begin.size());
+  const size_t o_units = pk.add(claim.data(), claim.size());
+  const int32_t zero = 0;  // the claim counter, fresh for every launch
+  const size_t o_next = pk.add(&zero, 1);
   const size_t o_pos = pk.add(q_pos, static_cast<size_t>(total));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   size_t off;
@@ -825,7 +799,7 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
   uint8_t* d = h->ring.dev + off;
   PrefillParams p{};
   p.units = reinterpret_cast<const PrefillUnit*>(d + o_units);
-  p.cta_begin = reinterpret_cast<const int32_t*>(d + o_cta);
+  p.next_unit = reinterpret_cast<int*>(d + o_next);
   p.q_pos = reinterpret_cast<const int32_t*>(d + o_pos);
   p.table = h->d_table;
   p.o = o;
@@ -853,10 +827,10 @@ int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_se
 
 int segkv_plan_prefill(segkv_t h, int layer, const int32_t* cu_seqlens, const int32_t* q_pos,
                        const int32_t* seq_ids, int n, int num_ctas, int32_t* units_out, int max_units,
-                       int32_t* cta_begin_out, int max_ctas, int* n_units, int* n_ctas) {
+                       int* n_units, int* n_ctas) {
   if (!h) return SEGKV_ERR_INVALID_ARG;
   if (layer < 0 || layer >= h->L) return fail(h, SEGKV_ERR_INVALID_ARG, "bad layer %d", layer);
-  if (n < 0 || max_units < 0 || max_ctas < 0 || !n_units || !n_ctas)
+  if (n < 0 || max_units < 0 || !n_units || !n_ctas)
     return fail(h, SEGKV_ERR_INVALID_ARG, "bad n or output sizes");
   if (!ids_valid(h, seq_ids, n)) return fail(h, SEGKV_ERR_INVALID_ARG, "bad seq_ids");
   *n_units = 0;
@@ -874,14 +848,13 @@ int segkv_plan_prefill(segkv_t h, int layer, const int32_t* cu_seqlens, const in
     return fail(h, SEGKV_ERR_INVALID_ARG, "num_ctas %d above %d", num_ctas, kMaxPlanCtas);
   const int ctas = num_ctas > 0 ? num_ctas : (h->num_sms > 0 ? h->num_sms : 1);
   prefill_plan(h, layer, cu_seqlens, q_pos, seq_ids, n, ctas);
-  const std::vector<PrefillUnit>& by_cta = h->pplan.by_cta;
-  const std::vector<int32_t>& cta_begin = h->pplan.cta_begin;
-  *n_units = static_cast<int>(by_cta.size());
-  *n_ctas = static_cast<int>(cta_begin.size()) - 1;
-  if (*n_units > max_units || *n_ctas > max_ctas || (max_units && !units_out) || !cta_begin_out)
-    return fail(h, SEGKV_ERR_INVALID_ARG, "plan needs %d units and %d CTAs", *n_units, *n_ctas);
-  for (size_t x = 0; x < by_cta.size(); ++x) {
-    const PrefillUnit& u = by_cta[x];
+  const std::vector<PrefillUnit>& claim = h->pplan.claim;
+  *n_units = static_cast<int>(claim.size());
+  *n_ctas = h->pplan.grid;
+  if (*n_units > max_units || (max_units && !units_out))
+    return fail(h, SEGKV_ERR_INVALID_ARG, "plan needs %d units", *n_units);
+  for (size_t x = 0; x < claim.size(); ++x) {
+    const PrefillUnit& u = claim[x];
     int32_t* o = units_out + 8 * x;
     o[0] = u.tok0;
     o[1] = u.ntok;
@@ -892,7 +865,6 @@ int segkv_plan_prefill(segkv_t h, int layer, const int32_t* cu_seqlens, const in
     o[6] = u.klo;
     o[7] = u.khi;
   }
-  for (int c = 0; c <= *n_ctas; ++c) cta_begin_out[c] = cta_begin[c];
   return SEGKV_OK;
 }
 
@@ -1784,7 +1756,7 @@ static int mass_plan(segkv* h, int layer, const int32_t* cu_seqlens, const int32
     }
   }
   units.swap(cut);
-  // LPT schedule, as for prefill: longest first, each to the least-loaded CTA
+  // LPT schedule: longest first, each to the least-loaded CTA
   std::stable_sort(units.begin(), units.end(), [](const MassUnit& x, const MassUnit& y) {
     return (x.qt1 - x.qt0) > (y.qt1 - y.qt0);
   });

@@ -87,8 +87,9 @@ struct PrefillUnit {
 };
 static_assert(sizeof(PrefillUnit) == 48, "prefill units are staged in 48-byte slots");
 struct PrefillParams {
-  const PrefillUnit* units;    // grouped by CTA
-  const int32_t* cta_begin;    // [grid + 1]: CTA c runs units cta_begin[c] .. cta_begin[c+1]-1
+  const PrefillUnit* units;    // [n_units], in claim order (descending key tiles)
+  int* next_unit;              // claim counter, 0 at launch: CTA c runs unit c first, and
+                               // each later claim k gets unit grid + k
   const int32_t* q_pos;
   const int32_t* table;
   void* o;        // bf16 [total_q, Hq, D]

@@ -378,22 +378,24 @@ int segkv_decode_attn_noalloc(segkv_t h, int layer, const void* q, const int32_t
 /* segkv_plan_prefill — the work plan that segkv_prefill_attn would use,
  * computed on the host only (no device work; host-only handles work too), for
  * tests and tools. A unit is one KV head x the query rows of two 128-row tiles
- * (2 x 128 / G tokens of one sequence); units are dealt to num_ctas lists by
- * longest-processing-time-first and grouped by list.
+ * (2 x 128 / G tokens of one sequence). The units are listed in claim order:
+ * descending key tiles, ties in building order (sequence, first token, KV
+ * head). The kernel's CTA c runs unit c first; each CTA that finishes a unit
+ * claims the next unclaimed unit of the list, so which CTA runs a later unit
+ * is decided on the GPU.
  *   num_ctas    > 0: plan for that many CTAs (at most 65,535, else
  *               SEGKV_ERR_INVALID_ARG); otherwise one per SM.
  *   units       host int32 [max_units][8], out: first token (index into the
  *               call's packed tokens), tokens, KV head, 1 if local, key tiles
  *               kt0 .. kt1 (128 keys each), lowest and highest key any of
  *               its rows sees.
- *   cta_begin   host int32 [max_ctas + 1], out: list c holds units
- *               cta_begin[c] .. cta_begin[c + 1] - 1.
- *   n_units, n_ctas  out: the plan's sizes, written even when an output
- *               array is too small (then SEGKV_ERR_INVALID_ARG).
+ *   n_units     out: the number of units, written even when the array is
+ *               too small (then SEGKV_ERR_INVALID_ARG).
+ *   n_ctas      out: the grid, min(n_units, num_ctas).
  * Errors: those of segkv_prefill_attn for the same arguments. */
 int segkv_plan_prefill(segkv_t h, int layer, const int32_t* cu_seqlens, const int32_t* q_pos,
                        const int32_t* seq_ids, int n, int num_ctas, int32_t* units, int max_units,
-                       int32_t* cta_begin, int max_ctas, int* n_units, int* n_ctas);
+                       int* n_units, int* n_ctas);
 
 /* segkv_plan_mass — the work plan that segkv_attn_mass would use for the same
  * chunks, computed on the host only (host-only handles work too), for tests

@@ -11,9 +11,11 @@ balanced:
   within one unit's charges of the most loaded CTA.
 
 `segkv_plan_prefill` returns the prefill plan: one unit per (KV head, chunk of
-two Q tiles' tokens), with the chunk's key range, dealt to CTA lists by LPT.
-The checks pin that every (chunk, head) appears once with the right key
-range, and the LPT bound on the lists' loads.
+two Q tiles' tokens), with the chunk's key range, in the order the kernel's
+CTAs claim them (CTA c runs unit c first, then each CTA that finishes a unit
+takes the next unclaimed one). The checks pin that every (chunk, head)
+appears once with the right key range, and the claim order exactly:
+descending key tiles, ties in building order.
 
 `segkv_plan_mass` returns the attention-mass plan: one unit per (KV head, key
 tile of a chunk) over the query tiles that see its keys, long ones cut into
@@ -172,13 +174,9 @@ def test_decode_plan_errors():
 
 
 # ---------------------------------------------------------------- prefill
-def prefill_cost(u):
-    return int(u[5] - u[4] + 1) + 1  # key tiles + the per-unit surcharge
-
-
 @pytest.mark.parametrize("G,hkv", [(1, 2), (4, 8), (8, 8), (16, 2)])
 @pytest.mark.parametrize("num_ctas", [152, 7])
-def test_prefill_plan_tiles_every_token_and_head_once_and_is_lpt(G, hkv, num_ctas):
+def test_prefill_plan_tiles_every_token_and_head_once_longest_first(G, hkv, num_ctas):
     hq, d, P = G * hkv, 128, 64
     hc = [GLOBAL if hd % 4 == 1 else LOCAL for hd in range(hkv)]
     W = 700
@@ -194,10 +192,9 @@ def test_prefill_plan_tiles_every_token_and_head_once_and_is_lpt(G, hkv, num_cta
         qp.extend(pos.tolist())
         cu.append(cu[-1] + len(pos))
     ids = list(range(len(lens)))
-    rc, units, cta = S.segkv_plan_prefill(h.handle, 0, cu, qp, ids, num_ctas)
+    rc, units, grid = S.segkv_plan_prefill(h.handle, 0, cu, qp, ids, num_ctas)
     assert rc == 0, S.segkv_last_error(h.handle)
-    assert cta[0] == 0 and cta[-1] == units.shape[0] and (np.diff(cta) >= 1).all()
-    assert len(cta) - 1 == min(num_ctas, units.shape[0])
+    assert grid == min(num_ctas, units.shape[0])
     unit_tok = 2 * (128 // G)
     qp = np.array(qp)
     # every (token chunk, head) exactly once, with the chunk's key range
@@ -215,16 +212,9 @@ def test_prefill_plan_tiles_every_token_and_head_once_and_is_lpt(G, hkv, num_cta
     want = {(t0, hd) for i in range(len(lens)) for t0 in range(cu[i], cu[i + 1], unit_tok)
             for hd in range(hkv)}
     assert seen == want
-    # LPT: each list runs longest first, and the most loaded list exceeds the
-    # least loaded by at most the cost of the last unit it was given
-    loads = []
-    for c in range(len(cta) - 1):
-        costs = [prefill_cost(u) for u in units[cta[c]:cta[c + 1]]]
-        assert costs == sorted(costs, reverse=True)
-        loads.append(sum(costs))
-    worst = int(np.argmax(loads))
-    last = prefill_cost(units[cta[worst + 1] - 1])
-    assert max(loads) - last <= min(loads)
+    # claimed longest first
+    tiles = units[:, 5] - units[:, 4] + 1
+    assert (np.diff(tiles) <= 0).all()
 
 
 def test_prefill_plan_errors():
@@ -234,28 +224,19 @@ def test_prefill_plan_errors():
     assert S.segkv_plan_prefill(h.handle, 0, [0, 1], [0], [3], 8)[0] == S.SEGKV_ERR_INVALID_ARG
     assert h.trim(0, [0]) == 0
     assert S.segkv_plan_prefill(h.handle, 0, [0, 1], [50], [0], 8)[0] == S.SEGKV_ERR_EVICTED
-    rc, units, cta = S.segkv_plan_prefill(h.handle, 0, [0], [], [], 8)
-    assert rc == 0 and units.shape == (0, 8)
+    rc, units, grid = S.segkv_plan_prefill(h.handle, 0, [0], [], [], 8)
+    assert rc == 0 and units.shape == (0, 8) and grid == 0
 
 
-def replay_lpt(units, num_ctas):
-    """The LPT schedule replayed from its definition: units in building order
-    (token chunk, then KV head), stably sorted by key tiles, longest first;
-    each goes to the least loaded list, the lowest index on ties."""
+def claim_order(units):
+    """The claim order replayed from its definition: units in building order
+    (token chunk, then KV head), stably sorted by key tiles, longest first."""
     build = sorted(range(len(units)), key=lambda x: (int(units[x][0]), int(units[x][2])))
-    order = sorted(build, key=lambda x: -int(units[x][5] - units[x][4]))
-    grid = min(num_ctas, len(units))
-    loads = np.zeros(grid, np.int64)
-    lists = [[] for _ in range(grid)]
-    for x in order:
-        c = int(np.argmin(loads))  # first minimum: the lowest index on ties
-        lists[c].append(x)
-        loads[c] += prefill_cost(units[x])
-    return lists
+    return sorted(build, key=lambda x: -int(units[x][5] - units[x][4]))
 
 
 @pytest.mark.parametrize("G,hkv,num_ctas", [(4, 8, 152), (8, 8, 7), (1, 2, 3)])
-def test_prefill_plan_is_exactly_the_lpt_schedule(G, hkv, num_ctas):
+def test_prefill_plan_is_exactly_the_claim_order(G, hkv, num_ctas):
     hq, d, P, W = G * hkv, 128, 64, 500
     hc = [GLOBAL] + [LOCAL] * (hkv - 1)
     rng = np.random.default_rng(G + 5 * hkv + num_ctas)
@@ -264,14 +245,10 @@ def test_prefill_plan_is_exactly_the_lpt_schedule(G, hkv, num_ctas):
     fill(h, lens)
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     qp = np.concatenate([np.arange(n) for n in lens]).astype(np.int32)
-    rc, units, cta = S.segkv_plan_prefill(h.handle, 0, cu, qp, list(range(len(lens))), num_ctas)
+    rc, units, grid = S.segkv_plan_prefill(h.handle, 0, cu, qp, list(range(len(lens))), num_ctas)
     assert rc == 0, S.segkv_last_error(h.handle)
-    lists = replay_lpt(units, num_ctas)
-    assert len(cta) - 1 == len(lists)
-    for c, want in enumerate(lists):
-        got = units[cta[c]:cta[c + 1]]
-        assert got.shape[0] == len(want)
-        assert (got == units[want]).all(), c
+    assert grid == min(num_ctas, len(units))
+    assert claim_order(units) == list(range(len(units)))
 
 
 def test_plans_on_a_reused_handle_match_fresh_handles():
