@@ -31,8 +31,10 @@
 //   warps 2..5  softmax of tile A, warps 6..9 softmax of tile B (one thread
 //               per row): read S from TMEM, mask only on edge tiles, update
 //               the running max (O is rescaled in TMEM only when the max grows
-//               by more than 2^8, which is exact), write P as bf16 over S; at
-//               the end of a unit, normalise O and store it. Unit descriptors
+//               by more than 2^8, which is exact), write P as bf16 over S; a
+//               unit's O is normalised and stored after the next unit's first
+//               P is written (the first P of a unit is on the tensor pipe's
+//               critical path, the output is not). Unit descriptors
 //               come from the producer through a shared-memory ring, which
 //               the MMA issuer reads too; a descriptor with no key tiles ends
 //               the CTA's work.
@@ -41,7 +43,8 @@
 //
 // Ordering: the MMA issuer issues S_X of tile j+1 after P_X V of tile j, and
 // tcgen05 operations of one thread complete in order, so when the softmax sees
-// S_X(j+1) complete, P_X(j) has been consumed and O_X is stable.
+// S_X(j+1) complete, P_X(j) has been consumed and O_X is stable (across a unit
+// boundary: the last O_X of the old unit is final).
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -285,7 +288,8 @@ __device__ void mma_issuer(const PrefillParams& p, const Ctx& c) {
     ok = false;
   }
   // The MMAs run as one stream across the CTA's units: S_A and S_B of the
-  // next unit's first key tile follow this unit's last P V MMAs directly.
+  // next unit's first key tile follow this unit's last P V MMAs directly
+  // (S_A already between P_A V and P_B V when its operands are there).
   // A unit's key-tile count comes from the producer's descriptor ring, where
   // the producer has published it a key tile or more before it is needed;
   // zero tiles means no unit is left.
@@ -312,6 +316,7 @@ __device__ void mma_issuer(const PrefillParams& p, const Ctx& c) {
   for (int ui = 0; ok && nt_next > 0; ++ui) {
     const int nt = nt_next;
     const uint32_t qpar = ui & 1;
+    bool early_a = false;
     for (int i = 0; i < nt && ok; ++i) {
       const int gi = g + i, st = gi & 1, gn = gi + 1;
       const uint32_t ph = (gi >> 1) & 1;
@@ -325,6 +330,27 @@ __device__ void mma_issuer(const PrefillParams& p, const Ctx& c) {
         if (x == 1) mma_commit(c.bar(B_KV_EMPTY + st));
         if (last) {
           mma_commit(c.bar(B_O_FULL + x));
+          // The next unit's S_A right behind this unit's last P_A V, if its
+          // descriptor, K tile and Q_A tile are already there (tested, not
+          // waited for: a wait here would hold up P_B V): tile A's first
+          // softmax of the next unit then runs while the pipe does P_B V
+          // and S_B, instead of both tiles' first softmax running with the
+          // pipe idle.
+          if (x == 0) {
+            const int un = ui + 1, gn2 = g + nt;
+            if (mbar_peek(c.bar(B_DESC + un % kDescSlots), (un / kDescSlots) & 1)) {
+              const PrefillUnit& d = ring[un % kDescSlots];
+              const int ntn = d.kt1 - d.kt0 + 1;
+              if (ntn > 0 && mbar_peek(c.bar(B_K_FULL + (gn2 & 1)), (gn2 >> 1) & 1) &&
+                  mbar_peek(c.bar(B_Q_FULL + 0), qpar ^ 1)) {
+                tc_fence_after();
+                issue_s<D>(c, md, 0, gn2 & 1);
+                mma_commit(c.bar(B_S_FULL + 0));
+                if (ntn == 1) mma_commit(c.bar(B_Q_EMPTY + 0));
+                early_a = true;
+              }
+            }
+          }
           continue;
         }
         if (x == 0 && !wait1(c.bar(B_K_FULL + (gn & 1)), (gn >> 1) & 1, c.wc)) { ok = false; break; }
@@ -341,6 +367,7 @@ __device__ void mma_issuer(const PrefillParams& p, const Ctx& c) {
       const int gn = g + nt;
       if (!wait1(c.bar(B_K_FULL + (gn & 1)), (gn >> 1) & 1, c.wc)) { ok = false; break; }
       for (int x = 0; x < 2; ++x) {
+        if (x == 0 && early_a) continue;
         if (!wait1(c.bar(B_Q_FULL + x), qpar ^ 1, c.wc)) { ok = false; break; }
         tc_fence_after();
         issue_s<D>(c, md, x, gn & 1);
@@ -357,6 +384,79 @@ __device__ void mma_issuer(const PrefillParams& p, const Ctx& c) {
 }
 
 // ---------------------------------------------------------------- softmax
+// What the output of a finished unit needs, kept in registers while the warp
+// runs the next unit's first softmax tile.
+struct Pending {
+  int ui;        // the unit's index in this CTA (O_FULL parity)
+  int head, tok0, ntok;
+  int tok;       // this row's token (valid when row_ok)
+  bool row_ok;
+  float inv_l;   // 1 / O's normaliser (0 for an invalid row)
+  float lse;     // natural-log LSE of the row
+};
+
+// O / l of a finished unit as bf16: read O_X from TMEM (after its last P V),
+// free O_X for the next unit's P V, then store the rows and the LSE.
+template <int D>
+__device__ __forceinline__ bool write_output(const CUtensorMap* tmo, const PrefillParams& p, const Ctx& c,
+                                             int x, int wq, int lane, uint32_t t_o, const Pending& e) {
+  using L = Layout<D>;
+  constexpr int NC = D / 64;
+  if (!waitw(c.bar(B_O_FULL + x), e.ui & 1, c.wc)) return false;
+  tc_fence_after();
+  if (lane == 0) bulk_wait_read();  // the last unit's stores have read the staging rows
+  uint32_t ob[D / 2];
+#pragma unroll
+  for (int q = 0; q < D / 32; ++q) {
+    uint32_t v[32];
+    tmem_ld32(t_o + q * 32, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      ob[q * 16 + k] = pack_bf16x2(__uint_as_float(v[2 * k]) * e.inv_l, __uint_as_float(v[2 * k + 1]) * e.inv_l);
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(c.bar(B_O_EMPTY + x));
+  const int gg = (wq * 32 + lane) % p.G;
+  if (e.ntok >= x * p.tpt + (wq + 1) * 32 / p.G) {
+    // The warp's 32 rows are 32 / G whole tokens: they go to the warp's
+    // 128B-swizzled staging rows, 64 columns at a time, and lane 0 writes
+    // them with one bulk tensor store each (the rows are one box of the O
+    // tensor map). Per-thread row stores would touch 32 rows per
+    // instruction and hold this SM's shared-memory and barrier operations
+    // up behind them.
+    uint8_t* stg = c.smem + L::OFF_STAGE + (x * 4 + wq) * L::STAGE_WARP;
+#pragma unroll
+    for (int cc = 0; cc < NC; ++cc) {
+      if (cc > 0) {  // the previous store has read the staging rows
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+            make_uint4(ob[cc * 32 + 4 * j], ob[cc * 32 + 4 * j + 1], ob[cc * 32 + 4 * j + 2],
+                       ob[cc * 32 + 4 * j + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(tmo, smem_addr(stg), cc * 64, e.head * p.G, e.tok0 + x * p.tpt + wq * 32 / p.G);
+        bulk_commit();
+      }
+    }
+  } else if (e.row_ok) {  // rows of a sequence's last, partial tile: row stores
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
+                                          (static_cast<int64_t>(e.tok) * p.hq + e.head * p.G + gg) * D);
+#pragma unroll
+    for (int k = 0; k < D / 8; ++k)
+      dst[k] = make_uint4(ob[4 * k], ob[4 * k + 1], ob[4 * k + 2], ob[4 * k + 3]);
+  }
+  if (e.row_ok && p.lse != nullptr)
+    p.lse[static_cast<int64_t>(e.head * p.G + gg) * p.total_q + e.tok] = e.lse;
+  return true;
+}
+
 template <int D>
 __device__ void softmax_epilogue(const CUtensorMap* tmo, const PrefillParams& p, const Ctx& c, int x,
                                  int warp, int lane) {
@@ -369,6 +469,8 @@ __device__ void softmax_epilogue(const CUtensorMap* tmo, const PrefillParams& p,
   const uint32_t t_o = c.tmem + lane_off + L::TM_O + x * L::TM_O_STRIDE;
   const float scale = p.scale_log2;
   int g = 0;
+  Pending pend{};
+  bool have = false;  // pend holds a finished unit whose output is not written yet
   for (int ui = 0;; ++ui) {
     // the unit's descriptor, from the producer's ring (no key tiles: no unit
     // is left); consecutive query positions come with it (pos0), so no
@@ -377,7 +479,7 @@ __device__ void softmax_epilogue(const CUtensorMap* tmo, const PrefillParams& p,
     const PrefillUnit U = reinterpret_cast<const PrefillUnit*>(c.smem + L::OFF_DESC)[ui % kDescSlots];
     const int nt = U.kt1 - U.kt0 + 1;
     if (nt <= 0) break;
-    const int t = x * p.tpt + r / p.G, gg = r % p.G;
+    const int t = x * p.tpt + r / p.G;
     const bool row_ok = t < U.ntok;
     const int tok = U.tok0 + t;
     int hi = -1, lo = 1 << 30;  // an invalid row sees no key
@@ -498,67 +600,27 @@ __device__ void softmax_epilogue(const CUtensorMap* tmo, const PrefillParams& p,
       __syncwarp();  // one arrival per warp: the barrier is on the softmax -> P V path
       if (lane == 0) mbar_arrive(c.bar(B_P_FULL + x));
       m_used = m_tgt;
+      // The previous unit's output, now that this unit's first P is in TMEM:
+      // its S MMAs were issued after that unit's last P V, so the wait for
+      // O_FULL returns at once, and the next P V waits for O_EMPTY.
+      if (i == 0 && have) {
+        if (!write_output<D>(tmo, p, c, x, wq, lane, t_o, pend)) { ok = false; break; }
+        have = false;
+      }
     }
     if (!ok) break;
-
-    if (!waitw(c.bar(B_O_FULL + x), ui & 1, c.wc)) break;
-    tc_fence_after();
-    const float inv_l = row_ok ? 1.f / (l + lc) : 0.f;
-    // O / l as bf16 in registers; then O_X in TMEM is free for the next unit
-    if (lane == 0) bulk_wait_read();  // the last unit's stores have read the staging rows
-    uint32_t ob[D / 2];
-#pragma unroll
-    for (int q = 0; q < D / 32; ++q) {
-      uint32_t v[32];
-      tmem_ld32(t_o + q * 32, v);
-      tmem_wait_ld();
-#pragma unroll
-      for (int e = 0; e < 16; ++e)
-        ob[q * 16 + e] =
-            pack_bf16x2(__uint_as_float(v[2 * e]) * inv_l, __uint_as_float(v[2 * e + 1]) * inv_l);
-    }
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(c.bar(B_O_EMPTY + x));
-    if (U.ntok >= x * p.tpt + (wq + 1) * 32 / p.G) {
-      // The warp's 32 rows are 32 / G whole tokens: they go to the warp's
-      // 128B-swizzled staging rows, 64 columns at a time, and lane 0 writes
-      // them with one bulk tensor store each (the rows are one box of the O
-      // tensor map). Per-thread row stores would touch 32 rows per
-      // instruction and hold this SM's shared-memory and barrier operations
-      // up behind them.
-      uint8_t* stg = c.smem + L::OFF_STAGE + (x * 4 + wq) * L::STAGE_WARP;
-#pragma unroll
-      for (int cc = 0; cc < NC; ++cc) {
-        if (cc > 0) {  // the previous store has read the staging rows
-          if (lane == 0) bulk_wait_read();
-          __syncwarp();
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-              make_uint4(ob[cc * 32 + 4 * j], ob[cc * 32 + 4 * j + 1], ob[cc * 32 + 4 * j + 2],
-                         ob[cc * 32 + 4 * j + 3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_3d(tmo, smem_addr(stg), cc * 64, U.head * p.G,
-                       U.tok0 + x * p.tpt + wq * 32 / p.G);
-          bulk_commit();
-        }
-      }
-    } else if (row_ok) {  // rows of a sequence's last, partial tile: row stores
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
-                                            (static_cast<int64_t>(tok) * p.hq + U.head * p.G + gg) * D);
-#pragma unroll
-      for (int e = 0; e < D / 8; ++e)
-        dst[e] = make_uint4(ob[4 * e], ob[4 * e + 1], ob[4 * e + 2], ob[4 * e + 3]);
-    }
-    if (row_ok && p.lse != nullptr)
-      p.lse[static_cast<int64_t>(U.head * p.G + gg) * p.total_q + tok] =
-          (m_used + log2f(l)) * 0.69314718055994530942f;
+    pend.ui = ui;
+    pend.head = U.head;
+    pend.tok0 = U.tok0;
+    pend.ntok = U.ntok;
+    pend.tok = tok;
+    pend.row_ok = row_ok;
+    pend.inv_l = row_ok ? 1.f / (l + lc) : 0.f;
+    pend.lse = (m_used + log2f(l)) * 0.69314718055994530942f;
+    have = true;
     g += nt;
   }
+  if (have) write_output<D>(tmo, p, c, x, wq, lane, t_o, pend);
   if (lane == 0) bulk_wait();  // this warp's bulk stores are complete
 }
 
