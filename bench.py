@@ -32,7 +32,7 @@ N_INPUT_SETS = 4
 # DRAM read+write bytes per prefill launch of the 64-layer step, weighted by
 # layer kind, from one one-pass ncu capture of the current prefill kernel on
 # full-size layers (--case prefill-128k-layers); None once the kernel changes.
-PREFILL_TRAFFIC_PER_LAUNCH = 5.04e9
+PREFILL_TRAFFIC_PER_LAUNCH = 5.05e9
 
 
 def useful_flops_layer(w, layer, n):
