@@ -64,6 +64,26 @@ def test_ragged_varlen_page_sizes(P, G):
     np.testing.assert_allclose(lse.cpu().numpy().T, ref_lse, atol=1e-3, rtol=0)
 
 
+def test_prefill_repeats_bit_for_bit_whichever_cta_runs_a_unit():
+    """CTAs claim units at run time, so which CTA runs a unit changes from call
+    to call; a unit's result must not. Many short sequences (small units,
+    claimed last) beside two long ones, run five times and compared bit for
+    bit; the first run also against the oracle."""
+    hkv = 4
+    lens = [1500, 3000] + [int(x) for x in np.random.default_rng(11).integers(1, 200, size=60)]
+    w = I.Workload("claims", 1, 4 * hkv, hkv, 128, 64, [[I.GLOBAL, I.LOCAL, I.LOCAL, I.LOCAL]], [300],
+                   lens, seed=11)
+    c, q, cu, qp, ids = prefill_case(w)
+    o0, l0 = run_prefill(c, 0, q, cu, qp, ids)
+    for _ in range(4):
+        o, l = run_prefill(c, 0, q, cu, qp, ids)
+        assert torch.equal(o, o0) and torch.equal(l, l0)
+    rc, ref, ref_lse = c.oracle_attention(0, q, ids, q_index(cu), qp.numpy())
+    assert rc == 0
+    check_close(o0, ref, "claimed units")
+    np.testing.assert_allclose(l0.cpu().numpy().T, ref_lse, atol=1e-3, rtol=0)
+
+
 def test_head_dim_64_many_heads():
     w = I.Workload("d64", 1, 16, 4, 64, 32, [[I.LOCAL, I.GLOBAL, I.LOCAL, I.LOCAL]], [7],
                    [300, 45], seed=5)
