@@ -13,9 +13,9 @@
 // and per-row masks keep every row to its own key set: j <= p, and j >= p-W+1
 // for a local head.
 //
-// Warp roles (320 threads, one CTA per SM). The units form one list in
-// descending cost; CTA c starts with unit c and then claims the next unclaimed
-// unit from a counter in global memory, so a CTA on a slower SM simply runs
+// Warp roles (320 threads, one CTA per SM). The units form one list, in
+// descending key tiles; CTA c starts with unit c and then claims the next
+// unclaimed unit from a counter in global memory, so a CTA on a slower SM runs
 // fewer units (greedy list scheduling with the measured rather than the
 // estimated unit times):
 //   warp 0      TMA producer: claims the units (one ahead of the one it
