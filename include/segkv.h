@@ -136,6 +136,9 @@ int segkv_append(segkv_t h, int layer, const void* k, const void* v, const int32
  *   o       device bf16 [cu_seqlens[n], Hq, D]; lse device fp32 [Hq, cu_seqlens[n]]
  *           (natural log) or NULL.
  *   workspace, workspace_bytes  unused by this call (pass NULL, 0).
+ * The kernel's CTAs claim work units at run time (from a counter in the
+ * call's own uploaded plan), but every unit is computed in a fixed order, so
+ * repeated calls return the same bits.
  * Errors: INVALID_ARG, EVICTED (a local head already dropped a needed key).
  */
 int segkv_prefill_attn(segkv_t h, int layer, const void* q, const int32_t* cu_seqlens,
